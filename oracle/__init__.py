@@ -1,0 +1,164 @@
+"""Plain fp64 CPU oracle for the CSA + HCA attention path.
+
+TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's CPU
+baseline leg may call it; the library's product path never does.  It shares no
+code with the CUDA library.  The arithmetic lives in ``oracle.c`` (plain C,
+fp64, OpenMP over query rows); this module only builds it with gcc and
+marshals numpy arrays.
+
+Each wrapper works on ONE sequence; ragged batches loop over sequences here.
+The function-level citations are in ``oracle.c``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``liboracle.so`` next to it (gcc, -O2, OpenMP)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            D = ctypes.POINTER(ctypes.c_double)
+            I64 = ctypes.POINTER(ctypes.c_int64)
+            I32 = ctypes.POINTER(ctypes.c_int32)
+            i64, i32, dbl = ctypes.c_int64, ctypes.c_int32, ctypes.c_double
+            lib.oracle_num_threads.restype = ctypes.c_int
+            lib.oracle_compress.argtypes = [D, D, i64, i32, i32, D]
+            lib.oracle_compress.restype = None
+            lib.oracle_index.argtypes = [D, D, D, I64, i64, i64, i32, i32, i32, D]
+            lib.oracle_index.restype = None
+            lib.oracle_topk.argtypes = [D, i64, i64, I64, i32, I32]
+            lib.oracle_topk.restype = None
+            lib.oracle_sparse_attn.argtypes = [D, D, D, i64, I32, i32, D, D, i64, i64,
+                                               I64, i64, i32, i32, i32, dbl, D, D]
+            lib.oracle_sparse_attn.restype = i64
+            lib.oracle_hca_attn.argtypes = [D, D, D, i64, i32, D, D, i64, i64,
+                                            I64, i64, i32, i32, i32, dbl, D, D]
+            lib.oracle_hca_attn.restype = i64
+            _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def _f64(a) -> np.ndarray:
+    if hasattr(a, "detach"):  # torch tensor
+        a = a.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _i64(a) -> np.ndarray:
+    if hasattr(a, "detach"):
+        a = a.detach().to("cpu").numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int64))
+
+
+def _i32(a) -> np.ndarray:
+    if hasattr(a, "detach"):
+        a = a.detach().to("cpu").numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _p(a: np.ndarray, ct):
+    return a.ctypes.data_as(ctypes.POINTER(ct))
+
+
+def n_visible(t, m: int):
+    """Entries visible from absolute position t: floor((t+1)/m)."""
+    return (np.asarray(t, dtype=np.int64) + 1) // m
+
+
+def compress(X, G, m: int) -> np.ndarray:
+    """X [T, d], G [m, d] -> Xc [floor(T/m), d] (fp64)."""
+    X, G = _f64(X), _f64(G)
+    T, d = X.shape
+    assert G.shape == (m, d)
+    out = np.zeros((T // m, d), dtype=np.float64)
+    _load().oracle_compress(_p(X, ctypes.c_double), _p(G, ctypes.c_double), T, d, m,
+                            _p(out, ctypes.c_double))
+    return out
+
+
+def index(qI, w, kI, tpos, m: int) -> np.ndarray:
+    """qI [Nq, HI, dI], w [Nq, HI], kI [Tc, HI, dI], tpos [Nq] -> I [Nq, Tc]
+    (invisible entries = -inf)."""
+    qI, w, kI, tpos = _f64(qI), _f64(w), _f64(kI), _i64(tpos)
+    Nq, HI, dI = qI.shape
+    Tc = kI.shape[0]
+    assert kI.shape[1:] == (HI, dI) and w.shape == (Nq, HI) and tpos.shape == (Nq,)
+    assert np.all(n_visible(tpos, m) <= Tc), "query sees entries that are not stored"
+    out = np.zeros((Nq, Tc), dtype=np.float64)
+    _load().oracle_index(_p(qI, ctypes.c_double), _p(w, ctypes.c_double), _p(kI, ctypes.c_double),
+                         _p(tpos, ctypes.c_int64), Nq, Tc, HI, dI, m, _p(out, ctypes.c_double))
+    return out
+
+
+def topk(I, nvis, k: int) -> np.ndarray:
+    """I [Nq, ld] scores (only columns < nvis[r] are read), nvis [Nq] -> idx [Nq, k] int32."""
+    I, nvis = _f64(I), _i64(nvis)
+    Nq, ld = I.shape
+    assert nvis.shape == (Nq,) and np.all(nvis <= ld) and np.all(nvis >= 0)
+    out = np.zeros((Nq, k), dtype=np.int32)
+    _load().oracle_topk(_p(I, ctypes.c_double), Nq, ld, _p(nvis, ctypes.c_int64), k,
+                        _p(out, ctypes.c_int32))
+    return out
+
+
+def sparse_attn(Q, Kc, Vc, idx, Kraw, Vraw, raw_pos0: int, tpos, W: int, scale: float):
+    """CSA core attention for one sequence.  Returns (O [Nq,H,d], lse [Nq,H])."""
+    Q, Kc, Vc, Kraw, Vraw = _f64(Q), _f64(Kc), _f64(Vc), _f64(Kraw), _f64(Vraw)
+    idx, tpos = _i32(idx), _i64(tpos)
+    Nq, H, d = Q.shape
+    k = idx.shape[1]
+    O = np.zeros((Nq, H, d), dtype=np.float64)
+    lse = np.zeros((Nq, H), dtype=np.float64)
+    rc = _load().oracle_sparse_attn(
+        _p(Q, ctypes.c_double), _p(Kc, ctypes.c_double), _p(Vc, ctypes.c_double), Kc.shape[0],
+        _p(idx, ctypes.c_int32), k, _p(Kraw, ctypes.c_double), _p(Vraw, ctypes.c_double),
+        Kraw.shape[0], raw_pos0, _p(tpos, ctypes.c_int64), Nq, H, d, W, scale,
+        _p(O, ctypes.c_double), _p(lse, ctypes.c_double))
+    if rc != 0:
+        raise ValueError(f"oracle_sparse_attn: invalid input at row {-rc - 1}")
+    return O, lse
+
+
+def hca_attn(Q, Kc, Vc, m: int, Kraw, Vraw, raw_pos0: int, tpos, W: int, scale: float):
+    """HCA attention for one sequence.  Returns (O [Nq,H,d], lse [Nq,H])."""
+    Q, Kc, Vc, Kraw, Vraw = _f64(Q), _f64(Kc), _f64(Vc), _f64(Kraw), _f64(Vraw)
+    tpos = _i64(tpos)
+    Nq, H, d = Q.shape
+    O = np.zeros((Nq, H, d), dtype=np.float64)
+    lse = np.zeros((Nq, H), dtype=np.float64)
+    rc = _load().oracle_hca_attn(
+        _p(Q, ctypes.c_double), _p(Kc, ctypes.c_double), _p(Vc, ctypes.c_double), Kc.shape[0], m,
+        _p(Kraw, ctypes.c_double), _p(Vraw, ctypes.c_double), Kraw.shape[0], raw_pos0,
+        _p(tpos, ctypes.c_int64), Nq, H, d, W, scale, _p(O, ctypes.c_double),
+        _p(lse, ctypes.c_double))
+    if rc != 0:
+        raise ValueError(f"oracle_hca_attn: invalid input at row {-rc - 1}")
+    return O, lse

@@ -1,0 +1,328 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself:
+the pages' printed compressed lengths, closed forms, textbook reductions that
+a library routine computes independently (torch SDPA, numpy sort/matmul,
+scipy expit), invariants of the definitions, and brute force on tiny inputs.
+Each test is chosen so that a plausible slip in ``oracle.c`` (a dropped term,
+a swapped index, a wrong sign, an off-by-one in visibility or the window)
+fails it."""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+from scipy.special import expit
+
+import oracle
+
+RNG = np.random.default_rng(1234)
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------- compressor
+
+def _golden_lengths():
+    rows = []
+    with open(os.path.join(GOLDEN, "compressed_lengths.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                T, m, n, _ = line.split()
+                rows.append((int(T), int(m), int(n)))
+    return rows
+
+
+@pytest.mark.parametrize("T,m,n", _golden_lengths())
+def test_compressed_length_matches_pages(T, m, n):
+    d = 2 if T > 100000 else 8
+    X = np.zeros((T, d))
+    G = np.zeros((m, d))
+    assert oracle.compress(X, G, m).shape == (n, d)
+
+
+@pytest.mark.parametrize("T,m", [(1027, 4), (3, 4), (255, 128), (0, 4), (130, 128)])
+def test_tail_shorter_than_block_is_dropped(T, m):
+    d = 4
+    X = RNG.standard_normal((T, d))
+    G = RNG.standard_normal((m, d))
+    out = oracle.compress(X, G, m)
+    assert out.shape == (T // m, d)
+    if T // m:
+        full = oracle.compress(X[: (T // m) * m], G, m)
+        np.testing.assert_array_equal(out, full)
+
+
+@pytest.mark.parametrize("m", [1, 4, 128])
+def test_zero_gates_give_block_mean(m):
+    T, d = 4 * m + 3, 16
+    X = RNG.standard_normal((T, d))
+    out = oracle.compress(X, np.zeros((m, d)), m)
+    ref = X[: (T // m) * m].reshape(T // m, m, d).mean(axis=1)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-14)
+
+
+def test_two_position_gate_is_logistic():
+    # m=2: the weight of position 0 is sigmoid(g0 - g1) per channel.
+    T, d = 10, 8
+    X = RNG.standard_normal((T, d))
+    G = RNG.standard_normal((2, d)) * 3
+    w0 = expit(G[0] - G[1])
+    ref = w0 * X[0::2] + (1 - w0) * X[1::2]
+    np.testing.assert_allclose(oracle.compress(X, G, 2), ref, rtol=0, atol=1e-14)
+
+
+def test_dominant_gate_copies_its_token_per_channel():
+    # a +60 logit at a different position in every channel: each output
+    # channel copies the token at that channel's own position.
+    m, d, T = 4, 8, 12
+    X = RNG.standard_normal((T, d))
+    G = np.zeros((m, d))
+    pick = np.array([0, 1, 2, 3, 3, 2, 1, 0])
+    G[pick, np.arange(d)] = 60.0
+    out = oracle.compress(X, G, m)
+    ref = np.stack([X[j * m + pick, np.arange(d)] for j in range(T // m)])
+    # the other weights are below 3*exp(-60); fp64 rounding dominates
+    np.testing.assert_allclose(out, ref, rtol=0, atol=4e-16 * np.abs(X).max())
+
+
+def test_compress_linear_and_position_permutation():
+    m, d, T = 4, 6, 20
+    X1, X2 = RNG.standard_normal((T, d)), RNG.standard_normal((T, d))
+    G = RNG.standard_normal((m, d))
+    a, b = 0.75, -2.5
+    np.testing.assert_allclose(oracle.compress(a * X1 + b * X2, G, m),
+                               a * oracle.compress(X1, G, m) + b * oracle.compress(X2, G, m),
+                               rtol=0, atol=1e-13)
+    perm = np.array([2, 0, 3, 1])
+    Xp = X1.reshape(T // m, m, d)[:, perm].reshape(T, d)
+    np.testing.assert_allclose(oracle.compress(Xp, G[perm], m), oracle.compress(X1, G, m),
+                               rtol=0, atol=1e-14)
+    # a per-channel shift of the logits changes nothing (softmax), a
+    # per-position one does
+    np.testing.assert_allclose(oracle.compress(X1, G + RNG.standard_normal(d), m),
+                               oracle.compress(X1, G, m), rtol=0, atol=1e-13)
+    shifted = G.copy()
+    shifted[0] += 1.0
+    assert np.abs(oracle.compress(X1, shifted, m) - oracle.compress(X1, G, m)).max() > 1e-3
+
+
+# -------------------------------------------------------------------- indexer
+
+def test_visibility_boundary():
+    # entry j is visible exactly from position (j+1)*m - 1 on
+    m, Tc = 4, 5
+    for t in range(0, Tc * m):
+        nv = int(oracle.n_visible(t, m))
+        assert nv == sum(1 for j in range(Tc) if (j + 1) * m - 1 <= t)
+    assert oracle.n_visible(2, 4) == 0 and oracle.n_visible(3, 4) == 1
+    assert oracle.n_visible(126, 128) == 0 and oracle.n_visible(127, 128) == 1
+
+
+def test_single_head_unit_weight_is_relu_of_matmul():
+    Nq, Tc, dI, m = 24, 6, 16, 4
+    q = RNG.standard_normal((Nq, 1, dI))
+    k = RNG.standard_normal((Tc, 1, dI))
+    t = np.arange(Nq)
+    I = oracle.index(q, np.ones((Nq, 1)), k, t, m)
+    ref = np.maximum(q[:, 0] @ k[:, 0].T, 0.0)
+    for r in range(Nq):
+        nv = (r + 1) // m
+        np.testing.assert_allclose(I[r, :nv], ref[r, :nv], rtol=0, atol=1e-12)
+        assert np.all(np.isneginf(I[r, nv:]))
+
+
+def test_index_sums_single_head_indexers():
+    Nq, Tc, HI, dI, m = 36, 9, 4, 8, 4
+    q = RNG.standard_normal((Nq, HI, dI))
+    k = RNG.standard_normal((Tc, HI, dI))
+    w = RNG.random((Nq, HI))
+    t = np.arange(Nq)
+    I = oracle.index(q, w, k, t, m)
+    parts = sum(oracle.index(q[:, h:h + 1], w[:, h:h + 1], k[:, h:h + 1], t, m) for h in range(HI))
+    vis = np.isfinite(I)
+    np.testing.assert_array_equal(vis, np.isfinite(parts))
+    np.testing.assert_allclose(I[vis], parts[vis], rtol=1e-13, atol=1e-12)
+    # positive rescaling of the head weights rescales the score
+    np.testing.assert_allclose(oracle.index(q, 3.0 * w, k, t, m)[vis], 3.0 * I[vis], rtol=1e-13)
+    # heads whose dot product is negative contribute nothing: flipping the
+    # sign of q for a head changes the score by exactly that head's part
+    q2 = q.copy()
+    q2[:, 1] *= -1
+    I2 = oracle.index(q2, w, k, t, m)
+    p1 = oracle.index(q[:, 1:2], w[:, 1:2], k[:, 1:2], t, m)
+    p1n = oracle.index(q2[:, 1:2], w[:, 1:2], k[:, 1:2], t, m)
+    with np.errstate(invalid="ignore"):
+        np.testing.assert_allclose(I2[vis], (I - p1 + p1n)[vis], rtol=1e-12, atol=1e-12)
+    assert np.all(I[vis] >= 0)
+
+
+# ---------------------------------------------------------------------- top-k
+
+def _brute_topk(row, nv, k):
+    order = sorted(range(nv), key=lambda j: (-row[j], j))[:k]
+    return sorted(order) + [-1] * (k - min(k, nv))
+
+
+def test_topk_hand_worked_ties():
+    I = np.array([[1.0, 3.0, 3.0, 0.0, 3.0, 2.0]])
+    nv = np.array([6])
+    assert oracle.topk(I, nv, 3).tolist() == [[1, 2, 4]]
+    assert oracle.topk(I, nv, 2).tolist() == [[1, 2]]
+    assert oracle.topk(I, nv, 4).tolist() == [[1, 2, 4, 5]]
+    assert oracle.topk(I, nv, 8).tolist() == [[0, 1, 2, 3, 4, 5, -1, -1]]
+    # entries beyond the visible count are never read, however large
+    I2 = np.array([[1.0, 0.5, 9.0, 9.0]])
+    assert oracle.topk(I2, np.array([2]), 1).tolist() == [[0]]
+    assert oracle.topk(I2, np.array([0]), 2).tolist() == [[-1, -1]]
+
+
+def test_topk_signed_zero_ties():
+    assert oracle.topk(np.array([[-0.0, 0.0]]), np.array([2]), 1).tolist() == [[0]]
+    assert oracle.topk(np.array([[0.0, -0.0]]), np.array([2]), 1).tolist() == [[0]]
+    assert oracle.topk(np.array([[-1.0, -0.0, 0.0]]), np.array([3]), 2).tolist() == [[1, 2]]
+
+
+@pytest.mark.parametrize("levels", [None, 4, 2])
+def test_topk_brute_force_and_stable_argsort(levels):
+    Nq, ld, k = 64, 50, 7
+    if levels is None:
+        I = RNG.standard_normal((Nq, ld))
+    else:
+        I = RNG.integers(0, levels, (Nq, ld)).astype(np.float64)
+    nv = RNG.integers(0, ld + 1, Nq)
+    got = oracle.topk(I, nv, k)
+    for r in range(Nq):
+        assert got[r].tolist() == _brute_topk(I[r], int(nv[r]), k)
+        sel = np.argsort(-I[r, : nv[r]], kind="stable")[:k]
+        keep = min(k, int(nv[r]))
+        assert got[r, :keep].tolist() == sorted(sel.tolist())
+        assert np.all(got[r, keep:] == -1)
+
+
+# ------------------------------------------------------------------ attention
+
+def _sdpa(Q, K, V, mask, scale):
+    """torch scaled_dot_product_attention in fp64 (a library routine), MQA:
+    one K/V shared by every head.  Q [Nq,H,d], K/V [n,d], mask [Nq,n] bool."""
+    q = torch.from_numpy(Q).permute(1, 0, 2)  # [H, Nq, d]
+    k = torch.from_numpy(K)[None].expand(Q.shape[1], -1, -1)
+    v = torch.from_numpy(V)[None].expand(Q.shape[1], -1, -1)
+    o = torch.nn.functional.scaled_dot_product_attention(
+        q, k, v, attn_mask=torch.from_numpy(mask)[None], scale=scale)
+    logits = (q @ k.transpose(-1, -2)) * scale
+    logits = logits.masked_fill(~torch.from_numpy(mask)[None], -math.inf)
+    lse = torch.logsumexp(logits, dim=-1)
+    return o.permute(1, 0, 2).numpy(), lse.permute(1, 0).numpy()
+
+
+def test_m1_no_window_is_causal_attention():
+    T, H, d = 33, 3, 8
+    Q = RNG.standard_normal((T, H, d))
+    K, V = RNG.standard_normal((T, d)), RNG.standard_normal((T, d))
+    scale = 1 / math.sqrt(d)
+    t = np.arange(T)
+    mask = t[None, :] <= t[:, None]
+    ref_o, ref_l = _sdpa(Q, K, V, mask, scale)
+    # HCA form with m'=1: every past token is an entry
+    o, l = oracle.hca_attn(Q, K, V, 1, K[:0], V[:0], 0, t, 0, scale)
+    np.testing.assert_allclose(o, ref_o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l, ref_l, rtol=0, atol=1e-12)
+    # CSA form with m=1 and k >= t+1: select every visible entry
+    idx = np.full((T, T), -1, dtype=np.int32)
+    for r in range(T):
+        idx[r, : r + 1] = np.arange(r + 1)
+    o2, l2 = oracle.sparse_attn(Q, K, V, idx, K[:0], V[:0], 0, t, 0, scale)
+    np.testing.assert_allclose(o2, ref_o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l2, ref_l, rtol=0, atol=1e-12)
+
+
+def test_window_only_is_banded_attention():
+    # with no compressed entries visible, only the raw window remains
+    T, H, d, W = 20, 2, 4, 5
+    Q = RNG.standard_normal((T, H, d))
+    K, V = RNG.standard_normal((T, d)), RNG.standard_normal((T, d))
+    t = np.arange(T)
+    mask = (t[None, :] <= t[:, None]) & (t[None, :] > t[:, None] - W)
+    ref_o, ref_l = _sdpa(Q, K, V, mask, 0.5)
+    o, l = oracle.hca_attn(Q, K[:0], V[:0], 1000, K, V, 0, t, W, 0.5)
+    np.testing.assert_allclose(o, ref_o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l, ref_l, rtol=0, atol=1e-12)
+    # W = 1: the output is the token's own value row
+    o1, _ = oracle.hca_attn(Q, K[:0], V[:0], 1000, K, V, 0, t, 1, 0.5)
+    np.testing.assert_allclose(o1, np.broadcast_to(V[:, None, :], o1.shape), rtol=0, atol=1e-15)
+
+
+def test_hca_equals_masked_dense_attention_over_entries_and_window():
+    m, T, H, d, W = 8, 70, 4, 8, 6
+    Q = RNG.standard_normal((T, H, d))
+    Kc, Vc = RNG.standard_normal((T // m, d)), RNG.standard_normal((T // m, d))
+    K, V = RNG.standard_normal((T, d)), RNG.standard_normal((T, d))
+    t = np.arange(T)
+    j = np.arange(T // m)
+    mask_c = (j[None, :] + 1) * m - 1 <= t[:, None]
+    mask_r = (t[None, :] <= t[:, None]) & (t[None, :] > t[:, None] - W)
+    ref_o, ref_l = _sdpa(Q, np.concatenate([Kc, K]), np.concatenate([Vc, V]),
+                         np.concatenate([mask_c, mask_r], axis=1), 0.3)
+    o, l = oracle.hca_attn(Q, Kc, Vc, m, K, V, 0, t, W, 0.3)
+    np.testing.assert_allclose(o, ref_o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l, ref_l, rtol=0, atol=1e-12)
+
+
+def test_sparse_with_all_visible_selected_equals_hca():
+    m, T, H, d, W, k = 4, 64, 2, 8, 4, 20
+    Q = RNG.standard_normal((T, H, d))
+    Kc, Vc = RNG.standard_normal((T // m, d)), RNG.standard_normal((T // m, d))
+    K, V = RNG.standard_normal((T, d)), RNG.standard_normal((T, d))
+    t = np.arange(T)
+    nv = oracle.n_visible(t, m)
+    assert nv.max() <= k
+    idx = oracle.topk(RNG.standard_normal((T, T // m)), nv, k)
+    o1, l1 = oracle.sparse_attn(Q, Kc, Vc, idx, K, V, 0, t, W, 0.4)
+    o2, l2 = oracle.hca_attn(Q, Kc, Vc, m, K, V, 0, t, W, 0.4)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-13)
+
+
+def test_single_key_and_empty_set():
+    H, d = 3, 5
+    Q = RNG.standard_normal((1, H, d))
+    Kc, Vc = RNG.standard_normal((4, d)), RNG.standard_normal((4, d))
+    o, l = oracle.sparse_attn(Q, Kc, Vc, np.array([[2, -1, -1]]), Kc[:0], Vc[:0], 0, [11], 0, 0.7)
+    np.testing.assert_allclose(o[0], np.broadcast_to(Vc[2], (H, d)), rtol=0, atol=1e-15)
+    np.testing.assert_allclose(l[0], 0.7 * Q[0] @ Kc[2], rtol=0, atol=1e-14)
+    o, l = oracle.sparse_attn(Q, Kc, Vc, np.array([[-1, -1]]), Kc[:0], Vc[:0], 0, [11], 0, 0.7)
+    assert np.all(o == 0) and np.all(np.isneginf(l))
+
+
+def test_lse_merge_of_disjoint_key_sets():
+    H, d, n = 4, 8, 12
+    Q = RNG.standard_normal((1, H, d))
+    Kc, Vc = RNG.standard_normal((n, d)), RNG.standard_normal((n, d))
+    A, B = [0, 3, 5, 7, 8], [1, 2, 9, 11]
+    z = Kc[:0]
+    oa, la = oracle.sparse_attn(Q, Kc, Vc, np.array([A]), z, z, 0, [10 ** 6], 0, 0.5)
+    ob, lb = oracle.sparse_attn(Q, Kc, Vc, np.array([B]), z, z, 0, [10 ** 6], 0, 0.5)
+    ou, lu = oracle.sparse_attn(Q, Kc, Vc, np.array([A + B]), z, z, 0, [10 ** 6], 0, 0.5)
+    lm = np.logaddexp(la, lb)
+    om = np.exp(la - lm)[..., None] * oa + np.exp(lb - lm)[..., None] * ob
+    np.testing.assert_allclose(lu, lm, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(ou, om, rtol=0, atol=1e-13)
+
+
+def test_head_permutation_equivariance_and_window_source_offset():
+    m, T, H, d, W = 4, 40, 6, 8, 8
+    Q = RNG.standard_normal((T, H, d))
+    Kc, Vc = RNG.standard_normal((T // m, d)), RNG.standard_normal((T // m, d))
+    K, V = RNG.standard_normal((T, d)), RNG.standard_normal((T, d))
+    t = np.arange(T)
+    idx = oracle.topk(RNG.standard_normal((T, T // m)), oracle.n_visible(t, m), 3)
+    o, l = oracle.sparse_attn(Q, Kc, Vc, idx, K, V, 0, t, W, 0.3)
+    perm = RNG.permutation(H)
+    op, lp = oracle.sparse_attn(Q[:, perm], Kc, Vc, idx, K, V, 0, t, W, 0.3)
+    np.testing.assert_allclose(op, o[:, perm], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lp, l[:, perm], rtol=0, atol=1e-14)
+    # a raw cache holding only positions 30.. answers the rows t >= 37 alike
+    rows = t >= 30 + W - 1
+    o2, l2 = oracle.sparse_attn(Q[rows], Kc, Vc, idx[rows], K[30:], V[30:], 30, t[rows], W, 0.3)
+    np.testing.assert_allclose(o2, o[rows], rtol=0, atol=1e-14)
+    with pytest.raises(ValueError):
+        oracle.sparse_attn(Q, Kc, Vc, idx, K[30:], V[30:], 30, t, W, 0.3)
