@@ -1,0 +1,179 @@
+/*
+ * lcattn — Compressed Sparse Attention (CSA) and Heavily Compressed Attention
+ * (HCA) for one NVIDIA B300 (sm_103a).
+ *
+ * The method (page "DeepSeek-V4 技术解析：架构革新与 Coding Agent 后训练优化",
+ * §1.1 混合注意力：CSA 与 HCA 的协同; page "DeepSeek-V4 技术报告解读：百万Token
+ * 上下文是怎么做到的", §三大架构改动 1-2): the KV of every m tokens is folded
+ * into one compressed entry; a Lightning Indexer scores every query against
+ * the compressed entries; a causal top-k keeps the k best; MQA attention runs
+ * over the kept entries plus an uncompressed sliding window.  HCA folds every
+ * m' >> m tokens and attends densely over all visible entries plus the window.
+ *
+ * Conventions shared by every call
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, unless
+ *     the comment says otherwise.  The library never allocates, frees, or
+ *     keeps a pointer past the call; scratch memory is the caller's
+ *     `ws` buffer of at least lc_workspace_size() bytes.
+ *   - Every call is asynchronous on `stream` (0 = legacy default stream):
+ *     it validates its host-side arguments, enqueues kernels and returns.
+ *     It never synchronises unless the environment variable LC_DEBUG_SYNC=1
+ *     is set, in which case it waits for its kernels and reports device-side
+ *     errors through the return value.
+ *   - Layouts are row-major with a contiguous last dimension.  `lc_dtype`
+ *     selects the type of the activations (Q, K, V, compressed entries,
+ *     indexer q/k, O); gate logits, head weights, scores and LSE are fp32.
+ *     All arithmetic is fp32; outputs are rounded once (round-to-nearest-even).
+ *   - Errors: invalid host arguments return LC_ERR_INVALID_ARG and enqueue
+ *     nothing; a shape outside the supported set returns LC_ERR_UNSUPPORTED;
+ *     a CUDA launch failure returns LC_ERR_CUDA (see lc_last_cuda_error()).
+ *     Kernels never trap.  A bad value found on the device (an entry index out
+ *     of range or not yet visible, a window position the raw cache does not
+ *     hold, an inconsistent batch descriptor) is skipped and OR-ed as a bit of
+ *     lc_dev_error into *dev_err when dev_err is not NULL.
+ *
+ * Notation: t = absolute position of a query row; entry j of a sequence is
+ * visible from t iff (j+1)*m - 1 <= t, so n_vis(t) = floor((t+1)/m); the
+ * window of t is raw positions max(0, t-W+1) .. t.
+ */
+#ifndef LCATTN_H
+#define LCATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *lc_stream; /* a cudaStream_t */
+
+typedef enum {
+    LC_OK = 0,
+    LC_ERR_INVALID_ARG = 1,
+    LC_ERR_UNSUPPORTED = 2,
+    LC_ERR_CUDA = 3,
+    LC_ERR_TIMEOUT = 4,       /* a bounded device wait expired */
+    LC_ERR_DEVICE_CHECK = 5,  /* LC_DEBUG_SYNC=1 only: *dev_err != 0 */
+    LC_ERR_WORKSPACE = 6      /* ws too small for this call */
+} lc_status;
+
+typedef enum { LC_F32 = 0, LC_BF16 = 1 } lc_dtype;
+
+/* Bits OR-ed into *dev_err by kernels. */
+typedef enum {
+    LC_DEVERR_INDEX = 1,   /* selected entry index >= stored entries or not visible */
+    LC_DEVERR_WINDOW = 2,  /* window position outside the sequence's raw rows */
+    LC_DEVERR_BATCH = 4,   /* batch descriptor inconsistent (e.g. n_vis > entries) */
+    LC_DEVERR_TIMEOUT = 8  /* a bounded wait inside a kernel gave up */
+} lc_dev_error;
+
+/* Ragged batch.  Every array is on the DEVICE (int64); the three maxima are
+ * host values used to size grids.  Sequence b owns query rows
+ * cu_q[b] .. cu_q[b+1]-1 at consecutive absolute positions q_pos0[b], ...;
+ * compressed entries cu_c[b] .. cu_c[b+1]-1 (sequence-local entry j is row
+ * cu_c[b]+j of Kc/Vc/kI); raw rows cu_raw[b] .. cu_raw[b+1]-1 holding
+ * positions raw_pos0[b], raw_pos0[b]+1, ... (the window's source). */
+typedef struct {
+    int32_t B;
+    const int64_t *cu_q;     /* [B+1] */
+    const int64_t *q_pos0;   /* [B]   */
+    const int64_t *cu_c;     /* [B+1] */
+    const int64_t *cu_raw;   /* [B+1] */
+    const int64_t *raw_pos0; /* [B]   */
+    int64_t total_q;         /* host: cu_q[B] */
+    int64_t max_q;           /* host: max over b of rows of sequence b */
+    int64_t max_c;           /* host: max over b of entries of sequence b */
+} lc_batch;
+
+/* CSA token compressor (page "DeepSeek-V4 技术解析…", §1.1, CSA paragraph:
+ * a token-level compressor merges the KV of every m tokens into one entry).
+ * Form (the pages give none): softmax-gated pooling with position gates,
+ *   Kc[j,c] = sum_{p<m} softmax_p(G_K[:,c])[p] * K[j*m+p, c],  j < floor(T/m)
+ * and the same for V with G_V.  A tail of T mod m tokens makes no entry.
+ *   K, V   [T, d] dtype          G_K, G_V [m, d] fp32 (may alias)
+ *   Kc, Vc [floor(T/m), d] dtype (written; must not overlap the inputs)
+ * Supported: d in {64, 128}; 1 <= m <= 256; T >= 0. */
+lc_status csa_compress(const void *K, const void *V, const float *G_K, const float *G_V,
+                       int64_t T, int32_t d, int32_t m, lc_dtype dtype, void *Kc, void *Vc,
+                       lc_stream stream);
+
+/* HCA compressor (same page, §1.1, HCA paragraph: every m' tokens become one
+ * entry, m' much larger than m).  Same arithmetic and arguments as
+ * csa_compress; kept as its own entry point because the HCA ratio (128)
+ * selects a different launch shape. */
+lc_status hca_compress(const void *K, const void *V, const float *G_K, const float *G_V,
+                       int64_t T, int32_t d, int32_t m, lc_dtype dtype, void *Kc, void *Vc,
+                       lc_stream stream);
+
+/* Lightning Indexer (same page, §1.1, CSA paragraph: a light indexer scores
+ * the compressed KV blocks against the query), with the form
+ *   I[r,j] = sum_{h<HI} w[r,h] * max(0, qI[r,h,:] . kI[cu_c[b]+j,h,:])
+ * for j < n_vis(t_r); other columns < ld are -inf.
+ *   qI [total_q, HI, dI] dtype;  w [total_q, HI] fp32;  kI [cu_c[B], HI, dI] dtype
+ *   scores [total_q, ld] fp32, ld >= max_c, or NULL
+ *   topk   [total_q, k] int32 or NULL: when non-NULL the call also selects
+ *          (as topk_select) and, if scores is NULL, keeps the scores in ws.
+ * At least one of scores / topk must be non-NULL; kI must be 16-byte aligned.
+ * Supported: HI in {1,2,4,8}; dI in {32,64}; 1 <= k <= 4096. */
+lc_status lightning_index(const void *qI, const float *w, const void *kI, const lc_batch *batch,
+                          int32_t HI, int32_t dI, int32_t m, lc_dtype dtype, float *scores,
+                          int64_t ld, int32_t k, int32_t *topk, void *ws, size_t ws_bytes,
+                          int32_t *dev_err, lc_stream stream);
+
+/* Causal top-k selector (same page, §1.1: the top-k selector keeps the most
+ * relevant compressed entries, 1024 in the Pro setting).  For row r keep the
+ * min(k, n_vis(t_r)) columns j < n_vis(t_r) that rank first under the total
+ * order (larger score first; equal scores: lower j first; -0.0 equals +0.0),
+ * written as ascending sequence-local j, then -1 up to k.  Scores must be
+ * finite in the visible columns (not checked).
+ *   scores [total_q, ld] fp32;  topk [total_q, k] int32 */
+lc_status topk_select(const float *scores, int64_t ld, const lc_batch *batch, int32_t m,
+                      int32_t k, int32_t *topk, void *ws, size_t ws_bytes, int32_t *dev_err,
+                      lc_stream stream);
+
+/* CSA core attention (same page, §1.1: MQA core attention over the kept
+ * entries; extra sliding-window branch).  For query row r, head h:
+ *   S = { Kc/Vc row cu_c[b]+topk[r,i] : topk[r,i] >= 0 }  then
+ *       { raw row of position p : max(0,t-W+1) <= p <= t }
+ *   O[r,h] = sum_{s in S} softmax_s(scale * Q[r,h].K_s) V_s   (one softmax)
+ *   lse[r,h] = log sum_s exp(scale * Q[r,h].K_s)   (-inf and O = 0 if S empty)
+ *   Q [total_q, H, d]; Kc, Vc [cu_c[B], d]; Kraw, Vraw [cu_raw[B], d] (dtype)
+ *   topk [total_q, k] int32 (-1 = unused slot); O [total_q, H, d] dtype;
+ *   lse [total_q, H] fp32 or NULL.
+ * Supported: d in {64,128}; H % 8 == 0, 8 <= H <= 128; 0 <= W <= 4096. */
+lc_status sparse_mqa_attn(const void *Q, const void *Kc, const void *Vc, const int32_t *topk,
+                          int32_t k, const void *Kraw, const void *Vraw, const lc_batch *batch,
+                          int32_t H, int32_t d, int32_t m, int32_t W, float scale,
+                          lc_dtype dtype, void *O, float *lse, void *ws, size_t ws_bytes,
+                          int32_t *dev_err, lc_stream stream);
+
+/* HCA dense attention (same page, §1.1, HCA paragraph: dense attention over
+ * every compressed entry).  As sparse_mqa_attn with
+ *   S = { entries j < n_vis(t) in order }  then the window. */
+lc_status hca_dense_attn(const void *Q, const void *Kc, const void *Vc, const void *Kraw,
+                         const void *Vraw, const lc_batch *batch, int32_t H, int32_t d,
+                         int32_t m, int32_t W, float scale, lc_dtype dtype, void *O, float *lse,
+                         void *ws, size_t ws_bytes, int32_t *dev_err, lc_stream stream);
+
+/* Bytes of `ws` a call needs (0 = none).  `op` is one of lc_op; unused
+ * arguments are ignored.  Host only; reads only the batch's host fields. */
+typedef enum {
+    LC_OP_LIGHTNING_INDEX = 0, /* with topk != NULL and scores == NULL */
+    LC_OP_TOPK_SELECT = 1,
+    LC_OP_SPARSE_MQA_ATTN = 2,
+    LC_OP_HCA_DENSE_ATTN = 3
+} lc_op;
+size_t lc_workspace_size(int32_t op, const lc_batch *batch, int32_t H, int32_t d, int32_t HI,
+                         int32_t dI, int32_t k);
+
+/* Diagnostics (host only). */
+const char *lc_status_string(int32_t status);
+int32_t lc_last_cuda_error(void);   /* cudaError_t of the last failed launch */
+uint64_t lc_launch_count(void);     /* kernels this library has launched so far */
+const char *lc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LCATTN_H */

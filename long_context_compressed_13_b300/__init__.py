@@ -1,0 +1,291 @@
+"""Python binding of lcattn: CSA + HCA compressed attention on one B300.
+
+Thin ctypes layer over ``liblcattn.so`` (built from ``csrc/`` for sm_103a).
+Every function has the name of the C entry point it calls and only marshals
+arguments: torch tensors provide device memory and the current CUDA stream;
+all arithmetic runs in the library's CUDA kernels.  There is no CPU fallback:
+if the library is missing or no CUDA device is present, calls raise.
+
+Shapes and meanings are those of ``include/lcattn.h``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "liblcattn.so")
+
+LC_OK, LC_ERR_INVALID_ARG, LC_ERR_UNSUPPORTED, LC_ERR_CUDA, LC_ERR_TIMEOUT = 0, 1, 2, 3, 4
+LC_ERR_DEVICE_CHECK, LC_ERR_WORKSPACE = 5, 6
+LC_F32, LC_BF16 = 0, 1
+LC_DEVERR_INDEX, LC_DEVERR_WINDOW, LC_DEVERR_BATCH, LC_DEVERR_TIMEOUT = 1, 2, 4, 8
+LC_OP_LIGHTNING_INDEX, LC_OP_TOPK_SELECT, LC_OP_SPARSE_MQA_ATTN, LC_OP_HCA_DENSE_ATTN = 0, 1, 2, 3
+
+ENTRY_POINTS = ("csa_compress", "hca_compress", "lightning_index", "topk_select",
+                "sparse_mqa_attn", "hca_dense_attn", "lc_workspace_size", "lc_status_string",
+                "lc_last_cuda_error", "lc_launch_count", "lc_version")
+
+
+class LCError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: {msg} (status {status})")
+        self.status = status
+
+
+class _LcBatch(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("cu_q", ctypes.c_void_p), ("q_pos0", ctypes.c_void_p),
+                ("cu_c", ctypes.c_void_p), ("cu_raw", ctypes.c_void_p),
+                ("raw_pos0", ctypes.c_void_p), ("total_q", ctypes.c_int64),
+                ("max_q", ctypes.c_int64), ("max_c", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load liblcattn.so (no CUDA device needed to load it)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"liblcattn.so not built at {path}; run "
+                          "`python -m long_context_compressed_13_b300._build`")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                             ctypes.c_size_t)
+    bp = ctypes.POINTER(_LcBatch)
+    sig = {
+        "csa_compress": [vp, vp, vp, vp, i64, i32, i32, i32, vp, vp, vp],
+        "hca_compress": [vp, vp, vp, vp, i64, i32, i32, i32, vp, vp, vp],
+        "lightning_index": [vp, vp, vp, bp, i32, i32, i32, i32, vp, i64, i32, vp, vp, sz, vp, vp],
+        "topk_select": [vp, i64, bp, i32, i32, vp, vp, sz, vp, vp],
+        "sparse_mqa_attn": [vp, vp, vp, vp, i32, vp, vp, bp, i32, i32, i32, i32, f32, i32, vp,
+                            vp, vp, sz, vp, vp],
+        "hca_dense_attn": [vp, vp, vp, vp, vp, bp, i32, i32, i32, i32, f32, i32, vp, vp, vp, sz,
+                           vp, vp],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = i32
+    lib.lc_workspace_size.argtypes = [i32, bp, i32, i32, i32, i32, i32]
+    lib.lc_workspace_size.restype = sz
+    lib.lc_status_string.argtypes = [i32]
+    lib.lc_status_string.restype = ctypes.c_char_p
+    lib.lc_last_cuda_error.restype = i32
+    lib.lc_launch_count.restype = ctypes.c_uint64
+    lib.lc_version.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def launch_count() -> int:
+    """Kernels the library has enqueued in this process."""
+    return int(load_library().lc_launch_count())
+
+
+def _check(fn: str, status: int):
+    if status != LC_OK:
+        lib = load_library()
+        msg = lib.lc_status_string(status).decode()
+        if status == LC_ERR_CUDA:
+            msg += f" (cudaError {lib.lc_last_cuda_error()})"
+        raise LCError(fn, status, msg)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return LC_F32
+    if t.dtype == torch.bfloat16:
+        return LC_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _dev(t: Optional[torch.Tensor], name: str, dtype=None) -> int:
+    if t is None:
+        return 0
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+@dataclass
+class DeviceBatch:
+    """lc_batch with its arrays on the device.  Build with from_host()."""
+    B: int
+    cu_q: torch.Tensor
+    q_pos0: torch.Tensor
+    cu_c: torch.Tensor
+    cu_raw: torch.Tensor
+    raw_pos0: torch.Tensor
+    total_q: int
+    max_q: int
+    max_c: int
+    host: object = None
+
+    @staticmethod
+    def from_host(cu_q: Sequence[int], q_pos0: Sequence[int], cu_c: Sequence[int],
+                  cu_raw: Sequence[int], raw_pos0: Sequence[int], device="cuda") -> "DeviceBatch":
+        B = len(q_pos0)
+        if not (len(cu_q) == len(cu_c) == len(cu_raw) == B + 1 and len(raw_pos0) == B):
+            raise ValueError("batch arrays have inconsistent lengths")
+        mk = lambda a: torch.tensor(list(a), dtype=torch.int64, device=device)
+        nq = [cu_q[b + 1] - cu_q[b] for b in range(B)]
+        nc = [cu_c[b + 1] - cu_c[b] for b in range(B)]
+        return DeviceBatch(B, mk(cu_q), mk(q_pos0), mk(cu_c), mk(cu_raw), mk(raw_pos0),
+                           int(cu_q[-1]), max(nq) if nq else 0, max(nc) if nc else 0)
+
+    @staticmethod
+    def from_workload(batch, device="cuda") -> "DeviceBatch":
+        db = DeviceBatch.from_host(batch.cu_q, batch.q_pos0, batch.cu_c, batch.cu_raw,
+                                   batch.raw_pos0, device=device)
+        db.host = batch
+        return db
+
+    def c_struct(self) -> _LcBatch:
+        return _LcBatch(self.B, self.cu_q.data_ptr(), self.q_pos0.data_ptr(),
+                        self.cu_c.data_ptr(), self.cu_raw.data_ptr(), self.raw_pos0.data_ptr(),
+                        self.total_q, self.max_q, self.max_c)
+
+
+def workspace_size(op: int, batch: DeviceBatch, H=0, d=0, HI=0, dI=0, k=0) -> int:
+    cb = batch.c_struct()
+    return int(load_library().lc_workspace_size(op, ctypes.byref(cb), H, d, HI, dI, k))
+
+
+def _compress(fn_name, K, V, G_K, G_V, m, Kc=None, Vc=None, stream=None):
+    lib = load_library()
+    T, d = K.shape
+    if V.shape != K.shape or V.dtype != K.dtype:
+        raise ValueError("K and V must have the same shape and dtype")
+    if Kc is None:
+        Kc = torch.empty((T // m, d), dtype=K.dtype, device=K.device)
+    if Vc is None:
+        Vc = torch.empty((T // m, d), dtype=K.dtype, device=K.device)
+    if Kc.shape[0] < T // m or Vc.shape[0] < T // m:
+        raise ValueError("output too small")
+    st = getattr(lib, fn_name)(_dev(K, "K"), _dev(V, "V"), _dev(G_K, "G_K", torch.float32),
+                               _dev(G_V, "G_V", torch.float32), T, d, m, _dtype_code(K),
+                               _dev(Kc, "Kc", K.dtype), _dev(Vc, "Vc", K.dtype), _stream(stream))
+    _check(fn_name, st)
+    return Kc, Vc
+
+
+def csa_compress(K, V, G_K, G_V=None, m: int = 4, Kc=None, Vc=None, stream=None):
+    """K, V [T,d] -> (Kc, Vc) [floor(T/m), d]; gates [m,d] fp32."""
+    return _compress("csa_compress", K, V, G_K, G_K if G_V is None else G_V, m, Kc, Vc, stream)
+
+
+def hca_compress(K, V, G_K, G_V=None, m: int = 128, Kc=None, Vc=None, stream=None):
+    """K, V [T,d] -> (Kc, Vc) [floor(T/m), d]; gates [m,d] fp32."""
+    return _compress("hca_compress", K, V, G_K, G_K if G_V is None else G_V, m, Kc, Vc, stream)
+
+
+def lightning_index(qI, w, kI, batch: DeviceBatch, m: int, *, scores: bool | torch.Tensor = True,
+                    k: int = 0, topk: bool | torch.Tensor = False, ws=None, dev_err=None,
+                    stream=None):
+    """Indexer scores [total_q, max_c] (fp32, -inf where invisible) and/or
+    the fused top-k [total_q, k].  Returns (scores or None, topk or None)."""
+    lib = load_library()
+    Nq, HI, dI = qI.shape
+    if isinstance(scores, torch.Tensor):
+        sc = scores
+    elif scores:
+        sc = torch.empty((Nq, max(batch.max_c, 1)), dtype=torch.float32, device=qI.device)
+    else:
+        sc = None
+    if isinstance(topk, torch.Tensor):
+        tk = topk
+    elif topk:
+        tk = torch.empty((Nq, k), dtype=torch.int32, device=qI.device)
+    else:
+        tk = None
+    if tk is not None and sc is None and ws is None:
+        need = workspace_size(LC_OP_LIGHTNING_INDEX, batch)
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=qI.device)
+    cb = batch.c_struct()
+    ld = sc.shape[1] if sc is not None else 0
+    st = lib.lightning_index(_dev(qI, "qI"), _dev(w, "w", torch.float32), _dev(kI, "kI", qI.dtype),
+                             ctypes.byref(cb), HI, dI, m, _dtype_code(qI), _dev(sc, "scores"),
+                             ld, k, _dev(tk, "topk", torch.int32), _dev(ws, "ws"),
+                             ws.numel() if ws is not None else 0,
+                             _dev(dev_err, "dev_err", torch.int32), _stream(stream))
+    _check("lightning_index", st)
+    return sc, tk
+
+
+def topk_select(scores, batch: DeviceBatch, m: int, k: int, topk=None, dev_err=None,
+                stream=None):
+    """scores [total_q, ld] fp32 -> topk [total_q, k] int32."""
+    lib = load_library()
+    if topk is None:
+        topk = torch.empty((scores.shape[0], k), dtype=torch.int32, device=scores.device)
+    cb = batch.c_struct()
+    st = lib.topk_select(_dev(scores, "scores", torch.float32), scores.shape[1], ctypes.byref(cb),
+                         m, k, _dev(topk, "topk", torch.int32), None, 0,
+                         _dev(dev_err, "dev_err", torch.int32), _stream(stream))
+    _check("topk_select", st)
+    return topk
+
+
+def sparse_mqa_attn(Q, Kc, Vc, topk, Kraw, Vraw, batch: DeviceBatch, m: int, W: int,
+                    scale: float, O=None, lse: bool | torch.Tensor = True, dev_err=None,
+                    stream=None):
+    """CSA core attention.  Returns (O [total_q,H,d], lse [total_q,H] or None)."""
+    lib = load_library()
+    Nq, H, d = Q.shape
+    if O is None:
+        O = torch.empty_like(Q)
+    if isinstance(lse, torch.Tensor):
+        L = lse
+    elif lse:
+        L = torch.empty((Nq, H), dtype=torch.float32, device=Q.device)
+    else:
+        L = None
+    cb = batch.c_struct()
+    st = lib.sparse_mqa_attn(_dev(Q, "Q"), _dev(Kc, "Kc", Q.dtype), _dev(Vc, "Vc", Q.dtype),
+                             _dev(topk, "topk", torch.int32), topk.shape[1],
+                             _dev(Kraw, "Kraw", Q.dtype), _dev(Vraw, "Vraw", Q.dtype),
+                             ctypes.byref(cb), H, d, m, W, float(scale), _dtype_code(Q),
+                             _dev(O, "O", Q.dtype), _dev(L, "lse", torch.float32), None, 0,
+                             _dev(dev_err, "dev_err", torch.int32), _stream(stream))
+    _check("sparse_mqa_attn", st)
+    return O, L
+
+
+def hca_dense_attn(Q, Kc, Vc, Kraw, Vraw, batch: DeviceBatch, m: int, W: int, scale: float,
+                   O=None, lse: bool | torch.Tensor = True, dev_err=None, ws=None, stream=None):
+    """HCA dense attention.  Returns (O [total_q,H,d], lse [total_q,H] or None)."""
+    lib = load_library()
+    Nq, H, d = Q.shape
+    if O is None:
+        O = torch.empty_like(Q)
+    if isinstance(lse, torch.Tensor):
+        L = lse
+    elif lse:
+        L = torch.empty((Nq, H), dtype=torch.float32, device=Q.device)
+    else:
+        L = None
+    cb = batch.c_struct()
+    st = lib.hca_dense_attn(_dev(Q, "Q"), _dev(Kc, "Kc", Q.dtype), _dev(Vc, "Vc", Q.dtype),
+                            _dev(Kraw, "Kraw", Q.dtype), _dev(Vraw, "Vraw", Q.dtype),
+                            ctypes.byref(cb), H, d, m, W, float(scale), _dtype_code(Q),
+                            _dev(O, "O", Q.dtype), _dev(L, "lse", torch.float32),
+                            _dev(ws, "ws"), ws.numel() if ws is not None else 0,
+                            _dev(dev_err, "dev_err", torch.int32), _stream(stream))
+    _check("hca_dense_attn", st)
+    return O, L

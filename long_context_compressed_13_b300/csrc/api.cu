@@ -1,0 +1,219 @@
+// C ABI of the lcattn library: host-side validation, workspace sizing and
+// dispatch to the kernels.  Nothing here allocates device memory.
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+
+#include "lc_common.cuh"
+
+namespace lc {
+
+lc_status compress_launch(const void *X, const float *G, int64_t T_, int d, int m, lc_dtype dt,
+                          void *Xc, cudaStream_t st);
+lc_status index_launch(const void *qI, const float *w, const void *kI, const lc_batch &b, int HI,
+                       int dI, int m, lc_dtype dt, float *scores, int64_t ld, int32_t *dev_err,
+                       cudaStream_t st);
+lc_status topk_launch(const float *scores, int64_t ld, const lc_batch &b, int m, int k,
+                      int32_t *topk, int32_t *dev_err, cudaStream_t st);
+lc_status attn_simt_launch(bool sparse, const void *Q, const void *Kc, const void *Vc,
+                           const int32_t *topk, int k, const void *Kraw, const void *Vraw,
+                           const lc_batch &b, int H, int d, int m, int W, float scale,
+                           lc_dtype dt, void *O, float *lse, int32_t *dev_err, cudaStream_t st);
+
+static std::atomic<uint64_t> g_launches{0};
+static std::atomic<int32_t> g_last_cuda{0};
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+lc_status check_launch() {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        g_last_cuda.store((int32_t)e);
+        return LC_ERR_CUDA;
+    }
+    return LC_OK;
+}
+
+static bool debug_sync() {
+    static int v = -1;
+    if (v < 0) {
+        const char *s = std::getenv("LC_DEBUG_SYNC");
+        v = (s && s[0] == '1') ? 1 : 0;
+    }
+    return v == 1;
+}
+
+// With LC_DEBUG_SYNC=1: wait for the call's kernels and surface device errors.
+static lc_status finish(lc_status s, cudaStream_t st, int32_t *dev_err) {
+    if (s != LC_OK || !debug_sync()) return s;
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) {
+        g_last_cuda.store((int32_t)e);
+        return LC_ERR_CUDA;
+    }
+    if (dev_err) {
+        int32_t h = 0;
+        if (cudaMemcpy(&h, dev_err, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
+            return LC_ERR_CUDA;
+        if (h & LC_DEVERR_TIMEOUT) return LC_ERR_TIMEOUT;
+        if (h) return LC_ERR_DEVICE_CHECK;
+    }
+    return LC_OK;
+}
+
+static bool batch_ok(const lc_batch *b) {
+    return b && b->B >= 1 && b->cu_q && b->q_pos0 && b->cu_c && b->cu_raw && b->raw_pos0 &&
+           b->total_q >= 0 && b->max_q >= 0 && b->max_c >= 0 && b->max_q <= b->total_q;
+}
+
+static bool dtype_ok(lc_dtype dt) { return dt == LC_F32 || dt == LC_BF16; }
+
+static size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
+
+static size_t index_ws_bytes(const lc_batch *b) {
+    return align_up(sizeof(float) * (size_t)b->total_q * (size_t)b->max_c);
+}
+
+static lc_status compress_common(const void *K, const void *V, const float *G_K,
+                                 const float *G_V, int64_t T, int32_t d, int32_t m,
+                                 lc_dtype dt, void *Kc, void *Vc, cudaStream_t st) {
+    if (!K || !V || !G_K || !G_V || !Kc || !Vc || T < 0 || m < 1 || !dtype_ok(dt))
+        return LC_ERR_INVALID_ARG;
+    if ((d != 64 && d != 128) || m > 256) return LC_ERR_UNSUPPORTED;
+    lc_status s = compress_launch(K, G_K, T, d, m, dt, Kc, st);
+    if (s == LC_OK) s = compress_launch(V, G_V, T, d, m, dt, Vc, st);
+    return finish(s, st, nullptr);
+}
+
+}  // namespace lc
+
+using namespace lc;
+
+extern "C" {
+
+lc_status csa_compress(const void *K, const void *V, const float *G_K, const float *G_V,
+                       int64_t T, int32_t d, int32_t m, lc_dtype dtype, void *Kc, void *Vc,
+                       lc_stream stream) {
+    return compress_common(K, V, G_K, G_V, T, d, m, dtype, Kc, Vc, (cudaStream_t)stream);
+}
+
+lc_status hca_compress(const void *K, const void *V, const float *G_K, const float *G_V,
+                       int64_t T, int32_t d, int32_t m, lc_dtype dtype, void *Kc, void *Vc,
+                       lc_stream stream) {
+    return compress_common(K, V, G_K, G_V, T, d, m, dtype, Kc, Vc, (cudaStream_t)stream);
+}
+
+lc_status lightning_index(const void *qI, const float *w, const void *kI, const lc_batch *batch,
+                          int32_t HI, int32_t dI, int32_t m, lc_dtype dtype, float *scores,
+                          int64_t ld, int32_t k, int32_t *topk, void *ws, size_t ws_bytes,
+                          int32_t *dev_err, lc_stream stream) {
+    cudaStream_t st = (cudaStream_t)stream;
+    if (!qI || !w || !kI || !batch_ok(batch) || m < 1 || !dtype_ok(dtype) || (!scores && !topk))
+        return LC_ERR_INVALID_ARG;
+    if (scores && ld < batch->max_c) return LC_ERR_INVALID_ARG;
+    if (topk && k < 1) return LC_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(kI) & 15u) != 0) return LC_ERR_INVALID_ARG;  // 16-B loads
+    if ((HI != 1 && HI != 2 && HI != 4 && HI != 8) || (dI != 32 && dI != 64) ||
+        (topk && k > 4096))
+        return LC_ERR_UNSUPPORTED;
+    if (batch->total_q == 0) return LC_OK;
+    float *sc = scores;
+    int64_t sld = ld;
+    if (!scores) {
+        const size_t need = index_ws_bytes(batch);
+        if (need > 0 && (!ws || ws_bytes < need)) return LC_ERR_WORKSPACE;
+        sc = reinterpret_cast<float *>(ws);
+        sld = batch->max_c;
+        if (sld == 0) {
+            lc_status s = topk_launch(sc, 0, *batch, m, k, topk, dev_err, st);
+            return finish(s, st, dev_err);
+        }
+    }
+    lc_status s = index_launch(qI, w, kI, *batch, HI, dI, m, dtype, sc, sld, dev_err, st);
+    if (s == LC_OK && topk) s = topk_launch(sc, sld, *batch, m, k, topk, dev_err, st);
+    return finish(s, st, dev_err);
+}
+
+lc_status topk_select(const float *scores, int64_t ld, const lc_batch *batch, int32_t m,
+                      int32_t k, int32_t *topk, void *ws, size_t ws_bytes, int32_t *dev_err,
+                      lc_stream stream) {
+    (void)ws;
+    (void)ws_bytes;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (!batch_ok(batch) || !topk || k < 1 || m < 1 || ld < batch->max_c ||
+        (!scores && batch->max_c > 0))
+        return LC_ERR_INVALID_ARG;
+    if (k > 4096) return LC_ERR_UNSUPPORTED;
+    lc_status s = topk_launch(scores, ld, *batch, m, k, topk, dev_err, st);
+    return finish(s, st, dev_err);
+}
+
+lc_status sparse_mqa_attn(const void *Q, const void *Kc, const void *Vc, const int32_t *topk,
+                          int32_t k, const void *Kraw, const void *Vraw, const lc_batch *batch,
+                          int32_t H, int32_t d, int32_t m, int32_t W, float scale,
+                          lc_dtype dtype, void *O, float *lse, void *ws, size_t ws_bytes,
+                          int32_t *dev_err, lc_stream stream) {
+    (void)ws;
+    (void)ws_bytes;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (!Q || !Kc || !Vc || !topk || !O || !batch_ok(batch) || k < 1 || m < 1 || W < 0 ||
+        !dtype_ok(dtype) || !(scale > 0.f) || (W > 0 && (!Kraw || !Vraw)))
+        return LC_ERR_INVALID_ARG;
+    if ((d != 64 && d != 128) || H < 8 || H > 128 || H % 8 || W > 4096 || k > 4096)
+        return LC_ERR_UNSUPPORTED;
+    lc_status s = attn_simt_launch(true, Q, Kc, Vc, topk, k, Kraw, Vraw, *batch, H, d, m, W,
+                                   scale, dtype, O, lse, dev_err, st);
+    return finish(s, st, dev_err);
+}
+
+lc_status hca_dense_attn(const void *Q, const void *Kc, const void *Vc, const void *Kraw,
+                         const void *Vraw, const lc_batch *batch, int32_t H, int32_t d,
+                         int32_t m, int32_t W, float scale, lc_dtype dtype, void *O, float *lse,
+                         void *ws, size_t ws_bytes, int32_t *dev_err, lc_stream stream) {
+    (void)ws;
+    (void)ws_bytes;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (!Q || !O || !batch_ok(batch) || m < 1 || W < 0 || !dtype_ok(dtype) || !(scale > 0.f) ||
+        (batch->max_c > 0 && (!Kc || !Vc)) || (W > 0 && (!Kraw || !Vraw)))
+        return LC_ERR_INVALID_ARG;
+    if ((d != 64 && d != 128) || H < 8 || H > 128 || H % 8 || W > 4096)
+        return LC_ERR_UNSUPPORTED;
+    lc_status s = attn_simt_launch(false, Q, Kc, Vc, nullptr, 0, Kraw, Vraw, *batch, H, d, m, W,
+                                   scale, dtype, O, lse, dev_err, st);
+    return finish(s, st, dev_err);
+}
+
+size_t lc_workspace_size(int32_t op, const lc_batch *batch, int32_t H, int32_t d, int32_t HI,
+                         int32_t dI, int32_t k) {
+    (void)H;
+    (void)d;
+    (void)HI;
+    (void)dI;
+    (void)k;
+    if (!batch) return 0;
+    switch (op) {
+        case LC_OP_LIGHTNING_INDEX: return index_ws_bytes(batch);
+        default: return 0;
+    }
+}
+
+const char *lc_status_string(int32_t status) {
+    switch (status) {
+        case LC_OK: return "ok";
+        case LC_ERR_INVALID_ARG: return "invalid argument";
+        case LC_ERR_UNSUPPORTED: return "unsupported shape or option";
+        case LC_ERR_CUDA: return "CUDA error";
+        case LC_ERR_TIMEOUT: return "a bounded device wait timed out";
+        case LC_ERR_DEVICE_CHECK: return "device-side check failed (see dev_err)";
+        case LC_ERR_WORKSPACE: return "workspace missing or too small";
+        default: return "unknown status";
+    }
+}
+
+int32_t lc_last_cuda_error(void) { return g_last_cuda.load(); }
+
+uint64_t lc_launch_count(void) { return g_launches.load(); }
+
+const char *lc_version(void) { return "lcattn 0.1 sm_103a"; }
+
+}  // extern "C"

@@ -1,0 +1,296 @@
+"""GPU parity of every step against the CPU oracle, through the C ABI.
+
+Inputs are drawn by ``workloads`` on the CPU and copied to the device, so both
+sides read identical values.  Bars:
+  - compressed entries: fp32 within 1e-5; bf16 a faithful rounding of the
+    fp64 value (within one bf16 ulp);
+  - indexer scores: within a derived fp32 accumulation bound; invisible
+    entries exactly -inf;
+  - top-k: bit-exact on identical score tensors;
+  - attention: max-abs 1e-4 (fp32 inputs) and 2e-2 (bf16 inputs);
+  - fused index + top-k: rows whose selection differs from the oracle's are
+    allowed only where the oracle's gap between its k-th and (k+1)-th score
+    is below 1e-5.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+TOL_ATTN = {"f32": 1e-4, "bf16": 2e-2}
+GAP = 1e-5
+
+
+@pytest.fixture(scope="module")
+def lc():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import long_context_compressed_13_b300 as m
+    from long_context_compressed_13_b300 import _build
+    _build.build()
+    m.load_library()
+    return m
+
+
+def dev(x):
+    return x.to("cuda")
+
+
+def f64(x):
+    return x.detach().to("cpu").double().numpy()
+
+
+def cast(x: np.ndarray, dtype: str) -> torch.Tensor:
+    return torch.from_numpy(x).to(wl.DTYPES[dtype])
+
+
+def assert_faithful_bf16(got: torch.Tensor, exact: np.ndarray):
+    g = f64(got)
+    tol = np.abs(exact) * 2.0 ** -7 + 1e-30
+    bad = np.abs(g - exact) > tol
+    assert not bad.any(), f"{bad.sum()} entries off by more than one bf16 ulp"
+
+
+def valid_selection(sel: np.ndarray, nvis: np.ndarray, k: int):
+    for r in range(sel.shape[0]):
+        keep = min(k, int(nvis[r]))
+        row = sel[r]
+        assert np.all(row[keep:] == -1), r
+        v = row[:keep]
+        assert np.all(np.diff(v) > 0) and (keep == 0 or (v[0] >= 0 and v[-1] < nvis[r])), r
+
+
+def boundary_gap(scores_row: np.ndarray, nv: int, k: int) -> float:
+    if nv <= k:
+        return math.inf
+    s = np.sort(scores_row[:nv])[::-1]
+    return float(s[k - 1] - s[k])
+
+
+# ------------------------------------------------------------- compressors
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("m,T,d", [(4, 2048, 64), (4, 1027, 128), (128, 4096 + 77, 128),
+                                   (128, 100, 64), (4, 3, 64), (1, 65, 64)])
+def test_compress(lc, dtype, m, T, d):
+    g = wl._gen(11, "cpu")
+    K, V = wl.normal(g, (T, d), dtype, "cpu"), wl.normal(g, (T, d), dtype, "cpu")
+    GK, GV = wl.normal(g, (m, d), "f32", "cpu"), wl.normal(g, (m, d), "f32", "cpu")
+    fn = lc.csa_compress if m < 128 else lc.hca_compress
+    Kc, Vc = fn(dev(K), dev(V), dev(GK), dev(GV), m=m)
+    torch.cuda.synchronize()
+    assert Kc.shape == (T // m, d)
+    for got, X, G in ((Kc, K, GK), (Vc, V, GV)):
+        exact = oracle.compress(X, G, m)
+        if dtype == "f32":
+            np.testing.assert_allclose(f64(got), exact, rtol=0, atol=1e-5)
+        else:
+            assert_faithful_bf16(got, exact)
+
+
+# ----------------------------------------------------------------- indexer
+
+def _index_bound(qI, w, kI, tpos, m):
+    """Rigorous bound on an fp32 evaluation of the score: gamma_n times the
+    sum of |terms|, n = dI + HI + 2 rounding steps."""
+    q, k, ww = f64(qI), f64(kI), f64(w)
+    absdot = np.einsum("rhe,jhe->rjh", np.abs(q), np.abs(k))
+    mag = np.einsum("rh,rjh->rj", np.abs(ww), absdot)
+    n = q.shape[2] + q.shape[1] + 2
+    u = 2.0 ** -24
+    return mag * (n * u / (1 - n * u)) + 1e-30
+
+
+@pytest.mark.parametrize("dtype,HI,dI,T,m", [("f32", 4, 32, 2048, 4), ("bf16", 8, 64, 1536, 4),
+                                             ("bf16", 8, 64, 700, 8)])
+def test_index_scores(lc, dtype, HI, dI, T, m):
+    L = wl.csa_layer(T=T, H=8, d=64, HI=HI, dI=dI, m=m, k=16, W=16, dtype=dtype, seed=5)
+    b = lc.DeviceBatch.from_workload(L["batch"])
+    tpos = np.array(L["batch"].positions())
+    sc, _ = lc.lightning_index(dev(L["qI"]), dev(L["w"]), dev(L["kI"]), b, m)
+    torch.cuda.synchronize()
+    ref = oracle.index(L["qI"], L["w"], L["kI"], tpos, m)
+    got = sc.cpu().double().numpy()
+    vis = np.isfinite(ref)
+    assert np.array_equal(np.isneginf(got), ~vis)
+    bound = _index_bound(L["qI"], L["w"], L["kI"], tpos, m)
+    assert np.all(np.abs(got[vis] - ref[vis]) <= bound[vis])
+
+
+def test_index_scan_ragged_decode(lc):
+    # few rows per sequence: the streaming (decode) launch shape
+    D = wl.csa_decode(B=5, ctx_lo=37, ctx_hi=3000, H=8, d=64, HI=8, dI=64, m=4, k=64, W=16,
+                      dtype="bf16", seed=9)
+    b = lc.DeviceBatch.from_workload(D["batch"])
+    sc, sel = lc.lightning_index(dev(D["qI"]), dev(D["w"]), dev(D["kI"]), b, 4, k=64, topk=True)
+    torch.cuda.synchronize()
+    got, gsel = sc.cpu().double().numpy(), sel.cpu().numpy()
+    bt = D["batch"]
+    for s in range(bt.B):
+        c0, c1 = bt.cu_c[s], bt.cu_c[s + 1]
+        t = bt.q_pos0[s]
+        ref = oracle.index(D["qI"][s:s + 1], D["w"][s:s + 1], D["kI"][c0:c1], [t], 4)
+        nv = c1 - c0
+        assert np.all(np.isneginf(got[s, nv:]))
+        bound = _index_bound(D["qI"][s:s + 1], D["w"][s:s + 1], D["kI"][c0:c1], [t], 4)
+        assert np.all(np.abs(got[s, :nv] - ref[0]) <= bound[0])
+        osel = oracle.topk(ref, [nv], 64)[0]
+        if not np.array_equal(osel, gsel[s]):
+            assert boundary_gap(ref[0], nv, 64) < GAP
+
+
+# ------------------------------------------------------------------- top-k
+
+def _score_rows(kind, Nq, ld, seed):
+    g = torch.Generator().manual_seed(seed)
+    if kind == "normal":
+        return torch.randn(Nq, ld, generator=g)
+    if kind == "ties":
+        return torch.randint(0, 4, (Nq, ld), generator=g).float()
+    if kind == "zeros":  # ReLU-style exact zeros with mixed signs
+        x = torch.randint(0, 3, (Nq, ld), generator=g).float() - 1.0
+        x = torch.where(x < 0, torch.zeros_like(x), x)
+        sign = torch.randint(0, 2, (Nq, ld), generator=g).bool()
+        return torch.where((x == 0) & sign, -torch.zeros_like(x), x)
+    if kind == "wide":  # magnitudes across many binades, both signs
+        e = torch.randint(-60, 60, (Nq, ld), generator=g).float()
+        s = torch.randint(0, 2, (Nq, ld), generator=g).float() * 2 - 1
+        return s * torch.exp2(e) * (1 + torch.rand(Nq, ld, generator=g))
+    raise ValueError(kind)
+
+
+@pytest.mark.parametrize("kind", ["normal", "ties", "zeros", "wide"])
+@pytest.mark.parametrize("k,m,ld,Nq,t0", [(1, 4, 300, 64, 900), (32, 4, 512, 200, 0),
+                                          (512, 4, 8192, 48, 20000), (1024, 4, 3000, 40, 9000),
+                                          (4096, 1, 6000, 8, 5990), (7, 128, 40, 30, 4000)])
+def test_topk_bit_exact(lc, kind, k, m, ld, Nq, t0):
+    S = _score_rows(kind, Nq, ld, seed=k + ld)
+    nvis = np.minimum((np.arange(t0, t0 + Nq) + 1) // m, ld)
+    Tc = int(nvis.max())
+    batch = wl.single(T_raw=0, q_pos0=t0, Nq=Nq, Tc=Tc)
+    b = lc.DeviceBatch.from_workload(batch)
+    got = lc.topk_select(dev(S), b, m, k).cpu().numpy()
+    torch.cuda.synchronize()
+    ref = oracle.topk(S.double().numpy(), nvis, k)
+    assert np.array_equal(got, ref)
+
+
+# --------------------------------------------------------------- attention
+
+def _attn_case(dtype, H, d, m, k, W, T, seed, q_from=0):
+    L = wl.csa_layer(T=T, H=H, d=d, HI=4, dI=32, m=m, k=k, W=W, dtype=dtype, seed=seed,
+                     q_from=q_from)
+    # compressed entries: the oracle's own compression, rounded to the dtype
+    Kc = cast(oracle.compress(L["K"], L["G"], m), dtype)
+    Vc = cast(oracle.compress(L["V"], L["G"], m), dtype)
+    return L, Kc, Vc
+
+
+@pytest.mark.parametrize("dtype,H,d,m,k,W,T", [
+    ("f32", 8, 64, 4, 32, 64, 2048),
+    ("bf16", 64, 128, 4, 64, 128, 1200),
+    ("bf16", 16, 64, 4, 512, 0, 700),     # k > n_vis everywhere: -1 padding
+    ("f32", 8, 128, 2, 5, 3, 300),
+    ("bf16", 128, 128, 4, 16, 16, 160),
+])
+def test_sparse_attn(lc, dtype, H, d, m, k, W, T):
+    L, Kc, Vc = _attn_case(dtype, H, d, m, k, W, T, seed=21)
+    tpos = np.array(L["batch"].positions())
+    rng = np.random.default_rng(3)
+    sel = oracle.topk(rng.standard_normal((len(tpos), max(1, T // m))), (tpos + 1) // m, k)
+    b = lc.DeviceBatch.from_workload(L["batch"])
+    O, lse = lc.sparse_mqa_attn(dev(L["Q"]), dev(Kc), dev(Vc), dev(torch.from_numpy(sel)),
+                                dev(L["K"]), dev(L["V"]), b, m, W, L["scale"])
+    torch.cuda.synchronize()
+    rO, rl = oracle.sparse_attn(L["Q"], Kc, Vc, sel, L["K"], L["V"], 0, tpos, W, L["scale"])
+    tol = TOL_ATTN[dtype]
+    np.testing.assert_allclose(f64(O), rO, rtol=0, atol=tol)
+    g = f64(lse)
+    assert np.array_equal(np.isneginf(g), np.isneginf(rl))
+    fin = np.isfinite(rl)
+    np.testing.assert_allclose(g[fin], rl[fin], rtol=0, atol=tol)
+
+
+@pytest.mark.parametrize("dtype,H,d,m,W,T,q_from", [
+    ("f32", 8, 64, 128, 128, 1000, 0),
+    ("bf16", 64, 128, 128, 128, 2100, 0),
+    ("bf16", 64, 128, 4, 0, 300, 0),
+    ("f32", 16, 128, 1, 0, 90, 0),        # m'=1, W=0: plain causal attention
+    ("bf16", 128, 128, 128, 128, 8192 + 300, 8192 - 200),
+])
+def test_hca_attn(lc, dtype, H, d, m, W, T, q_from):
+    L = wl.hca_layer(T=T, H=H, d=d, m=m, W=W, dtype=dtype, seed=31, q_from=q_from)
+    Kc = cast(oracle.compress(L["K"], L["G"], m), dtype)
+    Vc = cast(oracle.compress(L["V"], L["G"], m), dtype)
+    tpos = np.array(L["batch"].positions())
+    b = lc.DeviceBatch.from_workload(L["batch"])
+    O, lse = lc.hca_dense_attn(dev(L["Q"]), dev(Kc), dev(Vc), dev(L["K"]), dev(L["V"]), b, m, W,
+                               L["scale"])
+    torch.cuda.synchronize()
+    rO, rl = oracle.hca_attn(L["Q"], Kc, Vc, m, L["K"], L["V"], 0, tpos, W, L["scale"])
+    tol = TOL_ATTN[dtype]
+    np.testing.assert_allclose(f64(O), rO, rtol=0, atol=tol)
+    fin = np.isfinite(rl)
+    assert np.array_equal(np.isneginf(f64(lse)), ~fin)
+    np.testing.assert_allclose(f64(lse)[fin], rl[fin], rtol=0, atol=tol)
+
+
+# -------------------------------------------------------------- end to end
+
+def test_csa_tiny_end_to_end(lc):
+    """The tiny fp32 setting (T=2048, 8 heads x 64, indexer 4 x 32, k=32,
+    W=64, seed 0) through compress -> index + top-k -> attention."""
+    L = wl.CONFIGS["csa_tiny"]()
+    m, k, W = L["m"], L["k"], L["W"]
+    b = lc.DeviceBatch.from_workload(L["batch"])
+    tpos = np.array(L["batch"].positions())
+    Kc, Vc = lc.csa_compress(dev(L["K"]), dev(L["V"]), dev(L["G"]), m=m)
+    _, sel = lc.lightning_index(dev(L["qI"]), dev(L["w"]), dev(L["kI"]), b, m, scores=False,
+                                k=k, topk=True)
+    O, lse = lc.sparse_mqa_attn(dev(L["Q"]), Kc, Vc, sel, dev(L["K"]), dev(L["V"]), b, m, W,
+                                L["scale"])
+    torch.cuda.synchronize()
+    # oracle pipeline on the same inputs
+    rKc = cast(oracle.compress(L["K"], L["G"], m), "f32")
+    rVc = cast(oracle.compress(L["V"], L["G"], m), "f32")
+    I = oracle.index(L["qI"], L["w"], L["kI"], tpos, m)
+    nvis = (tpos + 1) // m
+    rsel = oracle.topk(I, nvis, k)
+    rO, rl = oracle.sparse_attn(L["Q"], rKc, rVc, rsel, L["K"], L["V"], 0, tpos, W, L["scale"])
+    gsel = sel.cpu().numpy()
+    valid_selection(gsel, nvis, k)
+    differ = np.any(gsel != rsel, axis=1)
+    for r in np.nonzero(differ)[0]:
+        assert boundary_gap(I[r], int(nvis[r]), k) < GAP, f"row {r} selection differs"
+    same = ~differ
+    np.testing.assert_allclose(f64(O)[same], rO[same], rtol=0, atol=TOL_ATTN["f32"])
+    print(f"excused selection mismatches: {differ.sum()} of {len(differ)} rows")
+
+
+def test_device_errors_are_flagged_not_trapped(lc):
+    L, Kc, Vc = _attn_case("bf16", 8, 64, 4, 4, 4, 64, seed=41)
+    b = lc.DeviceBatch.from_workload(L["batch"])
+    Nq = L["Q"].shape[0]
+    sel = torch.full((Nq, 4), -1, dtype=torch.int32)
+    sel[10, 0] = 999          # beyond the stored entries
+    sel[12, 1] = 5            # stored, but not visible from t=12 (n_vis = 3)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    O, _ = lc.sparse_mqa_attn(dev(L["Q"]), dev(Kc), dev(Vc), dev(sel), dev(L["K"]), dev(L["V"]),
+                              b, 4, 4, L["scale"], dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & lc.LC_DEVERR_INDEX
+    assert torch.isfinite(O.float()).all()
+    # a raw cache that does not hold the window's positions
+    err.zero_()
+    short = wl.single(T_raw=8, q_pos0=0, Nq=Nq, Tc=Nq // 4)
+    bs = lc.DeviceBatch.from_workload(short)
+    lc.hca_dense_attn(dev(L["Q"]), dev(Kc), dev(Vc), dev(L["K"][:8]), dev(L["V"][:8]), bs, 4, 4,
+                      L["scale"], dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & lc.LC_DEVERR_WINDOW
