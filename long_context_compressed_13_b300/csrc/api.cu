@@ -77,8 +77,9 @@ static size_t index_ws_bytes(const lc_batch *b) {
 static lc_status compress_common(const void *K, const void *V, const float *G_K,
                                  const float *G_V, int64_t T, int32_t d, int32_t m,
                                  lc_dtype dt, void *Kc, void *Vc, cudaStream_t st) {
-    if (!K || !V || !G_K || !G_V || !Kc || !Vc || T < 0 || m < 1 || !dtype_ok(dt))
-        return LC_ERR_INVALID_ARG;
+    if (T < 0 || m < 1 || !dtype_ok(dt) || !G_K || !G_V) return LC_ERR_INVALID_ARG;
+    // with fewer than m tokens there is no entry to write: outputs may be empty
+    if (T / m > 0 && (!K || !V || !Kc || !Vc)) return LC_ERR_INVALID_ARG;
     if ((d != 64 && d != 128) || m > 256) return LC_ERR_UNSUPPORTED;
     lc_status s = compress_launch(K, G_K, T, d, m, dt, Kc, st);
     if (s == LC_OK) s = compress_launch(V, G_V, T, d, m, dt, Vc, st);

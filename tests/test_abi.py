@@ -73,6 +73,8 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     b = _batch()
     # compressors: null pointers, bad sizes, unsupported d
     assert lib.csa_compress(N, P, P, P, 16, 64, 4, lc.LC_F32, P, P, N) == lc.LC_ERR_INVALID_ARG
+    assert lib.csa_compress(P, P, N, P, 16, 64, 4, lc.LC_F32, P, P, N) == lc.LC_ERR_INVALID_ARG
+    assert lib.csa_compress(P, P, P, P, 16, 64, 4, lc.LC_F32, N, P, N) == lc.LC_ERR_INVALID_ARG
     assert lib.csa_compress(P, P, P, P, -1, 64, 4, lc.LC_F32, P, P, N) == lc.LC_ERR_INVALID_ARG
     assert lib.hca_compress(P, P, P, P, 16, 64, 0, lc.LC_F32, P, P, N) == lc.LC_ERR_INVALID_ARG
     assert lib.csa_compress(P, P, P, P, 16, 96, 4, lc.LC_F32, P, P, N) == lc.LC_ERR_UNSUPPORTED
