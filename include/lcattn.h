@@ -156,6 +156,30 @@ lc_status hca_dense_attn(const void *Q, const void *Kc, const void *Vc, const vo
                          int32_t m, int32_t W, float scale, lc_dtype dtype, void *O, float *lse,
                          void *ws, size_t ws_bytes, int32_t *dev_err, lc_stream stream);
 
+/* Index + top-k that allocates nothing (the pages have no counterpart: this
+ * is an addition for callers that cannot allocate device memory, such as a
+ * host program whose device memory belongs to another runtime's pool, or a
+ * latency-critical loop where cudaMalloc/cudaFree could synchronise the
+ * device).  Same arguments and results as lightning_index with scores ==
+ * NULL and topk != NULL, but the fp32 score matrix [total_q, max_c] lives in
+ * a fixed array of LC_NOALLOC_SCRATCH_BYTES compiled into the library instead
+ * of a caller workspace.
+ *   - Each device that loads the library's image holds that array until the
+ *     process exits.
+ *   - The first call on a device looks the array's device address up (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call on a device shares the one array, so calls that overlap on
+ *     the GPU (other streams, other host threads) race.  Nothing needs
+ *     clearing between calls: each call writes every score it reads.
+ *   - total_q * max_c * 4 > LC_NOALLOC_SCRATCH_BYTES returns LC_ERR_WORKSPACE
+ *     and enqueues nothing.
+ *   - No cudaMalloc, cudaFree or allocating library routine is called. */
+#define LC_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+lc_status lightning_index_topk_noalloc(const void *qI, const float *w, const void *kI,
+                                       const lc_batch *batch, int32_t HI, int32_t dI, int32_t m,
+                                       lc_dtype dtype, int32_t k, int32_t *topk,
+                                       int32_t *dev_err, lc_stream stream);
+
 /* Bytes of `ws` a call needs (0 = none).  `op` is one of lc_op; unused
  * arguments are ignored.  Host only; reads only the batch's host fields. */
 typedef enum {
