@@ -73,7 +73,9 @@ typedef enum {
  * cu_q[b] .. cu_q[b+1]-1 at consecutive absolute positions q_pos0[b], ...;
  * compressed entries cu_c[b] .. cu_c[b+1]-1 (sequence-local entry j is row
  * cu_c[b]+j of Kc/Vc/kI); raw rows cu_raw[b] .. cu_raw[b+1]-1 holding
- * positions raw_pos0[b], raw_pos0[b]+1, ... (the window's source). */
+ * positions raw_pos0[b], raw_pos0[b]+1, ... (the window's source).  The
+ * host fields must agree with the device arrays; the tensor-core kernels size
+ * their TMA descriptors from total_c and total_raw. */
 typedef struct {
     int32_t B;
     const int64_t *cu_q;     /* [B+1] */
@@ -84,6 +86,8 @@ typedef struct {
     int64_t total_q;         /* host: cu_q[B] */
     int64_t max_q;           /* host: max over b of rows of sequence b */
     int64_t max_c;           /* host: max over b of entries of sequence b */
+    int64_t total_c;         /* host: cu_c[B] (rows of Kc/Vc/kI) */
+    int64_t total_raw;       /* host: cu_raw[B] (rows of Kraw/Vraw) */
 } lc_batch;
 
 /* CSA token compressor (page "DeepSeek-V4 技术解析…", §1.1, CSA paragraph:

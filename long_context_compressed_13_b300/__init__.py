@@ -41,7 +41,8 @@ class _LcBatch(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("cu_q", ctypes.c_void_p), ("q_pos0", ctypes.c_void_p),
                 ("cu_c", ctypes.c_void_p), ("cu_raw", ctypes.c_void_p),
                 ("raw_pos0", ctypes.c_void_p), ("total_q", ctypes.c_int64),
-                ("max_q", ctypes.c_int64), ("max_c", ctypes.c_int64)]
+                ("max_q", ctypes.c_int64), ("max_c", ctypes.c_int64),
+                ("total_c", ctypes.c_int64), ("total_raw", ctypes.c_int64)]
 
 
 _lib = None
@@ -135,6 +136,8 @@ class DeviceBatch:
     total_q: int
     max_q: int
     max_c: int
+    total_c: int = 0
+    total_raw: int = 0
     host: object = None
 
     @staticmethod
@@ -147,7 +150,8 @@ class DeviceBatch:
         nq = [cu_q[b + 1] - cu_q[b] for b in range(B)]
         nc = [cu_c[b + 1] - cu_c[b] for b in range(B)]
         return DeviceBatch(B, mk(cu_q), mk(q_pos0), mk(cu_c), mk(cu_raw), mk(raw_pos0),
-                           int(cu_q[-1]), max(nq) if nq else 0, max(nc) if nc else 0)
+                           int(cu_q[-1]), max(nq) if nq else 0, max(nc) if nc else 0,
+                           int(cu_c[-1]), int(cu_raw[-1]))
 
     @staticmethod
     def from_workload(batch, device="cuda") -> "DeviceBatch":
@@ -159,7 +163,7 @@ class DeviceBatch:
     def c_struct(self) -> _LcBatch:
         return _LcBatch(self.B, self.cu_q.data_ptr(), self.q_pos0.data_ptr(),
                         self.cu_c.data_ptr(), self.cu_raw.data_ptr(), self.raw_pos0.data_ptr(),
-                        self.total_q, self.max_q, self.max_c)
+                        self.total_q, self.max_q, self.max_c, self.total_c, self.total_raw)
 
 
 def workspace_size(op: int, batch: DeviceBatch, H=0, d=0, HI=0, dI=0, k=0) -> int:

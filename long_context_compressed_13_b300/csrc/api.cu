@@ -15,6 +15,10 @@ lc_status index_launch(const void *qI, const float *w, const void *kI, const lc_
                        cudaStream_t st);
 lc_status topk_launch(const float *scores, int64_t ld, const lc_batch &b, int m, int k,
                       int32_t *topk, int32_t *dev_err, cudaStream_t st);
+lc_status hca_tc_launch(const void *Q, const void *Kc, const void *Vc, const void *Kraw,
+                        const void *Vraw, const lc_batch &b, int H, int d, int m, int W,
+                        float scale, lc_dtype dt, void *O, float *lse, int32_t *dev_err,
+                        cudaStream_t st);
 lc_status attn_simt_launch(bool sparse, const void *Q, const void *Kc, const void *Vc,
                            const int32_t *topk, int k, const void *Kraw, const void *Vraw,
                            const lc_batch &b, int H, int d, int m, int W, float scale,
@@ -63,7 +67,8 @@ static lc_status finish(lc_status s, cudaStream_t st, int32_t *dev_err) {
 
 static bool batch_ok(const lc_batch *b) {
     return b && b->B >= 1 && b->cu_q && b->q_pos0 && b->cu_c && b->cu_raw && b->raw_pos0 &&
-           b->total_q >= 0 && b->max_q >= 0 && b->max_c >= 0 && b->max_q <= b->total_q;
+           b->total_q >= 0 && b->max_q >= 0 && b->max_c >= 0 && b->max_q <= b->total_q &&
+           b->total_c >= b->max_c && b->total_raw >= 0;
 }
 
 static bool dtype_ok(lc_dtype dt) { return dt == LC_F32 || dt == LC_BF16; }
@@ -179,8 +184,11 @@ lc_status hca_dense_attn(const void *Q, const void *Kc, const void *Vc, const vo
         return LC_ERR_INVALID_ARG;
     if ((d != 64 && d != 128) || H < 8 || H > 128 || H % 8 || W > 4096)
         return LC_ERR_UNSUPPORTED;
-    lc_status s = attn_simt_launch(false, Q, Kc, Vc, nullptr, 0, Kraw, Vraw, *batch, H, d, m, W,
-                                   scale, dtype, O, lse, dev_err, st);
+    lc_status s = hca_tc_launch(Q, Kc, Vc, Kraw, Vraw, *batch, H, d, m, W, scale, dtype, O, lse,
+                                dev_err, st);
+    if (s == LC_ERR_UNSUPPORTED)
+        s = attn_simt_launch(false, Q, Kc, Vc, nullptr, 0, Kraw, Vraw, *batch, H, d, m, W, scale,
+                             dtype, O, lse, dev_err, st);
     return finish(s, st, dev_err);
 }
 

@@ -63,7 +63,7 @@ def test_host_only_helpers(lib):
 
 def _batch(total_q=4, max_q=4, max_c=8, B=1, null=False):
     p = 0 if null else 0x1000
-    return lc._LcBatch(B, p, p, p, p, p, total_q, max_q, max_c)
+    return lc._LcBatch(B, p, p, p, p, p, total_q, max_q, max_c, max_c * B, 0)
 
 
 def test_invalid_arguments_are_rejected_on_the_host(lib):

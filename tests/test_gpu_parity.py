@@ -223,6 +223,9 @@ def test_sparse_attn(lc, dtype, H, d, m, k, W, T):
     ("bf16", 64, 128, 4, 0, 300, 0),
     ("f32", 16, 128, 1, 0, 90, 0),        # m'=1, W=0: plain causal attention
     ("bf16", 128, 128, 128, 128, 8192 + 300, 8192 - 200),
+    ("bf16", 64, 128, 128, 128, 301, 0),   # last CTA holds 64 of 128 rows
+    ("bf16", 32, 128, 16, 48, 700, 100),   # 4 tokens per tile, window crosses tiles
+    ("bf16", 128, 128, 128, 0, 1000, 0),   # no window: rows t < 127 see nothing
 ])
 def test_hca_attn(lc, dtype, H, d, m, W, T, q_from):
     L = wl.hca_layer(T=T, H=H, d=d, m=m, W=W, dtype=dtype, seed=31, q_from=q_from)
@@ -271,6 +274,25 @@ def test_csa_tiny_end_to_end(lc):
     same = ~differ
     np.testing.assert_allclose(f64(O)[same], rO[same], rtol=0, atol=TOL_ATTN["f32"])
     print(f"excused selection mismatches: {differ.sum()} of {len(differ)} rows")
+
+
+def test_hca_tc_short_raw_cache_is_flagged(lc):
+    # raw cache holding positions 200.. only: windows reaching below 200 are
+    # cut there and flagged; rows whose window lies inside it are exact
+    L = wl.hca_layer(T=400, H=64, d=128, m=8, W=32, dtype="bf16", seed=43)
+    Kc = cast(oracle.compress(L["K"], L["G"], 8), "bf16")
+    Vc = cast(oracle.compress(L["V"], L["G"], 8), "bf16")
+    batch = wl.Batch(cu_q=[0, 400], q_pos0=[0], cu_c=[0, 50], cu_raw=[0, 200], raw_pos0=[200])
+    b = lc.DeviceBatch.from_workload(batch)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    O, _ = lc.hca_dense_attn(dev(L["Q"]), dev(Kc), dev(Vc), dev(L["K"][200:]), dev(L["V"][200:]),
+                             b, 8, 32, L["scale"], dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & lc.LC_DEVERR_WINDOW
+    rows = np.arange(231, 400)
+    rO, _ = oracle.hca_attn(L["Q"][rows], Kc, Vc, 8, L["K"][200:], L["V"][200:], 200, rows, 32,
+                            L["scale"])
+    np.testing.assert_allclose(f64(O)[rows], rO, rtol=0, atol=TOL_ATTN["bf16"])
 
 
 def test_device_errors_are_flagged_not_trapped(lc):
