@@ -15,6 +15,14 @@ lc_status index_launch(const void *qI, const float *w, const void *kI, const lc_
                        cudaStream_t st);
 lc_status topk_launch(const float *scores, int64_t ld, const lc_batch &b, int m, int k,
                       int32_t *topk, int32_t *dev_err, cudaStream_t st);
+lc_status index_tc_materialize(const void *qI, const float *w, const void *kI, const lc_batch &b,
+                               int HI, int dI, int m, lc_dtype dt, float *scores, int64_t ld,
+                               int32_t *dev_err, cudaStream_t st);
+lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
+                               const lc_batch &b, int HI, int dI, int m, lc_dtype dt, int k,
+                               int32_t *topk, void *ws, size_t ws_bytes, int32_t *dev_err,
+                               cudaStream_t st);
+size_t index_tc_workspace(const lc_batch &b, int k);
 lc_status hca_tc_launch(const void *Q, const void *Kc, const void *Vc, const void *Kraw,
                         const void *Vraw, const lc_batch &b, int H, int d, int m, int W,
                         float scale, lc_dtype dt, void *O, float *lse, int32_t *dev_err,
@@ -123,6 +131,12 @@ lc_status lightning_index(const void *qI, const float *w, const void *kI, const 
         (topk && k > 4096))
         return LC_ERR_UNSUPPORTED;
     if (batch->total_q == 0) return LC_OK;
+    if (!scores) {
+        // fused selection on the tensor cores when the shape allows it
+        lc_status s = index_topk_tc_launch(qI, w, kI, *batch, HI, dI, m, dtype, k, topk, ws,
+                                           ws_bytes, dev_err, st);
+        if (s != LC_ERR_UNSUPPORTED) return finish(s, st, dev_err);
+    }
     float *sc = scores;
     int64_t sld = ld;
     if (!scores) {
@@ -135,7 +149,10 @@ lc_status lightning_index(const void *qI, const float *w, const void *kI, const 
             return finish(s, st, dev_err);
         }
     }
-    lc_status s = index_launch(qI, w, kI, *batch, HI, dI, m, dtype, sc, sld, dev_err, st);
+    lc_status s = LC_ERR_UNSUPPORTED;
+    if (scores) s = index_tc_materialize(qI, w, kI, *batch, HI, dI, m, dtype, sc, sld, dev_err, st);
+    if (s == LC_ERR_UNSUPPORTED)
+        s = index_launch(qI, w, kI, *batch, HI, dI, m, dtype, sc, sld, dev_err, st);
     if (s == LC_OK && topk) s = topk_launch(sc, sld, *batch, m, k, topk, dev_err, st);
     return finish(s, st, dev_err);
 }
@@ -201,7 +218,10 @@ size_t lc_workspace_size(int32_t op, const lc_batch *batch, int32_t H, int32_t d
     (void)k;
     if (!batch) return 0;
     switch (op) {
-        case LC_OP_LIGHTNING_INDEX: return index_ws_bytes(batch);
+        case LC_OP_LIGHTNING_INDEX: {
+            const size_t a = index_ws_bytes(batch), b = index_tc_workspace(*batch, k);
+            return a > b ? a : b;
+        }
         default: return 0;
     }
 }

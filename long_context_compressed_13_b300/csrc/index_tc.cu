@@ -1,0 +1,557 @@
+// Lightning Indexer on the tensor cores (tcgen05 + TMEM), bf16 q/k with
+// d_I = 64, H_I in {4, 8}, one sequence, plus the fused exact top-k that
+// never writes the full score matrix.
+//
+// k_index_tc: one CTA = 128 query rows x a contiguous range of entries.
+//   warp 8      TMA producer: q_I of the 128 rows for every head once (H_I
+//               boxes of 128 x 64), then k_I tiles of 32 entries x H_I heads
+//               into a 2-stage ring
+//   warp 9      TMEM owner and MMA issuer: per tile and head one
+//               M=128, N=32, K=64 product q_h k_h^T into TMEM (H_I x 32
+//               columns per buffer, two buffers)
+//   warps 0-7   epilogue: warp w reads TMEM lanes 32(w%4).. and columns
+//               16(w/4).. of every head, forms sum_h w_h * max(s_h, 0) in fp32
+//               and either stores the scores (MATERIALIZE) or keeps the
+//               entries whose order key reaches the row's threshold
+//               (FILTER) in a per-row candidate list.
+// The fused top-k of a row (see index_topk_tc_launch):
+//   1. scores of every s-th entry (MATERIALIZE over a strided tensor map);
+//   2. theta = the rho-th largest sampled key, a lower bound for the k-th
+//      largest key of the full row with overwhelming probability;
+//   3. FILTER pass over all entries: candidates = entries with key >= theta;
+//   4. exact top-k of the candidates (bitonic sort on (key, -index)), valid
+//      when the row has between k and `cap` candidates: then every member of
+//      the true top-k is a candidate;
+//   5. rows outside that range (rare: massive ties or an unlucky sample) are
+//      redone exactly from fully materialised scores.
+#include <cmath>
+
+#include "lc_common.cuh"
+#include "sm100.cuh"
+#include "topk_common.cuh"
+
+namespace lc {
+
+using namespace sm100;
+
+lc_status index_scan_launch(const void *qI, const float *w, const void *kI, const lc_batch &b,
+                            int HI, int dI, int m, lc_dtype dt, float *scores, int64_t ld,
+                            const int32_t *row_mask, int32_t *dev_err, cudaStream_t st);
+lc_status topk_launch_masked(const float *scores, int64_t ld, const lc_batch &b, int m, int k,
+                             int32_t *topk, const int32_t *row_mask, int32_t *dev_err,
+                             cudaStream_t st);
+
+namespace {
+constexpr int IBM = 128;          // query rows per CTA
+constexpr int IBN = 32;           // entries per tile
+constexpr int IDI = 64;           // indexer head dim
+constexpr int I_THREADS = 320;    // 8 epilogue warps + producer + MMA
+constexpr int MODE_MATERIALIZE = 0, MODE_FILTER = 1;
+
+struct IdxBars {
+    uint64_t q_full, k_full[2], k_empty[2], acc_full[2], acc_empty[2];
+    uint32_t taddr;
+    int abort;
+};
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+}  // namespace
+
+struct IdxTcArgs {
+    int64_t Nq;              // query rows of the (single) sequence
+    const int64_t *q_pos0;   // device: absolute position of row 0
+    int64_t Tc;              // stored entries
+    int stride;              // map entry e is entry e*stride
+    int m;
+    int64_t chunk;           // map entries per CTA (multiple of IBN)
+    int64_t col_end;         // MATERIALIZE: columns [0, col_end) are written
+    const float *w;          // [Nq, HI]
+    float *out;              // MATERIALIZE: [Nq, ld]
+    int64_t ld;
+    const uint32_t *theta;   // FILTER: [Nq] order-key thresholds
+    int32_t *count;          // FILTER: [Nq] candidate counts (zeroed beforehand)
+    uint32_t *cand_key;      // FILTER: [Nq, cap]
+    int32_t *cand_idx;       // FILTER: [Nq, cap]
+    int cap;
+    int32_t *dev_err;
+};
+
+template <int MODE, int HI>
+__global__ void __launch_bounds__(I_THREADS, 1)
+    k_index_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+               IdxTcArgs a) {
+    constexpr uint32_t SM_Q = 0;                          // HI x [128 x 128 B]
+    constexpr uint32_t SM_K = HI * IBM * 128;             // 2 x HI x [32 x 128 B]
+    constexpr uint32_t K_STAGE = HI * IBN * 128;
+    constexpr uint32_t SM_BAR = SM_K + 2 * K_STAGE;
+    constexpr uint32_t TCOLS = 2 * HI * IBN;              // two accumulator buffers
+    extern __shared__ __align__(1024) uint8_t smem[];
+    IdxBars &bars = *reinterpret_cast<IdxBars *>(smem + SM_BAR);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    volatile int *abort = &bars.abort;
+    const unsigned FULL = 0xffffffffu;
+
+    const int64_t q_pos0 = __ldg(a.q_pos0);
+    const int64_t row0 = (int64_t)blockIdx.x * IBM;
+    const int64_t last_row = min(row0 + IBM, a.Nq) - 1;
+    int64_t nv_last = n_vis(q_pos0 + last_row, a.m);
+    if (nv_last > a.Tc) nv_last = a.Tc;
+    const int64_t nvm = (nv_last + a.stride - 1) / a.stride;  // visible map entries (max)
+    const int64_t c0 = (int64_t)blockIdx.y * a.chunk;
+    const int64_t c_end = MODE == MODE_MATERIALIZE ? min(c0 + a.chunk, a.col_end)
+                                                   : min(c0 + a.chunk, nvm);
+    const int64_t comp_end = min(c_end, nvm);  // computed columns [c0, comp_end)
+    const int n_t = comp_end > c0 ? (int)((comp_end - c0 + IBN - 1) / IBN) : 0;
+
+    if (tid == 0) {
+        bars.abort = (smem_u32(smem) & 1023u) != 0 ? 1 : 0;
+        if (bars.abort) flag(a.dev_err, LC_DEVERR_TIMEOUT);
+        mbar_init(&bars.q_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars.k_full[s], 1);
+            mbar_init(&bars.k_empty[s], 1);
+            mbar_init(&bars.acc_full[s], 1);
+            mbar_init(&bars.acc_empty[s], 256);
+        }
+        fence_barrier_init();
+    }
+    if (warp == 9 && n_t > 0) {
+        tmem_alloc(&bars.taddr, TCOLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t taddr = bars.taddr;
+    const bool dead = bars.abort != 0;
+
+    if (warp == 8) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0 && !dead && n_t > 0) {
+            prefetch_tmap(&mK);
+            mbar_expect_tx(&bars.q_full, HI * IBM * 128);
+#pragma unroll
+            for (int h = 0; h < HI; ++h)
+                tma_load_2d(smem + SM_Q + h * IBM * 128, &mQ, &bars.q_full, h * IDI,
+                            (int32_t)row0);
+            int issued = 0;
+            for (int i = 0; i < n_t; ++i) {
+                const int s = i & 1;
+                if (i >= 2 && !mbar_wait(&bars.k_empty[s], ((i - 2) >> 1) & 1, abort)) break;
+                const int32_t y = (int32_t)(c0 + (int64_t)i * IBN);
+                uint8_t *kd = smem + SM_K + s * K_STAGE;
+                mbar_expect_tx(&bars.k_full[s], HI * IBN * 128);
+#pragma unroll
+                for (int h = 0; h < HI; ++h)
+                    tma_load_2d(kd + h * IBN * 128, &mK, &bars.k_full[s], h * IDI, y);
+                ++issued;
+            }
+            int dummy = 0;
+            for (int i = max(0, issued - 2); i < issued; ++i)
+                mbar_wait(&bars.k_full[i & 1], (i >> 1) & 1, &dummy, 400000000LL);
+            mbar_wait(&bars.q_full, 0, &dummy, 400000000LL);
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0 && !dead && n_t > 0) {
+            constexpr uint32_t IDESC = idesc_bf16_f32(IBM, IBN, 0, 0);
+            const uint32_t q_base = smem_u32(smem + SM_Q);
+            bool ok = mbar_wait(&bars.q_full, 0, abort);
+            for (int i = 0; ok && i < n_t; ++i) {
+                const int s = i & 1, bf = i & 1;
+                if (!mbar_wait(&bars.k_full[s], (i >> 1) & 1, abort)) break;
+                if (i >= 2 && !mbar_wait(&bars.acc_empty[bf], ((i - 2) >> 1) & 1, abort)) break;
+                tc_fence_after();
+                const uint32_t k_base = smem_u32(smem + SM_K + s * K_STAGE);
+#pragma unroll
+                for (int h = 0; h < HI; ++h) {
+#pragma unroll
+                    for (int kk = 0; kk < IDI / 16; ++kk) {
+                        const uint64_t ad =
+                            sw128_desc(q_base + h * IBM * 128 + kk * 32, 16, 1024);
+                        const uint64_t bd =
+                            sw128_desc(k_base + h * IBN * 128 + kk * 32, 16, 1024);
+                        mma_bf16(taddr + (uint32_t)(bf * HI * IBN + h * IBN), ad, bd, IDESC,
+                                 kk > 0);
+                    }
+                }
+                mma_commit(&bars.acc_full[bf]);
+                mma_commit(&bars.k_empty[s]);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------ epilogue
+        const int quad = warp & 3, half = warp >> 2;
+        const int64_t row = row0 + quad * 32 + lane;
+        const bool row_ok = row < a.Nq;
+        const int64_t t = q_pos0 + (row_ok ? row : last_row);
+        int64_t nv = n_vis(t, a.m);
+        if (nv > a.Tc) nv = a.Tc;
+        float wh[HI];
+#pragma unroll
+        for (int h = 0; h < HI; ++h) wh[h] = row_ok ? __ldg(a.w + row * HI + h) : 0.f;
+        uint32_t theta = 0;
+        if (MODE == MODE_FILTER && row_ok) theta = __ldg(a.theta + row);
+        const uint32_t lane_addr = taddr + ((uint32_t)(quad * 32) << 16) + half * 16;
+        bool ok = !dead;
+        for (int i = 0; ok && i < n_t; ++i) {
+            const int bf = i & 1;
+            if (!__all_sync(FULL, mbar_wait(&bars.acc_full[bf], (i >> 1) & 1, abort))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float acc[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) acc[c] = 0.f;
+#pragma unroll
+            for (int h0 = 0; h0 < HI; h0 += 4) {
+                float v[4][16];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    tmem_ld16(lane_addr + (uint32_t)(bf * HI * IBN + (h0 + u) * IBN), v[u]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        acc[c] = fmaf(wh[h0 + u], fmaxf(v[u][c], 0.f), acc[c]);
+            }
+            tc_fence_before();
+            mbar_arrive(&bars.acc_empty[bf]);
+            const int64_t e0 = c0 + (int64_t)i * IBN + half * 16;  // map entry of acc[0]
+            if (!row_ok) continue;
+            if (MODE == MODE_MATERIALIZE) {
+                float *dst = a.out + row * a.ld;
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const int64_t e = e0 + c;
+                    if (e < c_end) dst[e] = (e * a.stride < nv) ? acc[c] : -INFINITY;
+                }
+            } else {
+                uint32_t keys[16];
+                uint32_t selm = 0;
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const int64_t e = e0 + c;
+                    keys[c] = order_key(acc[c]);
+                    if (e < nv && keys[c] >= theta) selm |= 1u << c;
+                }
+                if (selm) {
+                    int base = atomicAdd(a.count + row, __popc(selm));
+                    uint32_t *ck = a.cand_key + row * a.cap;
+                    int32_t *ci = a.cand_idx + row * a.cap;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        if (selm & (1u << c)) {
+                            if (base < a.cap) {
+                                ck[base] = keys[c];
+                                ci[base] = (int32_t)(e0 + c);
+                            }
+                            ++base;
+                        }
+                    }
+                }
+            }
+        }
+        if (!ok) {
+            if (row_ok) flag(a.dev_err, LC_DEVERR_TIMEOUT);
+        } else if (MODE == MODE_MATERIALIZE && row_ok) {
+            // columns of this CTA past the last visible entry
+            float *dst = a.out + row * a.ld;
+            for (int64_t e = max(c0, comp_end) + half; e < c_end; e += 2) dst[e] = -INFINITY;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9 && n_t > 0) {
+        tc_fence_after();
+        tmem_dealloc(taddr, TCOLS);
+    }
+}
+
+// theta[r] = the rho-th largest order key among the row's visible sampled
+// scores (0, i.e. "keep everything", when the row has at most k visible
+// entries or fewer than rho samples); count[r] = fail[r] = 0.
+__global__ void __launch_bounds__(512) k_sample_threshold(const float *__restrict__ samp,
+                                                          int64_t lds, Batch bt, int m,
+                                                          int stride, int k, int rho,
+                                                          uint32_t *theta, int32_t *count,
+                                                          int32_t *fail) {
+    __shared__ RadixScratch rs;
+    const int64_t r = blockIdx.x;
+    const int64_t t = bt.q_pos0[0] + r;
+    const int64_t Tc = bt.cu_c[1] - bt.cu_c[0];
+    int64_t nv = n_vis(t, m);
+    if (nv > Tc) nv = Tc;
+    const int64_t nvs = (nv + stride - 1) / stride;
+    uint32_t th = 0;
+    if (nv > k && rho <= nvs) {
+        int need_left;
+        th = radix_kth_largest<512>(samp + r * lds, nvs, rho, rs, &need_left);
+    }
+    if (threadIdx.x == 0) {
+        theta[r] = th;
+        count[r] = 0;
+        fail[r] = 0;
+    }
+}
+
+// Exact top-k of each row's candidates; rows whose candidate count is outside
+// [k, cap] are marked in fail[] for the exact fallback.
+__global__ void __launch_bounds__(512) k_cand_topk(Batch bt, int m, int k, int cap, int P,
+                                                   int PK, const int32_t *__restrict__ count,
+                                                   const uint32_t *__restrict__ cand_key,
+                                                   const int32_t *__restrict__ cand_idx,
+                                                   int32_t *__restrict__ topk, int32_t *fail) {
+    extern __shared__ uint64_t sk[];  // [P] then [PK] (as u64 for the index sort)
+    const int64_t r = blockIdx.x;
+    const int64_t t = bt.q_pos0[0] + r;
+    const int64_t Tc = bt.cu_c[1] - bt.cu_c[0];
+    int64_t nv = n_vis(t, m);
+    if (nv > Tc) nv = Tc;
+    int32_t *out = topk + r * k;
+    if (nv <= k) {
+        for (int i = threadIdx.x; i < k; i += 512) out[i] = i < nv ? i : -1;
+        return;
+    }
+    const int n = count[r];
+    if (n < k || n > cap) {
+        if (threadIdx.x == 0) fail[r] = 1;
+        return;
+    }
+    const uint32_t *ck = cand_key + r * cap;
+    const int32_t *ci = cand_idx + r * cap;
+    for (int i = threadIdx.x; i < P; i += 512)
+        sk[i] = i < n ? ((uint64_t)ck[i] << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)ci[i]) : 0ull;
+    bitonic_sort_u64<512, true>(sk, P);
+    uint64_t *si = sk + P;
+    for (int i = threadIdx.x; i < PK; i += 512)
+        si[i] = i < k ? (uint64_t)(0xFFFFFFFFu - (uint32_t)(sk[i] & 0xFFFFFFFFull))
+                      : 0xFFFFFFFFFFFFFFFFull;
+    bitonic_sort_u64<512, false>(si, PK);
+    for (int i = threadIdx.x; i < k; i += 512) out[i] = (int32_t)si[i];
+}
+
+namespace {
+int pow2_at_least(int x) {
+    int p = 1;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+struct FusedPlan {
+    int stride, rho, cap, P, PK;
+    int64_t ns, lds;
+    size_t off_samp, off_theta, off_count, off_fail, off_ckey, off_cidx, off_full, total;
+};
+
+size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+FusedPlan plan_fused(const lc_batch &b, int k) {
+    FusedPlan p{};
+    const int64_t n = b.max_c;
+    p.stride = 1;
+    while (p.stride < 32 && n / (2 * p.stride) >= 8 * (int64_t)k) p.stride *= 2;
+    if (p.stride == 1) {
+        p.rho = k;
+    } else {
+        const double x = 2.0 + std::sqrt(4.0 + (double)k / p.stride);
+        p.rho = (int)std::ceil(x * x);
+    }
+    int cap = 4 * k;
+    if (cap < 2 * p.rho * p.stride) cap = 2 * p.rho * p.stride;
+    if (cap < 2048) cap = 2048;
+    cap = (cap + 31) & ~31;
+    if (cap > 16384) cap = 16384;
+    p.cap = cap;
+    p.P = pow2_at_least(cap);
+    p.PK = pow2_at_least(k);
+    p.ns = (n + p.stride - 1) / p.stride;
+    p.lds = (p.ns + 3) & ~(int64_t)3;
+    const size_t Nq = (size_t)b.total_q;
+    size_t o = 0;
+    p.off_samp = o;  o += al256(sizeof(float) * Nq * (size_t)p.lds);
+    p.off_theta = o; o += al256(sizeof(uint32_t) * Nq);
+    p.off_count = o; o += al256(sizeof(int32_t) * Nq);
+    p.off_fail = o;  o += al256(sizeof(int32_t) * Nq);
+    p.off_ckey = o;  o += al256(sizeof(uint32_t) * Nq * (size_t)p.cap);
+    p.off_cidx = o;  o += al256(sizeof(int32_t) * Nq * (size_t)p.cap);
+    p.off_full = o;  o += al256(sizeof(float) * Nq * (size_t)n);
+    p.total = o;
+    return p;
+}
+
+bool index_tc_eligible(const void *qI, const void *kI, const lc_batch &b, int HI, int dI,
+                       lc_dtype dt) {
+    auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    return dt == LC_BF16 && dI == IDI && (HI == 4 || HI == 8) && b.B == 1 && b.max_q >= 64 &&
+           b.max_c > 0 && al16(qI) && al16(kI) && b.total_q < (1ll << 31) &&
+           b.max_c < (1ll << 31);
+}
+
+template <int MODE, int HI>
+lc_status launch_tc(const CUtensorMap &mQ, const CUtensorMap &mK, const IdxTcArgs &a,
+                    int64_t n_cols, cudaStream_t st) {
+    constexpr uint32_t SMEM = HI * IBM * 128 + 2 * HI * IBN * 128 + 256;
+    auto kfn = k_index_tc<MODE, HI>;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) !=
+            cudaSuccess)
+            return LC_ERR_CUDA;
+        attr = true;
+    }
+    const int64_t gy = (n_cols + a.chunk - 1) / a.chunk;
+    if (gy < 1 || gy > 65535) return LC_ERR_UNSUPPORTED;
+    dim3 grid((unsigned)((a.Nq + IBM - 1) / IBM), (unsigned)gy);
+    LC_LAUNCH(kfn, grid, dim3(I_THREADS), SMEM, st, mQ, mK, a);
+    return check_launch();
+}
+
+template <int MODE>
+lc_status launch_tc_hi(int HI, const CUtensorMap &mQ, const CUtensorMap &mK,
+                       const IdxTcArgs &a, int64_t n_cols, cudaStream_t st) {
+    return HI == 8 ? launch_tc<MODE, 8>(mQ, mK, a, n_cols, st)
+                   : launch_tc<MODE, 4>(mQ, mK, a, n_cols, st);
+}
+
+// entries per CTA: about eight waves of CTAs over the 148 SMs
+int64_t pick_chunk(int64_t Nq, int64_t n_cols) {
+    const int64_t row_tiles = (Nq + IBM - 1) / IBM;
+    int64_t want_y = (148 * 8 + row_tiles - 1) / row_tiles;
+    if (want_y < 1) want_y = 1;
+    int64_t chunk = (n_cols + want_y - 1) / want_y;
+    chunk = (chunk + IBN - 1) / IBN * IBN;
+    if (chunk < 4 * IBN) chunk = 4 * IBN;
+    while ((n_cols + chunk - 1) / chunk > 65535) chunk *= 2;
+    return chunk;
+}
+
+IdxTcArgs base_args(const lc_batch &b, const float *w, int m, int32_t *dev_err) {
+    IdxTcArgs a{};
+    a.Nq = b.total_q;
+    a.q_pos0 = b.q_pos0;
+    a.Tc = b.max_c;
+    a.stride = 1;
+    a.m = m;
+    a.w = w;
+    a.dev_err = dev_err;
+    return a;
+}
+}  // namespace
+
+size_t index_tc_workspace(const lc_batch &b, int k) {
+    if (b.B != 1 || k < 1) return 0;
+    return plan_fused(b, k).total;
+}
+
+// Scores [total_q, ld] on the tensor cores, or LC_ERR_UNSUPPORTED.
+lc_status index_tc_materialize(const void *qI, const float *w, const void *kI, const lc_batch &b,
+                               int HI, int dI, int m, lc_dtype dt, float *scores, int64_t ld,
+                               int32_t *dev_err, cudaStream_t st) {
+    if (!index_tc_eligible(qI, kI, b, HI, dI, dt)) return LC_ERR_UNSUPPORTED;
+    CUtensorMap mQ, mK;
+    if (!make_tmap_bf16_2d(&mQ, qI, (uint64_t)b.total_q, (uint64_t)HI * IDI, HI * IDI * 2, IDI,
+                           IBM) ||
+        !make_tmap_bf16_2d(&mK, kI, (uint64_t)b.total_c, (uint64_t)HI * IDI, HI * IDI * 2, IDI,
+                           IBN))
+        return LC_ERR_CUDA;
+    IdxTcArgs a = base_args(b, w, m, dev_err);
+    a.Tc = b.total_c;
+    a.col_end = ld;
+    a.out = scores;
+    a.ld = ld;
+    a.chunk = pick_chunk(b.total_q, ld);
+    return launch_tc_hi<MODE_MATERIALIZE>(HI, mQ, mK, a, ld, st);
+}
+
+// Fused exact top-k on the tensor cores (ws holds the plan's buffers), or
+// LC_ERR_UNSUPPORTED.
+lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
+                               const lc_batch &b, int HI, int dI, int m, lc_dtype dt, int k,
+                               int32_t *topk, void *ws, size_t ws_bytes, int32_t *dev_err,
+                               cudaStream_t st) {
+    if (!index_tc_eligible(qI, kI, b, HI, dI, dt)) return LC_ERR_UNSUPPORTED;
+    const FusedPlan p = plan_fused(b, k);
+    if (!ws || ws_bytes < p.total) return LC_ERR_WORKSPACE;
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    float *samp = reinterpret_cast<float *>(base + p.off_samp);
+    uint32_t *theta = reinterpret_cast<uint32_t *>(base + p.off_theta);
+    int32_t *count = reinterpret_cast<int32_t *>(base + p.off_count);
+    int32_t *fail = reinterpret_cast<int32_t *>(base + p.off_fail);
+    uint32_t *ckey = reinterpret_cast<uint32_t *>(base + p.off_ckey);
+    int32_t *cidx = reinterpret_cast<int32_t *>(base + p.off_cidx);
+    float *full = reinterpret_cast<float *>(base + p.off_full);
+    const int64_t Tc = b.total_c;
+    const uint64_t pitch = (uint64_t)HI * IDI * 2;
+
+    CUtensorMap mQ, mKs, mK;
+    if (!make_tmap_bf16_2d(&mQ, qI, (uint64_t)b.total_q, (uint64_t)HI * IDI, pitch, IDI, IBM) ||
+        !make_tmap_bf16_2d(&mK, kI, (uint64_t)Tc, (uint64_t)HI * IDI, pitch, IDI, IBN) ||
+        !make_tmap_bf16_2d(&mKs, kI, (uint64_t)((Tc + p.stride - 1) / p.stride),
+                           (uint64_t)HI * IDI, pitch * p.stride, IDI, IBN))
+        return LC_ERR_CUDA;
+    lc_status s;
+    // 1. sampled scores
+    {
+        IdxTcArgs a = base_args(b, w, m, dev_err);
+        a.Tc = Tc;
+        a.stride = p.stride;
+        a.col_end = p.ns;
+        a.out = samp;
+        a.ld = p.lds;
+        a.chunk = pick_chunk(b.total_q, p.ns);
+        s = launch_tc_hi<MODE_MATERIALIZE>(HI, mQ, mKs, a, p.ns, st);
+        if (s != LC_OK) return s;
+    }
+    // 2. thresholds
+    LC_LAUNCH(k_sample_threshold, dim3((unsigned)b.total_q), dim3(512), 0, st, samp, p.lds,
+              to_dev(b), m, p.stride, k, p.rho, theta, count, fail);
+    if ((s = check_launch()) != LC_OK) return s;
+    // 3. candidates
+    {
+        IdxTcArgs a = base_args(b, w, m, dev_err);
+        a.Tc = Tc;
+        a.theta = theta;
+        a.count = count;
+        a.cand_key = ckey;
+        a.cand_idx = cidx;
+        a.cap = p.cap;
+        a.chunk = pick_chunk(b.total_q, Tc);
+        s = launch_tc_hi<MODE_FILTER>(HI, mQ, mK, a, Tc, st);
+        if (s != LC_OK) return s;
+    }
+    // 4. exact selection among candidates
+    {
+        const size_t smem = sizeof(uint64_t) * (size_t)(p.P + p.PK);
+        static size_t attr = 0;
+        if (smem > 48 * 1024 && smem > attr) {
+            if (cudaFuncSetAttribute(k_cand_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem) != cudaSuccess)
+                return LC_ERR_CUDA;
+            attr = smem;
+        }
+        LC_LAUNCH(k_cand_topk, dim3((unsigned)b.total_q), dim3(512), smem, st, to_dev(b), m, k,
+                  p.cap, p.P, p.PK, count, ckey, cidx, topk, fail);
+        if ((s = check_launch()) != LC_OK) return s;
+    }
+    // 5. exact fallback for the rows marked in fail[] (no work when none is)
+    s = index_scan_launch(qI, w, kI, b, HI, dI, m, dt, full, Tc, fail, dev_err, st);
+    if (s != LC_OK) return s;
+    return topk_launch_masked(full, Tc, b, m, k, topk, fail, dev_err, st);
+}
+
+}  // namespace lc

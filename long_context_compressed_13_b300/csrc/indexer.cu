@@ -101,93 +101,117 @@ __global__ void __launch_bounds__(256) k_index_tiled(const T *__restrict__ qI,
     }
 }
 
-// One query row per grid.y; threads cover (entry, head) pairs, HI lanes per
-// entry reduce with shuffles.  DI * sizeof(T) bytes are read per thread with
-// 16-byte vector loads.
+// Query rows blockIdx.y, blockIdx.y + gridDim.y, ...; threads cover (entry,
+// head) pairs, HI lanes per entry reduce with shuffles.  DI * sizeof(T) bytes
+// are read per thread with 16-byte vector loads.  row_mask (nullable): rows
+// with row_mask[r] == 0 are skipped.
 template <typename T, int DI, int HI>
 __global__ void __launch_bounds__(256) k_index_scan(const T *__restrict__ qI,
                                                     const float *__restrict__ w,
                                                     const T *__restrict__ kI, Batch bt, int m,
                                                     float *__restrict__ scores, int64_t ld,
+                                                    int64_t total_q,
+                                                    const int32_t *__restrict__ row_mask,
                                                     int32_t *dev_err) {
     __shared__ float sq[HI][DI];
     __shared__ float sw[HI];
-    const int64_t r = blockIdx.y;
-    const int b = seq_of_row(bt, r);
-    const int64_t t = bt.q_pos0[b] + (r - bt.cu_q[b]);
-    const int64_t c_beg = bt.cu_c[b], Tc = bt.cu_c[b + 1] - c_beg;
-    int64_t nv = n_vis(t, m);
-    if (nv > Tc) {
-        if (blockIdx.x == 0 && threadIdx.x == 0) flag(dev_err, LC_DEVERR_BATCH);
-        nv = Tc;
-    }
-    for (int i = threadIdx.x; i < HI * DI; i += blockDim.x)
-        sq[i / DI][i % DI] = io<T>::ld(qI + r * HI * DI + i);
-    if (threadIdx.x < HI) sw[threadIdx.x] = w[r * HI + threadIdx.x];
-    __syncthreads();
-
     constexpr int EPB = 256 / HI;                 // entries per block pass
     constexpr int NV = DI * (int)sizeof(T) / 16;  // 16-byte vectors per slice
     constexpr int EPV = 16 / (int)sizeof(T);      // elements per vector
     const int h = threadIdx.x % HI;
     const int el = threadIdx.x / HI;
-    float *out = scores + r * ld;
-    for (int64_t j0 = (int64_t)blockIdx.x * EPB; j0 < ld; j0 += (int64_t)gridDim.x * EPB) {
-        const int64_t j = j0 + el;
-        float part = 0.f;
-        if (j < nv) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(kI + ((c_beg + j) * HI + h) * DI);
-            uint4 v[NV];
-#pragma unroll
-            for (int i = 0; i < NV; ++i) v[i] = __ldg(src + i);
-            float dot = 0.f;
-#pragma unroll
-            for (int i = 0; i < NV; ++i) {
-                const T *e = reinterpret_cast<const T *>(&v[i]);
-#pragma unroll
-                for (int u = 0; u < EPV; ++u) dot = fmaf(sq[h][i * EPV + u], io<T>::to_f(e[u]), dot);
-            }
-            part = sw[h] * fmaxf(dot, 0.f);
+    for (int64_t r = blockIdx.y; r < total_q; r += gridDim.y) {
+        if (row_mask && row_mask[r] == 0) continue;
+        const int b = seq_of_row(bt, r);
+        const int64_t t = bt.q_pos0[b] + (r - bt.cu_q[b]);
+        const int64_t c_beg = bt.cu_c[b], Tc = bt.cu_c[b + 1] - c_beg;
+        int64_t nv = n_vis(t, m);
+        if (nv > Tc) {
+            if (blockIdx.x == 0 && threadIdx.x == 0) flag(dev_err, LC_DEVERR_BATCH);
+            nv = Tc;
         }
+        __syncthreads();
+        for (int i = threadIdx.x; i < HI * DI; i += blockDim.x)
+            sq[i / DI][i % DI] = io<T>::ld(qI + r * HI * DI + i);
+        if (threadIdx.x < HI) sw[threadIdx.x] = w[r * HI + threadIdx.x];
+        __syncthreads();
+        float *out = scores + r * ld;
+        for (int64_t j0 = (int64_t)blockIdx.x * EPB; j0 < ld; j0 += (int64_t)gridDim.x * EPB) {
+            const int64_t j = j0 + el;
+            float part = 0.f;
+            if (j < nv) {
+                const uint4 *src =
+                    reinterpret_cast<const uint4 *>(kI + ((c_beg + j) * HI + h) * DI);
+                uint4 v[NV];
 #pragma unroll
-        for (int off = HI / 2; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-        if (h == 0 && j < ld) out[j] = j < nv ? part : -INFINITY;
+                for (int i = 0; i < NV; ++i) v[i] = __ldg(src + i);
+                float dot = 0.f;
+#pragma unroll
+                for (int i = 0; i < NV; ++i) {
+                    const T *e = reinterpret_cast<const T *>(&v[i]);
+#pragma unroll
+                    for (int u = 0; u < EPV; ++u)
+                        dot = fmaf(sq[h][i * EPV + u], io<T>::to_f(e[u]), dot);
+                }
+                part = sw[h] * fmaxf(dot, 0.f);
+            }
+#pragma unroll
+            for (int off = HI / 2; off > 0; off >>= 1)
+                part += __shfl_xor_sync(0xffffffffu, part, off);
+            if (h == 0 && j < ld) out[j] = j < nv ? part : -INFINITY;
+        }
     }
 }
 
 template <typename T, int DI, int HI>
 static void launch_scan(const void *qI, const float *w, const void *kI, const lc_batch &b, int m,
-                        float *scores, int64_t ld, int32_t *dev_err, cudaStream_t st) {
+                        float *scores, int64_t ld, const int32_t *row_mask, int32_t *dev_err,
+                        cudaStream_t st) {
     constexpr int EPB = 256 / HI;
+    const int64_t rows = b.total_q < 65535 ? b.total_q : 65535;
     int64_t gx = (ld + EPB - 1) / EPB;
-    int64_t want = (148 * 8 + b.total_q - 1) / b.total_q;  // ~8 blocks per SM overall
+    int64_t want = (148 * 8 + rows - 1) / rows;  // ~8 blocks per SM overall
     if (gx > want) gx = want;
     if (gx < 1) gx = 1;
     auto kfn = k_index_scan<T, DI, HI>;
-    LC_LAUNCH(kfn, dim3((unsigned)gx, (unsigned)b.total_q), dim3(256), 0, st, (const T *)qI, w,
-              (const T *)kI, to_dev(b), m, scores, ld, dev_err);
+    LC_LAUNCH(kfn, dim3((unsigned)gx, (unsigned)rows), dim3(256), 0, st, (const T *)qI, w,
+              (const T *)kI, to_dev(b), m, scores, ld, b.total_q, row_mask, dev_err);
 }
 
 template <typename T, int DI>
 static lc_status scan_hi(const void *qI, const float *w, const void *kI, const lc_batch &b, int HI,
-                         int m, float *scores, int64_t ld, int32_t *dev_err, cudaStream_t st) {
+                         int m, float *scores, int64_t ld, const int32_t *row_mask,
+                         int32_t *dev_err, cudaStream_t st) {
     switch (HI) {
-        case 1: launch_scan<T, DI, 1>(qI, w, kI, b, m, scores, ld, dev_err, st); break;
-        case 2: launch_scan<T, DI, 2>(qI, w, kI, b, m, scores, ld, dev_err, st); break;
-        case 4: launch_scan<T, DI, 4>(qI, w, kI, b, m, scores, ld, dev_err, st); break;
-        case 8: launch_scan<T, DI, 8>(qI, w, kI, b, m, scores, ld, dev_err, st); break;
+        case 1: launch_scan<T, DI, 1>(qI, w, kI, b, m, scores, ld, row_mask, dev_err, st); break;
+        case 2: launch_scan<T, DI, 2>(qI, w, kI, b, m, scores, ld, row_mask, dev_err, st); break;
+        case 4: launch_scan<T, DI, 4>(qI, w, kI, b, m, scores, ld, row_mask, dev_err, st); break;
+        case 8: launch_scan<T, DI, 8>(qI, w, kI, b, m, scores, ld, row_mask, dev_err, st); break;
         default: return LC_ERR_UNSUPPORTED;
     }
     return check_launch();
+}
+
+// Streaming (per-row) scores for the rows with row_mask[r] != 0 (all rows if
+// row_mask is null).
+lc_status index_scan_launch(const void *qI, const float *w, const void *kI, const lc_batch &b,
+                            int HI, int dI, int m, lc_dtype dt, float *scores, int64_t ld,
+                            const int32_t *row_mask, int32_t *dev_err, cudaStream_t st) {
+    if (dt == LC_F32)
+        return dI == 32 ? scan_hi<float, 32>(qI, w, kI, b, HI, m, scores, ld, row_mask, dev_err, st)
+                        : scan_hi<float, 64>(qI, w, kI, b, HI, m, scores, ld, row_mask, dev_err, st);
+    return dI == 32
+               ? scan_hi<__nv_bfloat16, 32>(qI, w, kI, b, HI, m, scores, ld, row_mask, dev_err, st)
+               : scan_hi<__nv_bfloat16, 64>(qI, w, kI, b, HI, m, scores, ld, row_mask, dev_err, st);
 }
 
 template <typename T>
 static lc_status launch_index(const void *qI, const float *w, const void *kI, const lc_batch &b,
                               int HI, int dI, int m, float *scores, int64_t ld, int32_t *dev_err,
                               cudaStream_t st) {
-    if (b.max_q < 16 && b.total_q <= 65535) {
-        if (dI == 32) return scan_hi<T, 32>(qI, w, kI, b, HI, m, scores, ld, dev_err, st);
-        return scan_hi<T, 64>(qI, w, kI, b, HI, m, scores, ld, dev_err, st);
+    if (b.max_q < 16) {
+        if (dI == 32) return scan_hi<T, 32>(qI, w, kI, b, HI, m, scores, ld, nullptr, dev_err, st);
+        return scan_hi<T, 64>(qI, w, kI, b, HI, m, scores, ld, nullptr, dev_err, st);
     }
     const size_t smem = sizeof(float) * ((size_t)(TQ + TE) * (dI + 1) + TQ);
     if (smem > 48 * 1024 &&

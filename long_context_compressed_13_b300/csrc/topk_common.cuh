@@ -1,0 +1,126 @@
+// Block-level helpers shared by the top-k kernels: prefix sums, radix
+// selection of the k-th largest order key, and an in-shared-memory bitonic
+// sort.  NT = threads per block.
+#pragma once
+
+#include "lc_common.cuh"
+
+namespace lc {
+
+// Exclusive block-wide prefix sum of v; *total receives the block sum.
+// warp_sums needs NT/32 ints of shared memory.
+template <int NT>
+__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int *total) {
+    constexpr int NW = NT / 32;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+    }
+    if (lane == 31) warp_sums[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        int s = lane < NW ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, s, off);
+            if (lane >= off) s += y;
+        }
+        if (lane < NW) warp_sums[lane] = s;  // inclusive prefix over warps
+    }
+    __syncthreads();
+    const int before = wid ? warp_sums[wid - 1] : 0;
+    *total = warp_sums[NW - 1];
+    __syncthreads();
+    return before + x - v;
+}
+
+struct RadixScratch {
+    uint32_t hist[256];
+    uint32_t digit;
+    int need;
+};
+
+// The `need`-th largest order key (1-based) among order_key(row[0..n-1]),
+// by four 8-bit radix passes (most significant digit first).  Returns the
+// key; *need_left receives how many keys equal to it rank within the top
+// `need`.  Requires 1 <= need <= n.  All threads of the block call it.
+template <int NT>
+__device__ uint32_t radix_kth_largest(const float *__restrict__ row, int64_t n, int need,
+                                      RadixScratch &rs, int *need_left) {
+    uint32_t prefix = 0, mask = 0;
+#pragma unroll 1
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        for (int i = threadIdx.x; i < 256; i += NT) rs.hist[i] = 0;
+        __syncthreads();
+        for (int64_t j = threadIdx.x; j < n; j += NT) {
+            const uint32_t key = order_key(__ldg(row + j));
+            if ((key & mask) == prefix) atomicAdd(&rs.hist[(key >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            // suffix sums over the 256 bins, 8 bins per lane, highest first
+            const int lane = threadIdx.x;
+            uint32_t c[8];
+            uint32_t mine = 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                c[u] = rs.hist[255 - (lane * 8 + u)];
+                mine += c[u];
+            }
+            uint32_t incl = mine;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += y;
+            }
+            const uint32_t excl = incl - mine;
+            if (excl < (uint32_t)need && incl >= (uint32_t)need) {
+                uint32_t cum = excl;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    if (cum + c[u] >= (uint32_t)need) {
+                        rs.digit = 255u - (uint32_t)(lane * 8 + u);
+                        rs.need = need - (int)cum;
+                        break;
+                    }
+                    cum += c[u];
+                }
+            }
+        }
+        __syncthreads();
+        prefix |= rs.digit << shift;
+        mask |= 255u << shift;
+        need = rs.need;
+        __syncthreads();
+    }
+    *need_left = need;
+    return prefix;
+}
+
+// Bitonic sort of P (power of two) 64-bit keys in shared memory, descending
+// if DESC.  All threads of the block call it.
+template <int NT, bool DESC>
+__device__ void bitonic_sort_u64(uint64_t *a, int P) {
+    for (int size = 2; size <= P; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            __syncthreads();
+            for (int i = threadIdx.x; i < (P >> 1); i += NT) {
+                const int lo = 2 * stride * (i / stride) + (i % stride);
+                const int hi = lo + stride;
+                const bool up = ((lo & size) == 0) != DESC;  // this pair sorts ascending
+                const uint64_t x = a[lo], y = a[hi];
+                if ((x > y) == up) {
+                    a[lo] = y;
+                    a[hi] = x;
+                }
+            }
+        }
+    }
+    __syncthreads();
+}
+
+}  // namespace lc

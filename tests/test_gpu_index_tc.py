@@ -1,0 +1,130 @@
+"""GPU parity of the tensor-core Lightning Indexer and of its fused exact
+top-k (sampled threshold -> candidate filter -> exact selection -> per-row
+fallback) against the CPU oracle.
+
+Bars: scores within a rigorous fp32 accumulation bound, invisible entries
+exactly -inf; fused selections equal the oracle's except in rows whose oracle
+gap between the k-th and (k+1)-th score is below 1e-5."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+GAP = 1e-5
+
+
+@pytest.fixture(scope="module")
+def lc():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import long_context_compressed_13_b300 as m
+    from long_context_compressed_13_b300 import _build
+    _build.build()
+    m.load_library()
+    return m
+
+
+def f64(x):
+    return x.detach().to("cpu").double().numpy()
+
+
+def _bound(qI, w, kI):
+    q, k, ww = f64(qI), f64(kI), f64(w)
+    mag = np.einsum("rh,rjh->rj", np.abs(ww), np.einsum("rhe,jhe->rjh", np.abs(q), np.abs(k)))
+    n = q.shape[2] + q.shape[1] + 2
+    u = 2.0 ** -24
+    return mag * (n * u / (1 - n * u)) + 1e-30
+
+
+def _check_selection(gsel, I, nvis, k):
+    """gsel: GPU top-k; I: oracle scores.  Returns the number of excused rows."""
+    rsel = oracle.topk(I, nvis, k)
+    excused = 0
+    for r in range(gsel.shape[0]):
+        keep = min(k, int(nvis[r]))
+        row = gsel[r]
+        assert np.all(row[keep:] == -1), r
+        v = row[:keep]
+        assert np.all(np.diff(v) > 0) and (keep == 0 or (v[0] >= 0 and v[-1] < nvis[r])), r
+        if not np.array_equal(row, rsel[r]):
+            s = np.sort(I[r, : nvis[r]])[::-1]
+            assert s[k - 1] - s[k] < GAP, f"row {r}: selection differs, gap {s[k-1]-s[k]}"
+            excused += 1
+    return excused
+
+
+@pytest.mark.parametrize("HI,T,m,q_from", [(8, 2048, 4, 0), (4, 2304, 4, 100), (8, 1400, 8, 0)])
+def test_tc_scores(lc, HI, T, m, q_from):
+    L = wl.csa_layer(T=T, H=8, d=64, HI=HI, dI=64, m=m, k=16, W=16, dtype="bf16", seed=71,
+                     q_from=q_from)
+    b = lc.DeviceBatch.from_workload(L["batch"])
+    tpos = np.array(L["batch"].positions())
+    ld = b.max_c + 12  # columns past the stored entries are -inf too
+    sc = torch.full((b.total_q, ld), 7.0, device="cuda")
+    lc.lightning_index(L["qI"].cuda(), L["w"].cuda(), L["kI"].cuda(), b, m, scores=sc)
+    torch.cuda.synchronize()
+    ref = oracle.index(L["qI"], L["w"], L["kI"], tpos, m)
+    got = sc.cpu().double().numpy()
+    assert np.all(np.isneginf(got[:, b.max_c:]))
+    got = got[:, : b.max_c]
+    vis = np.isfinite(ref)
+    assert np.array_equal(np.isneginf(got), ~vis)
+    bound = _bound(L["qI"], L["w"], L["kI"])
+    err = np.abs(got[vis] - ref[vis])
+    assert np.all(err <= bound[vis]), f"max err {err.max()}"
+
+
+@pytest.mark.parametrize("k,T,q_from", [(64, 4096, 0), (32, 2048, 1000), (512, 16384, 12000)])
+def test_fused_topk_prefill(lc, k, T, q_from):
+    L = wl.csa_layer(T=T, H=8, d=64, HI=8, dI=64, m=4, k=k, W=16, dtype="bf16", seed=72,
+                     q_from=q_from)
+    b = lc.DeviceBatch.from_workload(L["batch"])
+    tpos = np.array(L["batch"].positions())
+    _, sel = lc.lightning_index(L["qI"].cuda(), L["w"].cuda(), L["kI"].cuda(), b, 4,
+                                scores=False, k=k, topk=True)
+    torch.cuda.synchronize()
+    I = oracle.index(L["qI"], L["w"], L["kI"], tpos, 4)
+    n = _check_selection(sel.cpu().numpy(), I, (tpos + 1) // 4, k)
+    print(f"excused rows: {n} of {len(tpos)}")
+
+
+def test_fused_topk_long_rows_sampled(lc):
+    # 32768 entries per row: the sampled threshold uses every 32nd entry
+    T, k = 131072, 64
+    L = wl.csa_layer(T=T, H=8, d=64, HI=8, dI=64, m=4, k=k, W=16, dtype="bf16", seed=73,
+                     q_from=T - 256)
+    b = lc.DeviceBatch.from_workload(L["batch"])
+    tpos = np.array(L["batch"].positions())
+    _, sel = lc.lightning_index(L["qI"].cuda(), L["w"].cuda(), L["kI"].cuda(), b, 4,
+                                scores=False, k=k, topk=True)
+    torch.cuda.synchronize()
+    I = oracle.index(L["qI"], L["w"], L["kI"], tpos, 4)
+    _check_selection(sel.cpu().numpy(), I, (tpos + 1) // 4, k)
+
+
+def test_fused_topk_ties_take_the_fallback(lc):
+    # rows with all-zero indexer queries or head weights score every entry 0:
+    # the candidate list overflows and the exact fallback keeps the lowest
+    # indices; the other rows go through the candidate path
+    T, k = 16384, 128
+    L = wl.csa_layer(T=T, H=8, d=64, HI=8, dI=64, m=4, k=k, W=16, dtype="bf16", seed=74,
+                     q_from=T - 512)
+    qI, w = L["qI"].clone(), L["w"].clone()
+    qI[5:9] = 0
+    w[100:103] = 0
+    qI[200, :, :] = -qI[200, :, :].abs()  # some heads positive, some negative per entry
+    b = lc.DeviceBatch.from_workload(L["batch"])
+    tpos = np.array(L["batch"].positions())
+    _, sel = lc.lightning_index(qI.cuda(), w.cuda(), L["kI"].cuda(), b, 4, scores=False, k=k,
+                                topk=True)
+    torch.cuda.synchronize()
+    I = oracle.index(qI, w, L["kI"], tpos, 4)
+    gsel = sel.cpu().numpy()
+    for r in list(range(5, 9)) + [100, 101, 102]:
+        assert gsel[r].tolist() == list(range(k))
+    _check_selection(gsel, I, (tpos + 1) // 4, k)
