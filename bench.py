@@ -143,7 +143,8 @@ class LayerPair:
                         Kc=self.Kh[: self.q0 // self.m_h], Vc=self.Vh[: self.q0 // self.m_h])
         self.b_csa = lc.DeviceBatch.from_workload(c["batch"], device=device)
         self.b_hca = lc.DeviceBatch.from_workload(h["batch"], device=device)
-        self.ws = torch.empty(lc.workspace_size(lc.LC_OP_LIGHTNING_INDEX, self.b_csa),
+        self.ws = torch.empty(lc.workspace_size(lc.LC_OP_LIGHTNING_INDEX, self.b_csa,
+                                                HI=c["HI"], dI=c["dI"], k=self.k),
                               dtype=torch.uint8, device=device)
         self.sel = torch.empty((chunk, self.k), dtype=torch.int32, device=device)
         self.O_csa = torch.empty_like(c["Q"])

@@ -219,7 +219,7 @@ def lightning_index(qI, w, kI, batch: DeviceBatch, m: int, *, scores: bool | tor
     else:
         tk = None
     if tk is not None and sc is None and ws is None:
-        need = workspace_size(LC_OP_LIGHTNING_INDEX, batch)
+        need = workspace_size(LC_OP_LIGHTNING_INDEX, batch, HI=HI, dI=dI, k=k)
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device=qI.device)
     cb = batch.c_struct()
     ld = sc.shape[1] if sc is not None else 0
