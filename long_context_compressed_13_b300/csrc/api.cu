@@ -27,6 +27,10 @@ lc_status hca_tc_launch(const void *Q, const void *Kc, const void *Vc, const voi
                         const void *Vraw, const lc_batch &b, int H, int d, int m, int W,
                         float scale, lc_dtype dt, void *O, float *lse, int32_t *dev_err,
                         cudaStream_t st);
+lc_status sparse_tc_launch(const void *Q, const void *Kc, const void *Vc, const int32_t *topk,
+                           int k, const void *Kraw, const void *Vraw, const lc_batch &b, int H,
+                           int d, int m, int W, float scale, lc_dtype dt, void *O, float *lse,
+                           int32_t *dev_err, cudaStream_t st);
 lc_status attn_simt_launch(bool sparse, const void *Q, const void *Kc, const void *Vc,
                            const int32_t *topk, int k, const void *Kraw, const void *Vraw,
                            const lc_batch &b, int H, int d, int m, int W, float scale,
@@ -184,8 +188,11 @@ lc_status sparse_mqa_attn(const void *Q, const void *Kc, const void *Vc, const i
         return LC_ERR_INVALID_ARG;
     if ((d != 64 && d != 128) || H < 8 || H > 128 || H % 8 || W > 4096 || k > 4096)
         return LC_ERR_UNSUPPORTED;
-    lc_status s = attn_simt_launch(true, Q, Kc, Vc, topk, k, Kraw, Vraw, *batch, H, d, m, W,
-                                   scale, dtype, O, lse, dev_err, st);
+    lc_status s = sparse_tc_launch(Q, Kc, Vc, topk, k, Kraw, Vraw, *batch, H, d, m, W, scale,
+                                   dtype, O, lse, dev_err, st);
+    if (s == LC_ERR_UNSUPPORTED)
+        s = attn_simt_launch(true, Q, Kc, Vc, topk, k, Kraw, Vraw, *batch, H, d, m, W, scale,
+                             dtype, O, lse, dev_err, st);
     return finish(s, st, dev_err);
 }
 
