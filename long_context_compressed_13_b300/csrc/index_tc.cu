@@ -48,8 +48,10 @@ constexpr int IDI = 64;           // indexer head dim
 constexpr int I_THREADS = 320;    // 8 epilogue warps + producer + MMA
 constexpr int MODE_MATERIALIZE = 0, MODE_FILTER = 1;
 
+constexpr int MAX_ST = 6;         // K-tile ring depth (8 heads: 3, 4 heads: 6)
+
 struct IdxBars {
-    uint64_t q_full, k_full[2], k_empty[2], acc_full[2], acc_empty[2];
+    uint64_t q_full, k_full[MAX_ST], k_empty[MAX_ST], acc_full[2], acc_empty[2];
     uint32_t taddr;
     int abort;
 };
@@ -94,7 +96,8 @@ __global__ void __launch_bounds__(I_THREADS, 1)
     constexpr uint32_t SM_Q = 0;                          // HI x [128 x 128 B]
     constexpr uint32_t SM_K = HI * IBM * 128;             // 2 x HI x [32 x 128 B]
     constexpr uint32_t K_STAGE = HI * IBN * 128;
-    constexpr uint32_t SM_BAR = SM_K + 2 * K_STAGE;
+    constexpr int NST = HI == 8 ? 3 : 6;                  // ring depth
+    constexpr uint32_t SM_BAR = SM_K + NST * K_STAGE;
     constexpr uint32_t TCOLS = 2 * HI * IBN;              // two accumulator buffers
     extern __shared__ __align__(1024) uint8_t smem[];
     IdxBars &bars = *reinterpret_cast<IdxBars *>(smem + SM_BAR);
@@ -118,9 +121,11 @@ __global__ void __launch_bounds__(I_THREADS, 1)
         bars.abort = (smem_u32(smem) & 1023u) != 0 ? 1 : 0;
         if (bars.abort) flag(a.dev_err, LC_DEVERR_TIMEOUT);
         mbar_init(&bars.q_full, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < NST; ++s) {
             mbar_init(&bars.k_full[s], 1);
             mbar_init(&bars.k_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
             mbar_init(&bars.acc_full[s], 1);
             mbar_init(&bars.acc_empty[s], 256);
         }
@@ -147,8 +152,9 @@ __global__ void __launch_bounds__(I_THREADS, 1)
                             (int32_t)row0);
             int issued = 0;
             for (int i = 0; i < n_t; ++i) {
-                const int s = i & 1;
-                if (i >= 2 && !mbar_wait(&bars.k_empty[s], ((i - 2) >> 1) & 1, abort)) break;
+                const int s = i % NST;
+                if (i >= NST && !mbar_wait(&bars.k_empty[s], ((i - NST) / NST) & 1, abort))
+                    break;
                 const int32_t y = (int32_t)(c0 + (int64_t)i * IBN);
                 uint8_t *kd = smem + SM_K + s * K_STAGE;
                 mbar_expect_tx(&bars.k_full[s], HI * IBN * 128);
@@ -158,8 +164,8 @@ __global__ void __launch_bounds__(I_THREADS, 1)
                 ++issued;
             }
             int dummy = 0;
-            for (int i = max(0, issued - 2); i < issued; ++i)
-                mbar_wait(&bars.k_full[i & 1], (i >> 1) & 1, &dummy, 400000000LL);
+            for (int i = max(0, issued - NST); i < issued; ++i)
+                mbar_wait(&bars.k_full[i % NST], (i / NST) & 1, &dummy, 400000000LL);
             mbar_wait(&bars.q_full, 0, &dummy, 400000000LL);
         }
     } else if (warp == 9) {
@@ -169,8 +175,8 @@ __global__ void __launch_bounds__(I_THREADS, 1)
             const uint32_t q_base = smem_u32(smem + SM_Q);
             bool ok = mbar_wait(&bars.q_full, 0, abort);
             for (int i = 0; ok && i < n_t; ++i) {
-                const int s = i & 1, bf = i & 1;
-                if (!mbar_wait(&bars.k_full[s], (i >> 1) & 1, abort)) break;
+                const int s = i % NST, bf = i & 1;
+                if (!mbar_wait(&bars.k_full[s], (i / NST) & 1, abort)) break;
                 if (i >= 2 && !mbar_wait(&bars.acc_empty[bf], ((i - 2) >> 1) & 1, abort)) break;
                 tc_fence_after();
                 const uint32_t k_base = smem_u32(smem + SM_K + s * K_STAGE);
@@ -345,6 +351,114 @@ __global__ void __launch_bounds__(512) k_cand_topk(Batch bt, int m, int k, int c
     for (int i = threadIdx.x; i < k; i += 512) out[i] = (int32_t)si[i];
 }
 
+// Exact top-k of each row's candidates without sorting them: radix selection
+// of the k-th largest key K* in shared memory; every candidate above K* and
+// the `need` lowest-index candidates equal to K* are marked in a bitmap over
+// the row's entries, which a prefix sum turns into ascending indices.  Rows
+// whose candidate count is outside [k, cap] are marked in fail[].
+// Shared memory: cap keys, cap indices, nwords bitmap words, then
+// pow2(cap) tie slots.
+__global__ void __launch_bounds__(512) k_cand_select(Batch bt, int m, int k, int cap, int nwords,
+                                                     const int32_t *__restrict__ count,
+                                                     const uint32_t *__restrict__ cand_key,
+                                                     const int32_t *__restrict__ cand_idx,
+                                                     int32_t *__restrict__ topk, int32_t *fail) {
+    constexpr int NT = 512;
+    extern __shared__ uint32_t sbuf[];
+    uint32_t *keys = sbuf;                                      // [cap]
+    int32_t *idx = reinterpret_cast<int32_t *>(sbuf + cap);     // [cap]
+    uint32_t *bits = sbuf + 2 * cap;                            // [nwords]
+    __shared__ RadixScratch rs;
+    __shared__ int warp_sums[NT / 32];
+    __shared__ int s_ties;
+    const int64_t r = blockIdx.x;
+    const int64_t t = bt.q_pos0[0] + r;
+    const int64_t Tc = bt.cu_c[1] - bt.cu_c[0];
+    int64_t nv = n_vis(t, m);
+    if (nv > Tc) nv = Tc;
+    int32_t *out = topk + r * k;
+    if (nv <= k) {
+        for (int i = threadIdx.x; i < k; i += NT) out[i] = i < nv ? i : -1;
+        return;
+    }
+    const int n = count[r];
+    if (n < k || n > cap) {
+        if (threadIdx.x == 0) fail[r] = 1;
+        return;
+    }
+    const int words = (int)((nv + 31) / 32);
+    for (int i = threadIdx.x; i < n; i += NT) {
+        keys[i] = cand_key[r * cap + i];
+        idx[i] = cand_idx[r * cap + i];
+    }
+    for (int i = threadIdx.x; i < words; i += NT) bits[i] = 0u;
+    if (threadIdx.x == 0) s_ties = 0;
+    __syncthreads();
+    int need;
+    const uint32_t kstar = radix_kth_largest_smem<NT>(keys, n, k, rs, &need);
+    // keys above K* are in; count the ties at K*
+    int my_ties = 0;
+    for (int i = threadIdx.x; i < n; i += NT) {
+        if (keys[i] > kstar) atomicOr(&bits[idx[i] >> 5], 1u << (idx[i] & 31));
+        else if (keys[i] == kstar) ++my_ties;
+    }
+    if (my_ties) atomicAdd(&s_ties, my_ties);
+    __syncthreads();
+    const int ties = s_ties;
+    if (ties == need) {
+        for (int i = threadIdx.x; i < n; i += NT)
+            if (keys[i] == kstar) atomicOr(&bits[idx[i] >> 5], 1u << (idx[i] & 31));
+    } else {
+        // more ties than places (rare): the lowest indices win.  The tie list
+        // lives after the bitmap and is sorted ascending.
+        uint32_t *tl = bits + words;
+        __syncthreads();
+        if (threadIdx.x == 0) s_ties = 0;
+        __syncthreads();
+        for (int i = threadIdx.x; i < n; i += NT)
+            if (keys[i] == kstar) tl[atomicAdd(&s_ties, 1)] = (uint32_t)idx[i];
+        int P = 1;
+        while (P < ties) P <<= 1;
+        for (int i = ties + threadIdx.x; i < P; i += NT) tl[i] = 0xFFFFFFFFu;
+        __syncthreads();
+        for (int size = 2; size <= P; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                for (int i = threadIdx.x; i < (P >> 1); i += NT) {
+                    const int lo = 2 * stride * (i / stride) + (i % stride);
+                    const int hi = lo + stride;
+                    const bool up = (lo & size) == 0;
+                    const uint32_t x = tl[lo], y = tl[hi];
+                    if ((x > y) == up) {
+                        tl[lo] = y;
+                        tl[hi] = x;
+                    }
+                }
+                __syncthreads();
+            }
+        }
+        for (int i = threadIdx.x; i < need; i += NT)
+            atomicOr(&bits[tl[i] >> 5], 1u << (tl[i] & 31));
+    }
+    __syncthreads();
+    // ascending compaction of the bitmap
+    const int per = (words + NT - 1) / NT;
+    const int w0 = threadIdx.x * per, w1 = min(words, w0 + per);
+    int mine = 0;
+    for (int w = w0; w < w1; ++w) mine += __popc(bits[w]);
+    int total;
+    int pos = block_exclusive_scan<NT>(mine, warp_sums, &total);
+    for (int w = w0; w < w1; ++w) {
+        uint32_t x = bits[w];
+        while (x) {
+            const int b = __ffs(x) - 1;
+            x &= x - 1;
+            if (pos < k) out[pos] = w * 32 + b;
+            ++pos;
+        }
+    }
+    (void)nwords;
+}
+
 namespace {
 int pow2_at_least(int x) {
     int p = 1;
@@ -405,7 +519,7 @@ bool index_tc_eligible(const void *qI, const void *kI, const lc_batch &b, int HI
 template <int MODE, int HI>
 lc_status launch_tc(const CUtensorMap &mQ, const CUtensorMap &mK, const IdxTcArgs &a,
                     int64_t n_cols, cudaStream_t st) {
-    constexpr uint32_t SMEM = HI * IBM * 128 + 2 * HI * IBN * 128 + 256;
+    constexpr uint32_t SMEM = HI * IBM * 128 + (HI == 8 ? 3 : 6) * HI * IBN * 128 + 256;
     auto kfn = k_index_tc<MODE, HI>;
     static bool attr = false;
     if (!attr) {
@@ -534,18 +648,33 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
         s = launch_tc_hi<MODE_FILTER>(HI, mQ, mK, a, Tc, st);
         if (s != LC_OK) return s;
     }
-    // 4. exact selection among candidates
+    // 4. exact selection among candidates: bitmap compaction when the row's
+    //    bitmap fits in shared memory, a full bitonic sort otherwise
     {
-        const size_t smem = sizeof(uint64_t) * (size_t)(p.P + p.PK);
-        static size_t attr = 0;
-        if (smem > 48 * 1024 && smem > attr) {
-            if (cudaFuncSetAttribute(k_cand_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem) != cudaSuccess)
-                return LC_ERR_CUDA;
-            attr = smem;
+        const int64_t nwords = (Tc + 31) / 32;
+        const size_t smem_bm = sizeof(uint32_t) * (size_t)(2 * p.cap + nwords + p.P);
+        if (smem_bm <= 200 * 1024) {
+            static size_t attr = 0;
+            if (smem_bm > 48 * 1024 && smem_bm > attr) {
+                if (cudaFuncSetAttribute(k_cand_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem_bm) != cudaSuccess)
+                    return LC_ERR_CUDA;
+                attr = smem_bm;
+            }
+            LC_LAUNCH(k_cand_select, dim3((unsigned)b.total_q), dim3(512), smem_bm, st, to_dev(b),
+                      m, k, p.cap, (int)nwords, count, ckey, cidx, topk, fail);
+        } else {
+            const size_t smem = sizeof(uint64_t) * (size_t)(p.P + p.PK);
+            static size_t attr = 0;
+            if (smem > 48 * 1024 && smem > attr) {
+                if (cudaFuncSetAttribute(k_cand_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem) != cudaSuccess)
+                    return LC_ERR_CUDA;
+                attr = smem;
+            }
+            LC_LAUNCH(k_cand_topk, dim3((unsigned)b.total_q), dim3(512), smem, st, to_dev(b), m,
+                      k, p.cap, p.P, p.PK, count, ckey, cidx, topk, fail);
         }
-        LC_LAUNCH(k_cand_topk, dim3((unsigned)b.total_q), dim3(512), smem, st, to_dev(b), m, k,
-                  p.cap, p.P, p.PK, count, ckey, cidx, topk, fail);
         if ((s = check_launch()) != LC_OK) return s;
     }
     // 5. exact fallback for the rows marked in fail[] (no work when none is)

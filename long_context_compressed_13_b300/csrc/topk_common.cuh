@@ -101,6 +101,60 @@ __device__ uint32_t radix_kth_largest(const float *__restrict__ row, int64_t n, 
     return prefix;
 }
 
+// As radix_kth_largest, over n order keys held in shared memory.
+template <int NT>
+__device__ uint32_t radix_kth_largest_smem(const uint32_t *keys, int n, int need,
+                                           RadixScratch &rs, int *need_left) {
+    uint32_t prefix = 0, mask = 0;
+#pragma unroll 1
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        for (int i = threadIdx.x; i < 256; i += NT) rs.hist[i] = 0;
+        __syncthreads();
+        for (int j = threadIdx.x; j < n; j += NT) {
+            const uint32_t key = keys[j];
+            if ((key & mask) == prefix) atomicAdd(&rs.hist[(key >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            const int lane = threadIdx.x;
+            uint32_t c[8];
+            uint32_t mine = 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                c[u] = rs.hist[255 - (lane * 8 + u)];
+                mine += c[u];
+            }
+            uint32_t incl = mine;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += y;
+            }
+            const uint32_t excl = incl - mine;
+            if (excl < (uint32_t)need && incl >= (uint32_t)need) {
+                uint32_t cum = excl;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    if (cum + c[u] >= (uint32_t)need) {
+                        rs.digit = 255u - (uint32_t)(lane * 8 + u);
+                        rs.need = need - (int)cum;
+                        break;
+                    }
+                    cum += c[u];
+                }
+            }
+        }
+        __syncthreads();
+        prefix |= rs.digit << shift;
+        mask |= 255u << shift;
+        need = rs.need;
+        __syncthreads();
+    }
+    *need_left = need;
+    return prefix;
+}
+
 // Bitonic sort of P (power of two) 64-bit keys in shared memory, descending
 // if DESC.  All threads of the block call it.
 template <int NT, bool DESC>
