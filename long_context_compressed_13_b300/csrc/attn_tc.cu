@@ -142,10 +142,10 @@ __global__ void __launch_bounds__(THREADS, 2)
             mbar_init(&bars.v_full[s], 1);
             mbar_init(&bars.kv_empty[s], 1);
             mbar_init(&bars.s_full[s], 1);
-            mbar_init(&bars.s_free[s], 128);
+            mbar_init(&bars.s_free[s], 4);  // one arrival per softmax warp
             mbar_init(&bars.mask_full[s], 1);
         }
-        mbar_init(&bars.p_full, 128);
+        mbar_init(&bars.p_full, 4);
         mbar_init(&bars.o_done, 1);
         fence_barrier_init();
     }
@@ -327,7 +327,8 @@ __global__ void __launch_bounds__(THREADS, 2)
                 }
             }
             tc_fence_before();
-            mbar_arrive(&bars.s_free[b]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.s_free[b]);
             // valid keys: a 64-bit mask (CSA selected tiles) or a column range
             uint64_t vmask;
             if (SPARSE && i < nct) {
@@ -409,7 +410,8 @@ __global__ void __launch_bounds__(THREADS, 2)
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&bars.p_full);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.p_full);
         }
         // epilogue (ok is warp-uniform here)
         if (ok && n_tiles > 0 &&
@@ -491,38 +493,6 @@ bool make_maps(CUtensorMap (&maps)[5], const void *Q, int64_t q_rows, const void
            make_tmap_bf16_2d(&maps[4], have_r ? Vr : Q, have_r ? r_rows : 1, HD, HD * 2, 64, BN);
 }
 }  // namespace
-
-// HCA on the tensor cores: bf16, d = 128, one sequence, H dividing 128.
-// LC_ERR_UNSUPPORTED when the shape does not fit (the caller falls back).
-lc_status hca_tc_launch(const void *Q, const void *Kc, const void *Vc, const void *Kraw,
-                        const void *Vraw, const lc_batch &b, int H, int d, int m, int W,
-                        float scale, lc_dtype dt, void *O, float *lse, int32_t *dev_err,
-                        cudaStream_t st) {
-    if (dt != LC_BF16 || d != HD || b.B != 1 || (BM % H) != 0) return LC_ERR_UNSUPPORTED;
-    if (!al16(Q) || !al16(O) || (Kc && !al16(Kc)) || (Vc && !al16(Vc)) ||
-        (Kraw && !al16(Kraw)) || (Vraw && !al16(Vraw)))
-        return LC_ERR_UNSUPPORTED;
-    const int64_t n_rows = b.total_q * H;
-    if (n_rows == 0) return LC_OK;
-    const bool have_r = W > 0 && b.total_raw > 0 && Kraw && Vraw;
-    CUtensorMap maps[5];
-    if (!make_maps(maps, Q, n_rows, Kc, Vc, b.total_c, Kraw, Vraw, have_r ? b.total_raw : 0,
-                   false))
-        return LC_ERR_CUDA;
-    AttnTcArgs a{};
-    a.n_rows = n_rows;
-    a.H = H;
-    a.bt = to_dev(b);
-    a.Tc = (b.total_c > 0 && Kc && Vc) ? b.total_c : 0;
-    a.Nraw = have_r ? b.total_raw : 0;
-    a.m = m;
-    a.W = have_r ? W : 0;
-    a.scale_log2 = scale * LOG2E_F;
-    a.O = reinterpret_cast<__nv_bfloat16 *>(O);
-    a.lse = lse;
-    a.dev_err = dev_err;
-    return launch_attn_tc<false>(maps, a, (unsigned)((n_rows + BM - 1) / BM), st);
-}
 
 // CSA sparse attention on the tensor cores: bf16, d = 128, H <= 128, any
 // ragged batch (one CTA per query token).  LC_ERR_UNSUPPORTED otherwise.

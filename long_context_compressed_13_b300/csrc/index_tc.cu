@@ -3,27 +3,33 @@
 // never writes the full score matrix.
 //
 // k_index_tc: one CTA = 128 query rows x a contiguous range of entries.
-//   warp 8      TMA producer: q_I of the 128 rows for every head once (H_I
-//               boxes of 128 x 64), then k_I tiles of 32 entries x H_I heads
-//               into a 2-stage ring
-//   warp 9      TMEM owner and MMA issuer: per tile and head one
-//               M=128, N=32, K=64 product q_h k_h^T into TMEM (H_I x 32
-//               columns per buffer, two buffers)
-//   warps 0-7   epilogue: warp w reads TMEM lanes 32(w%4).. and columns
-//               16(w/4).. of every head, forms sum_h w_h * max(s_h, 0) in fp32
-//               and either stores the scores (MATERIALIZE) or keeps the
-//               entries whose order key reaches the row's threshold
-//               (FILTER) in a per-row candidate list.
+//   q_I of the 128 rows lives in tensor memory (H_I x 32 columns of packed
+//   bf16 pairs) and is the A operand of every MMA, so shared memory only
+//   feeds the B operand (the entries' keys): 64 B per tensor-core clock.
+//   warp 16     TMA producer: k_I tiles of 64 entries x H_I heads into a
+//               ring of shared-memory stages
+//   warp 17     TMEM owner and MMA issuer: per tile, head by head, one
+//               M=128, N=64, K=64 product q_h k_h^T into a ring of four
+//               64-column TMEM buffers
+//   warps 0-15  epilogue: warp w owns TMEM lanes 32(w%4).. (its query rows)
+//               and columns 16(w/4).. of each buffer; it folds the heads in
+//               order, acc = fma(w_h, max(s_h, 0), acc), two columns per
+//               packed fp32x2 FMA, loading head h+1 from TMEM while it folds
+//               head h, then either stores the 64 scores of the tile
+//               (MATERIALIZE) or appends the entries whose score reaches the
+//               row's threshold to the row's candidate list (FILTER).  The
+//               threshold test is a sign-bit collect of acc - theta.
 // The fused top-k of a row (see index_topk_tc_launch):
 //   1. scores of every s-th entry (MATERIALIZE over a strided tensor map);
 //   2. theta = the rho-th largest sampled key, a lower bound for the k-th
 //      largest key of the full row with overwhelming probability;
 //   3. FILTER pass over all entries: candidates = entries with key >= theta;
-//   4. exact top-k of the candidates (bitonic sort on (key, -index)), valid
-//      when the row has between k and `cap` candidates: then every member of
-//      the true top-k is a candidate;
+//   4. exact top-k of the candidates, valid when the row has between k and
+//      `cap` candidates: then every member of the true top-k is a candidate;
 //   5. rows outside that range (rare: massive ties or an unlucky sample) are
 //      redone exactly from fully materialised scores.
+// Both passes run the same arithmetic, so a sampled score and the FILTER
+// pass's score of the same entry are bit-identical.
 #include <cmath>
 
 #include "lc_common.cuh"
@@ -43,19 +49,57 @@ lc_status topk_launch_masked(const float *scores, int64_t ld, const lc_batch &b,
 
 namespace {
 constexpr int IBM = 128;          // query rows per CTA
-constexpr int IBN = 32;           // entries per tile
+constexpr int IBN = 64;           // entries per tile
 constexpr int IDI = 64;           // indexer head dim
-constexpr int I_THREADS = 320;    // 8 epilogue warps + producer + MMA
+constexpr int NEPI = 512;         // epilogue threads (16 warps)
+constexpr int I_THREADS = NEPI + 64;  // + producer warp + MMA warp
+constexpr int EPI_COLS = 16;      // columns of a score buffer per epilogue thread
+constexpr int NBUF = 4;           // TMEM score buffers (one head each)
+constexpr uint32_t I_TMEM_COLS = 512;
 constexpr int MODE_MATERIALIZE = 0, MODE_FILTER = 1;
 
-constexpr int MAX_ST = 6;         // K-tile ring depth (8 heads: 3, 4 heads: 6)
+template <int HI>
+struct IdxCfg {
+    static constexpr uint32_t HEAD_BOX = IBN * 128;        // 64 entries x 128 B
+    static constexpr uint32_t STAGE = HI * HEAD_BOX;
+    static constexpr int NST = HI == 8 ? 3 : 6;             // 192 KB of stages
+    static constexpr uint32_t SM_STG = NST * STAGE;         // FILTER staging, 64 B / thread
+    static constexpr uint32_t SM_BAR = SM_STG + NEPI * EPI_COLS * 4;
+    static constexpr uint32_t SMEM = SM_BAR + 256;
+    static constexpr uint32_t D_COL0 = HI * 32;             // score buffers after q_I
+};
 
 struct IdxBars {
-    uint64_t q_full, k_full[MAX_ST], k_empty[MAX_ST], acc_full[2], acc_empty[2];
+    uint64_t q_full, k_full[6], k_empty[6], d_full[NBUF], d_empty[NBUF];
     uint32_t taddr;
     int abort;
 };
 
+// tcgen05.mma with the A operand in tensor memory.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32_u(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+// 32 lanes x 16 columns of 32-bit (thread i: lane base + i).
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     uint32_t r[16];
     asm volatile(
@@ -68,11 +112,20 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+
+// Inverse of order_key: the float whose key is `key` (+0 for the key of
+// +-0).  Key 0 (below every finite score) maps to -inf.
+__device__ __forceinline__ float key_to_float(uint32_t key) {
+    if (key == 0u) return -INFINITY;
+    const uint32_t u = (key & 0x80000000u) ? (key & 0x7fffffffu) : ~key;
+    return __uint_as_float(u);
+}
 }  // namespace
 
 struct IdxTcArgs {
     int64_t Nq;              // query rows of the (single) sequence
     const int64_t *q_pos0;   // device: absolute position of row 0
+    const __nv_bfloat16 *qI; // [Nq, HI, 64]
     int64_t Tc;              // stored entries
     int stride;              // map entry e is entry e*stride
     int m;
@@ -81,6 +134,7 @@ struct IdxTcArgs {
     const float *w;          // [Nq, HI]
     float *out;              // MATERIALIZE: [Nq, ld]
     int64_t ld;
+    int vec_out;             // MATERIALIZE: out and ld allow 16-byte stores
     const uint32_t *theta;   // FILTER: [Nq] order-key thresholds
     int32_t *count;          // FILTER: [Nq] candidate counts (zeroed beforehand)
     uint32_t *cand_key;      // FILTER: [Nq, cap]
@@ -91,16 +145,11 @@ struct IdxTcArgs {
 
 template <int MODE, int HI>
 __global__ void __launch_bounds__(I_THREADS, 1)
-    k_index_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
-               IdxTcArgs a) {
-    constexpr uint32_t SM_Q = 0;                          // HI x [128 x 128 B]
-    constexpr uint32_t SM_K = HI * IBM * 128;             // 2 x HI x [32 x 128 B]
-    constexpr uint32_t K_STAGE = HI * IBN * 128;
-    constexpr int NST = HI == 8 ? 3 : 6;                  // ring depth
-    constexpr uint32_t SM_BAR = SM_K + NST * K_STAGE;
-    constexpr uint32_t TCOLS = 2 * HI * IBN;              // two accumulator buffers
+    k_index_tc(const __grid_constant__ CUtensorMap mK, IdxTcArgs a) {
+    using C = IdxCfg<HI>;
+    constexpr int NST = C::NST;
     extern __shared__ __align__(1024) uint8_t smem[];
-    IdxBars &bars = *reinterpret_cast<IdxBars *>(smem + SM_BAR);
+    IdxBars &bars = *reinterpret_cast<IdxBars *>(smem + C::SM_BAR);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int *abort = &bars.abort;
     const unsigned FULL = 0xffffffffu;
@@ -120,19 +169,20 @@ __global__ void __launch_bounds__(I_THREADS, 1)
     if (tid == 0) {
         bars.abort = (smem_u32(smem) & 1023u) != 0 ? 1 : 0;
         if (bars.abort) flag(a.dev_err, LC_DEVERR_TIMEOUT);
-        mbar_init(&bars.q_full, 1);
+        mbar_init(&bars.q_full, NEPI / 32);
         for (int s = 0; s < NST; ++s) {
             mbar_init(&bars.k_full[s], 1);
             mbar_init(&bars.k_empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars.acc_full[s], 1);
-            mbar_init(&bars.acc_empty[s], 256);
+        for (int b = 0; b < NBUF; ++b) {
+            mbar_init(&bars.d_full[b], 1);
+            mbar_init(&bars.d_empty[b], NEPI / 32);  // one arrival per epilogue warp
         }
         fence_barrier_init();
     }
-    if (warp == 9 && n_t > 0) {
-        tmem_alloc(&bars.taddr, TCOLS);
+    constexpr int W_PROD = NEPI / 32, W_MMA = NEPI / 32 + 1;
+    if (warp == W_MMA && n_t > 0) {
+        tmem_alloc(&bars.taddr, I_TMEM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -141,133 +191,199 @@ __global__ void __launch_bounds__(I_THREADS, 1)
     const uint32_t taddr = bars.taddr;
     const bool dead = bars.abort != 0;
 
-    if (warp == 8) {
+    if (warp == W_PROD) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0 && !dead && n_t > 0) {
             prefetch_tmap(&mK);
-            mbar_expect_tx(&bars.q_full, HI * IBM * 128);
-#pragma unroll
-            for (int h = 0; h < HI; ++h)
-                tma_load_2d(smem + SM_Q + h * IBM * 128, &mQ, &bars.q_full, h * IDI,
-                            (int32_t)row0);
             int issued = 0;
             for (int i = 0; i < n_t; ++i) {
                 const int s = i % NST;
                 if (i >= NST && !mbar_wait(&bars.k_empty[s], ((i - NST) / NST) & 1, abort))
                     break;
                 const int32_t y = (int32_t)(c0 + (int64_t)i * IBN);
-                uint8_t *kd = smem + SM_K + s * K_STAGE;
-                mbar_expect_tx(&bars.k_full[s], HI * IBN * 128);
+                uint8_t *kd = smem + s * C::STAGE;
+                mbar_expect_tx(&bars.k_full[s], C::STAGE);
 #pragma unroll
                 for (int h = 0; h < HI; ++h)
-                    tma_load_2d(kd + h * IBN * 128, &mK, &bars.k_full[s], h * IDI, y);
+                    tma_load_2d(kd + h * C::HEAD_BOX, &mK, &bars.k_full[s], h * IDI, y);
                 ++issued;
             }
             int dummy = 0;
             for (int i = max(0, issued - NST); i < issued; ++i)
                 mbar_wait(&bars.k_full[i % NST], (i / NST) & 1, &dummy, 400000000LL);
-            mbar_wait(&bars.q_full, 0, &dummy, 400000000LL);
         }
-    } else if (warp == 9) {
+    } else if (warp == W_MMA) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0 && !dead && n_t > 0) {
             constexpr uint32_t IDESC = idesc_bf16_f32(IBM, IBN, 0, 0);
-            const uint32_t q_base = smem_u32(smem + SM_Q);
             bool ok = mbar_wait(&bars.q_full, 0, abort);
+            tc_fence_after();
             for (int i = 0; ok && i < n_t; ++i) {
-                const int s = i % NST, bf = i & 1;
+                const int s = i % NST;
                 if (!mbar_wait(&bars.k_full[s], (i / NST) & 1, abort)) break;
-                if (i >= 2 && !mbar_wait(&bars.acc_empty[bf], ((i - 2) >> 1) & 1, abort)) break;
                 tc_fence_after();
-                const uint32_t k_base = smem_u32(smem + SM_K + s * K_STAGE);
-#pragma unroll
+                const uint32_t k_base = smem_u32(smem + s * C::STAGE);
+#pragma unroll 1
                 for (int h = 0; h < HI; ++h) {
+                    const int n = i * HI + h, b = n % NBUF;
+                    if (n >= NBUF && !mbar_wait(&bars.d_empty[b], ((n - NBUF) / NBUF) & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < IDI / 16; ++kk) {
-                        const uint64_t ad =
-                            sw128_desc(q_base + h * IBM * 128 + kk * 32, 16, 1024);
                         const uint64_t bd =
-                            sw128_desc(k_base + h * IBN * 128 + kk * 32, 16, 1024);
-                        mma_bf16(taddr + (uint32_t)(bf * HI * IBN + h * IBN), ad, bd, IDESC,
-                                 kk > 0);
+                            sw128_desc(k_base + h * C::HEAD_BOX + kk * 32, 16, 1024);
+                        mma_bf16_ta(taddr + C::D_COL0 + b * IBN, taddr + h * 32 + kk * 8, bd,
+                                    IDESC, kk > 0);
                     }
+                    mma_commit(&bars.d_full[b]);
                 }
-                mma_commit(&bars.acc_full[bf]);
                 mma_commit(&bars.k_empty[s]);
             }
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------ epilogue
-        const int quad = warp & 3, half = warp >> 2;
+        const int quad = warp & 3, part = warp >> 2;
         const int64_t row = row0 + quad * 32 + lane;
         const bool row_ok = row < a.Nq;
         const int64_t t = q_pos0 + (row_ok ? row : last_row);
         int64_t nv = n_vis(t, a.m);
         if (nv > a.Tc) nv = a.Tc;
+        const int64_t nvr = (nv + a.stride - 1) / a.stride;  // this row's visible map entries
         float wh[HI];
 #pragma unroll
         for (int h = 0; h < HI; ++h) wh[h] = row_ok ? __ldg(a.w + row * HI + h) : 0.f;
-        uint32_t theta = 0;
-        if (MODE == MODE_FILTER && row_ok) theta = __ldg(a.theta + row);
-        const uint32_t lane_addr = taddr + ((uint32_t)(quad * 32) << 16) + half * 16;
+        float thf = 0.f;
+        if (MODE == MODE_FILTER) thf = row_ok ? key_to_float(__ldg(a.theta + row)) : INFINITY;
+        const uint32_t lane_addr = taddr + ((uint32_t)(quad * 32) << 16);
+        const uint32_t buf_addr = lane_addr + C::D_COL0 + part * EPI_COLS;
         bool ok = !dead;
-        for (int i = 0; ok && i < n_t; ++i) {
-            const int bf = i & 1;
-            if (!__all_sync(FULL, mbar_wait(&bars.acc_full[bf], (i >> 1) & 1, abort))) {
-                ok = false;
-                break;
+        if (n_t > 0 && ok) {
+            // q_I rows into TMEM: this thread's row, heads part*HI/4 ..
+#pragma unroll 1
+            for (int hh = 0; hh < HI / 4; ++hh) {
+                const int h = part * (HI / 4) + hh;
+                uint32_t r[32];
+                if (row_ok) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(a.qI + (row * HI + h) * IDI);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const uint4 x = __ldg(src + u);
+                        r[4 * u] = x.x;
+                        r[4 * u + 1] = x.y;
+                        r[4 * u + 2] = x.z;
+                        r[4 * u + 3] = x.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) r[u] = 0u;
+                }
+                tmem_st32_u(lane_addr + h * 32, r);
             }
-            tc_fence_after();
-            float acc[16];
-#pragma unroll
-            for (int c = 0; c < 16; ++c) acc[c] = 0.f;
-#pragma unroll
-            for (int h0 = 0; h0 < HI; h0 += 4) {
-                float v[4][16];
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    tmem_ld16(lane_addr + (uint32_t)(bf * HI * IBN + (h0 + u) * IBN), v[u]);
-                tmem_wait_ld();
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-#pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        acc[c] = fmaf(wh[h0 + u], fmaxf(v[u][c], 0.f), acc[c]);
-            }
+            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&bars.acc_empty[bf]);
-            const int64_t e0 = c0 + (int64_t)i * IBN + half * 16;  // map entry of acc[0]
-            if (!row_ok) continue;
-            if (MODE == MODE_MATERIALIZE) {
-                float *dst = a.out + row * a.ld;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.q_full);
+        }
+        float *stg = reinterpret_cast<float *>(smem + C::SM_STG) + tid * EPI_COLS;
+        const int n_all = n_t * HI;  // score buffers this CTA consumes
+        // v[n & 1] holds head n; head n+1 is loaded while head n is folded
+        float v[2][EPI_COLS];
+        if (ok && n_all > 0) {
+            if (!__all_sync(FULL, mbar_wait(&bars.d_full[0], 0, abort))) {
+                ok = false;
+            } else {
+                tc_fence_after();
+                tmem_ld16(buf_addr, v[0]);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars.d_empty[0]);
+            }
+        }
+        for (int i = 0; ok && i < n_t; ++i) {
+            float2 acc[EPI_COLS / 2];
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const int64_t e = e0 + c;
-                    if (e < c_end) dst[e] = (e * a.stride < nv) ? acc[c] : -INFINITY;
+            for (int c = 0; c < EPI_COLS / 2; ++c) acc[c] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int h = 0; h < HI; ++h) {
+                const int n = i * HI + h, nb = (n + 1) % NBUF;
+                const bool more = n + 1 < n_all;
+                if (more) {
+                    if (!__all_sync(FULL, mbar_wait(&bars.d_full[nb], ((n + 1) / NBUF) & 1, abort))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    tmem_ld16(buf_addr + nb * IBN, v[(h + 1) & 1]);
+                }
+                const float2 w2 = make_float2(wh[h], wh[h]);
+#pragma unroll
+                for (int c = 0; c < EPI_COLS / 2; ++c)
+                    acc[c] = __ffma2_rn(w2, make_float2(fmaxf(v[h & 1][2 * c], 0.f),
+                                                        fmaxf(v[h & 1][2 * c + 1], 0.f)),
+                                        acc[c]);
+                if (more) {
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars.d_empty[nb]);
+                }
+            }
+            if (!ok) break;
+            if (!row_ok) continue;
+            const int64_t e0 = c0 + (int64_t)i * IBN + part * EPI_COLS;  // map entry of column 0
+            if (MODE == MODE_MATERIALIZE) {
+                float *dst = a.out + row * a.ld + e0;
+                const int64_t vis = nvr - e0, lim = c_end - e0;
+                if (a.vec_out && vis >= EPI_COLS && lim >= EPI_COLS) {
+#pragma unroll
+                    for (int u = 0; u < EPI_COLS / 4; ++u)
+                        reinterpret_cast<float4 *>(dst)[u] =
+                            make_float4(acc[2 * u].x, acc[2 * u].y, acc[2 * u + 1].x,
+                                        acc[2 * u + 1].y);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < EPI_COLS; ++c) {
+                        const float s = (c & 1) ? acc[c >> 1].y : acc[c >> 1].x;
+                        if (c < lim) dst[c] = c < vis ? s : -INFINITY;
+                    }
                 }
             } else {
-                uint32_t keys[16];
-                uint32_t selm = 0;
+                // bit c of `below` (after the reversal) = column c is under theta
+                const float2 nt = make_float2(-thf, -thf);
+                uint32_t below = 0;
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const int64_t e = e0 + c;
-                    keys[c] = order_key(acc[c]);
-                    if (e < nv && keys[c] >= theta) selm |= 1u << c;
+                for (int c = 0; c < EPI_COLS / 2; ++c) {
+                    const float2 d = __fadd2_rn(acc[c], nt);
+                    below = __funnelshift_l(__float_as_uint(d.x), below, 1);
+                    below = __funnelshift_l(__float_as_uint(d.y), below, 1);
                 }
-                if (selm) {
-                    int base = atomicAdd(a.count + row, __popc(selm));
+                uint32_t cand = __brev(~below) >> (32 - EPI_COLS);
+                const int64_t lim = min(nvr, c_end) - e0;
+                if (lim < EPI_COLS) cand &= lim <= 0 ? 0u : ((1u << lim) - 1u);
+                if (cand) {
+                    // stage the row's scores so a candidate can be read by column
+                    const int sw = lane & 3;
+#pragma unroll
+                    for (int u = 0; u < EPI_COLS / 4; ++u)
+                        reinterpret_cast<float4 *>(stg)[u ^ sw] =
+                            make_float4(acc[2 * u].x, acc[2 * u].y, acc[2 * u + 1].x,
+                                        acc[2 * u + 1].y);
+                    int base = atomicAdd(a.count + row, __popc(cand));
                     uint32_t *ck = a.cand_key + row * a.cap;
                     int32_t *ci = a.cand_idx + row * a.cap;
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        if (selm & (1u << c)) {
-                            if (base < a.cap) {
-                                ck[base] = keys[c];
-                                ci[base] = (int32_t)(e0 + c);
-                            }
-                            ++base;
+                    while (cand) {
+                        const int c = __ffs(cand) - 1;
+                        cand &= cand - 1;
+                        if (base < a.cap) {
+                            ck[base] = order_key(stg[(((c >> 2) ^ sw) << 2) | (c & 3)]);
+                            ci[base] = (int32_t)(e0 + c);
                         }
+                        ++base;
                     }
                 }
             }
@@ -275,16 +391,16 @@ __global__ void __launch_bounds__(I_THREADS, 1)
         if (!ok) {
             if (row_ok) flag(a.dev_err, LC_DEVERR_TIMEOUT);
         } else if (MODE == MODE_MATERIALIZE && row_ok) {
-            // columns of this CTA past the last visible entry
+            // columns of this CTA past the last computed tile
             float *dst = a.out + row * a.ld;
-            for (int64_t e = max(c0, comp_end) + half; e < c_end; e += 2) dst[e] = -INFINITY;
+            for (int64_t e = max(c0, comp_end) + part; e < c_end; e += 4) dst[e] = -INFINITY;
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 9 && n_t > 0) {
+    if (warp == W_MMA && n_t > 0) {
         tc_fence_after();
-        tmem_dealloc(taddr, TCOLS);
+        tmem_dealloc(taddr, I_TMEM_COLS);
     }
 }
 
@@ -517,9 +633,9 @@ bool index_tc_eligible(const void *qI, const void *kI, const lc_batch &b, int HI
 }
 
 template <int MODE, int HI>
-lc_status launch_tc(const CUtensorMap &mQ, const CUtensorMap &mK, const IdxTcArgs &a,
-                    int64_t n_cols, cudaStream_t st) {
-    constexpr uint32_t SMEM = HI * IBM * 128 + (HI == 8 ? 3 : 6) * HI * IBN * 128 + 256;
+lc_status launch_tc(const CUtensorMap &mK, const IdxTcArgs &a, int64_t n_cols, cudaStream_t st) {
+    constexpr uint32_t SMEM = IdxCfg<HI>::SMEM;
+    static_assert(SMEM <= 227 * 1024, "indexer shared memory");
     auto kfn = k_index_tc<MODE, HI>;
     static bool attr = false;
     if (!attr) {
@@ -531,15 +647,14 @@ lc_status launch_tc(const CUtensorMap &mQ, const CUtensorMap &mK, const IdxTcArg
     const int64_t gy = (n_cols + a.chunk - 1) / a.chunk;
     if (gy < 1 || gy > 65535) return LC_ERR_UNSUPPORTED;
     dim3 grid((unsigned)((a.Nq + IBM - 1) / IBM), (unsigned)gy);
-    LC_LAUNCH(kfn, grid, dim3(I_THREADS), SMEM, st, mQ, mK, a);
+    LC_LAUNCH(kfn, grid, dim3(I_THREADS), SMEM, st, mK, a);
     return check_launch();
 }
 
 template <int MODE>
-lc_status launch_tc_hi(int HI, const CUtensorMap &mQ, const CUtensorMap &mK,
-                       const IdxTcArgs &a, int64_t n_cols, cudaStream_t st) {
-    return HI == 8 ? launch_tc<MODE, 8>(mQ, mK, a, n_cols, st)
-                   : launch_tc<MODE, 4>(mQ, mK, a, n_cols, st);
+lc_status launch_tc_hi(int HI, const CUtensorMap &mK, const IdxTcArgs &a, int64_t n_cols,
+                       cudaStream_t st) {
+    return HI == 8 ? launch_tc<MODE, 8>(mK, a, n_cols, st) : launch_tc<MODE, 4>(mK, a, n_cols, st);
 }
 
 // entries per CTA: about eight waves of CTAs over the 148 SMs
@@ -554,9 +669,11 @@ int64_t pick_chunk(int64_t Nq, int64_t n_cols) {
     return chunk;
 }
 
-IdxTcArgs base_args(const lc_batch &b, const float *w, int m, int32_t *dev_err) {
+IdxTcArgs base_args(const lc_batch &b, const void *qI, const float *w, int m,
+                    int32_t *dev_err) {
     IdxTcArgs a{};
     a.Nq = b.total_q;
+    a.qI = static_cast<const __nv_bfloat16 *>(qI);
     a.q_pos0 = b.q_pos0;
     a.Tc = b.max_c;
     a.stride = 1;
@@ -577,19 +694,18 @@ lc_status index_tc_materialize(const void *qI, const float *w, const void *kI, c
                                int HI, int dI, int m, lc_dtype dt, float *scores, int64_t ld,
                                int32_t *dev_err, cudaStream_t st) {
     if (!index_tc_eligible(qI, kI, b, HI, dI, dt)) return LC_ERR_UNSUPPORTED;
-    CUtensorMap mQ, mK;
-    if (!make_tmap_bf16_2d(&mQ, qI, (uint64_t)b.total_q, (uint64_t)HI * IDI, HI * IDI * 2, IDI,
-                           IBM) ||
-        !make_tmap_bf16_2d(&mK, kI, (uint64_t)b.total_c, (uint64_t)HI * IDI, HI * IDI * 2, IDI,
+    CUtensorMap mK;
+    if (!make_tmap_bf16_2d(&mK, kI, (uint64_t)b.total_c, (uint64_t)HI * IDI, HI * IDI * 2, IDI,
                            IBN))
         return LC_ERR_CUDA;
-    IdxTcArgs a = base_args(b, w, m, dev_err);
+    IdxTcArgs a = base_args(b, qI, w, m, dev_err);
     a.Tc = b.total_c;
     a.col_end = ld;
     a.out = scores;
     a.ld = ld;
+    a.vec_out = (reinterpret_cast<uintptr_t>(scores) & 15u) == 0 && (ld & 3) == 0;
     a.chunk = pick_chunk(b.total_q, ld);
-    return launch_tc_hi<MODE_MATERIALIZE>(HI, mQ, mK, a, ld, st);
+    return launch_tc_hi<MODE_MATERIALIZE>(HI, mK, a, ld, st);
 }
 
 // Fused exact top-k on the tensor cores (ws holds the plan's buffers), or
@@ -612,23 +728,23 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
     const int64_t Tc = b.total_c;
     const uint64_t pitch = (uint64_t)HI * IDI * 2;
 
-    CUtensorMap mQ, mKs, mK;
-    if (!make_tmap_bf16_2d(&mQ, qI, (uint64_t)b.total_q, (uint64_t)HI * IDI, pitch, IDI, IBM) ||
-        !make_tmap_bf16_2d(&mK, kI, (uint64_t)Tc, (uint64_t)HI * IDI, pitch, IDI, IBN) ||
+    CUtensorMap mKs, mK;
+    if (!make_tmap_bf16_2d(&mK, kI, (uint64_t)Tc, (uint64_t)HI * IDI, pitch, IDI, IBN) ||
         !make_tmap_bf16_2d(&mKs, kI, (uint64_t)((Tc + p.stride - 1) / p.stride),
                            (uint64_t)HI * IDI, pitch * p.stride, IDI, IBN))
         return LC_ERR_CUDA;
     lc_status s;
     // 1. sampled scores
     {
-        IdxTcArgs a = base_args(b, w, m, dev_err);
+        IdxTcArgs a = base_args(b, qI, w, m, dev_err);
         a.Tc = Tc;
         a.stride = p.stride;
         a.col_end = p.ns;
         a.out = samp;
         a.ld = p.lds;
+        a.vec_out = 1;  // 256-byte aligned buffer, ld a multiple of 4
         a.chunk = pick_chunk(b.total_q, p.ns);
-        s = launch_tc_hi<MODE_MATERIALIZE>(HI, mQ, mKs, a, p.ns, st);
+        s = launch_tc_hi<MODE_MATERIALIZE>(HI, mKs, a, p.ns, st);
         if (s != LC_OK) return s;
     }
     // 2. thresholds
@@ -637,7 +753,7 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
     if ((s = check_launch()) != LC_OK) return s;
     // 3. candidates
     {
-        IdxTcArgs a = base_args(b, w, m, dev_err);
+        IdxTcArgs a = base_args(b, qI, w, m, dev_err);
         a.Tc = Tc;
         a.theta = theta;
         a.count = count;
@@ -645,7 +761,7 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
         a.cand_idx = cidx;
         a.cap = p.cap;
         a.chunk = pick_chunk(b.total_q, Tc);
-        s = launch_tc_hi<MODE_FILTER>(HI, mQ, mK, a, Tc, st);
+        s = launch_tc_hi<MODE_FILTER>(HI, mK, a, Tc, st);
         if (s != LC_OK) return s;
     }
     // 4. exact selection among candidates: bitmap compaction when the row's
