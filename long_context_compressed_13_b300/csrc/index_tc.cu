@@ -8,9 +8,11 @@
 //   feeds the B operand (the entries' keys): 64 B per tensor-core clock.
 //   warp 16     TMA producer: k_I tiles of 64 entries x H_I heads into a
 //               ring of shared-memory stages
-//   warp 17     TMEM owner and MMA issuer: per tile, head by head, one
-//               M=128, N=64, K=64 product q_h k_h^T into a ring of four
-//               64-column TMEM buffers
+//   warps 17-18 MMA issuers (warp 17 also owns TMEM): per tile, head by
+//               head, one M=128, N=64, K=64 product q_h k_h^T into a ring of
+//               four 64-column TMEM buffers; warp 17 issues the even heads and
+//               warp 18 the odd ones, so the short tensor-core queue stays fed
+//               while the other issuer waits on a barrier
 //   warps 0-15  epilogue: warp w owns TMEM lanes 32(w%4).. (its query rows)
 //               and columns 16(w/4).. of each buffer; it folds the heads in
 //               order, acc = fma(w_h, max(s_h, 0), acc), two columns per
@@ -52,7 +54,7 @@ constexpr int IBM = 128;          // query rows per CTA
 constexpr int IBN = 64;           // entries per tile
 constexpr int IDI = 64;           // indexer head dim
 constexpr int NEPI = 512;         // epilogue threads (16 warps)
-constexpr int I_THREADS = NEPI + 64;  // + producer warp + MMA warp
+constexpr int I_THREADS = NEPI + 96;  // + producer warp + two MMA warps
 constexpr int EPI_COLS = 16;      // columns of a score buffer per epilogue thread
 constexpr int NBUF = 4;           // TMEM score buffers (one head each)
 constexpr uint32_t I_TMEM_COLS = 512;
@@ -172,7 +174,7 @@ __global__ void __launch_bounds__(I_THREADS, 1)
         mbar_init(&bars.q_full, NEPI / 32);
         for (int s = 0; s < NST; ++s) {
             mbar_init(&bars.k_full[s], 1);
-            mbar_init(&bars.k_empty[s], 1);
+            mbar_init(&bars.k_empty[s], 2);  // one commit per MMA issuer
         }
         for (int b = 0; b < NBUF; ++b) {
             mbar_init(&bars.d_full[b], 1);
@@ -180,7 +182,7 @@ __global__ void __launch_bounds__(I_THREADS, 1)
         }
         fence_barrier_init();
     }
-    constexpr int W_PROD = NEPI / 32, W_MMA = NEPI / 32 + 1;
+    constexpr int W_PROD = NEPI / 32, W_MMA = NEPI / 32 + 1, W_MMA2 = NEPI / 32 + 2;
     if (warp == W_MMA && n_t > 0) {
         tmem_alloc(&bars.taddr, I_TMEM_COLS);
         tmem_relinquish();
@@ -212,8 +214,9 @@ __global__ void __launch_bounds__(I_THREADS, 1)
             for (int i = max(0, issued - NST); i < issued; ++i)
                 mbar_wait(&bars.k_full[i % NST], (i / NST) & 1, &dummy, 400000000LL);
         }
-    } else if (warp == W_MMA) {
-        // ------------------------------------------------------ MMA issuer
+    } else if (warp == W_MMA || warp == W_MMA2) {
+        // ------------------------------------------------------ MMA issuers
+        const int par = warp - W_MMA;  // heads h with h % 2 == par
         if (lane == 0 && !dead && n_t > 0) {
             constexpr uint32_t IDESC = idesc_bf16_f32(IBM, IBN, 0, 0);
             bool ok = mbar_wait(&bars.q_full, 0, abort);
@@ -224,7 +227,7 @@ __global__ void __launch_bounds__(I_THREADS, 1)
                 tc_fence_after();
                 const uint32_t k_base = smem_u32(smem + s * C::STAGE);
 #pragma unroll 1
-                for (int h = 0; h < HI; ++h) {
+                for (int h = par; h < HI; h += 2) {
                     const int n = i * HI + h, b = n % NBUF;
                     if (n >= NBUF && !mbar_wait(&bars.d_empty[b], ((n - NBUF) / NBUF) & 1, abort)) {
                         ok = false;
@@ -289,49 +292,56 @@ __global__ void __launch_bounds__(I_THREADS, 1)
             if (lane == 0) mbar_arrive(&bars.q_full);
         }
         float *stg = reinterpret_cast<float *>(smem + C::SM_STG) + tid * EPI_COLS;
+        float2 acc[EPI_COLS / 2];
         const int n_all = n_t * HI;  // score buffers this CTA consumes
-        // v[n & 1] holds head n; head n+1 is loaded while head n is folded
+        // Heads are consumed in pairs: v[0], v[1] hold heads n, n+1.  The
+        // barriers of the next pair are tested (without blocking) before the
+        // current pair is folded, so their latency overlaps the arithmetic;
+        // both buffers of a pair are read with one TMEM wait.
         float v[2][EPI_COLS];
-        if (ok && n_all > 0) {
-            if (!__all_sync(FULL, mbar_wait(&bars.d_full[0], 0, abort))) {
-                ok = false;
-            } else {
-                tc_fence_after();
-                tmem_ld16(buf_addr, v[0]);
-                tmem_wait_ld();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars.d_empty[0]);
-            }
-        }
+        bool ready = false;  // the next pair's barriers were seen complete
         for (int i = 0; ok && i < n_t; ++i) {
-            float2 acc[EPI_COLS / 2];
 #pragma unroll
             for (int c = 0; c < EPI_COLS / 2; ++c) acc[c] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int h = 0; h < HI; ++h) {
-                const int n = i * HI + h, nb = (n + 1) % NBUF;
-                const bool more = n + 1 < n_all;
-                if (more) {
-                    if (!__all_sync(FULL, mbar_wait(&bars.d_full[nb], ((n + 1) / NBUF) & 1, abort))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    tmem_ld16(buf_addr + nb * IBN, v[(h + 1) & 1]);
+            for (int h = 0; h < HI; h += 2) {
+                const int n = i * HI + h;
+                // ---- load the pair (n, n+1) and free its buffers
+                const int b0 = n % NBUF, b1 = (n + 1) % NBUF;
+                if (!ready &&
+                    !__all_sync(FULL, mbar_wait(&bars.d_full[b0], (n / NBUF) & 1, abort) &&
+                                          mbar_wait(&bars.d_full[b1], ((n + 1) / NBUF) & 1, abort))) {
+                    ok = false;
+                    break;
                 }
-                const float2 w2 = make_float2(wh[h], wh[h]);
+                tc_fence_after();
+                tmem_ld16(buf_addr + b0 * IBN, v[0]);
+                tmem_ld16(buf_addr + b1 * IBN, v[1]);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bars.d_empty[b0]);
+                    mbar_arrive(&bars.d_empty[b1]);
+                }
+                // ---- early, non-blocking look at the next pair's barriers;
+                // the verdict is taken after the fold
+                const bool more = n + 2 < n_all;
+                bool t_next = more;
+                if (more)
+                    t_next = mbar_test(&bars.d_full[(n + 2) % NBUF], ((n + 2) / NBUF) & 1) &
+                             mbar_test(&bars.d_full[(n + 3) % NBUF], ((n + 3) / NBUF) & 1);
+                // ---- fold the pair into the tile's scores
 #pragma unroll
-                for (int c = 0; c < EPI_COLS / 2; ++c)
-                    acc[c] = __ffma2_rn(w2, make_float2(fmaxf(v[h & 1][2 * c], 0.f),
-                                                        fmaxf(v[h & 1][2 * c + 1], 0.f)),
-                                        acc[c]);
-                if (more) {
-                    tmem_wait_ld();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars.d_empty[nb]);
+                for (int u = 0; u < 2; ++u) {
+                    const float2 w2 = make_float2(wh[h + u], wh[h + u]);
+#pragma unroll
+                    for (int c = 0; c < EPI_COLS / 2; ++c)
+                        acc[c] = __ffma2_rn(w2, make_float2(fmaxf(v[u][2 * c], 0.f),
+                                                            fmaxf(v[u][2 * c + 1], 0.f)),
+                                            acc[c]);
                 }
+                ready = more && __all_sync(FULL, t_next);
             }
             if (!ok) break;
             if (!row_ok) continue;
