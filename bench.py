@@ -14,6 +14,12 @@ Entries of the positions before the chunk come from the same compressors in
 an untimed set-up (they are the layer's KV cache).  Metric: query tokens per
 second (4096 per step per GPU).
 
+With --workload csa_decode a step is instead one decode step of 64
+sequences (one query each at its last position, contexts ~U[65536, 262144],
+compressed caches and indexer keys resident): lightning_index fused with
+topk_select (k=1024) -> sparse_mqa_attn (128 heads x 128, window 128).  Its
+roofline is HBM bandwidth (the indexer streams every visible indexer key).
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload layer_pair_1m|csa_decode]
 
@@ -202,6 +208,37 @@ class LayerPair:
     STAGES = ["csa_compress", "lightning_index+topk", "sparse_mqa_attn", "hca_compress",
               "hca_dense_attn"]
 
+    def config(self, world):
+        return {"workload": f"layer_pair_{self.ctx // 1024}k: CSA (m=4, indexer 8x64, top-k "
+                            f"1024, window 128) + HCA (m'=128, window 128) over a "
+                            f"{self.ctx:,}-token context, last {self.chunk} positions queried, "
+                            f"Q [{self.chunk},128,128] per layer",
+                "context": self.ctx, "query_chunk": self.chunk, "heads": self.H,
+                "head_dim": self.d, "parallelism": f"replicas x{world}",
+                "l2": "inputs larger than L2 (raw K/V 256 MiB each, indexer keys 256 MiB)"}
+
+    def roofline(self, stage_ms, peaks, region_ms):
+        """Tensor roofline of the stage with the longest time."""
+        work = self.work()
+        flops_of = {"lightning_index+topk": work["index_flop"],
+                    "sparse_mqa_attn": work["csa_attn_flop"],
+                    "hca_dense_attn": work["hca_attn_flop"]}
+        dom = max(flops_of, key=lambda s: stage_ms[self.STAGES.index(s)])
+        dom_ms = stage_ms[self.STAGES.index(dom)]
+        achieved = flops_of[dom] / (dom_ms / 1e3) / 1e12
+        long_region = region_ms > 1000.0
+        peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
+        return {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                "peak_source": peaks["source"] + (" sustained" if long_region else " burst")}
+
+    def path_tflops(self, ms_step):
+        w = self.work()
+        return (w["index_flop"] + w["csa_attn_flop"] + w["hca_attn_flop"]) / (ms_step / 1e3) / 1e12
+
+    def cpu_baseline(self, budget_s):
+        return cpu_baseline(self, budget_s=budget_s)
+
     # per-step host inputs / outputs of the end-to-end measurement
     def host_io(self):
         c, h = self.P["csa"], self.P["hca"]
@@ -214,6 +251,84 @@ class LayerPair:
         }
         outs = {"O_csa": self.O_csa, "O_hca": self.O_hca}
         return ins, outs
+
+
+class Decode:
+    """Device buffers and the step of the batch-64 CSA decode workload."""
+
+    STAGES = ["lightning_index+topk", "sparse_mqa_attn"]
+
+    def __init__(self, lc, device, seed=3):
+        self.lc = lc
+        D = wl.csa_decode(B=64, ctx_lo=65536, ctx_hi=262144, H=128, d=128, HI=8, dI=64, m=4,
+                          k=1024, W=128, dtype="bf16", seed=seed, device=device)
+        self.D = D
+        self.chunk = D["B"]  # query tokens per step
+        self.m, self.k, self.W, self.H, self.d = D["m"], D["k"], D["W"], D["H"], D["d"]
+        self.b = lc.DeviceBatch.from_workload(D["batch"], device=device)
+        self.ws = torch.empty(lc.workspace_size(lc.LC_OP_LIGHTNING_INDEX, self.b, HI=D["HI"],
+                                                dI=D["dI"], k=self.k),
+                              dtype=torch.uint8, device=device)
+        self.sel = torch.empty((D["B"], self.k), dtype=torch.int32, device=device)
+        self.O = torch.empty_like(D["Q"])
+        self.lse = torch.empty((D["B"], self.H), dtype=torch.float32, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        torch.cuda.synchronize()
+
+    def work(self):
+        D = self.D
+        ctx = np.array(D["ctx"], dtype=np.int64)
+        nv = ctx // self.m
+        nwin = np.minimum(ctx, self.W)
+        keys = np.minimum(nv, self.k) + nwin
+        idx_bytes = float(nv.sum() * D["HI"] * D["dI"] * 2 + D["B"] * D["HI"] * (D["dI"] * 2 + 4)
+                          + D["B"] * self.k * 4)
+        attn_bytes = float(keys.sum() * self.d * 2 * 2 + 2 * D["B"] * self.H * self.d * 2
+                           + D["B"] * self.k * 4)
+        return {"index_bytes": idx_bytes, "attn_bytes": attn_bytes,
+                "attn_flop": float(4 * self.d * self.H * keys.sum())}
+
+    def step(self, events=None):
+        lc, D = self.lc, self.D
+        ev = events
+        if ev:
+            ev[0].record()
+        lc.lightning_index(D["qI"], D["w"], D["kI"], self.b, self.m, scores=False, k=self.k,
+                           topk=self.sel, ws=self.ws, dev_err=self.err)
+        if ev:
+            ev[1].record()
+        lc.sparse_mqa_attn(D["Q"], D["Kc"], D["Vc"], self.sel, D["Kraw"], D["Vraw"], self.b,
+                           self.m, self.W, D["scale"], O=self.O, lse=self.lse, dev_err=self.err)
+        if ev:
+            ev[2].record()
+
+    def host_io(self):
+        D = self.D
+        ins = {"Q": D["Q"], "qI": D["qI"], "w": D["w"]}
+        return ins, {"O": self.O}
+
+    def config(self, world):
+        return {"workload": "csa_decode: 64 sequences, one query token each at its last "
+                            "position, contexts ~U[65536, 262144] (seed 3), CSA m=4, indexer "
+                            "8x64, top-k 1024, window 128, Q [64,128,128]",
+                "batch": self.D["B"], "heads": self.H, "head_dim": self.d,
+                "context_mean": float(np.mean(self.D["ctx"])),
+                "parallelism": f"replicas x{world}",
+                "l2": "inputs larger than L2 (indexer keys 2.7 GB, compressed K/V 1.3 GB)"}
+
+    def path_tflops(self, ms_step):
+        return self.work()["attn_flop"] / (ms_step / 1e3) / 1e12
+
+    def cpu_baseline(self, budget_s):
+        return decode_cpu_baseline(self, budget_s=budget_s)
+
+    def roofline(self, stage_ms, peaks, region_ms):
+        w = self.work()
+        ms = stage_ms[self.STAGES.index("lightning_index+topk")]
+        gbs = w["index_bytes"] / (ms / 1e3) / 1e9
+        return {"bound": "hbm", "kernel": "lightning_index+topk", "achieved": gbs,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                "traffic": None, "peak_source": peaks["source"]}
 
 
 # ---------------------------------------------------------------- our arm
@@ -234,14 +349,14 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device(device))
     peaks = load_peaks()
 
-    wk = LayerPair(lc, device, ctx=args.ctx)
+    wk = Decode(lc, device) if args.workload == "csa_decode" else LayerPair(lc, device, ctx=args.ctx)
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
         wk.step()
     torch.cuda.synchronize()
 
     # ---- device-timed region
-    nst = len(LayerPair.STAGES)
+    nst = len(wk.STAGES)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
@@ -300,35 +415,17 @@ def run_ours(args):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_s = float(tt.item())
 
-    work = wk.work()
     tokens = wk.chunk * world
     ms_step = ms / args.steps
     value = tokens / (ms_step / 1e3)
-    # dominant kernel -> roofline
-    flops_of = {"lightning_index+topk": work["index_flop"], "sparse_mqa_attn": work["csa_attn_flop"],
-                "hca_dense_attn": work["hca_attn_flop"]}
-    dom = max(flops_of, key=lambda s: stage_ms[LayerPair.STAGES.index(s)])
-    dom_ms = stage_ms[LayerPair.STAGES.index(dom)]
-    achieved = flops_of[dom] / (dom_ms / 1e3) / 1e12
-    long_region = ms > 1000.0
-    peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
-    total_flop = work["index_flop"] + work["csa_attn_flop"] + work["hca_attn_flop"]
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"layer_pair_{wk.ctx // 1024}k: CSA (m=4, indexer 8x64, top-k "
-                               f"1024, window 128) + HCA (m'=128, window 128) over a "
-                               f"{wk.ctx:,}-token context, last {wk.chunk} positions queried, "
-                               f"Q [{wk.chunk},128,128] per layer",
-                   "context": wk.ctx, "query_chunk": wk.chunk, "heads": wk.H, "head_dim": wk.d,
-                   "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (raw K/V 256 MiB each, indexer keys 256 MiB)"},
-        "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
-                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
-                     "peak_source": peaks["source"] + (" sustained" if long_region else " burst")},
-        "stages_ms": dict(zip(LayerPair.STAGES, stage_ms)),
-        "path_tflops": total_flop / (ms_step / 1e3) / 1e12,
+        "config": wk.config(world),
+        "roofline": wk.roofline(stage_ms, peaks, ms),
+        "stages_ms": dict(zip(wk.STAGES, stage_ms)),
+        "path_tflops": wk.path_tflops(ms_step),
         "e2e": {"value": tokens / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
@@ -336,7 +433,7 @@ def run_ours(args):
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(wk, budget_s=args.cpu_budget)
+        out["cpu_baseline"] = wk.cpu_baseline(args.cpu_budget)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if dist:
@@ -408,6 +505,35 @@ def cpu_baseline(wk, budget_s=20.0):
                       f"built untimed", "seconds": dt}
 
 
+def decode_cpu_baseline(wk, budget_s=20.0):
+    """The oracle on whole sequences of the decode batch (index over every
+    visible entry, top-k, CSA attention), as many as fit the time budget."""
+    import oracle
+    D = wk.D
+    B = D["B"]
+    cu_c, cu_raw = D["batch"].cu_c, D["batch"].cu_raw
+    host = {k: D[k].cpu() for k in ("Q", "Kc", "Vc", "Kraw", "Vraw", "qI", "kI", "w")}
+    done, t_used = 0, 0.0
+    for b in range(B):
+        c0, c1, r0, r1 = cu_c[b], cu_c[b + 1], cu_raw[b], cu_raw[b + 1]
+        t = np.array([D["ctx"][b] - 1], dtype=np.int64)
+        kI = host["kI"][c0:c1].double().numpy()
+        Kc = host["Kc"][c0:c1].double().numpy()
+        Vc = host["Vc"][c0:c1].double().numpy()
+        t0 = time.perf_counter()
+        I = oracle.index(host["qI"][b:b + 1], host["w"][b:b + 1], kI, t, wk.m)
+        sel = oracle.topk(I, (t + 1) // wk.m, wk.k)
+        oracle.sparse_attn(host["Q"][b:b + 1], Kc, Vc, sel, host["Kraw"][r0:r1],
+                           host["Vraw"][r0:r1], D["batch"].raw_pos0[b], t, wk.W, D["scale"])
+        t_used += time.perf_counter() - t0
+        done += 1
+        if t_used > budget_s:
+            break
+    return {"value": done / t_used, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{done} of the 64 decode sequences (whole sequences: index over every "
+                      f"visible entry, top-k 1024, CSA attention, fp64)", "seconds": t_used}
+
+
 def run_reference(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -455,6 +581,7 @@ def main():
     # a shorter context keeps the same kernels on a smaller case (profiler
     # captures); the measured workload is the default 1,048,576 tokens
     ap.add_argument("--ctx", type=int, default=1 << 20)
+    ap.add_argument("--workload", default="layer_pair_1m", choices=["layer_pair_1m", "csa_decode"])
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

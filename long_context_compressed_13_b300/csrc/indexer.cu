@@ -7,7 +7,11 @@
 //                  head at a time.
 //   k_index_scan   few rows per sequence (decode): one row per grid.y, each
 //                  thread streams one (entry, head) slice of kI with 16-byte
-//                  loads; HBM-bound.
+//                  loads (fp32 keys, d_I = 32 or H_I < 4);
+//   k_index_stream the same rows for bf16 keys with d_I = 64, H_I in {4, 8}:
+//                  coalesced 512-byte warp loads, HBM-bound.
+#include <type_traits>
+
 #include "lc_common.cuh"
 
 namespace lc {
@@ -163,6 +167,122 @@ __global__ void __launch_bounds__(256) k_index_scan(const T *__restrict__ qI,
     }
 }
 
+// Decode-shaped streaming indexer for bf16 keys with d_I = 64 and H_I in {4, 8}:
+// one CTA per (query row, range of entries).  An entry's keys are H_I x 128 B;
+// a warp reads them as H_I/4 instructions of 512 contiguous bytes (4 heads),
+// lane = (head g within the four, 16-byte slice sl of the head).  Each lane
+// keeps the matching 8 q_I values per head in registers, so the dot product
+// is 8 FMAs per lane and load, reduced over the 8 lanes of a head and then
+// over the heads with shuffles.  Lane i keeps the score of the i-th entry of
+// each 32-entry block, which the warp stores with one coalesced write.
+// Columns [n_vis, ld) get -inf.
+template <int HI>
+__global__ void __launch_bounds__(256) k_index_stream(const __nv_bfloat16 *__restrict__ qI,
+                                                      const float *__restrict__ w,
+                                                      const __nv_bfloat16 *__restrict__ kI,
+                                                      Batch bt, int m, float *__restrict__ scores,
+                                                      int64_t ld, int64_t chunk,
+                                                      const int32_t *__restrict__ row_mask,
+                                                      int32_t *dev_err) {
+    constexpr int L = HI / 4;  // 512-byte loads per entry
+    const int64_t r = blockIdx.y;
+    if (row_mask && row_mask[r] == 0) return;
+    const int b = seq_of_row(bt, r);
+    const int64_t t = bt.q_pos0[b] + (r - bt.cu_q[b]);
+    const int64_t c_beg = bt.cu_c[b], Tc = bt.cu_c[b + 1] - c_beg;
+    int64_t nv = n_vis(t, m);
+    if (nv > Tc) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) flag(dev_err, LC_DEVERR_BATCH);
+        nv = Tc;
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 3, sl = lane & 7;
+    float q[L][8], wl[L];
+#pragma unroll
+    for (int l = 0; l < L; ++l) {
+        const int h = 4 * l + g;
+        const uint4 x = __ldg(reinterpret_cast<const uint4 *>(qI + (r * HI + h) * 64 + sl * 8));
+        const uint32_t u[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            q[l][2 * i] = __uint_as_float(u[i] << 16);
+            q[l][2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+        }
+        wl[l] = __ldg(w + r * HI + h);
+    }
+    const int64_t e_lo = (int64_t)blockIdx.x * chunk;
+    const int64_t e_hi = min(e_lo + chunk, ld);
+    const int64_t v_hi = min(e_hi, nv);
+    float *out = scores + r * ld;
+    const __nv_bfloat16 *krow = kI + (c_beg * HI + g) * 64 + sl * 8;
+    for (int64_t base = e_lo + 32 * warp; base < v_hi; base += 32 * 8) {
+        const int n_here = (int)min((int64_t)32, v_hi - base);
+        float mine = 0.f;
+#pragma unroll 1
+        for (int e4 = 0; e4 < 32; e4 += 4) {
+            uint4 v[4][L];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int l = 0; l < L; ++l)
+                    v[u][l] = e4 + u < n_here
+                                  ? __ldg(reinterpret_cast<const uint4 *>(
+                                        krow + ((base + e4 + u) * HI + 4 * l) * 64))
+                                  : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                float p = 0.f;
+#pragma unroll
+                for (int l = 0; l < L; ++l) {
+                    const uint32_t x[4] = {v[u][l].x, v[u][l].y, v[u][l].z, v[u][l].w};
+                    float d = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        d = fmaf(q[l][2 * i], __uint_as_float(x[i] << 16), d);
+                        d = fmaf(q[l][2 * i + 1], __uint_as_float(x[i] & 0xffff0000u), d);
+                    }
+                    d += __shfl_xor_sync(0xffffffffu, d, 1);
+                    d += __shfl_xor_sync(0xffffffffu, d, 2);
+                    d += __shfl_xor_sync(0xffffffffu, d, 4);
+                    p = fmaf(wl[l], fmaxf(d, 0.f), p);
+                }
+                p += __shfl_xor_sync(0xffffffffu, p, 8);
+                p += __shfl_xor_sync(0xffffffffu, p, 16);
+                if (lane == e4 + u) mine = p;
+            }
+            if (e4 + 4 >= n_here) break;
+        }
+        if (lane < n_here) out[base + lane] = mine;
+    }
+    for (int64_t e = max(e_lo, nv) + threadIdx.x; e < e_hi; e += 256) out[e] = -INFINITY;
+}
+
+static bool stream_ok(const void *qI, const void *kI, int HI, int dI, lc_dtype dt) {
+    auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    return dt == LC_BF16 && dI == 64 && (HI == 4 || HI == 8) && al16(qI) && al16(kI);
+}
+
+static lc_status launch_stream(const void *qI, const float *w, const void *kI, const lc_batch &b,
+                               int HI, int m, float *scores, int64_t ld,
+                               const int32_t *row_mask, int32_t *dev_err, cudaStream_t st) {
+    if (b.total_q > 65535) return LC_ERR_UNSUPPORTED;
+    // about eight CTAs per SM over the whole batch, at least 1024 entries each
+    const int64_t want_x = (148 * 8 + b.total_q - 1) / b.total_q;
+    int64_t chunk = (ld + want_x - 1) / want_x;
+    if (chunk < 1024) chunk = 1024;
+    chunk = (chunk + 255) / 256 * 256;
+    const int64_t gx = (ld + chunk - 1) / chunk;
+    if (gx > 65535) return LC_ERR_UNSUPPORTED;
+    const dim3 grid((unsigned)gx, (unsigned)b.total_q);
+    if (HI == 8)
+        LC_LAUNCH(k_index_stream<8>, grid, dim3(256), 0, st, (const __nv_bfloat16 *)qI, w,
+                  (const __nv_bfloat16 *)kI, to_dev(b), m, scores, ld, chunk, row_mask, dev_err);
+    else
+        LC_LAUNCH(k_index_stream<4>, grid, dim3(256), 0, st, (const __nv_bfloat16 *)qI, w,
+                  (const __nv_bfloat16 *)kI, to_dev(b), m, scores, ld, chunk, row_mask, dev_err);
+    return check_launch();
+}
+
 template <typename T, int DI, int HI>
 static void launch_scan(const void *qI, const float *w, const void *kI, const lc_batch &b, int m,
                         float *scores, int64_t ld, const int32_t *row_mask, int32_t *dev_err,
@@ -197,6 +317,10 @@ static lc_status scan_hi(const void *qI, const float *w, const void *kI, const l
 lc_status index_scan_launch(const void *qI, const float *w, const void *kI, const lc_batch &b,
                             int HI, int dI, int m, lc_dtype dt, float *scores, int64_t ld,
                             const int32_t *row_mask, int32_t *dev_err, cudaStream_t st) {
+    if (stream_ok(qI, kI, HI, dI, dt)) {
+        const lc_status s = launch_stream(qI, w, kI, b, HI, m, scores, ld, row_mask, dev_err, st);
+        if (s != LC_ERR_UNSUPPORTED) return s;
+    }
     if (dt == LC_F32)
         return dI == 32 ? scan_hi<float, 32>(qI, w, kI, b, HI, m, scores, ld, row_mask, dev_err, st)
                         : scan_hi<float, 64>(qI, w, kI, b, HI, m, scores, ld, row_mask, dev_err, st);
@@ -210,6 +334,10 @@ static lc_status launch_index(const void *qI, const float *w, const void *kI, co
                               int HI, int dI, int m, float *scores, int64_t ld, int32_t *dev_err,
                               cudaStream_t st) {
     if (b.max_q < 16) {
+        if (std::is_same<T, __nv_bfloat16>::value && stream_ok(qI, kI, HI, dI, LC_BF16)) {
+            const lc_status s = launch_stream(qI, w, kI, b, HI, m, scores, ld, nullptr, dev_err, st);
+            if (s != LC_ERR_UNSUPPORTED) return s;
+        }
         if (dI == 32) return scan_hi<T, 32>(qI, w, kI, b, HI, m, scores, ld, nullptr, dev_err, st);
         return scan_hi<T, 64>(qI, w, kI, b, HI, m, scores, ld, nullptr, dev_err, st);
     }
