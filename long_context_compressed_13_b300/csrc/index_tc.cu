@@ -5,22 +5,23 @@
 // k_index_tc: one CTA = 128 query rows x a contiguous range of entries.
 //   q_I of the 128 rows lives in tensor memory (H_I x 32 columns of packed
 //   bf16 pairs) and is the A operand of every MMA, so shared memory only
-//   feeds the B operand (the entries' keys): 64 B per tensor-core clock.
-//   warp 16     TMA producer: k_I tiles of 64 entries x H_I heads into a
-//               ring of shared-memory stages
+//   feeds the B operand (the entries' keys).
+//   warp 16     TMA producer: per tile of 128 entries, one 16 KB box per head
+//               into a ring of head boxes
 //   warps 17-18 MMA issuers (warp 17 also owns TMEM): per tile, head by
-//               head, one M=128, N=64, K=64 product q_h k_h^T into a ring of
-//               four 64-column TMEM buffers; warp 17 issues the even heads and
-//               warp 18 the odd ones, so the short tensor-core queue stays fed
-//               while the other issuer waits on a barrier
+//               head, one M=128, N=128, K=64 product q_h k_h^T into one of two
+//               128-column TMEM score buffers; warp 17 issues the even heads
+//               into buffer 0 and warp 18 the odd heads into buffer 1, so the
+//               short tensor-core queue stays fed while one issuer waits
 //   warps 0-15  epilogue: warp w owns TMEM lanes 32(w%4).. (its query rows)
-//               and columns 16(w/4).. of each buffer; it folds the heads in
+//               and columns 32(w/4).. of each buffer; it folds the heads in
 //               order, acc = fma(w_h, max(s_h, 0), acc), two columns per
-//               packed fp32x2 FMA, loading head h+1 from TMEM while it folds
-//               head h, then either stores the 64 scores of the tile
-//               (MATERIALIZE) or appends the entries whose score reaches the
-//               row's threshold to the row's candidate list (FILTER).  The
-//               threshold test is a sign-bit collect of acc - theta.
+//               packed fp32x2 FMA, then either stores the 32 scores of the
+//               tile (MATERIALIZE) or appends the entries whose score reaches
+//               the row's threshold to the row's candidate list (FILTER).  The
+//               threshold test is a sign-bit collect of acc - theta.  A
+//               buffer is handed back to its issuer through a shared-memory
+//               release counter as soon as the warp's TMEM read completes.
 // The fused top-k of a row (see index_topk_tc_launch):
 //   1. scores of every s-th entry (MATERIALIZE over a strided tensor map);
 //   2. theta = the rho-th largest sampled key, a lower bound for the k-th
@@ -51,28 +52,30 @@ lc_status topk_launch_masked(const float *scores, int64_t ld, const lc_batch &b,
 
 namespace {
 constexpr int IBM = 128;          // query rows per CTA
-constexpr int IBN = 64;           // entries per tile
+constexpr int IBN = 128;          // entries per tile
 constexpr int IDI = 64;           // indexer head dim
 constexpr int NEPI = 512;         // epilogue threads (16 warps)
 constexpr int I_THREADS = NEPI + 96;  // + producer warp + two MMA warps
-constexpr int EPI_COLS = 16;      // columns of a score buffer per epilogue thread
-constexpr int NBUF = 4;           // TMEM score buffers (one head each)
+constexpr int EPI_COLS = 32;      // columns of a score buffer per epilogue thread
+constexpr int NBUF = 2;           // TMEM score buffers (one head each)
+constexpr int NSB = 10;           // shared-memory head boxes in flight
 constexpr uint32_t I_TMEM_COLS = 512;
 constexpr int MODE_MATERIALIZE = 0, MODE_FILTER = 1;
 
-template <int HI>
 struct IdxCfg {
-    static constexpr uint32_t HEAD_BOX = IBN * 128;        // 64 entries x 128 B
-    static constexpr uint32_t STAGE = HI * HEAD_BOX;
-    static constexpr int NST = HI == 8 ? 3 : 6;             // 192 KB of stages
-    static constexpr uint32_t SM_STG = NST * STAGE;         // FILTER staging, 64 B / thread
+    static constexpr uint32_t HEAD_BOX = IBN * 128;         // 128 entries x 128 B
+    static constexpr uint32_t SM_STG = NSB * HEAD_BOX;       // FILTER staging, 128 B / thread
     static constexpr uint32_t SM_BAR = SM_STG + NEPI * EPI_COLS * 4;
     static constexpr uint32_t SMEM = SM_BAR + 256;
-    static constexpr uint32_t D_COL0 = HI * 32;             // score buffers after q_I
+    static constexpr uint32_t D_COL0 = 256;                  // score buffers after q_I
 };
 
 struct IdxBars {
-    uint64_t q_full, k_full[6], k_empty[6], d_full[NBUF], d_empty[NBUF];
+    uint64_t q_full, k_full[NSB], k_empty[NSB], d_full[NBUF];
+    // releases of each score buffer: every epilogue warp adds 1 once its
+    // reads of a use of the buffer are complete (a shared-memory counter is
+    // far cheaper for the MMA issuers to poll than an mbarrier)
+    uint32_t freed[NBUF];
     uint32_t taddr;
     int abort;
 };
@@ -101,18 +104,33 @@ __device__ __forceinline__ void tmem_st32_u(uint32_t taddr, const uint32_t (&r)[
         : "memory");
 }
 
-// 32 lanes x 16 columns of 32-bit (thread i: lane base + i).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+// Counter hand-off between the epilogue (after tcgen05.wait::ld and
+// tcgen05.fence::before_thread_sync) and an MMA issuer (followed by
+// tcgen05.fence::after_thread_sync): release add / acquire load at CTA scope.
+__device__ __forceinline__ void release_add(uint32_t *ctr) {
+    asm volatile("red.release.cta.shared::cta.add.u32 [%0], 1;" ::"r"(smem_u32(ctr)) : "memory");
+}
+// Bounded spin until *ctr >= target (same give-up rule as mbar_wait): plain
+// volatile polls, the clock checked every 256 polls, and one acquire fence
+// once the target is seen.
+__device__ __forceinline__ bool wait_count(const uint32_t *ctr, uint32_t target, volatile int *abort,
+                                           long long limit = 4000000000LL) {
+    const volatile uint32_t *vc = ctr;
+    if (*vc < target) {
+        const long long t0 = clock64();
+        for (uint32_t it = 1;; ++it) {
+            if (*vc >= target) break;
+            if ((it & 255u) == 0u) {
+                if (*abort) return false;
+                if (clock64() - t0 > limit) {
+                    *abort = 1;
+                    return false;
+                }
+            }
+        }
+    }
+    asm volatile("fence.acq_rel.cta;" ::: "memory");
+    return true;
 }
 
 // Inverse of order_key: the float whose key is `key` (+0 for the key of
@@ -148,8 +166,7 @@ struct IdxTcArgs {
 template <int MODE, int HI>
 __global__ void __launch_bounds__(I_THREADS, 1)
     k_index_tc(const __grid_constant__ CUtensorMap mK, IdxTcArgs a) {
-    using C = IdxCfg<HI>;
-    constexpr int NST = C::NST;
+    using C = IdxCfg;
     extern __shared__ __align__(1024) uint8_t smem[];
     IdxBars &bars = *reinterpret_cast<IdxBars *>(smem + C::SM_BAR);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -167,18 +184,19 @@ __global__ void __launch_bounds__(I_THREADS, 1)
                                                    : min(c0 + a.chunk, nvm);
     const int64_t comp_end = min(c_end, nvm);  // computed columns [c0, comp_end)
     const int n_t = comp_end > c0 ? (int)((comp_end - c0 + IBN - 1) / IBN) : 0;
+    const int n_all = n_t * HI;  // head boxes / score buffers of this CTA
 
     if (tid == 0) {
         bars.abort = (smem_u32(smem) & 1023u) != 0 ? 1 : 0;
         if (bars.abort) flag(a.dev_err, LC_DEVERR_TIMEOUT);
         mbar_init(&bars.q_full, NEPI / 32);
-        for (int s = 0; s < NST; ++s) {
+        for (int s = 0; s < NSB; ++s) {
             mbar_init(&bars.k_full[s], 1);
-            mbar_init(&bars.k_empty[s], 2);  // one commit per MMA issuer
+            mbar_init(&bars.k_empty[s], 1);
         }
         for (int b = 0; b < NBUF; ++b) {
             mbar_init(&bars.d_full[b], 1);
-            mbar_init(&bars.d_empty[b], NEPI / 32);  // one arrival per epilogue warp
+            bars.freed[b] = 0u;
         }
         fence_barrier_init();
     }
@@ -198,51 +216,37 @@ __global__ void __launch_bounds__(I_THREADS, 1)
         if (lane == 0 && !dead && n_t > 0) {
             prefetch_tmap(&mK);
             int issued = 0;
-            for (int i = 0; i < n_t; ++i) {
-                const int s = i % NST;
-                if (i >= NST && !mbar_wait(&bars.k_empty[s], ((i - NST) / NST) & 1, abort))
-                    break;
-                const int32_t y = (int32_t)(c0 + (int64_t)i * IBN);
-                uint8_t *kd = smem + s * C::STAGE;
-                mbar_expect_tx(&bars.k_full[s], C::STAGE);
-#pragma unroll
-                for (int h = 0; h < HI; ++h)
-                    tma_load_2d(kd + h * C::HEAD_BOX, &mK, &bars.k_full[s], h * IDI, y);
+            for (int g = 0; g < n_all; ++g) {
+                const int s = g % NSB, i = g / HI, h = g % HI;
+                if (g >= NSB && !mbar_wait(&bars.k_empty[s], ((g - NSB) / NSB) & 1, abort)) break;
+                mbar_expect_tx(&bars.k_full[s], C::HEAD_BOX);
+                tma_load_2d(smem + s * C::HEAD_BOX, &mK, &bars.k_full[s], h * IDI,
+                            (int32_t)(c0 + (int64_t)i * IBN));
                 ++issued;
             }
             int dummy = 0;
-            for (int i = max(0, issued - NST); i < issued; ++i)
-                mbar_wait(&bars.k_full[i % NST], (i / NST) & 1, &dummy, 400000000LL);
+            for (int g = max(0, issued - NSB); g < issued; ++g)
+                mbar_wait(&bars.k_full[g % NSB], (g / NSB) & 1, &dummy, 400000000LL);
         }
     } else if (warp == W_MMA || warp == W_MMA2) {
         // ------------------------------------------------------ MMA issuers
-        const int par = warp - W_MMA;  // heads h with h % 2 == par
+        const int par = warp - W_MMA;  // head boxes g with g % 2 == par, buffer par
         if (lane == 0 && !dead && n_t > 0) {
             constexpr uint32_t IDESC = idesc_bf16_f32(IBM, IBN, 0, 0);
             bool ok = mbar_wait(&bars.q_full, 0, abort);
             tc_fence_after();
-            for (int i = 0; ok && i < n_t; ++i) {
-                const int s = i % NST;
-                if (!mbar_wait(&bars.k_full[s], (i / NST) & 1, abort)) break;
+            for (int g = par; ok && g < n_all; g += 2) {
+                const int s = g % NSB, h = g % HI, u = g / NBUF;
+                if (!mbar_wait(&bars.k_full[s], (g / NSB) & 1, abort) ||
+                    (u > 0 && !wait_count(&bars.freed[par], (uint32_t)u * (NEPI / 32), abort)))
+                    break;
                 tc_fence_after();
-                const uint32_t k_base = smem_u32(smem + s * C::STAGE);
-#pragma unroll 1
-                for (int h = par; h < HI; h += 2) {
-                    const int n = i * HI + h, b = n % NBUF;
-                    if (n >= NBUF && !mbar_wait(&bars.d_empty[b], ((n - NBUF) / NBUF) & 1, abort)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
+                const uint32_t k_base = smem_u32(smem + s * C::HEAD_BOX);
 #pragma unroll
-                    for (int kk = 0; kk < IDI / 16; ++kk) {
-                        const uint64_t bd =
-                            sw128_desc(k_base + h * C::HEAD_BOX + kk * 32, 16, 1024);
-                        mma_bf16_ta(taddr + C::D_COL0 + b * IBN, taddr + h * 32 + kk * 8, bd,
-                                    IDESC, kk > 0);
-                    }
-                    mma_commit(&bars.d_full[b]);
-                }
+                for (int kk = 0; kk < IDI / 16; ++kk)
+                    mma_bf16_ta(taddr + C::D_COL0 + par * IBN, taddr + h * 32 + kk * 8,
+                                sw128_desc(k_base + kk * 32, 16, 1024), IDESC, kk > 0);
+                mma_commit(&bars.d_full[par]);
                 mma_commit(&bars.k_empty[s]);
             }
         }
@@ -293,54 +297,33 @@ __global__ void __launch_bounds__(I_THREADS, 1)
         }
         float *stg = reinterpret_cast<float *>(smem + C::SM_STG) + tid * EPI_COLS;
         float2 acc[EPI_COLS / 2];
-        const int n_all = n_t * HI;  // score buffers this CTA consumes
-        // Heads are consumed in pairs: v[0], v[1] hold heads n, n+1.  The
-        // barriers of the next pair are tested (without blocking) before the
-        // current pair is folded, so their latency overlaps the arithmetic;
-        // both buffers of a pair are read with one TMEM wait.
-        float v[2][EPI_COLS];
-        bool ready = false;  // the next pair's barriers were seen complete
+        bool ready = false;  // the next buffer's barrier was seen complete
         for (int i = 0; ok && i < n_t; ++i) {
 #pragma unroll
             for (int c = 0; c < EPI_COLS / 2; ++c) acc[c] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int h = 0; h < HI; h += 2) {
-                const int n = i * HI + h;
-                // ---- load the pair (n, n+1) and free its buffers
-                const int b0 = n % NBUF, b1 = (n + 1) % NBUF;
-                if (!ready &&
-                    !__all_sync(FULL, mbar_wait(&bars.d_full[b0], (n / NBUF) & 1, abort) &&
-                                          mbar_wait(&bars.d_full[b1], ((n + 1) / NBUF) & 1, abort))) {
+            for (int h = 0; h < HI; ++h) {
+                const int g = i * HI + h, b = g % NBUF;
+                if (!ready && !__all_sync(FULL, mbar_wait(&bars.d_full[b], (g / NBUF) & 1, abort))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                tmem_ld16(buf_addr + b0 * IBN, v[0]);
-                tmem_ld16(buf_addr + b1 * IBN, v[1]);
+                float v[EPI_COLS];
+                tmem_ld32(buf_addr + b * IBN, v);
                 tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&bars.d_empty[b0]);
-                    mbar_arrive(&bars.d_empty[b1]);
-                }
-                // ---- early, non-blocking look at the next pair's barriers;
-                // the verdict is taken after the fold
-                const bool more = n + 2 < n_all;
+                if (lane == 0) release_add(&bars.freed[b]);
+                // early, non-blocking look at the next buffer; verdict after the fold
+                const bool more = g + 1 < n_all;
                 bool t_next = more;
-                if (more)
-                    t_next = mbar_test(&bars.d_full[(n + 2) % NBUF], ((n + 2) / NBUF) & 1) &
-                             mbar_test(&bars.d_full[(n + 3) % NBUF], ((n + 3) / NBUF) & 1);
-                // ---- fold the pair into the tile's scores
+                if (more) t_next = mbar_test(&bars.d_full[(g + 1) % NBUF], ((g + 1) / NBUF) & 1);
+                const float2 w2 = make_float2(wh[h], wh[h]);
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const float2 w2 = make_float2(wh[h + u], wh[h + u]);
-#pragma unroll
-                    for (int c = 0; c < EPI_COLS / 2; ++c)
-                        acc[c] = __ffma2_rn(w2, make_float2(fmaxf(v[u][2 * c], 0.f),
-                                                            fmaxf(v[u][2 * c + 1], 0.f)),
-                                            acc[c]);
-                }
+                for (int c = 0; c < EPI_COLS / 2; ++c)
+                    acc[c] = __ffma2_rn(w2, make_float2(fmaxf(v[2 * c], 0.f), fmaxf(v[2 * c + 1], 0.f)),
+                                        acc[c]);
                 ready = more && __all_sync(FULL, t_next);
             }
             if (!ok) break;
@@ -372,12 +355,12 @@ __global__ void __launch_bounds__(I_THREADS, 1)
                     below = __funnelshift_l(__float_as_uint(d.x), below, 1);
                     below = __funnelshift_l(__float_as_uint(d.y), below, 1);
                 }
-                uint32_t cand = __brev(~below) >> (32 - EPI_COLS);
+                uint32_t cand = __brev(~below);
                 const int64_t lim = min(nvr, c_end) - e0;
                 if (lim < EPI_COLS) cand &= lim <= 0 ? 0u : ((1u << lim) - 1u);
                 if (cand) {
                     // stage the row's scores so a candidate can be read by column
-                    const int sw = lane & 3;
+                    const int sw = lane & 7;
 #pragma unroll
                     for (int u = 0; u < EPI_COLS / 4; ++u)
                         reinterpret_cast<float4 *>(stg)[u ^ sw] =
@@ -644,7 +627,7 @@ bool index_tc_eligible(const void *qI, const void *kI, const lc_batch &b, int HI
 
 template <int MODE, int HI>
 lc_status launch_tc(const CUtensorMap &mK, const IdxTcArgs &a, int64_t n_cols, cudaStream_t st) {
-    constexpr uint32_t SMEM = IdxCfg<HI>::SMEM;
+    constexpr uint32_t SMEM = IdxCfg::SMEM;
     static_assert(SMEM <= 227 * 1024, "indexer shared memory");
     auto kfn = k_index_tc<MODE, HI>;
     static bool attr = false;
