@@ -424,62 +424,46 @@ __global__ void __launch_bounds__(512) k_sample_threshold(const float *__restric
     }
 }
 
-// Exact top-k of each row's candidates; rows whose candidate count is outside
-// [k, cap] are marked in fail[] for the exact fallback.
-__global__ void __launch_bounds__(512) k_cand_topk(Batch bt, int m, int k, int cap, int P,
-                                                   int PK, const int32_t *__restrict__ count,
+// Ascending bitonic sort of P (power of two) uint32 values in shared memory.
+__device__ __forceinline__ void bitonic_sort_u32_asc(uint32_t *a, int P) {
+    constexpr int NT = 512;
+    for (int size = 2; size <= P; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            __syncthreads();
+            for (int i = threadIdx.x; i < (P >> 1); i += NT) {
+                const int lo = 2 * stride * (i / stride) + (i % stride);
+                const int hi = lo + stride;
+                const bool up = (lo & size) == 0;
+                const uint32_t x = a[lo], y = a[hi];
+                if ((x > y) == up) {
+                    a[lo] = y;
+                    a[hi] = x;
+                }
+            }
+        }
+    }
+    __syncthreads();
+}
+
+// Exact top-k of each row's candidates: radix selection of the k-th largest
+// key K* in shared memory; the candidates above K* and the `need` lowest-index
+// candidates equal to K* are collected (in any order) and their indices sorted
+// ascending.  Rows whose candidate count is outside [k, cap] are marked in
+// fail[].  Shared memory: cap keys, cap indices, PK collected indices, P tie
+// slots (PK, P: powers of two >= k, cap).
+__global__ void __launch_bounds__(512) k_cand_pick(Batch bt, int m, int k, int cap, int PK, int P,
+                                                   const int32_t *__restrict__ count,
                                                    const uint32_t *__restrict__ cand_key,
                                                    const int32_t *__restrict__ cand_idx,
                                                    int32_t *__restrict__ topk, int32_t *fail) {
-    extern __shared__ uint64_t sk[];  // [P] then [PK] (as u64 for the index sort)
-    const int64_t r = blockIdx.x;
-    const int64_t t = bt.q_pos0[0] + r;
-    const int64_t Tc = bt.cu_c[1] - bt.cu_c[0];
-    int64_t nv = n_vis(t, m);
-    if (nv > Tc) nv = Tc;
-    int32_t *out = topk + r * k;
-    if (nv <= k) {
-        for (int i = threadIdx.x; i < k; i += 512) out[i] = i < nv ? i : -1;
-        return;
-    }
-    const int n = count[r];
-    if (n < k || n > cap) {
-        if (threadIdx.x == 0) fail[r] = 1;
-        return;
-    }
-    const uint32_t *ck = cand_key + r * cap;
-    const int32_t *ci = cand_idx + r * cap;
-    for (int i = threadIdx.x; i < P; i += 512)
-        sk[i] = i < n ? ((uint64_t)ck[i] << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)ci[i]) : 0ull;
-    bitonic_sort_u64<512, true>(sk, P);
-    uint64_t *si = sk + P;
-    for (int i = threadIdx.x; i < PK; i += 512)
-        si[i] = i < k ? (uint64_t)(0xFFFFFFFFu - (uint32_t)(sk[i] & 0xFFFFFFFFull))
-                      : 0xFFFFFFFFFFFFFFFFull;
-    bitonic_sort_u64<512, false>(si, PK);
-    for (int i = threadIdx.x; i < k; i += 512) out[i] = (int32_t)si[i];
-}
-
-// Exact top-k of each row's candidates without sorting them: radix selection
-// of the k-th largest key K* in shared memory; every candidate above K* and
-// the `need` lowest-index candidates equal to K* are marked in a bitmap over
-// the row's entries, which a prefix sum turns into ascending indices.  Rows
-// whose candidate count is outside [k, cap] are marked in fail[].
-// Shared memory: cap keys, cap indices, nwords bitmap words, then
-// pow2(cap) tie slots.
-__global__ void __launch_bounds__(512) k_cand_select(Batch bt, int m, int k, int cap, int nwords,
-                                                     const int32_t *__restrict__ count,
-                                                     const uint32_t *__restrict__ cand_key,
-                                                     const int32_t *__restrict__ cand_idx,
-                                                     int32_t *__restrict__ topk, int32_t *fail) {
     constexpr int NT = 512;
     extern __shared__ uint32_t sbuf[];
     uint32_t *keys = sbuf;                                      // [cap]
-    int32_t *idx = reinterpret_cast<int32_t *>(sbuf + cap);     // [cap]
-    uint32_t *bits = sbuf + 2 * cap;                            // [nwords]
+    uint32_t *idx = sbuf + cap;                                 // [cap]
+    uint32_t *sel = sbuf + 2 * cap;                             // [PK]
+    uint32_t *tl = sel + PK;                                    // [P]
     __shared__ RadixScratch rs;
-    __shared__ int warp_sums[NT / 32];
-    __shared__ int s_ties;
+    __shared__ int s_n, s_ties;
     const int64_t r = blockIdx.x;
     const int64_t t = bt.q_pos0[0] + r;
     const int64_t Tc = bt.cu_c[1] - bt.cu_c[0];
@@ -495,77 +479,38 @@ __global__ void __launch_bounds__(512) k_cand_select(Batch bt, int m, int k, int
         if (threadIdx.x == 0) fail[r] = 1;
         return;
     }
-    const int words = (int)((nv + 31) / 32);
     for (int i = threadIdx.x; i < n; i += NT) {
         keys[i] = cand_key[r * cap + i];
-        idx[i] = cand_idx[r * cap + i];
+        idx[i] = (uint32_t)cand_idx[r * cap + i];
     }
-    for (int i = threadIdx.x; i < words; i += NT) bits[i] = 0u;
-    if (threadIdx.x == 0) s_ties = 0;
+    for (int i = threadIdx.x; i < PK; i += NT) sel[i] = 0xFFFFFFFFu;
+    if (threadIdx.x == 0) {
+        s_n = 0;
+        s_ties = 0;
+    }
     __syncthreads();
     int need;
     const uint32_t kstar = radix_kth_largest_smem<NT>(keys, n, k, rs, &need);
-    // keys above K* are in; count the ties at K*
-    int my_ties = 0;
+    // candidates above K* are in; the ties at K* go to a list
     for (int i = threadIdx.x; i < n; i += NT) {
-        if (keys[i] > kstar) atomicOr(&bits[idx[i] >> 5], 1u << (idx[i] & 31));
-        else if (keys[i] == kstar) ++my_ties;
+        if (keys[i] > kstar) sel[atomicAdd(&s_n, 1)] = idx[i];
+        else if (keys[i] == kstar) tl[atomicAdd(&s_ties, 1)] = idx[i];
     }
-    if (my_ties) atomicAdd(&s_ties, my_ties);
     __syncthreads();
-    const int ties = s_ties;
+    const int above = s_n, ties = s_ties;
     if (ties == need) {
-        for (int i = threadIdx.x; i < n; i += NT)
-            if (keys[i] == kstar) atomicOr(&bits[idx[i] >> 5], 1u << (idx[i] & 31));
+        for (int i = threadIdx.x; i < ties; i += NT) sel[above + i] = tl[i];
     } else {
-        // more ties than places (rare): the lowest indices win.  The tie list
-        // lives after the bitmap and is sorted ascending.
-        uint32_t *tl = bits + words;
-        __syncthreads();
-        if (threadIdx.x == 0) s_ties = 0;
-        __syncthreads();
-        for (int i = threadIdx.x; i < n; i += NT)
-            if (keys[i] == kstar) tl[atomicAdd(&s_ties, 1)] = (uint32_t)idx[i];
-        int P = 1;
-        while (P < ties) P <<= 1;
-        for (int i = ties + threadIdx.x; i < P; i += NT) tl[i] = 0xFFFFFFFFu;
-        __syncthreads();
-        for (int size = 2; size <= P; size <<= 1) {
-            for (int stride = size >> 1; stride > 0; stride >>= 1) {
-                for (int i = threadIdx.x; i < (P >> 1); i += NT) {
-                    const int lo = 2 * stride * (i / stride) + (i % stride);
-                    const int hi = lo + stride;
-                    const bool up = (lo & size) == 0;
-                    const uint32_t x = tl[lo], y = tl[hi];
-                    if ((x > y) == up) {
-                        tl[lo] = y;
-                        tl[hi] = x;
-                    }
-                }
-                __syncthreads();
-            }
-        }
-        for (int i = threadIdx.x; i < need; i += NT)
-            atomicOr(&bits[tl[i] >> 5], 1u << (tl[i] & 31));
+        // more ties than places (rare): the lowest indices win
+        int Pt = 1;
+        while (Pt < ties) Pt <<= 1;
+        for (int i = ties + threadIdx.x; i < Pt; i += NT) tl[i] = 0xFFFFFFFFu;
+        bitonic_sort_u32_asc(tl, Pt);
+        for (int i = threadIdx.x; i < need; i += NT) sel[above + i] = tl[i];
     }
-    __syncthreads();
-    // ascending compaction of the bitmap
-    const int per = (words + NT - 1) / NT;
-    const int w0 = threadIdx.x * per, w1 = min(words, w0 + per);
-    int mine = 0;
-    for (int w = w0; w < w1; ++w) mine += __popc(bits[w]);
-    int total;
-    int pos = block_exclusive_scan<NT>(mine, warp_sums, &total);
-    for (int w = w0; w < w1; ++w) {
-        uint32_t x = bits[w];
-        while (x) {
-            const int b = __ffs(x) - 1;
-            x &= x - 1;
-            if (pos < k) out[pos] = w * 32 + b;
-            ++pos;
-        }
-    }
-    (void)nwords;
+    bitonic_sort_u32_asc(sel, PK);
+    for (int i = threadIdx.x; i < k; i += NT) out[i] = (int32_t)sel[i];
+    (void)P;
 }
 
 namespace {
@@ -650,14 +595,16 @@ lc_status launch_tc_hi(int HI, const CUtensorMap &mK, const IdxTcArgs &a, int64_
     return HI == 8 ? launch_tc<MODE, 8>(mK, a, n_cols, st) : launch_tc<MODE, 4>(mK, a, n_cols, st);
 }
 
-// entries per CTA: about eight waves of CTAs over the 148 SMs
+// entries per CTA: about eight waves of CTAs over the 148 SMs, at least 16 tiles each
 int64_t pick_chunk(int64_t Nq, int64_t n_cols) {
     const int64_t row_tiles = (Nq + IBM - 1) / IBM;
     int64_t want_y = (148 * 8 + row_tiles - 1) / row_tiles;
     if (want_y < 1) want_y = 1;
     int64_t chunk = (n_cols + want_y - 1) / want_y;
     chunk = (chunk + IBN - 1) / IBN * IBN;
-    if (chunk < 4 * IBN) chunk = 4 * IBN;
+    // a CTA first moves its 128 query rows into TMEM; amortise that over at
+    // least 16 tiles
+    if (chunk < 16 * IBN) chunk = 16 * IBN;
     while ((n_cols + chunk - 1) / chunk > 65535) chunk *= 2;
     return chunk;
 }
@@ -757,33 +704,18 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
         s = launch_tc_hi<MODE_FILTER>(HI, mK, a, Tc, st);
         if (s != LC_OK) return s;
     }
-    // 4. exact selection among candidates: bitmap compaction when the row's
-    //    bitmap fits in shared memory, a full bitonic sort otherwise
+    // 4. exact selection among the candidates
     {
-        const int64_t nwords = (Tc + 31) / 32;
-        const size_t smem_bm = sizeof(uint32_t) * (size_t)(2 * p.cap + nwords + p.P);
-        if (smem_bm <= 200 * 1024) {
-            static size_t attr = 0;
-            if (smem_bm > 48 * 1024 && smem_bm > attr) {
-                if (cudaFuncSetAttribute(k_cand_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem_bm) != cudaSuccess)
-                    return LC_ERR_CUDA;
-                attr = smem_bm;
-            }
-            LC_LAUNCH(k_cand_select, dim3((unsigned)b.total_q), dim3(512), smem_bm, st, to_dev(b),
-                      m, k, p.cap, (int)nwords, count, ckey, cidx, topk, fail);
-        } else {
-            const size_t smem = sizeof(uint64_t) * (size_t)(p.P + p.PK);
-            static size_t attr = 0;
-            if (smem > 48 * 1024 && smem > attr) {
-                if (cudaFuncSetAttribute(k_cand_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem) != cudaSuccess)
-                    return LC_ERR_CUDA;
-                attr = smem;
-            }
-            LC_LAUNCH(k_cand_topk, dim3((unsigned)b.total_q), dim3(512), smem, st, to_dev(b), m,
-                      k, p.cap, p.P, p.PK, count, ckey, cidx, topk, fail);
+        const size_t smem = sizeof(uint32_t) * (size_t)(2 * p.cap + p.PK + p.P);
+        static size_t attr = 0;
+        if (smem > 48 * 1024 && smem > attr) {
+            if (cudaFuncSetAttribute(k_cand_pick, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem) != cudaSuccess)
+                return LC_ERR_CUDA;
+            attr = smem;
         }
+        LC_LAUNCH(k_cand_pick, dim3((unsigned)b.total_q), dim3(512), smem, st, to_dev(b), m, k,
+                  p.cap, p.PK, p.P, count, ckey, cidx, topk, fail);
         if ((s = check_launch()) != LC_OK) return s;
     }
     // 5. exact fallback for the rows marked in fail[] (no work when none is)
