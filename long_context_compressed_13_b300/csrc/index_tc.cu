@@ -3,23 +3,24 @@
 // never writes the full score matrix.
 //
 // k_index_tc: one CTA = 128 query rows x a contiguous range of entries.
-//   q_I of the 128 rows lives in tensor memory (H_I x 32 columns of packed
-//   bf16 pairs) and is the A operand of every MMA, so shared memory only
-//   feeds the B operand (the entries' keys).
-//   warp 16     TMA producer: per tile of 128 entries, one 16 KB box per head
-//               into a ring of head boxes
+//   q_I of the 128 rows stays in shared memory (one 16 KB TMA box per head)
+//   for the CTA's lifetime, so all 512 TMEM columns hold score buffers.
+//   warp 16     TMA producer: q_I once, then per tile of 128 entries one 16 KB
+//               box per head into a ring of head boxes
 //   warps 17-18 MMA issuers (warp 17 also owns TMEM): per tile, head by
-//               head, one M=128, N=128, K=64 product q_h k_h^T into one of two
-//               128-column TMEM score buffers; warp 17 issues the even heads
-//               into buffer 0 and warp 18 the odd heads into buffer 1, so the
-//               short tensor-core queue stays fed while one issuer waits
+//               head, one M=128, N=128, K=64 product q_h k_h^T into one of four
+//               128-column TMEM score buffers (score buffer g % 4 for the g-th
+//               head of the CTA); warp 17 issues the even heads and warp 18
+//               the odd ones, so the short tensor-core queue stays fed while
+//               one issuer waits; a buffer is reused three heads later
 //   warps 0-15  epilogue: warp w owns TMEM lanes 32(w%4).. (its query rows)
 //               and columns 32(w/4).. of each buffer; it folds the heads in
 //               order, acc = fma(w_h, max(s_h, 0), acc), two columns per
 //               packed fp32x2 FMA, then either stores the 32 scores of the
 //               tile (MATERIALIZE) or appends the entries whose score reaches
 //               the row's threshold to the row's candidate list (FILTER).  The
-//               threshold test is a sign-bit collect of acc - theta.  A
+//               threshold test is a sign-bit collect of acc - theta; the
+//               candidates are staged eight columns at a time.  A
 //               buffer is handed back to its issuer through a shared-memory
 //               release counter as soon as the warp's TMEM read completes.
 // The fused top-k of a row (see index_topk_tc_launch):
@@ -57,17 +58,19 @@ constexpr int IDI = 64;           // indexer head dim
 constexpr int NEPI = 512;         // epilogue threads (16 warps)
 constexpr int I_THREADS = NEPI + 96;  // + producer warp + two MMA warps
 constexpr int EPI_COLS = 32;      // columns of a score buffer per epilogue thread
-constexpr int NBUF = 2;           // TMEM score buffers (one head each)
-constexpr int NSB = 10;           // shared-memory head boxes in flight
+constexpr int NBUF = 4;           // TMEM score buffers (one head each)
+constexpr int NSB = 5;            // shared-memory head boxes in flight
 constexpr uint32_t I_TMEM_COLS = 512;
 constexpr int MODE_MATERIALIZE = 0, MODE_FILTER = 1;
 
 struct IdxCfg {
     static constexpr uint32_t HEAD_BOX = IBN * 128;         // 128 entries x 128 B
-    static constexpr uint32_t SM_STG = NSB * HEAD_BOX;       // FILTER staging, 128 B / thread
-    static constexpr uint32_t SM_BAR = SM_STG + NEPI * EPI_COLS * 4;
+    static constexpr uint32_t Q_BOX = IBM * 128;             // 128 query rows x 128 B
+    static constexpr uint32_t SM_Q = 0;                      // 8 heads of q_I
+    static constexpr uint32_t SM_K = SM_Q + 8 * Q_BOX;       // ring of head boxes
+    static constexpr uint32_t SM_STG = SM_K + NSB * HEAD_BOX;  // FILTER staging, 32 B / thread
+    static constexpr uint32_t SM_BAR = SM_STG + NEPI * 8 * 4;
     static constexpr uint32_t SMEM = SM_BAR + 256;
-    static constexpr uint32_t D_COL0 = 256;                  // score buffers after q_I
 };
 
 struct IdxBars {
@@ -80,29 +83,7 @@ struct IdxBars {
     int abort;
 };
 
-// tcgen05.mma with the A operand in tensor memory.
-__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
 
-__device__ __forceinline__ void tmem_st32_u(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-        "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
 
 // Counter hand-off between the epilogue (after tcgen05.wait::ld and
 // tcgen05.fence::before_thread_sync) and an MMA issuer (followed by
@@ -165,7 +146,8 @@ struct IdxTcArgs {
 
 template <int MODE, int HI>
 __global__ void __launch_bounds__(I_THREADS, 1)
-    k_index_tc(const __grid_constant__ CUtensorMap mK, IdxTcArgs a) {
+    k_index_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+               IdxTcArgs a) {
     using C = IdxCfg;
     extern __shared__ __align__(1024) uint8_t smem[];
     IdxBars &bars = *reinterpret_cast<IdxBars *>(smem + C::SM_BAR);
@@ -189,7 +171,7 @@ __global__ void __launch_bounds__(I_THREADS, 1)
     if (tid == 0) {
         bars.abort = (smem_u32(smem) & 1023u) != 0 ? 1 : 0;
         if (bars.abort) flag(a.dev_err, LC_DEVERR_TIMEOUT);
-        mbar_init(&bars.q_full, NEPI / 32);
+        mbar_init(&bars.q_full, 1);
         for (int s = 0; s < NSB; ++s) {
             mbar_init(&bars.k_full[s], 1);
             mbar_init(&bars.k_empty[s], 1);
@@ -215,38 +197,46 @@ __global__ void __launch_bounds__(I_THREADS, 1)
         // ------------------------------------------------------ TMA producer
         if (lane == 0 && !dead && n_t > 0) {
             prefetch_tmap(&mK);
+            mbar_expect_tx(&bars.q_full, HI * C::Q_BOX);
+#pragma unroll
+            for (int h = 0; h < HI; ++h)
+                tma_load_2d(smem + C::SM_Q + h * C::Q_BOX, &mQ, &bars.q_full, h * IDI,
+                            (int32_t)row0);
             int issued = 0;
             for (int g = 0; g < n_all; ++g) {
                 const int s = g % NSB, i = g / HI, h = g % HI;
                 if (g >= NSB && !mbar_wait(&bars.k_empty[s], ((g - NSB) / NSB) & 1, abort)) break;
                 mbar_expect_tx(&bars.k_full[s], C::HEAD_BOX);
-                tma_load_2d(smem + s * C::HEAD_BOX, &mK, &bars.k_full[s], h * IDI,
+                tma_load_2d(smem + C::SM_K + s * C::HEAD_BOX, &mK, &bars.k_full[s], h * IDI,
                             (int32_t)(c0 + (int64_t)i * IBN));
                 ++issued;
             }
             int dummy = 0;
             for (int g = max(0, issued - NSB); g < issued; ++g)
                 mbar_wait(&bars.k_full[g % NSB], (g / NSB) & 1, &dummy, 400000000LL);
+            mbar_wait(&bars.q_full, 0, &dummy, 400000000LL);
         }
     } else if (warp == W_MMA || warp == W_MMA2) {
         // ------------------------------------------------------ MMA issuers
-        const int par = warp - W_MMA;  // head boxes g with g % 2 == par, buffer par
+        const int par = warp - W_MMA;  // head boxes g with g % 2 == par
         if (lane == 0 && !dead && n_t > 0) {
             constexpr uint32_t IDESC = idesc_bf16_f32(IBM, IBN, 0, 0);
             bool ok = mbar_wait(&bars.q_full, 0, abort);
             tc_fence_after();
+            const uint32_t q_base = smem_u32(smem + C::SM_Q);
             for (int g = par; ok && g < n_all; g += 2) {
-                const int s = g % NSB, h = g % HI, u = g / NBUF;
+                const int s = g % NSB, h = g % HI, b = g % NBUF, u = g / NBUF;
                 if (!mbar_wait(&bars.k_full[s], (g / NSB) & 1, abort) ||
-                    (u > 0 && !wait_count(&bars.freed[par], (uint32_t)u * (NEPI / 32), abort)))
+                    (u > 0 && !wait_count(&bars.freed[b], (uint32_t)u * (NEPI / 32), abort)))
                     break;
                 tc_fence_after();
-                const uint32_t k_base = smem_u32(smem + s * C::HEAD_BOX);
+                const uint32_t k_base = smem_u32(smem + C::SM_K + s * C::HEAD_BOX);
+                const uint32_t qh = q_base + h * C::Q_BOX;
 #pragma unroll
                 for (int kk = 0; kk < IDI / 16; ++kk)
-                    mma_bf16_ta(taddr + C::D_COL0 + par * IBN, taddr + h * 32 + kk * 8,
-                                sw128_desc(k_base + kk * 32, 16, 1024), IDESC, kk > 0);
-                mma_commit(&bars.d_full[par]);
+                    mma_bf16(taddr + b * IBN, sw128_desc(qh + kk * 32, 16, 1024),
+                             sw128_desc(k_base + kk * 32, 16, 1024), IDESC, kk > 0);
+                mma_commit(&bars.d_full[b]);
                 mma_commit(&bars.k_empty[s]);
             }
         }
@@ -266,36 +256,9 @@ __global__ void __launch_bounds__(I_THREADS, 1)
         float thf = 0.f;
         if (MODE == MODE_FILTER) thf = row_ok ? key_to_float(__ldg(a.theta + row)) : INFINITY;
         const uint32_t lane_addr = taddr + ((uint32_t)(quad * 32) << 16);
-        const uint32_t buf_addr = lane_addr + C::D_COL0 + part * EPI_COLS;
+        const uint32_t buf_addr = lane_addr + part * EPI_COLS;
         bool ok = !dead;
-        if (n_t > 0 && ok) {
-            // q_I rows into TMEM: this thread's row, heads part*HI/4 ..
-#pragma unroll 1
-            for (int hh = 0; hh < HI / 4; ++hh) {
-                const int h = part * (HI / 4) + hh;
-                uint32_t r[32];
-                if (row_ok) {
-                    const uint4 *src = reinterpret_cast<const uint4 *>(a.qI + (row * HI + h) * IDI);
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const uint4 x = __ldg(src + u);
-                        r[4 * u] = x.x;
-                        r[4 * u + 1] = x.y;
-                        r[4 * u + 2] = x.z;
-                        r[4 * u + 3] = x.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int u = 0; u < 32; ++u) r[u] = 0u;
-                }
-                tmem_st32_u(lane_addr + h * 32, r);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars.q_full);
-        }
-        float *stg = reinterpret_cast<float *>(smem + C::SM_STG) + tid * EPI_COLS;
+        float *stg = reinterpret_cast<float *>(smem + C::SM_STG) + tid * 8;
         float2 acc[EPI_COLS / 2];
         bool ready = false;  // the next buffer's barrier was seen complete
         for (int i = 0; ok && i < n_t; ++i) {
@@ -359,24 +322,29 @@ __global__ void __launch_bounds__(I_THREADS, 1)
                 const int64_t lim = min(nvr, c_end) - e0;
                 if (lim < EPI_COLS) cand &= lim <= 0 ? 0u : ((1u << lim) - 1u);
                 if (cand) {
-                    // stage the row's scores so a candidate can be read by column
-                    const int sw = lane & 7;
-#pragma unroll
-                    for (int u = 0; u < EPI_COLS / 4; ++u)
-                        reinterpret_cast<float4 *>(stg)[u ^ sw] =
-                            make_float4(acc[2 * u].x, acc[2 * u].y, acc[2 * u + 1].x,
-                                        acc[2 * u + 1].y);
                     int base = atomicAdd(a.count + row, __popc(cand));
                     uint32_t *ck = a.cand_key + row * a.cap;
                     int32_t *ci = a.cand_idx + row * a.cap;
-                    while (cand) {
-                        const int c = __ffs(cand) - 1;
-                        cand &= cand - 1;
-                        if (base < a.cap) {
-                            ck[base] = order_key(stg[(((c >> 2) ^ sw) << 2) | (c & 3)]);
-                            ci[base] = (int32_t)(e0 + c);
+                    // stage eight columns at a time so a candidate can be read by column
+#pragma unroll
+                    for (int rd = 0; rd < EPI_COLS / 8; ++rd) {
+                        uint32_t m8 = (cand >> (8 * rd)) & 0xffu;
+                        if (!m8) continue;
+                        reinterpret_cast<float4 *>(stg)[0] =
+                            make_float4(acc[4 * rd].x, acc[4 * rd].y, acc[4 * rd + 1].x,
+                                        acc[4 * rd + 1].y);
+                        reinterpret_cast<float4 *>(stg)[1] =
+                            make_float4(acc[4 * rd + 2].x, acc[4 * rd + 2].y, acc[4 * rd + 3].x,
+                                        acc[4 * rd + 3].y);
+                        while (m8) {
+                            const int c = __ffs(m8) - 1;
+                            m8 &= m8 - 1;
+                            if (base < a.cap) {
+                                ck[base] = order_key(stg[c]);
+                                ci[base] = (int32_t)(e0 + 8 * rd + c);
+                            }
+                            ++base;
                         }
-                        ++base;
                     }
                 }
             }
@@ -571,7 +539,8 @@ bool index_tc_eligible(const void *qI, const void *kI, const lc_batch &b, int HI
 }
 
 template <int MODE, int HI>
-lc_status launch_tc(const CUtensorMap &mK, const IdxTcArgs &a, int64_t n_cols, cudaStream_t st) {
+lc_status launch_tc(const CUtensorMap &mQ, const CUtensorMap &mK, const IdxTcArgs &a, int64_t n_cols,
+                    cudaStream_t st) {
     constexpr uint32_t SMEM = IdxCfg::SMEM;
     static_assert(SMEM <= 227 * 1024, "indexer shared memory");
     auto kfn = k_index_tc<MODE, HI>;
@@ -585,14 +554,15 @@ lc_status launch_tc(const CUtensorMap &mK, const IdxTcArgs &a, int64_t n_cols, c
     const int64_t gy = (n_cols + a.chunk - 1) / a.chunk;
     if (gy < 1 || gy > 65535) return LC_ERR_UNSUPPORTED;
     dim3 grid((unsigned)((a.Nq + IBM - 1) / IBM), (unsigned)gy);
-    LC_LAUNCH(kfn, grid, dim3(I_THREADS), SMEM, st, mK, a);
+    LC_LAUNCH(kfn, grid, dim3(I_THREADS), SMEM, st, mQ, mK, a);
     return check_launch();
 }
 
 template <int MODE>
-lc_status launch_tc_hi(int HI, const CUtensorMap &mK, const IdxTcArgs &a, int64_t n_cols,
-                       cudaStream_t st) {
-    return HI == 8 ? launch_tc<MODE, 8>(mK, a, n_cols, st) : launch_tc<MODE, 4>(mK, a, n_cols, st);
+lc_status launch_tc_hi(int HI, const CUtensorMap &mQ, const CUtensorMap &mK, const IdxTcArgs &a,
+                       int64_t n_cols, cudaStream_t st) {
+    return HI == 8 ? launch_tc<MODE, 8>(mQ, mK, a, n_cols, st)
+                   : launch_tc<MODE, 4>(mQ, mK, a, n_cols, st);
 }
 
 // entries per CTA: about eight waves of CTAs over the 148 SMs, at least 16 tiles each
@@ -634,8 +604,10 @@ lc_status index_tc_materialize(const void *qI, const float *w, const void *kI, c
                                int HI, int dI, int m, lc_dtype dt, float *scores, int64_t ld,
                                int32_t *dev_err, cudaStream_t st) {
     if (!index_tc_eligible(qI, kI, b, HI, dI, dt)) return LC_ERR_UNSUPPORTED;
-    CUtensorMap mK;
-    if (!make_tmap_bf16_2d(&mK, kI, (uint64_t)b.total_c, (uint64_t)HI * IDI, HI * IDI * 2, IDI,
+    CUtensorMap mQ, mK;
+    if (!make_tmap_bf16_2d(&mQ, qI, (uint64_t)b.total_q, (uint64_t)HI * IDI, HI * IDI * 2, IDI,
+                           IBM) ||
+        !make_tmap_bf16_2d(&mK, kI, (uint64_t)b.total_c, (uint64_t)HI * IDI, HI * IDI * 2, IDI,
                            IBN))
         return LC_ERR_CUDA;
     IdxTcArgs a = base_args(b, qI, w, m, dev_err);
@@ -645,7 +617,7 @@ lc_status index_tc_materialize(const void *qI, const float *w, const void *kI, c
     a.ld = ld;
     a.vec_out = (reinterpret_cast<uintptr_t>(scores) & 15u) == 0 && (ld & 3) == 0;
     a.chunk = pick_chunk(b.total_q, ld);
-    return launch_tc_hi<MODE_MATERIALIZE>(HI, mK, a, ld, st);
+    return launch_tc_hi<MODE_MATERIALIZE>(HI, mQ, mK, a, ld, st);
 }
 
 // Fused exact top-k on the tensor cores (ws holds the plan's buffers), or
@@ -668,8 +640,9 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
     const int64_t Tc = b.total_c;
     const uint64_t pitch = (uint64_t)HI * IDI * 2;
 
-    CUtensorMap mKs, mK;
-    if (!make_tmap_bf16_2d(&mK, kI, (uint64_t)Tc, (uint64_t)HI * IDI, pitch, IDI, IBN) ||
+    CUtensorMap mQ, mKs, mK;
+    if (!make_tmap_bf16_2d(&mQ, qI, (uint64_t)b.total_q, (uint64_t)HI * IDI, pitch, IDI, IBM) ||
+        !make_tmap_bf16_2d(&mK, kI, (uint64_t)Tc, (uint64_t)HI * IDI, pitch, IDI, IBN) ||
         !make_tmap_bf16_2d(&mKs, kI, (uint64_t)((Tc + p.stride - 1) / p.stride),
                            (uint64_t)HI * IDI, pitch * p.stride, IDI, IBN))
         return LC_ERR_CUDA;
@@ -684,7 +657,7 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
         a.ld = p.lds;
         a.vec_out = 1;  // 256-byte aligned buffer, ld a multiple of 4
         a.chunk = pick_chunk(b.total_q, p.ns);
-        s = launch_tc_hi<MODE_MATERIALIZE>(HI, mKs, a, p.ns, st);
+        s = launch_tc_hi<MODE_MATERIALIZE>(HI, mQ, mKs, a, p.ns, st);
         if (s != LC_OK) return s;
     }
     // 2. thresholds
@@ -701,7 +674,7 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
         a.cand_idx = cidx;
         a.cap = p.cap;
         a.chunk = pick_chunk(b.total_q, Tc);
-        s = launch_tc_hi<MODE_FILTER>(HI, mK, a, Tc, st);
+        s = launch_tc_hi<MODE_FILTER>(HI, mQ, mK, a, Tc, st);
         if (s != LC_OK) return s;
     }
     // 4. exact selection among the candidates
@@ -725,3 +698,4 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
 }
 
 }  // namespace lc
+
