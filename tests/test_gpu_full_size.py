@@ -1,0 +1,130 @@
+"""Parity at the full benchmarked sizes, in the launch configuration the
+benchmark times, on sampled outputs the oracle computes one by one.
+
+- layer_pair_1m: 1,048,576-token context, last 4096 positions queried; CSA
+  (m=4, indexer 8x64 over 262,144 entries, top-k 1024, window 128) and HCA
+  (m'=128, window 128), 128 heads x 128.  The step is the benchmark's own.
+  Sampled query rows are checked against the oracle: the fused top-k (equal,
+  or the oracle's k-th / (k+1)-th gap below 1e-5), CSA attention (rows whose
+  selection equals the oracle's) and HCA attention, both within the bf16
+  tolerance; sampled compressed entries of the chunk within one bf16 ulp.
+- csa_decode: 64 sequences with contexts ~U[65536, 262144]; sampled
+  sequences are checked the same way.
+
+The oracle builds its own compressed caches from the raw inputs (rounded to
+bf16, the stored type) and never reads a value the CUDA path produced.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-2
+GAP = 1e-5
+
+
+@pytest.fixture(scope="module")
+def lc():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import long_context_compressed_13_b300 as m
+    m.load_library()
+    return m
+
+
+def _bf16_round(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).double().numpy()
+
+
+def _check_rows(gsel, I, nvis, k):
+    """Selections equal the oracle's, or are excused by the gap rule.
+    Returns the mask of rows whose selection is identical."""
+    rsel = oracle.topk(I, nvis, k)
+    same = np.all(gsel == rsel, axis=1)
+    for r in np.nonzero(~same)[0]:
+        s = np.sort(I[r, : nvis[r]])[::-1]
+        assert s[k - 1] - s[k] < GAP, f"row {r}: selection differs, gap {s[k - 1] - s[k]}"
+        keep = min(k, int(nvis[r]))
+        v = gsel[r, :keep]
+        assert np.all(np.diff(v) > 0) and v[0] >= 0 and v[-1] < nvis[r]
+        assert np.all(gsel[r, keep:] == -1)
+    return rsel, same
+
+
+def test_layer_pair_1m_sampled(lc):
+    import bench
+    wk = bench.LayerPair(lc, "cuda")
+    wk.step()
+    torch.cuda.synchronize()
+    assert int(wk.err.item()) == 0
+    P = wk.P
+    c, h = P["csa"], P["hca"]
+    Pc = {"csa": {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in c.items()},
+          "hca": {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in h.items()}}
+    st, raw, kI64 = bench._oracle_state(Pc, wk.q0, wk.ctx, wk.m_c, wk.m_h, wk.W)
+    Kc, Vc = _bf16_round(st["Kc"]), _bf16_round(st["Vc"])
+    Kh, Vh = _bf16_round(st["Kh"]), _bf16_round(st["Vh"])
+
+    # compressed entries written by the timed step (the chunk's entries)
+    rng = np.random.default_rng(11)
+    for name, gpu, ref, m in (("csa K", wk.Kc, Kc, wk.m_c), ("csa V", wk.Vc, Vc, wk.m_c),
+                              ("hca K", wk.Kh, Kh, wk.m_h), ("hca V", wk.Vh, Vh, wk.m_h)):
+        lo = wk.q0 // m
+        ents = np.unique(np.concatenate([[lo, ref.shape[0] - 1],
+                                         rng.integers(lo, ref.shape[0], 30)]))
+        got = gpu[torch.from_numpy(ents).cuda()].double().cpu().numpy()
+        ulp = np.abs(ref[ents]) * 2.0 ** -7 + 1e-30
+        assert np.all(np.abs(got - ref[ents]) <= ulp), name
+
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 2047, 4094, 4095],
+                                     rng.choice(wk.chunk, 9, replace=False)]))
+    t = (wk.q0 + rows).astype(np.int64)
+    I = oracle.index(c["qI"][rows].cpu(), c["w"][rows].cpu(), kI64, t, wk.m_c)
+    gsel = wk.sel[torch.from_numpy(rows).cuda()].cpu().numpy()
+    rsel, same = _check_rows(gsel, I, (t + 1) // wk.m_c, wk.k)
+    assert same.sum() >= len(rows) - 2
+
+    rO, rl = oracle.sparse_attn(c["Q"][rows].cpu(), Kc, Vc, rsel, raw["csa_K"], raw["csa_V"],
+                                raw["pos0"], t, wk.W, c["scale"])
+    gO = wk.O_csa[torch.from_numpy(rows).cuda()].double().cpu().numpy()
+    np.testing.assert_allclose(gO[same], rO[same], rtol=0, atol=TOL)
+    gl = wk.lse_csa[torch.from_numpy(rows).cuda()].double().cpu().numpy()
+    np.testing.assert_allclose(gl[same], rl[same], rtol=0, atol=TOL)
+
+    rOh, rlh = oracle.hca_attn(h["Q"][rows].cpu(), Kh, Vh, wk.m_h, raw["hca_K"], raw["hca_V"],
+                               raw["pos0"], t, wk.W, h["scale"])
+    gOh = wk.O_hca[torch.from_numpy(rows).cuda()].double().cpu().numpy()
+    np.testing.assert_allclose(gOh, rOh, rtol=0, atol=TOL)
+    glh = wk.lse_hca[torch.from_numpy(rows).cuda()].double().cpu().numpy()
+    np.testing.assert_allclose(glh, rlh, rtol=0, atol=TOL)
+
+
+def test_csa_decode_sampled(lc):
+    import bench
+    wk = bench.Decode(lc, "cuda")
+    wk.step()
+    torch.cuda.synchronize()
+    assert int(wk.err.item()) == 0
+    D = wk.D
+    bt = D["batch"]
+    gsel_all = wk.sel.cpu().numpy()
+    gO_all = wk.O.double().cpu().numpy()
+    gl_all = wk.lse.double().cpu().numpy()
+    # the shortest and longest contexts and a few more
+    order = np.argsort(D["ctx"])
+    seqs = np.unique(np.concatenate([order[:1], order[-1:], [0, 17, 40]]))
+    for s in seqs:
+        c0, c1, r0, r1 = bt.cu_c[s], bt.cu_c[s + 1], bt.cu_raw[s], bt.cu_raw[s + 1]
+        t = np.array([bt.q_pos0[s]], dtype=np.int64)
+        I = oracle.index(D["qI"][s:s + 1].cpu(), D["w"][s:s + 1].cpu(), D["kI"][c0:c1].cpu(), t,
+                         wk.m)
+        rsel, same = _check_rows(gsel_all[s:s + 1], I, (t + 1) // wk.m, wk.k)
+        if not same[0]:
+            continue
+        rO, rl = oracle.sparse_attn(D["Q"][s:s + 1].cpu(), D["Kc"][c0:c1].cpu(),
+                                    D["Vc"][c0:c1].cpu(), rsel, D["Kraw"][r0:r1].cpu(),
+                                    D["Vraw"][r0:r1].cpu(), bt.raw_pos0[s], t, wk.W, D["scale"])
+        np.testing.assert_allclose(gO_all[s:s + 1], rO, rtol=0, atol=TOL)
+        np.testing.assert_allclose(gl_all[s:s + 1], rl, rtol=0, atol=TOL)

@@ -145,6 +145,31 @@ def test_index_scan_ragged_decode(lc):
             assert boundary_gap(ref[0], nv, 64) < GAP
 
 
+@pytest.mark.parametrize("HI", [4, 8])
+def test_index_stream_long_rows(lc, HI):
+    # decode rows long enough to be split across several CTAs of the
+    # streaming indexer (1024+ entries each), both head counts it serves
+    D = wl.csa_decode(B=3, ctx_lo=9000, ctx_hi=24000, H=8, d=64, HI=HI, dI=64, m=4, k=128, W=16,
+                      dtype="bf16", seed=19)
+    b = lc.DeviceBatch.from_workload(D["batch"])
+    sc, sel = lc.lightning_index(dev(D["qI"]), dev(D["w"]), dev(D["kI"]), b, 4, k=128, topk=True)
+    torch.cuda.synchronize()
+    got, gsel = sc.cpu().double().numpy(), sel.cpu().numpy()
+    bt = D["batch"]
+    for s in range(bt.B):
+        c0, c1 = bt.cu_c[s], bt.cu_c[s + 1]
+        t = bt.q_pos0[s]
+        nv = c1 - c0
+        assert nv > 2048
+        ref = oracle.index(D["qI"][s:s + 1], D["w"][s:s + 1], D["kI"][c0:c1], [t], 4)
+        assert np.all(np.isneginf(got[s, nv:]))
+        bound = _index_bound(D["qI"][s:s + 1], D["w"][s:s + 1], D["kI"][c0:c1], [t], 4)
+        assert np.all(np.abs(got[s, :nv] - ref[0]) <= bound[0])
+        osel = oracle.topk(ref, [nv], 128)[0]
+        if not np.array_equal(osel, gsel[s]):
+            assert boundary_gap(ref[0], nv, 128) < GAP
+
+
 # ------------------------------------------------------------------- top-k
 
 def _score_rows(kind, Nq, ld, seed):
