@@ -50,6 +50,19 @@ METRIC = "CSA+HCA attention query-tokens/s (prefill & decode) and % of B300 roof
 UNIT = "query-tokens/s"
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per step of the
+# kernels of each workload's dominant stage, from one ncu capture of the
+# current kernels at the full benchmarked size (traffic well above the
+# algorithmic bytes would mean re-reads).  Re-measure when a kernel changes.
+NCU_STAGE_TRAFFIC = {
+    # index + top-k: candidate pass 331.3 MB, 1/32 sample 91.8 MB, threshold
+    # 134.5 MB, candidate top-k 68.4 MB
+    "layer_pair_1m": 626.0e6,
+    # index + top-k: streaming indexer 2505.6 MB, radix top-k 9.8 MB
+    "csa_decode": 2515.4e6,
+}
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -228,8 +241,11 @@ class LayerPair:
         achieved = flops_of[dom] / (dom_ms / 1e3) / 1e12
         long_region = region_ms > 1000.0
         peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
+        traffic = NCU_STAGE_TRAFFIC["layer_pair_1m"] if (dom == "lightning_index+topk" and
+                                                         self.ctx == 1 << 20) else None
         return {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                "traffic_unit": "bytes per launch of the stage's kernels (ncu)",
                 "peak_source": peaks["source"] + (" sustained" if long_region else " burst")}
 
     def path_tflops(self, ms_step):
@@ -328,7 +344,9 @@ class Decode:
         gbs = w["index_bytes"] / (ms / 1e3) / 1e9
         return {"bound": "hbm", "kernel": "lightning_index+topk", "achieved": gbs,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
-                "traffic": None, "peak_source": peaks["source"]}
+                "traffic": NCU_STAGE_TRAFFIC["csa_decode"],
+                "traffic_unit": "bytes per launch of the stage's kernels (ncu)",
+                "algorithmic_bytes": w["index_bytes"], "peak_source": peaks["source"]}
 
 
 # ---------------------------------------------------------------- our arm
