@@ -55,11 +55,13 @@ UNIT = "query-tokens/s"
 # current kernels at the full benchmarked size (traffic well above the
 # algorithmic bytes would mean re-reads).  Re-measure when a kernel changes.
 NCU_STAGE_TRAFFIC = {
-    # index + top-k: candidate pass 331.3 MB, 1/32 sample 91.8 MB, threshold
-    # 134.5 MB, candidate top-k 68.4 MB
-    "layer_pair_1m": 626.0e6,
+    # index + top-k: candidate pass 331.0 MB, 1/32 sample 91.6 MB, threshold
+    # 134.4 MB, candidate top-k 67.7 MB
+    ("layer_pair_1m", "lightning_index+topk"): 624.7e6,
+    # HCA attention: k_hca_tc 140.9 MB read, 88.7 MB written
+    ("layer_pair_1m", "hca_dense_attn"): 229.5e6,
     # index + top-k: streaming indexer 2505.6 MB, radix top-k 9.8 MB
-    "csa_decode": 2515.4e6,
+    ("csa_decode", "lightning_index+topk"): 2515.4e6,
 }
 
 
@@ -241,8 +243,7 @@ class LayerPair:
         achieved = flops_of[dom] / (dom_ms / 1e3) / 1e12
         long_region = region_ms > 1000.0
         peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
-        traffic = NCU_STAGE_TRAFFIC["layer_pair_1m"] if (dom == "lightning_index+topk" and
-                                                         self.ctx == 1 << 20) else None
+        traffic = NCU_STAGE_TRAFFIC.get(("layer_pair_1m", dom)) if self.ctx == 1 << 20 else None
         return {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                 "traffic_unit": "bytes per launch of the stage's kernels (ncu)",
@@ -344,7 +345,7 @@ class Decode:
         gbs = w["index_bytes"] / (ms / 1e3) / 1e9
         return {"bound": "hbm", "kernel": "lightning_index+topk", "achieved": gbs,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
-                "traffic": NCU_STAGE_TRAFFIC["csa_decode"],
+                "traffic": NCU_STAGE_TRAFFIC[("csa_decode", "lightning_index+topk")],
                 "traffic_unit": "bytes per launch of the stage's kernels (ncu)",
                 "algorithmic_bytes": w["index_bytes"], "peak_source": peaks["source"]}
 

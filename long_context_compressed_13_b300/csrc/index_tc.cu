@@ -20,9 +20,9 @@
 //               tile (MATERIALIZE) or appends the entries whose score reaches
 //               the row's threshold to the row's candidate list (FILTER).  The
 //               threshold test is a sign-bit collect of acc - theta; the
-//               candidates are staged eight columns at a time.  A
-//               buffer is handed back to its issuer through a shared-memory
-//               release counter as soon as the warp's TMEM read completes.
+//               candidates are staged eight columns at a time.  A buffer is handed
+//               back to its issuer through an mbarrier (one arrival per warp)
+//               as soon as the warp's TMEM read completes.
 // The fused top-k of a row (see index_topk_tc_launch):
 //   1. scores of every s-th entry (MATERIALIZE over a strided tensor map);
 //   2. theta = the rho-th largest sampled key, a lower bound for the k-th
@@ -75,43 +75,25 @@ struct IdxCfg {
 
 struct IdxBars {
     uint64_t q_full, k_full[NSB], k_empty[NSB], d_full[NBUF];
-    // releases of each score buffer: every epilogue warp adds 1 once its
-    // reads of a use of the buffer are complete (a shared-memory counter is
-    // far cheaper for the MMA issuers to poll than an mbarrier)
-    uint32_t freed[NBUF];
+    // releases of each score buffer: every epilogue warp arrives once its
+    // reads of a use of the buffer are complete
+    uint64_t freed[NBUF];
     uint32_t taddr;
     int abort;
 };
 
 
 
-// Counter hand-off between the epilogue (after tcgen05.wait::ld and
-// tcgen05.fence::before_thread_sync) and an MMA issuer (followed by
-// tcgen05.fence::after_thread_sync): release add / acquire load at CTA scope.
-__device__ __forceinline__ void release_add(uint32_t *ctr) {
-    asm volatile("red.release.cta.shared::cta.add.u32 [%0], 1;" ::"r"(smem_u32(ctr)) : "memory");
-}
-// Bounded spin until *ctr >= target (same give-up rule as mbar_wait): plain
-// volatile polls, the clock checked every 256 polls, and one acquire fence
-// once the target is seen.
-__device__ __forceinline__ bool wait_count(const uint32_t *ctr, uint32_t target, volatile int *abort,
-                                           long long limit = 4000000000LL) {
-    const volatile uint32_t *vc = ctr;
-    if (*vc < target) {
-        const long long t0 = clock64();
-        for (uint32_t it = 1;; ++it) {
-            if (*vc >= target) break;
-            if ((it & 255u) == 0u) {
-                if (*abort) return false;
-                if (clock64() - t0 > limit) {
-                    *abort = 1;
-                    return false;
-                }
-            }
-        }
-    }
-    asm volatile("fence.acq_rel.cta;" ::: "memory");
-    return true;
+// Lane 0 of the warp arrives on `bar` (a predicated instruction, no branch);
+// called after tcgen05.wait::ld and tcgen05.fence::before_thread_sync so the
+// MMA issuer that waits on `bar` may overwrite the buffer just read.
+__device__ __forceinline__ void arrive_lane0(uint64_t *bar, int lane) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.eq.s32 p, %1, 0;\n\t"
+        "@p mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n\t}" ::"r"(smem_u32(bar)),
+        "r"(lane)
+        : "memory");
 }
 
 // Inverse of order_key: the float whose key is `key` (+0 for the key of
@@ -138,8 +120,7 @@ struct IdxTcArgs {
     int vec_out;             // MATERIALIZE: out and ld allow 16-byte stores
     const uint32_t *theta;   // FILTER: [Nq] order-key thresholds
     int32_t *count;          // FILTER: [Nq] candidate counts (zeroed beforehand)
-    uint32_t *cand_key;      // FILTER: [Nq, cap]
-    int32_t *cand_idx;       // FILTER: [Nq, cap]
+    uint2 *cand;             // FILTER: [Nq, cap] (order key, entry index)
     int cap;
     int32_t *dev_err;
 };
@@ -178,7 +159,7 @@ __global__ void __launch_bounds__(I_THREADS, 1)
         }
         for (int b = 0; b < NBUF; ++b) {
             mbar_init(&bars.d_full[b], 1);
-            bars.freed[b] = 0u;
+            mbar_init(&bars.freed[b], NEPI / 32);
         }
         fence_barrier_init();
     }
@@ -227,7 +208,7 @@ __global__ void __launch_bounds__(I_THREADS, 1)
             for (int g = par; ok && g < n_all; g += 2) {
                 const int s = g % NSB, h = g % HI, b = g % NBUF, u = g / NBUF;
                 if (!mbar_wait(&bars.k_full[s], (g / NSB) & 1, abort) ||
-                    (u > 0 && !wait_count(&bars.freed[b], (uint32_t)u * (NEPI / 32), abort)))
+                    (u > 0 && !mbar_wait(&bars.freed[b], (uint32_t)(u - 1) & 1u, abort)))
                     break;
                 tc_fence_after();
                 const uint32_t k_base = smem_u32(smem + C::SM_K + s * C::HEAD_BOX);
@@ -260,14 +241,17 @@ __global__ void __launch_bounds__(I_THREADS, 1)
         bool ok = !dead;
         float *stg = reinterpret_cast<float *>(smem + C::SM_STG) + tid * 8;
         float2 acc[EPI_COLS / 2];
-        bool ready = false;  // the next buffer's barrier was seen complete
         for (int i = 0; ok && i < n_t; ++i) {
 #pragma unroll
             for (int c = 0; c < EPI_COLS / 2; ++c) acc[c] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int h = 0; h < HI; ++h) {
+                // buffer and phase of the g-th head are compile-time for HI = 8
                 const int g = i * HI + h, b = g % NBUF;
-                if (!ready && !__all_sync(FULL, mbar_wait(&bars.d_full[b], (g / NBUF) & 1, abort))) {
+                const uint32_t ph = (uint32_t)(g / NBUF) & 1u;
+                // the (suspending) try-wait normally succeeds; the bounded loop is the slow path
+                if (!__all_sync(FULL, mbar_try_wait(&bars.d_full[b], ph)) &&
+                    !__all_sync(FULL, mbar_wait(&bars.d_full[b], ph, abort))) {
                     ok = false;
                     break;
                 }
@@ -276,18 +260,12 @@ __global__ void __launch_bounds__(I_THREADS, 1)
                 tmem_ld32(buf_addr + b * IBN, v);
                 tmem_wait_ld();
                 tc_fence_before();
-                __syncwarp();
-                if (lane == 0) release_add(&bars.freed[b]);
-                // early, non-blocking look at the next buffer; verdict after the fold
-                const bool more = g + 1 < n_all;
-                bool t_next = more;
-                if (more) t_next = mbar_test(&bars.d_full[(g + 1) % NBUF], ((g + 1) / NBUF) & 1);
+                arrive_lane0(&bars.freed[b], lane);
                 const float2 w2 = make_float2(wh[h], wh[h]);
 #pragma unroll
                 for (int c = 0; c < EPI_COLS / 2; ++c)
                     acc[c] = __ffma2_rn(w2, make_float2(fmaxf(v[2 * c], 0.f), fmaxf(v[2 * c + 1], 0.f)),
                                         acc[c]);
-                ready = more && __all_sync(FULL, t_next);
             }
             if (!ok) break;
             if (!row_ok) continue;
@@ -323,8 +301,7 @@ __global__ void __launch_bounds__(I_THREADS, 1)
                 if (lim < EPI_COLS) cand &= lim <= 0 ? 0u : ((1u << lim) - 1u);
                 if (cand) {
                     int base = atomicAdd(a.count + row, __popc(cand));
-                    uint32_t *ck = a.cand_key + row * a.cap;
-                    int32_t *ci = a.cand_idx + row * a.cap;
+                    uint2 *cr = a.cand + row * a.cap;
                     // stage eight columns at a time so a candidate can be read by column
 #pragma unroll
                     for (int rd = 0; rd < EPI_COLS / 8; ++rd) {
@@ -339,10 +316,8 @@ __global__ void __launch_bounds__(I_THREADS, 1)
                         while (m8) {
                             const int c = __ffs(m8) - 1;
                             m8 &= m8 - 1;
-                            if (base < a.cap) {
-                                ck[base] = order_key(stg[c]);
-                                ci[base] = (int32_t)(e0 + 8 * rd + c);
-                            }
+                            if (base < a.cap)
+                                cr[base] = make_uint2(order_key(stg[c]), (uint32_t)(e0 + 8 * rd + c));
                             ++base;
                         }
                     }
@@ -367,12 +342,17 @@ __global__ void __launch_bounds__(I_THREADS, 1)
 
 // theta[r] = the rho-th largest order key among the row's visible sampled
 // scores (0, i.e. "keep everything", when the row has at most k visible
-// entries or fewer than rho samples); count[r] = fail[r] = 0.
+// entries or fewer than rho samples); count[r] = fail[r] = 0.  With
+// `staged`, the row's keys are first copied to shared memory (one read of
+// the row; the second half of the buffer takes the compacted keys) and the
+// radix passes run there.
 __global__ void __launch_bounds__(512) k_sample_threshold(const float *__restrict__ samp,
                                                           int64_t lds, Batch bt, int m,
-                                                          int stride, int k, int rho,
+                                                          int stride, int k, int rho, int staged,
                                                           uint32_t *theta, int32_t *count,
                                                           int32_t *fail) {
+    constexpr int NT = 512;
+    extern __shared__ uint32_t skeys[];
     __shared__ RadixScratch rs;
     const int64_t r = blockIdx.x;
     const int64_t t = bt.q_pos0[0] + r;
@@ -383,7 +363,19 @@ __global__ void __launch_bounds__(512) k_sample_threshold(const float *__restric
     uint32_t th = 0;
     if (nv > k && rho <= nvs) {
         int need_left;
-        th = radix_kth_largest<512>(samp + r * lds, nvs, rho, rs, &need_left);
+        if (staged) {
+            // lds is a multiple of 4 and the buffer 16-byte aligned
+            const float4 *row4 = reinterpret_cast<const float4 *>(samp + r * lds);
+            for (int j = threadIdx.x; 4 * j < nvs; j += NT) {
+                const float4 x = __ldg(row4 + j);
+                reinterpret_cast<uint4 *>(skeys)[j] =
+                    make_uint4(order_key(x.x), order_key(x.y), order_key(x.z), order_key(x.w));
+            }
+            __syncthreads();
+            th = radix_kth_largest_smem<NT>(skeys, (int)nvs, rho, rs, &need_left, skeys + lds);
+        } else {
+            th = radix_kth_largest<NT>(samp + r * lds, nvs, rho, rs, &need_left);
+        }
     }
     if (threadIdx.x == 0) {
         theta[r] = th;
@@ -415,23 +407,28 @@ __device__ __forceinline__ void bitonic_sort_u32_asc(uint32_t *a, int P) {
 
 // Exact top-k of each row's candidates: radix selection of the k-th largest
 // key K* in shared memory; the candidates above K* and the `need` lowest-index
-// candidates equal to K* are collected (in any order) and their indices sorted
-// ascending.  Rows whose candidate count is outside [k, cap] are marked in
-// fail[].  Shared memory: cap keys, cap indices, PK collected indices, P tie
-// slots (PK, P: powers of two >= k, cap).
-__global__ void __launch_bounds__(512) k_cand_pick(Batch bt, int m, int k, int cap, int PK, int P,
-                                                   const int32_t *__restrict__ count,
-                                                   const uint32_t *__restrict__ cand_key,
-                                                   const int32_t *__restrict__ cand_idx,
+// candidates equal to K* are collected (in any order, one shared atomic per
+// warp) and written out in ascending index order: through a bitmap over the
+// row's visible entries when it fits in the `R` words that held the keys and
+// indices, else by a bitonic sort.  Rows whose candidate count is outside
+// [k, cap] are marked in fail[].  Shared memory: R >= 2 cap words (keys,
+// indices, later the bitmap), PK collected indices, P tie slots (PK, P: powers
+// of two >= k, cap); the tie slots double as the radix selection's spare.
+__global__ void __launch_bounds__(512) k_cand_pick(Batch bt, int m, int k, int cap, int R, int PK,
+                                                   int P, const int32_t *__restrict__ count,
+                                                   const uint2 *__restrict__ cand,
                                                    int32_t *__restrict__ topk, int32_t *fail) {
-    constexpr int NT = 512;
+    constexpr int NT = 512, NW = NT / 32;
+    const unsigned FULL = 0xffffffffu;
     extern __shared__ uint32_t sbuf[];
     uint32_t *keys = sbuf;                                      // [cap]
     uint32_t *idx = sbuf + cap;                                 // [cap]
-    uint32_t *sel = sbuf + 2 * cap;                             // [PK]
+    uint32_t *bm = sbuf;                                        // [R], after the collection
+    uint32_t *sel = sbuf + R;                                   // [PK]
     uint32_t *tl = sel + PK;                                    // [P]
     __shared__ RadixScratch rs;
-    __shared__ int s_n, s_ties;
+    __shared__ int s_n, s_ties, wsum[NW];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t r = blockIdx.x;
     const int64_t t = bt.q_pos0[0] + r;
     const int64_t Tc = bt.cu_c[1] - bt.cu_c[0];
@@ -448,21 +445,34 @@ __global__ void __launch_bounds__(512) k_cand_pick(Batch bt, int m, int k, int c
         return;
     }
     for (int i = threadIdx.x; i < n; i += NT) {
-        keys[i] = cand_key[r * cap + i];
-        idx[i] = (uint32_t)cand_idx[r * cap + i];
+        const uint2 ki = cand[r * cap + i];
+        keys[i] = ki.x;
+        idx[i] = ki.y;
     }
-    for (int i = threadIdx.x; i < PK; i += NT) sel[i] = 0xFFFFFFFFu;
+    for (int i = threadIdx.x; i < PK; i += NT) sel[i] = 0xFFFFFFFFu;  // bitonic padding
     if (threadIdx.x == 0) {
         s_n = 0;
         s_ties = 0;
     }
     __syncthreads();
     int need;
-    const uint32_t kstar = radix_kth_largest_smem<NT>(keys, n, k, rs, &need);
+    const uint32_t kstar = radix_kth_largest_smem<NT>(keys, n, k, rs, &need, tl);
     // candidates above K* are in; the ties at K* go to a list
-    for (int i = threadIdx.x; i < n; i += NT) {
-        if (keys[i] > kstar) sel[atomicAdd(&s_n, 1)] = idx[i];
-        else if (keys[i] == kstar) tl[atomicAdd(&s_ties, 1)] = idx[i];
+    for (int j0 = threadIdx.x & ~31; j0 < n; j0 += NT) {
+        const int j = j0 + lane;
+        const uint32_t key = j < n ? keys[j] : 0u;
+        const bool up = j < n && key > kstar, eq = j < n && key == kstar;
+        const uint32_t mu = __ballot_sync(FULL, up), me = __ballot_sync(FULL, eq);
+        int bu = 0, be = 0;
+        if (lane == 0) {
+            if (mu) bu = atomicAdd(&s_n, __popc(mu));
+            if (me) be = atomicAdd(&s_ties, __popc(me));
+        }
+        bu = __shfl_sync(FULL, bu, 0);
+        be = __shfl_sync(FULL, be, 0);
+        const uint32_t lt = (1u << lane) - 1u;
+        if (up) sel[bu + __popc(mu & lt)] = idx[j];
+        if (eq) tl[be + __popc(me & lt)] = idx[j];
     }
     __syncthreads();
     const int above = s_n, ties = s_ties;
@@ -476,9 +486,49 @@ __global__ void __launch_bounds__(512) k_cand_pick(Batch bt, int m, int k, int c
         bitonic_sort_u32_asc(tl, Pt);
         for (int i = threadIdx.x; i < need; i += NT) sel[above + i] = tl[i];
     }
-    bitonic_sort_u32_asc(sel, PK);
-    for (int i = threadIdx.x; i < k; i += NT) out[i] = (int32_t)sel[i];
-    (void)P;
+    const int nw = (int)((nv + 31) >> 5);
+    if (nw > R) {
+        bitonic_sort_u32_asc(sel, PK);
+        for (int i = threadIdx.x; i < k; i += NT) out[i] = (int32_t)sel[i];
+        return;
+    }
+    // ascending order through a bitmap of the chosen entries (keys and indices are dead)
+    __syncthreads();
+    for (int w = threadIdx.x; w < nw; w += NT) bm[w] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < k; i += NT) {
+        const uint32_t e = sel[i];
+        atomicOr(&bm[e >> 5], 1u << (e & 31u));
+    }
+    __syncthreads();
+    // warp w owns words [wb, we); its lanes take consecutive words
+    const int per_w = (nw + NW - 1) / NW;
+    const int wb = min(warp * per_w, nw), we = min(wb + per_w, nw);
+    int cnt = 0;
+    for (int w = wb + lane; w < we; w += 32) cnt += __popc(bm[w]);
+    cnt = __reduce_add_sync(FULL, cnt);
+    if (lane == 0) wsum[warp] = cnt;
+    __syncthreads();
+    int off = 0;
+    for (int u = 0; u < warp; ++u) off += wsum[u];
+    for (int w0 = wb; w0 < we; w0 += 32) {
+        const int w = w0 + lane;
+        uint32_t x = w < we ? bm[w] : 0u;
+        const int c = __popc(x);
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(FULL, incl, o);
+            if (lane >= o) incl += y;
+        }
+        int pos = off + incl - c;
+        while (x) {
+            const int b = __ffs(x) - 1;
+            x &= x - 1;
+            out[pos++] = w * 32 + b;
+        }
+        off += __shfl_sync(FULL, incl, 31);
+    }
 }
 
 namespace {
@@ -489,9 +539,9 @@ int pow2_at_least(int x) {
 }
 
 struct FusedPlan {
-    int stride, rho, cap, P, PK;
+    int stride, rho, cap, P, PK, R, staged;
     int64_t ns, lds;
-    size_t off_samp, off_theta, off_count, off_fail, off_ckey, off_cidx, off_full, total;
+    size_t off_samp, off_theta, off_count, off_fail, off_cand, off_full, total;
 };
 
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -515,16 +565,21 @@ FusedPlan plan_fused(const lc_batch &b, int k) {
     p.cap = cap;
     p.P = pow2_at_least(cap);
     p.PK = pow2_at_least(k);
+    // k_cand_pick orders its output through a bitmap of the row when that fits
+    p.R = 2 * cap;
+    const int64_t nw = (n + 31) / 32;
+    if (nw > p.R && 4 * (nw + p.PK + p.P) <= 200 * 1024) p.R = (int)nw;
     p.ns = (n + p.stride - 1) / p.stride;
     p.lds = (p.ns + 3) & ~(int64_t)3;
+    // k_sample_threshold keeps the row (and its compacted keys) in shared memory
+    p.staged = 8 * p.lds <= 200 * 1024;
     const size_t Nq = (size_t)b.total_q;
     size_t o = 0;
     p.off_samp = o;  o += al256(sizeof(float) * Nq * (size_t)p.lds);
     p.off_theta = o; o += al256(sizeof(uint32_t) * Nq);
     p.off_count = o; o += al256(sizeof(int32_t) * Nq);
     p.off_fail = o;  o += al256(sizeof(int32_t) * Nq);
-    p.off_ckey = o;  o += al256(sizeof(uint32_t) * Nq * (size_t)p.cap);
-    p.off_cidx = o;  o += al256(sizeof(int32_t) * Nq * (size_t)p.cap);
+    p.off_cand = o;  o += al256(sizeof(uint2) * Nq * (size_t)p.cap);
     p.off_full = o;  o += al256(sizeof(float) * Nq * (size_t)n);
     p.total = o;
     return p;
@@ -634,8 +689,7 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
     uint32_t *theta = reinterpret_cast<uint32_t *>(base + p.off_theta);
     int32_t *count = reinterpret_cast<int32_t *>(base + p.off_count);
     int32_t *fail = reinterpret_cast<int32_t *>(base + p.off_fail);
-    uint32_t *ckey = reinterpret_cast<uint32_t *>(base + p.off_ckey);
-    int32_t *cidx = reinterpret_cast<int32_t *>(base + p.off_cidx);
+    uint2 *cand = reinterpret_cast<uint2 *>(base + p.off_cand);
     float *full = reinterpret_cast<float *>(base + p.off_full);
     const int64_t Tc = b.total_c;
     const uint64_t pitch = (uint64_t)HI * IDI * 2;
@@ -661,8 +715,19 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
         if (s != LC_OK) return s;
     }
     // 2. thresholds
-    LC_LAUNCH(k_sample_threshold, dim3((unsigned)b.total_q), dim3(512), 0, st, samp, p.lds,
-              to_dev(b), m, p.stride, k, p.rho, theta, count, fail);
+    {
+        const size_t smem = p.staged ? 2 * sizeof(uint32_t) * (size_t)p.lds : 0;
+        static size_t attr = 0;
+        if (smem > 48 * 1024 && smem > attr) {
+            if (cudaFuncSetAttribute(k_sample_threshold,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem) != cudaSuccess)
+                return LC_ERR_CUDA;
+            attr = smem;
+        }
+        LC_LAUNCH(k_sample_threshold, dim3((unsigned)b.total_q), dim3(512), smem, st, samp,
+                  p.lds, to_dev(b), m, p.stride, k, p.rho, p.staged, theta, count, fail);
+    }
     if ((s = check_launch()) != LC_OK) return s;
     // 3. candidates
     {
@@ -670,8 +735,7 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
         a.Tc = Tc;
         a.theta = theta;
         a.count = count;
-        a.cand_key = ckey;
-        a.cand_idx = cidx;
+        a.cand = cand;
         a.cap = p.cap;
         a.chunk = pick_chunk(b.total_q, Tc);
         s = launch_tc_hi<MODE_FILTER>(HI, mQ, mK, a, Tc, st);
@@ -679,7 +743,7 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
     }
     // 4. exact selection among the candidates
     {
-        const size_t smem = sizeof(uint32_t) * (size_t)(2 * p.cap + p.PK + p.P);
+        const size_t smem = sizeof(uint32_t) * (size_t)(p.R + p.PK + p.P);
         static size_t attr = 0;
         if (smem > 48 * 1024 && smem > attr) {
             if (cudaFuncSetAttribute(k_cand_pick, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -688,7 +752,7 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
             attr = smem;
         }
         LC_LAUNCH(k_cand_pick, dim3((unsigned)b.total_q), dim3(512), smem, st, to_dev(b), m, k,
-                  p.cap, p.PK, p.P, count, ckey, cidx, topk, fail);
+                  p.cap, p.R, p.PK, p.P, count, cand, topk, fail);
         if ((s = check_launch()) != LC_OK) return s;
     }
     // 5. exact fallback for the rows marked in fail[] (no work when none is)

@@ -41,6 +41,8 @@ struct RadixScratch {
     uint32_t hist[256];
     uint32_t digit;
     int need;
+    int cnt;   // keys in the chosen bin
+    int fill;  // compaction cursor
 };
 
 // The `need`-th largest order key (1-based) among order_key(row[0..n-1]),
@@ -101,18 +103,23 @@ __device__ uint32_t radix_kth_largest(const float *__restrict__ row, int64_t n, 
     return prefix;
 }
 
-// As radix_kth_largest, over n order keys held in shared memory.
+// As radix_kth_largest, over n order keys held in shared memory.  With
+// `spare` (room for n keys, NT a multiple of 32), the keys that still match
+// after the first pass are copied there when they are at most half of all,
+// and the last three passes scan only them.
 template <int NT>
 __device__ uint32_t radix_kth_largest_smem(const uint32_t *keys, int n, int need,
-                                           RadixScratch &rs, int *need_left) {
+                                           RadixScratch &rs, int *need_left,
+                                           uint32_t *spare = nullptr) {
     uint32_t prefix = 0, mask = 0;
+    const uint32_t *src = keys;
 #pragma unroll 1
     for (int pass = 0; pass < 4; ++pass) {
         const int shift = 24 - 8 * pass;
         for (int i = threadIdx.x; i < 256; i += NT) rs.hist[i] = 0;
         __syncthreads();
         for (int j = threadIdx.x; j < n; j += NT) {
-            const uint32_t key = keys[j];
+            const uint32_t key = src[j];
             if ((key & mask) == prefix) atomicAdd(&rs.hist[(key >> shift) & 255u], 1u);
         }
         __syncthreads();
@@ -139,17 +146,37 @@ __device__ uint32_t radix_kth_largest_smem(const uint32_t *keys, int n, int need
                     if (cum + c[u] >= (uint32_t)need) {
                         rs.digit = 255u - (uint32_t)(lane * 8 + u);
                         rs.need = need - (int)cum;
+                        rs.cnt = (int)c[u];
                         break;
                     }
                     cum += c[u];
                 }
             }
+            if (lane == 0) rs.fill = 0;
         }
         __syncthreads();
         prefix |= rs.digit << shift;
         mask |= 255u << shift;
         need = rs.need;
+        const int nsel = rs.cnt;
         __syncthreads();
+        if (spare != nullptr && pass == 0 && 2 * nsel <= n) {
+            // the keys of the chosen bin, in any order; one shared atomic per warp
+            const int lane = threadIdx.x & 31;
+            for (int j0 = threadIdx.x & ~31; j0 < n; j0 += NT) {
+                const int j = j0 + lane;
+                const uint32_t key = j < n ? src[j] : 0u;
+                const bool in = j < n && (key & mask) == prefix;
+                const uint32_t bal = __ballot_sync(0xffffffffu, in);
+                int base = 0;
+                if (lane == 0 && bal) base = atomicAdd(&rs.fill, __popc(bal));
+                base = __shfl_sync(0xffffffffu, base, 0);
+                if (in) spare[base + __popc(bal & ((1u << lane) - 1u))] = key;
+            }
+            __syncthreads();
+            src = spare;
+            n = nsel;
+        }
     }
     *need_left = need;
     return prefix;
