@@ -326,13 +326,17 @@ __global__ void __launch_bounds__(H_THREADS, 1)
 #pragma unroll
             for (int c0 = 0; c0 < HBN; c0 += 32) {
                 uint32_t pk[16];
+                float2 l2 = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int c = 0; c < 32; c += 2) {
-                    const float p0 = ex2(fmaf(v[c0 + c], sl2, neg));
-                    const float p1 = ex2(fmaf(v[c0 + c + 1], sl2, neg));
-                    l += p0 + p1;
-                    pk[c / 2] = pack_bf16x2(p0, p1);
+                    // packed fp32x2 scale-and-shift and row-sum adds
+                    const float2 x = __ffma2_rn(make_float2(v[c0 + c], v[c0 + c + 1]),
+                                                make_float2(sl2, sl2), make_float2(neg, neg));
+                    const float2 p = make_float2(ex2(x.x), ex2(x.y));
+                    l2 = __fadd2_rn(l2, p);
+                    pk[c / 2] = pack_bf16x2(p.x, p.y);
                 }
+                l += l2.x + l2.y;
                 tmem_st16_u(s_addr + c0 / 2, pk);
             }
             tmem_wait_st();

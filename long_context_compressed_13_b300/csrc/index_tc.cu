@@ -15,8 +15,10 @@
 //               one issuer waits; a buffer is reused three heads later
 //   warps 0-15  epilogue: warp w owns TMEM lanes 32(w%4).. (its query rows)
 //               and columns 32(w/4).. of each buffer; it folds the heads in
-//               order, acc = fma(w_h, max(s_h, 0), acc), two columns per
-//               packed fp32x2 FMA, then either stores the 32 scores of the
+//               order, acc = fma(w_h / 2, s_h + |s_h|, acc) (= w_h max(s_h, 0)
+//               in all but overflow cases), two columns per packed fp32x2
+//               add and FMA, then
+//               either stores the 32 scores of the
 //               tile (MATERIALIZE) or appends the entries whose score reaches
 //               the row's threshold to the row's candidate list (FILTER).  The
 //               threshold test is a sign-bit collect of acc - theta; the
@@ -261,11 +263,16 @@ __global__ void __launch_bounds__(I_THREADS, 1)
                 tmem_wait_ld();
                 tc_fence_before();
                 arrive_lane0(&bars.freed[b], lane);
-                const float2 w2 = make_float2(wh[h], wh[h]);
+                // w * max(s, 0) == (w / 2) * (s + |s|) (exact unless s + |s| overflows
+                // or w / 2 is subnormal): the ReLU runs as a packed add with
+                // absolute-value operands on the FMA pipe
+                const float2 w2 = make_float2(0.5f * wh[h], 0.5f * wh[h]);
 #pragma unroll
-                for (int c = 0; c < EPI_COLS / 2; ++c)
-                    acc[c] = __ffma2_rn(w2, make_float2(fmaxf(v[2 * c], 0.f), fmaxf(v[2 * c + 1], 0.f)),
-                                        acc[c]);
+                for (int c = 0; c < EPI_COLS / 2; ++c) {
+                    const float2 s2 = make_float2(v[2 * c], v[2 * c + 1]);
+                    const float2 r2 = __fadd2_rn(s2, make_float2(fabsf(s2.x), fabsf(s2.y)));
+                    acc[c] = __ffma2_rn(w2, r2, acc[c]);
+                }
             }
             if (!ok) break;
             if (!row_ok) continue;
