@@ -8,8 +8,9 @@
 
 namespace lc {
 
-lc_status compress_launch(const void *X, const float *G, int64_t T_, int d, int m, lc_dtype dt,
-                          void *Xc, cudaStream_t st);
+lc_status compress_launch(const void *K, const void *V, const float *GK, const float *GV,
+                          int64_t T_, int d, int m, lc_dtype dt, void *Kc, void *Vc,
+                          cudaStream_t st);
 lc_status index_launch(const void *qI, const float *w, const void *kI, const lc_batch &b, int HI,
                        int dI, int m, lc_dtype dt, float *scores, int64_t ld, int32_t *dev_err,
                        cudaStream_t st);
@@ -98,9 +99,7 @@ static lc_status compress_common(const void *K, const void *V, const float *G_K,
     // with fewer than m tokens there is no entry to write: outputs may be empty
     if (T / m > 0 && (!K || !V || !Kc || !Vc)) return LC_ERR_INVALID_ARG;
     if ((d != 64 && d != 128) || m > 256) return LC_ERR_UNSUPPORTED;
-    lc_status s = compress_launch(K, G_K, T, d, m, dt, Kc, st);
-    if (s == LC_OK) s = compress_launch(V, G_V, T, d, m, dt, Vc, st);
-    return finish(s, st, nullptr);
+    return finish(compress_launch(K, V, G_K, G_V, T, d, m, dt, Kc, Vc, st), st, nullptr);
 }
 
 }  // namespace lc

@@ -351,8 +351,7 @@ __global__ void __launch_bounds__(I_THREADS, 1)
 // scores (0, i.e. "keep everything", when the row has at most k visible
 // entries or fewer than rho samples); count[r] = fail[r] = 0.  With
 // `staged`, the row's keys are first copied to shared memory (one read of
-// the row; the second half of the buffer takes the compacted keys) and the
-// radix passes run there.
+// the row) and the radix passes run there.
 __global__ void __launch_bounds__(512) k_sample_threshold(const float *__restrict__ samp,
                                                           int64_t lds, Batch bt, int m,
                                                           int stride, int k, int rho, int staged,
@@ -379,7 +378,7 @@ __global__ void __launch_bounds__(512) k_sample_threshold(const float *__restric
                     make_uint4(order_key(x.x), order_key(x.y), order_key(x.z), order_key(x.w));
             }
             __syncthreads();
-            th = radix_kth_largest_smem<NT>(skeys, (int)nvs, rho, rs, &need_left, skeys + lds);
+            th = radix_kth_largest_smem<NT>(skeys, (int)nvs, rho, rs, &need_left);
         } else {
             th = radix_kth_largest<NT>(samp + r * lds, nvs, rho, rs, &need_left);
         }
@@ -578,8 +577,7 @@ FusedPlan plan_fused(const lc_batch &b, int k) {
     if (nw > p.R && 4 * (nw + p.PK + p.P) <= 200 * 1024) p.R = (int)nw;
     p.ns = (n + p.stride - 1) / p.stride;
     p.lds = (p.ns + 3) & ~(int64_t)3;
-    // k_sample_threshold keeps the row (and its compacted keys) in shared memory
-    p.staged = 8 * p.lds <= 200 * 1024;
+    p.staged = 4 * p.lds <= 200 * 1024;  // k_sample_threshold keeps the row in shared memory
     const size_t Nq = (size_t)b.total_q;
     size_t o = 0;
     p.off_samp = o;  o += al256(sizeof(float) * Nq * (size_t)p.lds);
@@ -723,7 +721,7 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
     }
     // 2. thresholds
     {
-        const size_t smem = p.staged ? 2 * sizeof(uint32_t) * (size_t)p.lds : 0;
+        const size_t smem = p.staged ? sizeof(uint32_t) * (size_t)p.lds : 0;
         static size_t attr = 0;
         if (smem > 48 * 1024 && smem > attr) {
             if (cudaFuncSetAttribute(k_sample_threshold,
