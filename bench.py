@@ -55,11 +55,11 @@ UNIT = "query-tokens/s"
 # current kernels at the full benchmarked size (traffic well above the
 # algorithmic bytes would mean re-reads).  Re-measure when a kernel changes.
 NCU_STAGE_TRAFFIC = {
-    # index + top-k: candidate pass 330.8 MB, 1/32 sample 92.2 MB, threshold
-    # 134.5 MB, candidate top-k 67.6 MB
-    ("layer_pair_1m", "lightning_index+topk"): 625.2e6,
+    # index + top-k: candidate pass 339.9 MB, 1/32 sample 92.5 MB, threshold
+    # 134.3 MB, candidate top-k 78.0 MB
+    ("layer_pair_1m", "lightning_index+topk"): 644.7e6,
     # HCA attention: k_hca_tc 140.8 MB read, 89.1 MB written
-    ("layer_pair_1m", "hca_dense_attn"): 229.8e6,
+    ("layer_pair_1m", "hca_dense_attn"): 229.9e6,
     # index + top-k: streaming indexer 2505.6 MB, radix top-k 9.8 MB
     ("csa_decode", "lightning_index+topk"): 2515.4e6,
 }

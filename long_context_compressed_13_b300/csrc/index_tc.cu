@@ -29,7 +29,9 @@
 //   1. scores of every s-th entry (MATERIALIZE over a strided tensor map);
 //   2. theta = the rho-th largest sampled key, a lower bound for the k-th
 //      largest key of the full row with overwhelming probability;
-//   3. FILTER pass over all entries: candidates = entries with key >= theta;
+//   3. FILTER pass over all entries: candidates = entries with key >= theta,
+//      written to slots private to (row, CTA column), reserved by a
+//      shared-memory atomic, with a shared overflow region per row;
 //   4. exact top-k of the candidates, valid when the row has between k and
 //      `cap` candidates: then every member of the true top-k is a candidate;
 //   5. rows outside that range (rare: massive ties or an unlucky sample) are
@@ -72,7 +74,8 @@ struct IdxCfg {
     static constexpr uint32_t SM_K = SM_Q + 8 * Q_BOX;       // ring of head boxes
     static constexpr uint32_t SM_STG = SM_K + NSB * HEAD_BOX;  // FILTER staging, 32 B / thread
     static constexpr uint32_t SM_BAR = SM_STG + NEPI * 8 * 4;
-    static constexpr uint32_t SMEM = SM_BAR + 256;
+    static constexpr uint32_t SM_LCNT = SM_BAR + 256;          // FILTER: per-row slot counters
+    static constexpr uint32_t SMEM = SM_LCNT + IBM * 4;
 };
 
 struct IdxBars {
@@ -121,8 +124,11 @@ struct IdxTcArgs {
     int64_t ld;
     int vec_out;             // MATERIALIZE: out and ld allow 16-byte stores
     const uint32_t *theta;   // FILTER: [Nq] order-key thresholds
-    int32_t *count;          // FILTER: [Nq] candidate counts (zeroed beforehand)
-    uint2 *cand;             // FILTER: [Nq, cap] (order key, entry index)
+    uint2 *cand;             // FILTER: [Nq, cap] overflow slots (order key, entry index)
+    int32_t *count;          // FILTER: [Nq] overflow slots used (zeroed beforehand)
+    uint2 *priv;             // FILTER: [Nq, gy, cloc] slots private to (row, CTA column)
+    int32_t *lcnt;           // FILTER: [Nq, gy] private slots used
+    int gy, cloc;
     int cap;
     int32_t *dev_err;
 };
@@ -165,6 +171,8 @@ __global__ void __launch_bounds__(I_THREADS, 1)
         }
         fence_barrier_init();
     }
+    int *lcount = reinterpret_cast<int *>(smem + C::SM_LCNT);  // FILTER: slots used per row
+    for (int i = tid; i < IBM; i += I_THREADS) lcount[i] = 0;
     constexpr int W_PROD = NEPI / 32, W_MMA = NEPI / 32 + 1, W_MMA2 = NEPI / 32 + 2;
     if (warp == W_MMA && n_t > 0) {
         tmem_alloc(&bars.taddr, I_TMEM_COLS);
@@ -307,8 +315,19 @@ __global__ void __launch_bounds__(I_THREADS, 1)
                 const int64_t lim = min(nvr, c_end) - e0;
                 if (lim < EPI_COLS) cand &= lim <= 0 ? 0u : ((1u << lim) - 1u);
                 if (cand) {
-                    int base = atomicAdd(a.count + row, __popc(cand));
+                    // slots lb .. lb+n-1 of the row in this CTA: the first `cloc` are
+                    // private to (row, CTA column) and reserved by a shared-memory
+                    // atomic; the rest overflow into the row's shared slots
+                    const int n = __popc(cand);
+                    const int lb = atomicAdd(lcount + quad * 32 + lane, n);
+                    uint2 *pr = a.priv + ((size_t)row * a.gy + blockIdx.y) * a.cloc;
                     uint2 *cr = a.cand + row * a.cap;
+                    int ob = 0;  // overflow slot of local slot s: s + ob
+                    if (lb + n > a.cloc) {
+                        const int first = max(lb, a.cloc);
+                        ob = atomicAdd(a.count + row, lb + n - first) - first;
+                    }
+                    int base = lb;
                     // stage eight columns at a time so a candidate can be read by column
 #pragma unroll
                     for (int rd = 0; rd < EPI_COLS / 8; ++rd) {
@@ -323,13 +342,22 @@ __global__ void __launch_bounds__(I_THREADS, 1)
                         while (m8) {
                             const int c = __ffs(m8) - 1;
                             m8 &= m8 - 1;
-                            if (base < a.cap)
-                                cr[base] = make_uint2(order_key(stg[c]), (uint32_t)(e0 + 8 * rd + c));
+                            const uint2 kv = make_uint2(order_key(stg[c]), (uint32_t)(e0 + 8 * rd + c));
+                            if (base < a.cloc)
+                                pr[base] = kv;
+                            else if (base + ob < a.cap)
+                                cr[base + ob] = kv;
                             ++base;
                         }
                     }
                 }
             }
+        }
+        if (MODE == MODE_FILTER) {
+            // every emission of the CTA is complete: publish the private counts
+            asm volatile("bar.sync 1, %0;" ::"n"(NEPI) : "memory");
+            if (part == 0 && row_ok)
+                a.lcnt[(size_t)row * a.gy + blockIdx.y] = min(lcount[quad * 32 + lane], a.cloc);
         }
         if (!ok) {
             if (row_ok) flag(a.dev_err, LC_DEVERR_TIMEOUT);
@@ -416,14 +444,19 @@ __device__ __forceinline__ void bitonic_sort_u32_asc(uint32_t *a, int P) {
 // candidates equal to K* are collected (in any order, one shared atomic per
 // warp) and written out in ascending index order: through a bitmap over the
 // row's visible entries when it fits in the `R` words that held the keys and
-// indices, else by a bitonic sort.  Rows whose candidate count is outside
-// [k, cap] are marked in fail[].  Shared memory: R >= 2 cap words (keys,
+// indices, else by a bitonic sort.  A row's candidates are the private slots
+// of each of its gy CTA columns (lcnt of them in each) followed by its
+// overflow slots (count); rows with a total outside [k, cap] are marked in
+// fail[].  Shared memory: R >= 2 cap words (keys,
 // indices, later the bitmap), PK collected indices, P tie slots (PK, P: powers
 // of two >= k, cap); the tie slots double as the radix selection's spare.
 __global__ void __launch_bounds__(512) k_cand_pick(Batch bt, int m, int k, int cap, int R, int PK,
                                                    int P, const int32_t *__restrict__ count,
                                                    const uint2 *__restrict__ cand,
-                                                   int32_t *__restrict__ topk, int32_t *fail) {
+                                                   const int32_t *__restrict__ lcnt,
+                                                   const uint2 *__restrict__ priv, int gy,
+                                                   int cloc, int32_t *__restrict__ topk,
+                                                   int32_t *fail) {
     constexpr int NT = 512, NW = NT / 32;
     const unsigned FULL = 0xffffffffu;
     extern __shared__ uint32_t sbuf[];
@@ -433,7 +466,7 @@ __global__ void __launch_bounds__(512) k_cand_pick(Batch bt, int m, int k, int c
     uint32_t *sel = sbuf + R;                                   // [PK]
     uint32_t *tl = sel + PK;                                    // [P]
     __shared__ RadixScratch rs;
-    __shared__ int s_n, s_ties, wsum[NW];
+    __shared__ int s_n, s_ties, s_fill, s_priv, wsum[NW];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t r = blockIdx.x;
     const int64_t t = bt.q_pos0[0] + r;
@@ -445,21 +478,46 @@ __global__ void __launch_bounds__(512) k_cand_pick(Batch bt, int m, int k, int c
         for (int i = threadIdx.x; i < k; i += NT) out[i] = i < nv ? i : -1;
         return;
     }
-    const int n = count[r];
+    // candidates: the private slots of the row's CTA columns, then its overflow slots
+    if (threadIdx.x == 0) {
+        s_priv = 0;
+        s_fill = 0;
+        s_n = 0;
+        s_ties = 0;
+    }
+    __syncthreads();
+    {
+        int c = 0;
+        for (int y = threadIdx.x; y < gy; y += NT) c += lcnt[r * gy + y];
+        c = __reduce_add_sync(FULL, c);
+        if (lane == 0 && c) atomicAdd(&s_priv, c);
+    }
+    __syncthreads();
+    const int n_priv = s_priv, n_over = count[r];
+    const int n = n_priv + n_over;
     if (n < k || n > cap) {
         if (threadIdx.x == 0) fail[r] = 1;
         return;
     }
-    for (int i = threadIdx.x; i < n; i += NT) {
+    for (int y = warp; y < gy; y += NW) {
+        const int c = lcnt[r * gy + y];
+        if (c == 0) continue;
+        int b = 0;
+        if (lane == 0) b = atomicAdd(&s_fill, c);
+        b = __shfl_sync(FULL, b, 0);
+        const uint2 *src = priv + ((size_t)r * gy + y) * cloc;
+        for (int i = lane; i < c; i += 32) {
+            const uint2 ki = src[i];
+            keys[b + i] = ki.x;
+            idx[b + i] = ki.y;
+        }
+    }
+    for (int i = threadIdx.x; i < n_over; i += NT) {
         const uint2 ki = cand[r * cap + i];
-        keys[i] = ki.x;
-        idx[i] = ki.y;
+        keys[n_priv + i] = ki.x;
+        idx[n_priv + i] = ki.y;
     }
     for (int i = threadIdx.x; i < PK; i += NT) sel[i] = 0xFFFFFFFFu;  // bitonic padding
-    if (threadIdx.x == 0) {
-        s_n = 0;
-        s_ties = 0;
-    }
     __syncthreads();
     int need;
     const uint32_t kstar = radix_kth_largest_smem<NT>(keys, n, k, rs, &need, tl);
@@ -544,10 +602,12 @@ int pow2_at_least(int x) {
     return p;
 }
 
+int64_t pick_chunk(int64_t Nq, int64_t n_cols);
+
 struct FusedPlan {
-    int stride, rho, cap, P, PK, R, staged;
-    int64_t ns, lds;
-    size_t off_samp, off_theta, off_count, off_fail, off_cand, off_full, total;
+    int stride, rho, cap, P, PK, R, staged, gy, cloc;
+    int64_t ns, lds, chunk;
+    size_t off_samp, off_theta, off_count, off_fail, off_cand, off_lcnt, off_priv, off_full, total;
 };
 
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -585,6 +645,17 @@ FusedPlan plan_fused(const lc_batch &b, int k) {
     p.off_count = o; o += al256(sizeof(int32_t) * Nq);
     p.off_fail = o;  o += al256(sizeof(int32_t) * Nq);
     p.off_cand = o;  o += al256(sizeof(uint2) * Nq * (size_t)p.cap);
+    // the candidate pass's CTA columns and each (row, column)'s private slots:
+    // twice the column's share of `cap`, so that overflow needs a skewed row
+    p.chunk = pick_chunk(b.total_q, n);
+    p.gy = (int)((n + p.chunk - 1) / p.chunk);
+    int64_t cl = (2 * (int64_t)p.cap * p.chunk + n - 1) / n;
+    cl = (cl + 31) / 32 * 32;
+    if (cl < 32) cl = 32;
+    if (cl > p.cap) cl = p.cap;
+    p.cloc = (int)cl;
+    p.off_lcnt = o;  o += al256(sizeof(int32_t) * Nq * (size_t)p.gy);
+    p.off_priv = o;  o += al256(sizeof(uint2) * Nq * (size_t)p.gy * (size_t)p.cloc);
     p.off_full = o;  o += al256(sizeof(float) * Nq * (size_t)n);
     p.total = o;
     return p;
@@ -695,6 +766,8 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
     int32_t *count = reinterpret_cast<int32_t *>(base + p.off_count);
     int32_t *fail = reinterpret_cast<int32_t *>(base + p.off_fail);
     uint2 *cand = reinterpret_cast<uint2 *>(base + p.off_cand);
+    int32_t *lcnt = reinterpret_cast<int32_t *>(base + p.off_lcnt);
+    uint2 *priv = reinterpret_cast<uint2 *>(base + p.off_priv);
     float *full = reinterpret_cast<float *>(base + p.off_full);
     const int64_t Tc = b.total_c;
     const uint64_t pitch = (uint64_t)HI * IDI * 2;
@@ -742,7 +815,12 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
         a.count = count;
         a.cand = cand;
         a.cap = p.cap;
-        a.chunk = pick_chunk(b.total_q, Tc);
+        a.priv = priv;
+        a.lcnt = lcnt;
+        a.gy = p.gy;
+        a.cloc = p.cloc;
+        a.chunk = p.chunk;
+        if ((Tc + p.chunk - 1) / p.chunk != p.gy) return LC_ERR_INVALID_ARG;  // gridDim.y == gy
         s = launch_tc_hi<MODE_FILTER>(HI, mQ, mK, a, Tc, st);
         if (s != LC_OK) return s;
     }
@@ -757,7 +835,7 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
             attr = smem;
         }
         LC_LAUNCH(k_cand_pick, dim3((unsigned)b.total_q), dim3(512), smem, st, to_dev(b), m, k,
-                  p.cap, p.R, p.PK, p.P, count, cand, topk, fail);
+                  p.cap, p.R, p.PK, p.P, count, cand, lcnt, priv, p.gy, p.cloc, topk, fail);
         if ((s = check_launch()) != LC_OK) return s;
     }
     // 5. exact fallback for the rows marked in fail[] (no work when none is)
