@@ -107,6 +107,28 @@ def test_fused_topk_long_rows_sampled(lc):
     _check_selection(sel.cpu().numpy(), I, (tpos + 1) // 4, k)
 
 
+def test_fused_topk_skewed_rows_overflow(lc):
+    # every row's best entries sit in one 1024-entry range (keys scaled by 4,
+    # head weights made non-negative), inside one 2048-entry CTA column of the
+    # candidate pass: about 640 candidates per row against 256 private slots,
+    # so most of them go through the row's shared overflow region
+    T, k = 131072, 64
+    L = wl.csa_layer(T=T, H=8, d=64, HI=8, dI=64, m=4, k=k, W=16, dtype="bf16", seed=75,
+                     q_from=T - 256)
+    w = L["w"].abs()
+    kI = L["kI"].clone()
+    kI[4096:5120] = kI[4096:5120] * 4
+    b = lc.DeviceBatch.from_workload(L["batch"])
+    tpos = np.array(L["batch"].positions())
+    _, sel = lc.lightning_index(L["qI"].cuda(), w.cuda(), kI.cuda(), b, 4, scores=False, k=k,
+                                topk=True)
+    torch.cuda.synchronize()
+    I = oracle.index(L["qI"], w, kI, tpos, 4)
+    gsel = sel.cpu().numpy()
+    _check_selection(gsel, I, (tpos + 1) // 4, k)
+    assert np.mean((gsel >= 4096) & (gsel < 5120)) > 0.9  # the skew is what was tested
+
+
 def test_fused_topk_ties_take_the_fallback(lc):
     # rows with all-zero indexer queries or head weights score every entry 0:
     # the candidate list overflows and the exact fallback keeps the lowest
