@@ -1,6 +1,5 @@
-// Block-level helpers shared by the top-k kernels: prefix sums, radix
-// selection of the k-th largest order key, and an in-shared-memory bitonic
-// sort.  NT = threads per block.
+// Block-level helpers shared by the top-k kernels: prefix sums and radix
+// selection of the k-th largest order key.  NT = threads per block.
 #pragma once
 
 #include "lc_common.cuh"
@@ -180,28 +179,6 @@ __device__ uint32_t radix_kth_largest_smem(const uint32_t *keys, int n, int need
     }
     *need_left = need;
     return prefix;
-}
-
-// Bitonic sort of P (power of two) 64-bit keys in shared memory, descending
-// if DESC.  All threads of the block call it.
-template <int NT, bool DESC>
-__device__ void bitonic_sort_u64(uint64_t *a, int P) {
-    for (int size = 2; size <= P; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            __syncthreads();
-            for (int i = threadIdx.x; i < (P >> 1); i += NT) {
-                const int lo = 2 * stride * (i / stride) + (i % stride);
-                const int hi = lo + stride;
-                const bool up = ((lo & size) == 0) != DESC;  // this pair sorts ascending
-                const uint64_t x = a[lo], y = a[hi];
-                if ((x > y) == up) {
-                    a[lo] = y;
-                    a[hi] = x;
-                }
-            }
-        }
-    }
-    __syncthreads();
 }
 
 }  // namespace lc
