@@ -350,6 +350,23 @@ class Decode:
                 "algorithmic_bytes": w["index_bytes"], "peak_source": peaks["source"]}
 
 
+# ---------------------------------------------------------------- ranks
+
+def max_over_ranks(dist, x: float, device) -> float:
+    """The largest x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Units all ranks processed per second: every rank runs one replica of
+    the step, so the job does world x units_per_rank per (slowest) step."""
+    return units_per_rank * world / (ms_per_step / 1e3)
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args):
@@ -395,11 +412,7 @@ def run_ours(args):
     if dist:
         dist.barrier()
     clocks = sampler.stop()
-    ms = t_start.elapsed_time(t_end)
-    if dist:
-        tt = torch.tensor([ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(dist, t_start.elapsed_time(t_end), device)
     stage_ms = [statistics.mean(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps))
                 for i in range(nst)]
     err = int(wk.err.item())
@@ -428,15 +441,10 @@ def run_ours(args):
         for k_, v in h_out.items():
             v.copy_(outs[k_], non_blocking=True)
         torch.cuda.synchronize()
-    e2e_s = (time.perf_counter() - e0) / e2e_steps
-    if dist:
-        tt = torch.tensor([e2e_s], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_s = float(tt.item())
+    e2e_s = max_over_ranks(dist, (time.perf_counter() - e0) / e2e_steps, device)
 
-    tokens = wk.chunk * world
     ms_step = ms / args.steps
-    value = tokens / (ms_step / 1e3)
+    value = whole_job_rate(wk.chunk, world, ms_step)
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -445,7 +453,8 @@ def run_ours(args):
         "roofline": wk.roofline(stage_ms, peaks, ms),
         "stages_ms": dict(zip(wk.STAGES, stage_ms)),
         "path_tflops": wk.path_tflops(ms_step),
-        "e2e": {"value": tokens / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": whole_job_rate(wk.chunk, world, e2e_s * 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
         "dev_err": err,
