@@ -53,10 +53,10 @@ def _load():
             lib.oracle_topk.argtypes = [D, i64, i64, I64, i32, I32]
             lib.oracle_topk.restype = None
             lib.oracle_sparse_attn.argtypes = [D, D, D, i64, I32, i32, D, D, i64, i64,
-                                               I64, i64, i32, i32, i32, dbl, D, D]
+                                               I64, i64, i32, i32, i32, dbl, D, D, D]
             lib.oracle_sparse_attn.restype = i64
             lib.oracle_hca_attn.argtypes = [D, D, D, i64, i32, D, D, i64, i64,
-                                            I64, i64, i32, i32, i32, dbl, D, D]
+                                            I64, i64, i32, i32, i32, dbl, D, D, D]
             lib.oracle_hca_attn.restype = i64
             _lib = lib
     return _lib
@@ -129,35 +129,51 @@ def topk(I, nvis, k: int) -> np.ndarray:
     return out
 
 
-def sparse_attn(Q, Kc, Vc, idx, Kraw, Vraw, raw_pos0: int, tpos, W: int, scale: float):
-    """CSA core attention for one sequence.  Returns (O [Nq,H,d], lse [Nq,H])."""
+def _sink(sink, H):
+    """Per-head sink logits as an fp64 pointer, or NULL for none."""
+    if sink is None:
+        return None, ctypes.cast(None, ctypes.POINTER(ctypes.c_double))
+    s = _f64(sink).reshape(-1)
+    assert s.shape == (H,)
+    return s, _p(s, ctypes.c_double)
+
+
+def sparse_attn(Q, Kc, Vc, idx, Kraw, Vraw, raw_pos0: int, tpos, W: int, scale: float,
+                sink=None):
+    """CSA core attention for one sequence.  Returns (O [Nq,H,d], lse [Nq,H]).
+    sink: per-head sink logits [H] (natural-log units, like scale * q.k) or
+    None."""
     Q, Kc, Vc, Kraw, Vraw = _f64(Q), _f64(Kc), _f64(Vc), _f64(Kraw), _f64(Vraw)
     idx, tpos = _i32(idx), _i64(tpos)
     Nq, H, d = Q.shape
     k = idx.shape[1]
     O = np.zeros((Nq, H, d), dtype=np.float64)
     lse = np.zeros((Nq, H), dtype=np.float64)
+    keep, sp = _sink(sink, H)
     rc = _load().oracle_sparse_attn(
         _p(Q, ctypes.c_double), _p(Kc, ctypes.c_double), _p(Vc, ctypes.c_double), Kc.shape[0],
         _p(idx, ctypes.c_int32), k, _p(Kraw, ctypes.c_double), _p(Vraw, ctypes.c_double),
-        Kraw.shape[0], raw_pos0, _p(tpos, ctypes.c_int64), Nq, H, d, W, scale,
+        Kraw.shape[0], raw_pos0, _p(tpos, ctypes.c_int64), Nq, H, d, W, scale, sp,
         _p(O, ctypes.c_double), _p(lse, ctypes.c_double))
     if rc != 0:
         raise ValueError(f"oracle_sparse_attn: invalid input at row {-rc - 1}")
     return O, lse
 
 
-def hca_attn(Q, Kc, Vc, m: int, Kraw, Vraw, raw_pos0: int, tpos, W: int, scale: float):
-    """HCA attention for one sequence.  Returns (O [Nq,H,d], lse [Nq,H])."""
+def hca_attn(Q, Kc, Vc, m: int, Kraw, Vraw, raw_pos0: int, tpos, W: int, scale: float,
+             sink=None):
+    """HCA attention for one sequence.  Returns (O [Nq,H,d], lse [Nq,H]).
+    sink: as for sparse_attn."""
     Q, Kc, Vc, Kraw, Vraw = _f64(Q), _f64(Kc), _f64(Vc), _f64(Kraw), _f64(Vraw)
     tpos = _i64(tpos)
     Nq, H, d = Q.shape
     O = np.zeros((Nq, H, d), dtype=np.float64)
     lse = np.zeros((Nq, H), dtype=np.float64)
+    keep, sp = _sink(sink, H)
     rc = _load().oracle_hca_attn(
         _p(Q, ctypes.c_double), _p(Kc, ctypes.c_double), _p(Vc, ctypes.c_double), Kc.shape[0], m,
         _p(Kraw, ctypes.c_double), _p(Vraw, ctypes.c_double), Kraw.shape[0], raw_pos0,
-        _p(tpos, ctypes.c_int64), Nq, H, d, W, scale, _p(O, ctypes.c_double),
+        _p(tpos, ctypes.c_int64), Nq, H, d, W, scale, sp, _p(O, ctypes.c_double),
         _p(lse, ctypes.c_double))
     if rc != 0:
         raise ValueError(f"oracle_hca_attn: invalid input at row {-rc - 1}")

@@ -27,7 +27,13 @@
  *               output ascending entry index, -1 padded
  *   window      raw positions max(0, t-W+1) .. t (W tokens, t included)
  *   attention   one softmax over (selected entries, then window tokens)
- *   empty set   O = 0, lse = -inf
+ *   sink        the same page, §1.1 (engineering details): a learnable
+ *               per-head attention-sink logit lets a head push its total
+ *               attention toward 0.  Read as one extra logit s_h that joins
+ *               the softmax's denominator and carries no value:
+ *               O = sum_i e^{z_i} V_i / (e^{s_h} + sum_i e^{z_i}),
+ *               lse = log(e^{s_h} + sum_i e^{z_i}); no sink = s_h = -inf
+ *   empty set   O = 0, lse = s_h (-inf without a sink)
  */
 #include <math.h>
 #include <stdint.h>
@@ -143,25 +149,27 @@ void oracle_topk(const double *I, int64_t Nq, int64_t ld, const int64_t *nvis,
 }
 
 /* Softmax attention of one query head over an explicit list of key rows.
- * logits_i = scale * q . K_i ; O = sum_i softmax_i * V_i ; lse = log sum exp. */
+ * logits_i = scale * q . K_i ; the sink logit (-inf: none) joins the
+ * denominator only: O = sum_i e^{logit_i} V_i / (e^{sink} + sum_i e^{logit_i}),
+ * lse = log of that denominator. */
 static void attend_list(const double *q, const double *const *K,
                         const double *const *V, int64_t n, int32_t d,
-                        double scale, double *o, double *lse)
+                        double scale, double sink, double *o, double *lse)
 {
     if (n == 0) {
         for (int32_t c = 0; c < d; ++c) o[c] = 0.0;
-        *lse = -INFINITY;
+        *lse = sink;
         return;
     }
     double *logit = (double *)malloc(sizeof(double) * (size_t)n);
-    double mx = -INFINITY;
+    double mx = sink;
     for (int64_t i = 0; i < n; ++i) {
         double dot = 0.0;
         for (int32_t c = 0; c < d; ++c) dot += q[c] * K[i][c];
         logit[i] = scale * dot;
         if (logit[i] > mx) mx = logit[i];
     }
-    double sum = 0.0;
+    double sum = sink == -INFINITY ? 0.0 : exp(sink - mx);
     for (int64_t i = 0; i < n; ++i) { logit[i] = exp(logit[i] - mx); sum += logit[i]; }
     for (int32_t c = 0; c < d; ++c) {
         double acc = 0.0;
@@ -195,14 +203,14 @@ static int64_t add_window(const double *Kraw, const double *Vraw, int64_t Nraw,
  * Q [Nq, H, d]; Kc, Vc [Tc, d]; idx [Nq, k] sequence-local entry numbers,
  * -1 = padding (skipped); raw Kraw, Vraw [Nraw, d] holding positions
  * raw_pos0 ..; tpos [Nq].  Key set of row r: the selected entries in the order
- * listed, then the window.  O [Nq, H, d], lse [Nq, H].
+ * listed, then the window.  sink [H] or NULL.  O [Nq, H, d], lse [Nq, H].
  * Returns 0, or the first row whose inputs are invalid + 1 (negated). */
 int64_t oracle_sparse_attn(const double *Q, const double *Kc, const double *Vc,
                            int64_t Tc, const int32_t *idx, int32_t k,
                            const double *Kraw, const double *Vraw, int64_t Nraw,
                            int64_t raw_pos0, const int64_t *tpos, int64_t Nq,
                            int32_t H, int32_t d, int32_t W, double scale,
-                           double *O, double *lse)
+                           const double *sink, double *O, double *lse)
 {
     int64_t bad = 0;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -227,7 +235,8 @@ int64_t oracle_sparse_attn(const double *Q, const double *Kc, const double *Vc,
         } else {
             for (int32_t h = 0; h < H; ++h)
                 attend_list(Q + (r * H + h) * d, Kl, Vl, n, d, scale,
-                            O + (r * H + h) * d, lse + r * H + h);
+                            sink ? sink[h] : -INFINITY, O + (r * H + h) * d,
+                            lse + r * H + h);
         }
         free(Kl);
         free(Vl);
@@ -241,7 +250,8 @@ int64_t oracle_hca_attn(const double *Q, const double *Kc, const double *Vc,
                         int64_t Tc, int32_t m, const double *Kraw,
                         const double *Vraw, int64_t Nraw, int64_t raw_pos0,
                         const int64_t *tpos, int64_t Nq, int32_t H, int32_t d,
-                        int32_t W, double scale, double *O, double *lse)
+                        int32_t W, double scale, const double *sink, double *O,
+                        double *lse)
 {
     int64_t bad = 0;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -264,7 +274,8 @@ int64_t oracle_hca_attn(const double *Q, const double *Kc, const double *Vc,
         } else {
             for (int32_t h = 0; h < H; ++h)
                 attend_list(Q + (r * H + h) * d, Kl, Vl, n, d, scale,
-                            O + (r * H + h) * d, lse + r * H + h);
+                            sink ? sink[h] : -INFINITY, O + (r * H + h) * d,
+                            lse + r * H + h);
         }
         free(Kl);
         free(Vl);

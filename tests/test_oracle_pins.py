@@ -326,3 +326,48 @@ def test_head_permutation_equivariance_and_window_source_offset():
     np.testing.assert_allclose(o2, o[rows], rtol=0, atol=1e-14)
     with pytest.raises(ValueError):
         oracle.sparse_attn(Q, Kc, Vc, idx, K[30:], V[30:], 30, t, W, 0.3)
+
+
+# ------------------------------------------------------ attention sink logit
+# The sink is one extra per-head logit in the softmax's denominator with no
+# value ("DeepSeek-V4 技术解析…", §1.1, engineering details: a learnable sink
+# logit lets a head push its total attention toward zero).
+
+
+def test_sink_single_key_is_logistic_gate():
+    # one key with logit z and a sink s: O = sigmoid(z - s) V, lse = log(e^z + e^s)
+    H, d = 3, 5
+    Q = RNG.standard_normal((1, H, d))
+    Kc, Vc = RNG.standard_normal((4, d)), RNG.standard_normal((4, d))
+    sink = np.array([-0.5, 1.25, 3.0])
+    o, l = oracle.sparse_attn(Q, Kc, Vc, np.array([[2, -1]]), Kc[:0], Vc[:0], 0, [11], 0, 0.7,
+                              sink=sink)
+    z = 0.7 * Q[0] @ Kc[2]
+    np.testing.assert_allclose(o[0], expit(z - sink)[:, None] * Vc[2][None, :], rtol=0,
+                               atol=1e-14)
+    np.testing.assert_allclose(l[0], np.logaddexp(z, sink), rtol=0, atol=1e-13)
+
+
+def test_sink_rescales_the_sinkless_result():
+    # O_s = O * e^lse / (e^lse + e^s) and lse_s = logaddexp(lse, s), per head;
+    # a sink of -inf is no sink; an empty key set gives O = 0 and lse = s
+    m, T, H, d, W = 4, 40, 6, 8, 8
+    Q = RNG.standard_normal((T, H, d))
+    Kc, Vc = RNG.standard_normal((T // m, d)), RNG.standard_normal((T // m, d))
+    K, V = RNG.standard_normal((T, d)), RNG.standard_normal((T, d))
+    t = np.arange(T)
+    sink = np.array([-np.inf, -2.0, 0.0, 0.5, 4.0, 30.0])
+    for attn in (lambda s: oracle.hca_attn(Q, Kc, Vc, m, K, V, 0, t, W, 0.3, sink=s),
+                 lambda s: oracle.sparse_attn(
+                     Q, Kc, Vc, oracle.topk(np.tile(np.arange(T // m, dtype=float), (T, 1)),
+                                            oracle.n_visible(t, m), 3),
+                     K, V, 0, t, W, 0.3, sink=s)):
+        o0, l0 = attn(None)
+        o1, l1 = attn(sink)
+        gate = np.exp(l0 - np.logaddexp(l0, sink[None, :]))
+        np.testing.assert_allclose(o1, o0 * gate[..., None], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(l1, np.logaddexp(l0, sink[None, :]), rtol=0, atol=1e-12)
+        assert np.array_equal(o1[:, 0], o0[:, 0]) and np.array_equal(l1[:, 0], l0[:, 0])
+    o, l = oracle.sparse_attn(Q[:1], Kc, Vc, np.array([[-1, -1]]), Kc[:0], Vc[:0], 0, [11], 0,
+                              0.7, sink=sink)
+    assert np.all(o == 0) and np.array_equal(l[0], sink)
