@@ -137,28 +137,34 @@ lc_status topk_select(const float *scores, int64_t ld, const lc_batch *batch, in
                       lc_stream stream);
 
 /* CSA core attention (same page, §1.1: MQA core attention over the kept
- * entries; extra sliding-window branch).  For query row r, head h:
+ * entries; extra sliding-window branch; a learnable attention-sink logit per
+ * head that can push the head's total attention toward 0).  For query row
+ * r, head h, with z_s = scale * Q[r,h].K_s and sink logit s_h:
  *   S = { Kc/Vc row cu_c[b]+topk[r,i] : topk[r,i] >= 0 }  then
  *       { raw row of position p : max(0,t-W+1) <= p <= t }
- *   O[r,h] = sum_{s in S} softmax_s(scale * Q[r,h].K_s) V_s   (one softmax)
- *   lse[r,h] = log sum_s exp(scale * Q[r,h].K_s)   (-inf and O = 0 if S empty)
+ *   O[r,h]   = sum_{s in S} e^{z_s} V_s / (e^{s_h} + sum_{s in S} e^{z_s})
+ *   lse[r,h] = log(e^{s_h} + sum_{s in S} e^{z_s})
+ * Without a sink (sink NULL, or s_h = -inf) this is one softmax over S; an
+ * empty S gives O = 0 and lse = s_h (-inf without a sink).
  *   Q [total_q, H, d]; Kc, Vc [cu_c[B], d]; Kraw, Vraw [cu_raw[B], d] (dtype)
  *   topk [total_q, k] int32 (-1 = unused slot); O [total_q, H, d] dtype;
+ *   sink [H] fp32 (natural-log units, like z) or NULL;
  *   lse [total_q, H] fp32 or NULL.
  * Supported: d in {64,128}; H % 8 == 0, 8 <= H <= 128; 0 <= W <= 4096. */
 lc_status sparse_mqa_attn(const void *Q, const void *Kc, const void *Vc, const int32_t *topk,
                           int32_t k, const void *Kraw, const void *Vraw, const lc_batch *batch,
                           int32_t H, int32_t d, int32_t m, int32_t W, float scale,
-                          lc_dtype dtype, void *O, float *lse, void *ws, size_t ws_bytes,
-                          int32_t *dev_err, lc_stream stream);
+                          const float *sink, lc_dtype dtype, void *O, float *lse, void *ws,
+                          size_t ws_bytes, int32_t *dev_err, lc_stream stream);
 
 /* HCA dense attention (same page, §1.1, HCA paragraph: dense attention over
- * every compressed entry).  As sparse_mqa_attn with
+ * every compressed entry).  As sparse_mqa_attn (sink included) with
  *   S = { entries j < n_vis(t) in order }  then the window. */
 lc_status hca_dense_attn(const void *Q, const void *Kc, const void *Vc, const void *Kraw,
                          const void *Vraw, const lc_batch *batch, int32_t H, int32_t d,
-                         int32_t m, int32_t W, float scale, lc_dtype dtype, void *O, float *lse,
-                         void *ws, size_t ws_bytes, int32_t *dev_err, lc_stream stream);
+                         int32_t m, int32_t W, float scale, const float *sink, lc_dtype dtype,
+                         void *O, float *lse, void *ws, size_t ws_bytes, int32_t *dev_err,
+                         lc_stream stream);
 
 /* Index + top-k that allocates nothing (the pages have no counterpart: this
  * is an addition for callers that cannot allocate device memory, such as a

@@ -65,9 +65,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "hca_compress": [vp, vp, vp, vp, i64, i32, i32, i32, vp, vp, vp],
         "lightning_index": [vp, vp, vp, bp, i32, i32, i32, i32, vp, i64, i32, vp, vp, sz, vp, vp],
         "topk_select": [vp, i64, bp, i32, i32, vp, vp, sz, vp, vp],
-        "sparse_mqa_attn": [vp, vp, vp, vp, i32, vp, vp, bp, i32, i32, i32, i32, f32, i32, vp,
+        "sparse_mqa_attn": [vp, vp, vp, vp, i32, vp, vp, bp, i32, i32, i32, i32, f32, vp, i32, vp,
                             vp, vp, sz, vp, vp],
-        "hca_dense_attn": [vp, vp, vp, vp, vp, bp, i32, i32, i32, i32, f32, i32, vp, vp, vp, sz,
+        "hca_dense_attn": [vp, vp, vp, vp, vp, bp, i32, i32, i32, i32, f32, vp, i32, vp, vp, vp, sz,
                            vp, vp],
     }
     for name, args in sig.items():
@@ -248,8 +248,9 @@ def topk_select(scores, batch: DeviceBatch, m: int, k: int, topk=None, dev_err=N
 
 def sparse_mqa_attn(Q, Kc, Vc, topk, Kraw, Vraw, batch: DeviceBatch, m: int, W: int,
                     scale: float, O=None, lse: bool | torch.Tensor = True, dev_err=None,
-                    stream=None):
-    """CSA core attention.  Returns (O [total_q,H,d], lse [total_q,H] or None)."""
+                    stream=None, sink=None):
+    """CSA core attention.  Returns (O [total_q,H,d], lse [total_q,H] or None).
+    sink: per-head attention-sink logits [H] fp32 on the device, or None."""
     lib = load_library()
     Nq, H, d = Q.shape
     if O is None:
@@ -264,7 +265,8 @@ def sparse_mqa_attn(Q, Kc, Vc, topk, Kraw, Vraw, batch: DeviceBatch, m: int, W: 
     st = lib.sparse_mqa_attn(_dev(Q, "Q"), _dev(Kc, "Kc", Q.dtype), _dev(Vc, "Vc", Q.dtype),
                              _dev(topk, "topk", torch.int32), topk.shape[1],
                              _dev(Kraw, "Kraw", Q.dtype), _dev(Vraw, "Vraw", Q.dtype),
-                             ctypes.byref(cb), H, d, m, W, float(scale), _dtype_code(Q),
+                             ctypes.byref(cb), H, d, m, W, float(scale),
+                             _dev(sink, "sink", torch.float32), _dtype_code(Q),
                              _dev(O, "O", Q.dtype), _dev(L, "lse", torch.float32), None, 0,
                              _dev(dev_err, "dev_err", torch.int32), _stream(stream))
     _check("sparse_mqa_attn", st)
@@ -272,8 +274,10 @@ def sparse_mqa_attn(Q, Kc, Vc, topk, Kraw, Vraw, batch: DeviceBatch, m: int, W: 
 
 
 def hca_dense_attn(Q, Kc, Vc, Kraw, Vraw, batch: DeviceBatch, m: int, W: int, scale: float,
-                   O=None, lse: bool | torch.Tensor = True, dev_err=None, ws=None, stream=None):
-    """HCA dense attention.  Returns (O [total_q,H,d], lse [total_q,H] or None)."""
+                   O=None, lse: bool | torch.Tensor = True, dev_err=None, ws=None, stream=None,
+                   sink=None):
+    """HCA dense attention.  Returns (O [total_q,H,d], lse [total_q,H] or None).
+    sink: per-head attention-sink logits [H] fp32 on the device, or None."""
     lib = load_library()
     Nq, H, d = Q.shape
     if O is None:
@@ -287,7 +291,8 @@ def hca_dense_attn(Q, Kc, Vc, Kraw, Vraw, batch: DeviceBatch, m: int, W: int, sc
     cb = batch.c_struct()
     st = lib.hca_dense_attn(_dev(Q, "Q"), _dev(Kc, "Kc", Q.dtype), _dev(Vc, "Vc", Q.dtype),
                             _dev(Kraw, "Kraw", Q.dtype), _dev(Vraw, "Vraw", Q.dtype),
-                            ctypes.byref(cb), H, d, m, W, float(scale), _dtype_code(Q),
+                            ctypes.byref(cb), H, d, m, W, float(scale),
+                            _dev(sink, "sink", torch.float32), _dtype_code(Q),
                             _dev(O, "O", Q.dtype), _dev(L, "lse", torch.float32),
                             _dev(ws, "ws"), ws.numel() if ws is not None else 0,
                             _dev(dev_err, "dev_err", torch.int32), _stream(stream))

@@ -26,16 +26,17 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
 size_t index_tc_workspace(const lc_batch &b, int k);
 lc_status hca_tc_launch(const void *Q, const void *Kc, const void *Vc, const void *Kraw,
                         const void *Vraw, const lc_batch &b, int H, int d, int m, int W,
-                        float scale, lc_dtype dt, void *O, float *lse, int32_t *dev_err,
-                        cudaStream_t st);
+                        float scale, const float *sink, lc_dtype dt, void *O, float *lse,
+                        int32_t *dev_err, cudaStream_t st);
 lc_status sparse_tc_launch(const void *Q, const void *Kc, const void *Vc, const int32_t *topk,
                            int k, const void *Kraw, const void *Vraw, const lc_batch &b, int H,
-                           int d, int m, int W, float scale, lc_dtype dt, void *O, float *lse,
-                           int32_t *dev_err, cudaStream_t st);
+                           int d, int m, int W, float scale, const float *sink, lc_dtype dt,
+                           void *O, float *lse, int32_t *dev_err, cudaStream_t st);
 lc_status attn_simt_launch(bool sparse, const void *Q, const void *Kc, const void *Vc,
                            const int32_t *topk, int k, const void *Kraw, const void *Vraw,
                            const lc_batch &b, int H, int d, int m, int W, float scale,
-                           lc_dtype dt, void *O, float *lse, int32_t *dev_err, cudaStream_t st);
+                           const float *sink, lc_dtype dt, void *O, float *lse,
+                           int32_t *dev_err, cudaStream_t st);
 
 static std::atomic<uint64_t> g_launches{0};
 static std::atomic<int32_t> g_last_cuda{0};
@@ -177,8 +178,8 @@ lc_status topk_select(const float *scores, int64_t ld, const lc_batch *batch, in
 lc_status sparse_mqa_attn(const void *Q, const void *Kc, const void *Vc, const int32_t *topk,
                           int32_t k, const void *Kraw, const void *Vraw, const lc_batch *batch,
                           int32_t H, int32_t d, int32_t m, int32_t W, float scale,
-                          lc_dtype dtype, void *O, float *lse, void *ws, size_t ws_bytes,
-                          int32_t *dev_err, lc_stream stream) {
+                          const float *sink, lc_dtype dtype, void *O, float *lse, void *ws,
+                          size_t ws_bytes, int32_t *dev_err, lc_stream stream) {
     (void)ws;
     (void)ws_bytes;
     cudaStream_t st = (cudaStream_t)stream;
@@ -188,17 +189,18 @@ lc_status sparse_mqa_attn(const void *Q, const void *Kc, const void *Vc, const i
     if ((d != 64 && d != 128) || H < 8 || H > 128 || H % 8 || W > 4096 || k > 4096)
         return LC_ERR_UNSUPPORTED;
     lc_status s = sparse_tc_launch(Q, Kc, Vc, topk, k, Kraw, Vraw, *batch, H, d, m, W, scale,
-                                   dtype, O, lse, dev_err, st);
+                                   sink, dtype, O, lse, dev_err, st);
     if (s == LC_ERR_UNSUPPORTED)
         s = attn_simt_launch(true, Q, Kc, Vc, topk, k, Kraw, Vraw, *batch, H, d, m, W, scale,
-                             dtype, O, lse, dev_err, st);
+                             sink, dtype, O, lse, dev_err, st);
     return finish(s, st, dev_err);
 }
 
 lc_status hca_dense_attn(const void *Q, const void *Kc, const void *Vc, const void *Kraw,
                          const void *Vraw, const lc_batch *batch, int32_t H, int32_t d,
-                         int32_t m, int32_t W, float scale, lc_dtype dtype, void *O, float *lse,
-                         void *ws, size_t ws_bytes, int32_t *dev_err, lc_stream stream) {
+                         int32_t m, int32_t W, float scale, const float *sink, lc_dtype dtype,
+                         void *O, float *lse, void *ws, size_t ws_bytes, int32_t *dev_err,
+                         lc_stream stream) {
     (void)ws;
     (void)ws_bytes;
     cudaStream_t st = (cudaStream_t)stream;
@@ -207,11 +209,11 @@ lc_status hca_dense_attn(const void *Q, const void *Kc, const void *Vc, const vo
         return LC_ERR_INVALID_ARG;
     if ((d != 64 && d != 128) || H < 8 || H > 128 || H % 8 || W > 4096)
         return LC_ERR_UNSUPPORTED;
-    lc_status s = hca_tc_launch(Q, Kc, Vc, Kraw, Vraw, *batch, H, d, m, W, scale, dtype, O, lse,
-                                dev_err, st);
+    lc_status s = hca_tc_launch(Q, Kc, Vc, Kraw, Vraw, *batch, H, d, m, W, scale, sink, dtype, O,
+                                lse, dev_err, st);
     if (s == LC_ERR_UNSUPPORTED)
         s = attn_simt_launch(false, Q, Kc, Vc, nullptr, 0, Kraw, Vraw, *batch, H, d, m, W, scale,
-                             dtype, O, lse, dev_err, st);
+                             sink, dtype, O, lse, dev_err, st);
     return finish(s, st, dev_err);
 }
 

@@ -94,6 +94,7 @@ struct HcaArgs {
     int64_t Nraw;         // stored raw rows
     int m, W;
     float scale_log2;
+    const float *sink;    // [H] per-head sink logits or NULL
     __nv_bfloat16 *O;
     float *lse;
     int32_t *dev_err;
@@ -352,7 +353,10 @@ __global__ void __launch_bounds__(H_THREADS, 1)
             if (row_ok) flag(a.dev_err, LC_DEVERR_TIMEOUT);
         } else {
             tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float of = fold_sink(m_used, l, row_ok && a.sink
+                                                      ? __ldg(a.sink + row % a.H) * H_LOG2E
+                                                      : -INFINITY);
+            const float inv = l > 0.f ? of / l : 0.f;
             uint4 *dst = reinterpret_cast<uint4 *>(a.O + row * HHD);
 #pragma unroll 1
             for (int c = 0; c < HHD; c += 32) {
@@ -394,8 +398,8 @@ bool al16h(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; 
 // LC_ERR_UNSUPPORTED when the shape does not fit (the caller falls back).
 lc_status hca_tc_launch(const void *Q, const void *Kc, const void *Vc, const void *Kraw,
                         const void *Vraw, const lc_batch &b, int H, int d, int m, int W,
-                        float scale, lc_dtype dt, void *O, float *lse, int32_t *dev_err,
-                        cudaStream_t st) {
+                        float scale, const float *sink, lc_dtype dt, void *O, float *lse,
+                        int32_t *dev_err, cudaStream_t st) {
     if (dt != LC_BF16 || d != HHD || b.B != 1 || (HBM_ % H) != 0) return LC_ERR_UNSUPPORTED;
     if (!al16h(Q) || !al16h(O) || (Kc && !al16h(Kc)) || (Vc && !al16h(Vc)) ||
         (Kraw && !al16h(Kraw)) || (Vraw && !al16h(Vraw)))
@@ -427,6 +431,7 @@ lc_status hca_tc_launch(const void *Q, const void *Kc, const void *Vc, const voi
     a.m = m;
     a.W = have_r ? W : 0;
     a.scale_log2 = scale * H_LOG2E;
+    a.sink = sink;
     a.O = reinterpret_cast<__nv_bfloat16 *>(O);
     a.lse = lse;
     a.dev_err = dev_err;

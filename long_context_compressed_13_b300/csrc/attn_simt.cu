@@ -24,6 +24,7 @@ struct AttnArgs {
     int k;         // slots of topk per row (CSA); 0 for HCA
     int H, m, W;
     float scale;
+    const float *sink;  // [H] per-head sink logits or NULL
     void *O;
     float *lse;
     int32_t *dev_err;
@@ -171,12 +172,20 @@ __global__ void __launch_bounds__(AT) k_attn_simt(AttnArgs a, Batch bt) {
         }
     }
     __syncthreads();
+    if (tid < HG) {
+        // the head's sink logit joins the denominator; sA takes the output factor
+        float mm = sM[tid], ll = sL[tid];
+        sA[tid] = fold_sink(mm, ll, a.sink ? __ldg(a.sink + h0 + tid) * LOG2E : -INFINITY);
+        sM[tid] = mm;
+        sL[tid] = ll;
+    }
+    __syncthreads();
     T *O = reinterpret_cast<T *>(a.O);
 #pragma unroll
     for (int i = 0; i < NO; ++i) {
         const int h = oh + HSTEP * i;
         const float l = sL[h];
-        O[(r * a.H + h0 + h) * D + oc] = io<T>::from_f(l > 0.f ? acc[i] / l : 0.f);
+        O[(r * a.H + h0 + h) * D + oc] = io<T>::from_f(l > 0.f ? acc[i] * sA[h] / l : 0.f);
     }
     if (a.lse && tid < HG) {
         const float l = sL[tid];
@@ -219,8 +228,9 @@ static lc_status launch_attn(const AttnArgs &a, const lc_batch &b, int d, lc_dty
 lc_status attn_simt_launch(bool sparse, const void *Q, const void *Kc, const void *Vc,
                            const int32_t *topk, int k, const void *Kraw, const void *Vraw,
                            const lc_batch &b, int H, int d, int m, int W, float scale,
-                           lc_dtype dt, void *O, float *lse, int32_t *dev_err, cudaStream_t st) {
-    AttnArgs a{Q, Kc, Vc, Kraw, Vraw, topk, sparse ? k : 0, H, m, W, scale, O, lse, dev_err};
+                           const float *sink, lc_dtype dt, void *O, float *lse,
+                           int32_t *dev_err, cudaStream_t st) {
+    AttnArgs a{Q, Kc, Vc, Kraw, Vraw, topk, sparse ? k : 0, H, m, W, scale, sink, O, lse, dev_err};
     return sparse ? launch_attn<true>(a, b, d, dt, st) : launch_attn<false>(a, b, d, dt, st);
 }
 

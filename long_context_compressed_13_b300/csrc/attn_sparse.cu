@@ -109,6 +109,7 @@ struct SparseArgs {
     int k;
     int m, W;
     float scale_log2;
+    const float *sink;    // [H] per-head sink logits or NULL
     __nv_bfloat16 *O;
     float *lse;
     int32_t *dev_err;
@@ -432,7 +433,9 @@ __global__ void __launch_bounds__(S_THREADS, 1)
             if (row_ok) flag(a.dev_err, LC_DEVERR_TIMEOUT);
         } else {
             tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float of = fold_sink(m_used, l, row_ok && a.sink ? __ldg(a.sink + tid) * S_LOG2E
+                                                                   : -INFINITY);
+            const float inv = l > 0.f ? of / l : 0.f;
             uint4 *dst = reinterpret_cast<uint4 *>(a.O + row * SHD);
 #pragma unroll 1
             for (int c = 0; c < SHD; c += 32) {
@@ -474,8 +477,8 @@ bool al16s(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; 
 // ragged batch (one CTA per query token).  LC_ERR_UNSUPPORTED otherwise.
 lc_status sparse_tc_launch(const void *Q, const void *Kc, const void *Vc, const int32_t *topk,
                            int k, const void *Kraw, const void *Vraw, const lc_batch &b, int H,
-                           int d, int m, int W, float scale, lc_dtype dt, void *O, float *lse,
-                           int32_t *dev_err, cudaStream_t st) {
+                           int d, int m, int W, float scale, const float *sink, lc_dtype dt,
+                           void *O, float *lse, int32_t *dev_err, cudaStream_t st) {
     if (dt != LC_BF16 || d != SHD || H > SBM || b.total_c < 1 || b.total_q > 0x7fffffff ||
         b.total_q * H >= 0x7fffffff || b.total_c >= 0x7fffffff || b.total_raw >= 0x7fffffff)
         return LC_ERR_UNSUPPORTED;
@@ -501,6 +504,7 @@ lc_status sparse_tc_launch(const void *Q, const void *Kc, const void *Vc, const 
     a.m = m;
     a.W = have_r ? W : 0;
     a.scale_log2 = scale * S_LOG2E;
+    a.sink = sink;
     a.O = reinterpret_cast<__nv_bfloat16 *>(O);
     a.lse = lse;
     a.dev_err = dev_err;

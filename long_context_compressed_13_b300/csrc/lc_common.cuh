@@ -74,4 +74,17 @@ __device__ __forceinline__ uint32_t order_key(float s) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Folds a per-head attention-sink logit sk2 (log2 units; -inf or NaN: none)
+// into a softmax row's running max m and sum l (log2 units, l = 0 when the row
+// had no key): the sink is one more logit of the denominator with no value.
+// Returns the factor that rescales the row's unnormalised output.
+__device__ __forceinline__ float fold_sink(float &m, float &l, float sk2) {
+    if (!(sk2 > -INFINITY)) return 1.f;
+    const float mf = fmaxf(m, sk2);
+    const float f = l > 0.f ? exp2f(m - mf) : 0.f;
+    l = l * f + exp2f(sk2 - mf);
+    m = mf;
+    return f;
+}
+
 }  // namespace lc

@@ -101,18 +101,18 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     # attention: unsupported heads/dims, negative window, missing raw cache
     args = dict(scale=ctypes.c_float(0.125))
     assert lib.sparse_mqa_attn(P, P, P, P, 8, P, P, ctypes.byref(b), 12, 128, 4, 128,
-                               args["scale"], lc.LC_BF16, P, N, N, 0, N, N) == lc.LC_ERR_UNSUPPORTED
+                               args["scale"], N, lc.LC_BF16, P, N, N, 0, N, N) == lc.LC_ERR_UNSUPPORTED
     assert lib.sparse_mqa_attn(P, P, P, P, 8, P, P, ctypes.byref(b), 64, 80, 4, 128,
-                               args["scale"], lc.LC_BF16, P, N, N, 0, N, N) == lc.LC_ERR_UNSUPPORTED
+                               args["scale"], N, lc.LC_BF16, P, N, N, 0, N, N) == lc.LC_ERR_UNSUPPORTED
     assert lib.sparse_mqa_attn(P, P, P, P, 8, P, P, ctypes.byref(b), 64, 128, 4, -1,
-                               args["scale"], lc.LC_BF16, P, N, N, 0, N, N) == lc.LC_ERR_INVALID_ARG
+                               args["scale"], N, lc.LC_BF16, P, N, N, 0, N, N) == lc.LC_ERR_INVALID_ARG
     assert lib.sparse_mqa_attn(P, P, P, P, 8, N, N, ctypes.byref(b), 64, 128, 4, 16,
-                               args["scale"], lc.LC_BF16, P, N, N, 0, N, N) == lc.LC_ERR_INVALID_ARG
+                               args["scale"], N, lc.LC_BF16, P, N, N, 0, N, N) == lc.LC_ERR_INVALID_ARG
     assert lib.hca_dense_attn(P, P, P, P, P, ctypes.byref(b), 64, 128, 128, 128,
-                              ctypes.c_float(0.0), lc.LC_BF16, P, N, N, 0, N,
-                              N) == lc.LC_ERR_INVALID_ARG
+                              ctypes.c_float(0.0), N, lc.LC_BF16, P, N, N, 0,
+                              N, N) == lc.LC_ERR_INVALID_ARG
     assert lib.hca_dense_attn(N, P, P, P, P, ctypes.byref(b), 64, 128, 128, 128,
-                              args["scale"], lc.LC_BF16, P, N, N, 0, N, N) == lc.LC_ERR_INVALID_ARG
+                              args["scale"], N, lc.LC_BF16, P, N, N, 0, N, N) == lc.LC_ERR_INVALID_ARG
     # nothing above reached a kernel
     assert lib.lc_launch_count() == launches_before
 

@@ -269,6 +269,58 @@ def test_hca_attn(lc, dtype, H, d, m, W, T, q_from):
     np.testing.assert_allclose(f64(lse)[fin], rl[fin], rtol=0, atol=tol)
 
 
+# ------------------------------------------------------- attention sink
+
+def _sinks(H, seed):
+    """Per-head sink logits: head 0 has none (-inf), head 1 one that takes
+    almost all of the attention, the rest moderate."""
+    s = np.random.default_rng(seed).normal(0.0, 2.0, H)
+    s[0] = -np.inf
+    s[1] = 40.0
+    return s.astype(np.float32)
+
+
+@pytest.mark.parametrize("kind,dtype,H,d,W,T", [
+    ("sparse", "f32", 8, 64, 64, 900),      # SIMT path
+    ("sparse", "bf16", 64, 128, 128, 1200),  # tensor-core path
+    ("hca", "f32", 8, 64, 64, 1000),
+    ("hca", "bf16", 64, 128, 128, 2100),
+    ("hca", "bf16", 128, 128, 0, 1000),      # no window: rows t < 127 see only the sink
+])
+def test_attention_sink(lc, kind, dtype, H, d, W, T):
+    sink = _sinks(H, 5)
+    sink_d = dev(torch.from_numpy(sink))
+    if kind == "sparse":
+        m, k = 4, 64
+        L, Kc, Vc = _attn_case(dtype, H, d, m, k, W, T, seed=41)
+        tpos = np.array(L["batch"].positions())
+        sel = oracle.topk(np.random.default_rng(4).standard_normal((len(tpos), T // m)),
+                          (tpos + 1) // m, k)
+        b = lc.DeviceBatch.from_workload(L["batch"])
+        O, lse = lc.sparse_mqa_attn(dev(L["Q"]), dev(Kc), dev(Vc), dev(torch.from_numpy(sel)),
+                                    dev(L["K"]), dev(L["V"]), b, m, W, L["scale"], sink=sink_d)
+        rO, rl = oracle.sparse_attn(L["Q"], Kc, Vc, sel, L["K"], L["V"], 0, tpos, W, L["scale"],
+                                    sink=sink)
+    else:
+        m = 128
+        L = wl.hca_layer(T=T, H=H, d=d, m=m, W=W, dtype=dtype, seed=42)
+        Kc = cast(oracle.compress(L["K"], L["G"], m), dtype)
+        Vc = cast(oracle.compress(L["V"], L["G"], m), dtype)
+        tpos = np.array(L["batch"].positions())
+        b = lc.DeviceBatch.from_workload(L["batch"])
+        O, lse = lc.hca_dense_attn(dev(L["Q"]), dev(Kc), dev(Vc), dev(L["K"]), dev(L["V"]), b,
+                                   m, W, L["scale"], sink=sink_d)
+        rO, rl = oracle.hca_attn(L["Q"], Kc, Vc, m, L["K"], L["V"], 0, tpos, W, L["scale"],
+                                 sink=sink)
+    torch.cuda.synchronize()
+    tol = TOL_ATTN[dtype]
+    np.testing.assert_allclose(f64(O), rO, rtol=0, atol=tol)
+    g, fin = f64(lse), np.isfinite(rl)
+    assert np.array_equal(np.isneginf(g), np.isneginf(rl))
+    np.testing.assert_allclose(g[fin], rl[fin], rtol=0, atol=tol)
+    assert np.abs(f64(O)[:, 1]).max() < 1e-6  # the dominant sink leaves almost nothing
+
+
 # -------------------------------------------------------------- end to end
 
 def test_csa_tiny_end_to_end(lc):
