@@ -12,19 +12,18 @@
 //               128-column TMEM score buffers (score buffer g % 4 for the g-th
 //               head of the CTA); warp 17 issues the even heads and warp 18
 //               the odd ones, so the short tensor-core queue stays fed while
-//               one issuer waits; a buffer is reused three heads later
+//               one issuer waits; a buffer is reused four heads later
 //   warps 0-15  epilogue: warp w owns TMEM lanes 32(w%4).. (its query rows)
 //               and columns 32(w/4).. of each buffer; it folds the heads in
 //               order, acc = fma(w_h / 2, s_h + |s_h|, acc) (= w_h max(s_h, 0)
 //               in all but overflow cases), two columns per packed fp32x2
-//               add and FMA, then
-//               either stores the 32 scores of the
-//               tile (MATERIALIZE) or appends the entries whose score reaches
-//               the row's threshold to the row's candidate list (FILTER).  The
+//               add and FMA, then either stores the 32 scores of the tile
+//               (MATERIALIZE) or appends the entries whose score reaches the
+//               row's threshold to the row's candidates (FILTER).  The
 //               threshold test is a sign-bit collect of acc - theta; the
-//               candidates are staged eight columns at a time.  A buffer is handed
-//               back to its issuer through an mbarrier (one arrival per warp)
-//               as soon as the warp's TMEM read completes.
+//               candidates are staged eight columns at a time.  A buffer is
+//               handed back to its issuer through an mbarrier (one arrival
+//               per warp) as soon as the warp's TMEM read completes.
 // The fused top-k of a row (see index_topk_tc_launch):
 //   1. scores of every s-th entry (MATERIALIZE over a strided tensor map);
 //   2. theta = the rho-th largest sampled key, a lower bound for the k-th
