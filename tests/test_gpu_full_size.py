@@ -4,12 +4,13 @@ benchmark times, on sampled outputs the oracle computes one by one.
 - layer_pair_1m: 1,048,576-token context, last 4096 positions queried; CSA
   (m=4, indexer 8x64 over 262,144 entries, top-k 1024, window 128) and HCA
   (m'=128, window 128), 128 heads x 128.  The step is the benchmark's own.
-  Sampled query rows are checked against the oracle: the fused top-k (equal,
-  or the oracle's k-th / (k+1)-th gap below 1e-5), CSA attention (rows whose
+  266 sampled query rows are checked against the oracle: the fused top-k
+  (equal, or different only inside the near-tie band of selection_check),
+  CSA attention (rows whose
   selection equals the oracle's) and HCA attention, both within the bf16
   tolerance; sampled compressed entries of the chunk within one bf16 ulp.
-- csa_decode: 64 sequences with contexts ~U[65536, 262144]; sampled
-  sequences are checked the same way.
+- csa_decode: 64 sequences with contexts ~U[65536, 262144]; every sequence
+  is checked the same way.
 
 The oracle builds its own compressed caches from the raw inputs (rounded to
 bf16, the stored type) and never reads a value the CUDA path produced.
@@ -19,10 +20,10 @@ import pytest
 import torch
 
 import oracle
+from selection_check import check_selection
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-2
-GAP = 1e-5
 
 
 @pytest.fixture(scope="module")
@@ -39,18 +40,9 @@ def _bf16_round(x):
 
 
 def _check_rows(gsel, I, nvis, k):
-    """Selections equal the oracle's, or are excused by the gap rule.
-    Returns the mask of rows whose selection is identical."""
-    rsel = oracle.topk(I, nvis, k)
-    same = np.all(gsel == rsel, axis=1)
-    for r in np.nonzero(~same)[0]:
-        s = np.sort(I[r, : nvis[r]])[::-1]
-        assert s[k - 1] - s[k] < GAP, f"row {r}: selection differs, gap {s[k - 1] - s[k]}"
-        keep = min(k, int(nvis[r]))
-        v = gsel[r, :keep]
-        assert np.all(np.diff(v) > 0) and v[0] >= 0 and v[-1] < nvis[r]
-        assert np.all(gsel[r, keep:] == -1)
-    return rsel, same
+    """Selections equal the oracle's, or differ only inside the near-tie
+    band (selection_check).  Returns (oracle selection, identical-row mask)."""
+    return check_selection(gsel, I, nvis, k)
 
 
 def test_layer_pair_1m_sampled(lc):
@@ -78,13 +70,17 @@ def test_layer_pair_1m_sampled(lc):
         ulp = np.abs(ref[ents]) * 2.0 ** -7 + 1e-30
         assert np.all(np.abs(got - ref[ents]) <= ulp), name
 
-    rows = np.unique(np.concatenate([[0, 1, 127, 128, 2047, 4094, 4095],
-                                     rng.choice(wk.chunk, 9, replace=False)]))
+    # 256+ query rows over the chunk: its first and last rows, the edges of
+    # the 128-row tiles of the indexer and the HCA CTAs, and seeded rows
+    fixed = [0, 1, 127, 128, 255, 256, 2047, 2048, 4094, 4095]
+    rest = np.setdiff1d(np.arange(wk.chunk), fixed)
+    rows = np.unique(np.concatenate([fixed, rng.choice(rest, 256, replace=False)]))
     t = (wk.q0 + rows).astype(np.int64)
     I = oracle.index(c["qI"][rows].cpu(), c["w"][rows].cpu(), kI64, t, wk.m_c)
     gsel = wk.sel[torch.from_numpy(rows).cuda()].cpu().numpy()
     rsel, same = _check_rows(gsel, I, (t + 1) // wk.m_c, wk.k)
-    assert same.sum() >= len(rows) - 2
+    del I
+    assert same.mean() >= 0.95
 
     rO, rl = oracle.sparse_attn(c["Q"][rows].cpu(), Kc, Vc, rsel, raw["csa_K"], raw["csa_V"],
                                 raw["pos0"], t, wk.W, c["scale"])
@@ -112,10 +108,8 @@ def test_csa_decode_sampled(lc):
     gsel_all = wk.sel.cpu().numpy()
     gO_all = wk.O.double().cpu().numpy()
     gl_all = wk.lse.double().cpu().numpy()
-    # the shortest and longest contexts and a few more
-    order = np.argsort(D["ctx"])
-    seqs = np.unique(np.concatenate([order[:1], order[-1:], [0, 17, 40]]))
-    for s in seqs:
+    # every sequence of the batch
+    for s in range(D["B"]):
         c0, c1, r0, r1 = bt.cu_c[s], bt.cu_c[s + 1], bt.cu_raw[s], bt.cu_raw[s + 1]
         t = np.array([bt.q_pos0[s]], dtype=np.int64)
         I = oracle.index(D["qI"][s:s + 1].cpu(), D["w"][s:s + 1].cpu(), D["kI"][c0:c1].cpu(), t,

@@ -3,8 +3,10 @@ top-k (sampled threshold -> candidate filter -> exact selection -> per-row
 fallback) against the CPU oracle.
 
 Bars: scores within a rigorous fp32 accumulation bound, invisible entries
-exactly -inf; fused selections equal the oracle's except in rows whose oracle
-gap between the k-th and (k+1)-th score is below 1e-5."""
+exactly -inf; fused selections equal the oracle's, or differ from it only
+inside the near-tie band at the k-th boundary (selection_check: boundary gap
+below 1e-5, every kept entry within 1e-5 below the oracle's k-th score,
+every left-out entry within 1e-5 above it)."""
 import math
 
 import numpy as np
@@ -13,9 +15,9 @@ import torch
 
 import oracle
 import workloads as wl
+from selection_check import check_selection
 
 pytestmark = pytest.mark.gpu
-GAP = 1e-5
 
 
 @pytest.fixture(scope="module")
@@ -43,19 +45,8 @@ def _bound(qI, w, kI):
 
 def _check_selection(gsel, I, nvis, k):
     """gsel: GPU top-k; I: oracle scores.  Returns the number of excused rows."""
-    rsel = oracle.topk(I, nvis, k)
-    excused = 0
-    for r in range(gsel.shape[0]):
-        keep = min(k, int(nvis[r]))
-        row = gsel[r]
-        assert np.all(row[keep:] == -1), r
-        v = row[:keep]
-        assert np.all(np.diff(v) > 0) and (keep == 0 or (v[0] >= 0 and v[-1] < nvis[r])), r
-        if not np.array_equal(row, rsel[r]):
-            s = np.sort(I[r, : nvis[r]])[::-1]
-            assert s[k - 1] - s[k] < GAP, f"row {r}: selection differs, gap {s[k-1]-s[k]}"
-            excused += 1
-    return excused
+    _, same = check_selection(gsel, I, nvis, k)
+    return int((~same).sum())
 
 
 @pytest.mark.parametrize("HI,T,m,q_from", [(8, 2048, 4, 0), (4, 2304, 4, 100), (8, 1400, 8, 0)])
