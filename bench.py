@@ -1,9 +1,8 @@
 #!/usr/bin/env python3
 """Benchmark of the CSA + HCA attention hot path on B300.
 
-One step = one pass of the whole path over one query chunk of the 1M-context
-interleaved layer pair (context 1,048,576 tokens, the last 4096 positions
-queried, bf16):
+The headline step is one query chunk of the 1M-context interleaved layer pair
+(context 1,048,576 tokens, the last 4096 positions queried, bf16):
   CSA layer: csa_compress (the chunk's 4096 tokens -> 1024 new entries)
              -> lightning_index fused with topk_select (8 x 64 indexer, k=1024,
                 over 262,144 entries) -> sparse_mqa_attn (128 heads x 128,
@@ -14,23 +13,30 @@ Entries of the positions before the chunk come from the same compressors in
 an untimed set-up (they are the layer's KV cache).  Metric: query tokens per
 second (4096 per step per GPU).
 
-With --workload csa_decode a step is instead one decode step of 64
-sequences (one query each at its last position, contexts ~U[65536, 262144],
-compressed caches and indexer keys resident): lightning_index fused with
-topk_select (k=1024) -> sparse_mqa_attn (128 heads x 128, window 128).  Its
-roofline is HBM bandwidth (the indexer streams every visible indexer key).
+The default run also measures the other three full-size settings and prints
+each as a sub-record of the same JSON line (same fields as the main record):
+  decode       one decode step of 64 sequences (one query each at its last
+               position, contexts ~U[65536, 262144], compressed caches and
+               indexer keys resident): lightning_index fused with topk_select
+               (k=1024) -> sparse_mqa_attn (128 heads, window 128).  HBM-bound:
+               its roofline is the whole step's algorithmic bytes over the
+               step's time against the measured copy bandwidth.
+  csa_prefill  a 32,768-token CSA prefill (64 heads x 128, indexer 8 x 64,
+               k=512, window 128): csa_compress -> lightning_index + top-k ->
+               sparse_mqa_attn.
+  hca_prefill  a 131,072-token HCA prefill (64 heads x 128, m'=128, window
+               128): hca_compress -> hca_dense_attn.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload layer_pair_1m|csa_decode]
+                  [--workload all|layer_pair_1m|csa_decode|csa_prefill|hca_prefill]
 
 Prints ONE JSON line on rank 0.  `--impl reference` times the CPU oracle on a
-bounded sample of the same workload (rank 0 only).
+bounded sample of the layer-pair workload (rank 0 only).
 """
 from __future__ import annotations
 
 import argparse
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -51,17 +57,13 @@ UNIT = "query-tokens/s"
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per step of the
-# kernels of each workload's dominant stage, from one ncu capture of the
+# kernels of each workload's roofline stage, from one ncu capture of the
 # current kernels at the full benchmarked size (traffic well above the
-# algorithmic bytes would mean re-reads).  Re-measure when a kernel changes.
+# algorithmic bytes would mean re-reads).  An entry is removed when one of its
+# kernels changes, until it is measured again.
 NCU_STAGE_TRAFFIC = {
-    # index + top-k: candidate pass 339.9 MB, 1/32 sample 92.5 MB, threshold
-    # 134.3 MB, candidate top-k 78.0 MB
-    ("layer_pair_1m", "lightning_index+topk"): 644.7e6,
     # HCA attention: k_hca_tc 140.8 MB read, 89.1 MB written
     ("layer_pair_1m", "hca_dense_attn"): 229.9e6,
-    # index + top-k: streaming indexer 2505.6 MB, radix top-k 9.8 MB
-    ("csa_decode", "lightning_index+topk"): 2515.4e6,
 }
 
 
@@ -136,10 +138,45 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+def _n_window(t, W):
+    return np.minimum(np.asarray(t, dtype=np.int64) + 1, W)
+
+
+def _cpu(d):
+    return {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in d.items()}
+
+
+def layer_pair_config(ctx, chunk, H, d, world):
+    return {"workload": f"layer_pair_{ctx // 1024}k: CSA (m=4, indexer 8x64, top-k 1024, "
+                        f"window 128) + HCA (m'=128, window 128) over a {ctx:,}-token context, "
+                        f"last {chunk} positions queried, Q [{chunk},{H},{d}] per layer",
+            "context": ctx, "query_chunk": chunk, "heads": H, "head_dim": d,
+            "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (raw K/V 256 MiB each, indexer keys 256 MiB)"}
+
+
+def tensor_roofline(stages, stage_ms, flops_of, peaks, region_ms, traffic_key=None):
+    """Tensor roofline of the stage (among flops_of) with the longest time."""
+    dom = max(flops_of, key=lambda s: stage_ms[stages.index(s)])
+    dom_ms = stage_ms[stages.index(dom)]
+    achieved = flops_of[dom] / (dom_ms / 1e3) / 1e12
+    long_region = region_ms > 1000.0
+    peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
+    traffic = NCU_STAGE_TRAFFIC.get((traffic_key, dom)) if traffic_key else None
+    return {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+            "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+            "traffic_unit": "DRAM bytes per launch of the stage's kernels (ncu)",
+            "algorithmic_flop": flops_of[dom],
+            "peak_source": peaks["source"] + (" sustained" if long_region else " burst")}
+
+
 # ---------------------------------------------------------------- workloads
 
 class LayerPair:
     """Device buffers and the step of the 1M-context layer pair."""
+
+    STAGES = ["csa_compress", "lightning_index+topk", "sparse_mqa_attn", "hca_compress",
+              "hca_dense_attn"]
 
     def __init__(self, lc, device, seed=4, ctx=1 << 20, chunk=4096):
         self.lc = lc
@@ -173,13 +210,12 @@ class LayerPair:
         self.lse_csa = torch.empty((chunk, self.H), dtype=torch.float32, device=device)
         self.lse_hca = torch.empty_like(self.lse_csa)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
-        self.stage_events = None
         torch.cuda.synchronize()
 
     # algorithmic work of one step (causal counts), for the roofline
     def work(self):
         t = np.arange(self.q0, self.ctx, dtype=np.int64)
-        nwin = np.minimum(t + 1, self.W)
+        nwin = _n_window(t, self.W)
         nv_c = (t + 1) // self.m_c
         nv_h = (t + 1) // self.m_h
         c = self.P["csa"]
@@ -190,7 +226,6 @@ class LayerPair:
             "index_flop": float(2 * HI * dI * nv_c.sum()),
             "csa_attn_flop": float(4 * self.d * self.H * keys_csa.sum()),
             "hca_attn_flop": float(4 * self.d * self.H * keys_hca.sum()),
-            "compress_bytes": float(2 * 2 * (self.chunk * self.d * 2 + self.chunk // self.m_c * self.d * 2)),
         }
 
     def step(self, events=None):
@@ -220,41 +255,22 @@ class LayerPair:
         if ev:
             ev[5].record()
 
-    STAGES = ["csa_compress", "lightning_index+topk", "sparse_mqa_attn", "hca_compress",
-              "hca_dense_attn"]
-
     def config(self, world):
-        return {"workload": f"layer_pair_{self.ctx // 1024}k: CSA (m=4, indexer 8x64, top-k "
-                            f"1024, window 128) + HCA (m'=128, window 128) over a "
-                            f"{self.ctx:,}-token context, last {self.chunk} positions queried, "
-                            f"Q [{self.chunk},128,128] per layer",
-                "context": self.ctx, "query_chunk": self.chunk, "heads": self.H,
-                "head_dim": self.d, "parallelism": f"replicas x{world}",
-                "l2": "inputs larger than L2 (raw K/V 256 MiB each, indexer keys 256 MiB)"}
+        return layer_pair_config(self.ctx, self.chunk, self.H, self.d, world)
 
     def roofline(self, stage_ms, peaks, region_ms):
-        """Tensor roofline of the stage with the longest time."""
-        work = self.work()
-        flops_of = {"lightning_index+topk": work["index_flop"],
-                    "sparse_mqa_attn": work["csa_attn_flop"],
-                    "hca_dense_attn": work["hca_attn_flop"]}
-        dom = max(flops_of, key=lambda s: stage_ms[self.STAGES.index(s)])
-        dom_ms = stage_ms[self.STAGES.index(dom)]
-        achieved = flops_of[dom] / (dom_ms / 1e3) / 1e12
-        long_region = region_ms > 1000.0
-        peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
-        traffic = NCU_STAGE_TRAFFIC.get(("layer_pair_1m", dom)) if self.ctx == 1 << 20 else None
-        return {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
-                "traffic_unit": "bytes per launch of the stage's kernels (ncu)",
-                "peak_source": peaks["source"] + (" sustained" if long_region else " burst")}
+        w = self.work()
+        flops_of = {"lightning_index+topk": w["index_flop"], "sparse_mqa_attn": w["csa_attn_flop"],
+                    "hca_dense_attn": w["hca_attn_flop"]}
+        key = "layer_pair_1m" if self.ctx == 1 << 20 else None
+        return tensor_roofline(self.STAGES, stage_ms, flops_of, peaks, region_ms, key)
 
     def path_tflops(self, ms_step):
         w = self.work()
         return (w["index_flop"] + w["csa_attn_flop"] + w["hca_attn_flop"]) / (ms_step / 1e3) / 1e12
 
     def cpu_baseline(self, budget_s):
-        return cpu_baseline(self, budget_s=budget_s)
+        return layer_pair_cpu_baseline(self, budget_s=budget_s)
 
     # per-step host inputs / outputs of the end-to-end measurement
     def host_io(self):
@@ -277,8 +293,8 @@ class Decode:
 
     def __init__(self, lc, device, seed=3):
         self.lc = lc
-        D = wl.csa_decode(B=64, ctx_lo=65536, ctx_hi=262144, H=128, d=128, HI=8, dI=64, m=4,
-                          k=1024, W=128, dtype="bf16", seed=seed, device=device)
+        D = wl.CONFIGS["csa_decode"](device=device)
+        assert D["seed"] == seed
         self.D = D
         self.chunk = D["B"]  # query tokens per step
         self.m, self.k, self.W, self.H, self.d = D["m"], D["k"], D["W"], D["H"], D["d"]
@@ -293,16 +309,20 @@ class Decode:
         torch.cuda.synchronize()
 
     def work(self):
+        """Algorithmic bytes of one step: every visible indexer key once, the
+        query's indexer q and head weights, the selected indices written and
+        read, every gathered K/V row (selected entries and window) once, Q
+        read and O written."""
         D = self.D
         ctx = np.array(D["ctx"], dtype=np.int64)
         nv = ctx // self.m
-        nwin = np.minimum(ctx, self.W)
-        keys = np.minimum(nv, self.k) + nwin
+        keys = np.minimum(nv, self.k) + _n_window(ctx - 1, self.W)
         idx_bytes = float(nv.sum() * D["HI"] * D["dI"] * 2 + D["B"] * D["HI"] * (D["dI"] * 2 + 4)
                           + D["B"] * self.k * 4)
         attn_bytes = float(keys.sum() * self.d * 2 * 2 + 2 * D["B"] * self.H * self.d * 2
                            + D["B"] * self.k * 4)
         return {"index_bytes": idx_bytes, "attn_bytes": attn_bytes,
+                "step_bytes": idx_bytes + attn_bytes,
                 "attn_flop": float(4 * self.d * self.H * keys.sum())}
 
     def step(self, events=None):
@@ -340,14 +360,189 @@ class Decode:
         return decode_cpu_baseline(self, budget_s=budget_s)
 
     def roofline(self, stage_ms, peaks, region_ms):
+        """HBM roofline of the whole step: its algorithmic bytes over the
+        step's time (the sum of its stages' event times)."""
         w = self.work()
-        ms = stage_ms[self.STAGES.index("lightning_index+topk")]
-        gbs = w["index_bytes"] / (ms / 1e3) / 1e9
-        return {"bound": "hbm", "kernel": "lightning_index+topk", "achieved": gbs,
-                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
-                "traffic": NCU_STAGE_TRAFFIC[("csa_decode", "lightning_index+topk")],
-                "traffic_unit": "bytes per launch of the stage's kernels (ncu)",
-                "algorithmic_bytes": w["index_bytes"], "peak_source": peaks["source"]}
+        ms = sum(stage_ms)
+        gbs = w["step_bytes"] / (ms / 1e3) / 1e9
+        return {"bound": "hbm", "kernel": "whole step (lightning_index+topk, sparse_mqa_attn)",
+                "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs / peaks["hbm_gbs"],
+                "traffic": NCU_STAGE_TRAFFIC.get(("csa_decode", "step")),
+                "traffic_unit": "DRAM bytes per step of the step's kernels (ncu)",
+                "algorithmic_bytes": w["step_bytes"], "peak_source": peaks["source"]}
+
+
+class CsaPrefill:
+    """A 32,768-token CSA prefill: compress -> index + top-k (k=512) ->
+    sparse attention, 64 heads."""
+
+    STAGES = ["csa_compress", "lightning_index+topk", "sparse_mqa_attn"]
+
+    def __init__(self, lc, device):
+        self.lc = lc
+        L = wl.CONFIGS["csa_prefill"](device=device)
+        self.L = L
+        self.T, self.m, self.k, self.W, self.H, self.d = (L["T"], L["m"], L["k"], L["W"], L["H"],
+                                                          L["d"])
+        self.chunk = self.T
+        self.b = lc.DeviceBatch.from_workload(L["batch"], device=device)
+        self.Kc = torch.empty((self.T // self.m, self.d), dtype=torch.bfloat16, device=device)
+        self.Vc = torch.empty_like(self.Kc)
+        self.ws = torch.empty(lc.workspace_size(lc.LC_OP_LIGHTNING_INDEX, self.b, HI=L["HI"],
+                                                dI=L["dI"], k=self.k),
+                              dtype=torch.uint8, device=device)
+        self.sel = torch.empty((self.T, self.k), dtype=torch.int32, device=device)
+        self.O = torch.empty_like(L["Q"])
+        self.lse = torch.empty((self.T, self.H), dtype=torch.float32, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        torch.cuda.synchronize()
+
+    def work(self):
+        L = self.L
+        t = np.arange(self.T, dtype=np.int64)
+        nv = (t + 1) // self.m
+        keys = np.minimum(nv, self.k) + _n_window(t, self.W)
+        return {"index_flop": float(2 * L["HI"] * L["dI"] * nv.sum()),
+                "attn_flop": float(4 * self.d * self.H * keys.sum())}
+
+    def step(self, events=None):
+        lc, L = self.lc, self.L
+        ev = events
+        if ev:
+            ev[0].record()
+        lc.csa_compress(L["K"], L["V"], L["G"], m=self.m, Kc=self.Kc, Vc=self.Vc)
+        if ev:
+            ev[1].record()
+        lc.lightning_index(L["qI"], L["w"], L["kI"], self.b, self.m, scores=False, k=self.k,
+                           topk=self.sel, ws=self.ws, dev_err=self.err)
+        if ev:
+            ev[2].record()
+        lc.sparse_mqa_attn(L["Q"], self.Kc, self.Vc, self.sel, L["K"], L["V"], self.b, self.m,
+                           self.W, L["scale"], O=self.O, lse=self.lse, dev_err=self.err)
+        if ev:
+            ev[3].record()
+
+    def host_io(self):
+        L = self.L
+        return ({"Q": L["Q"], "K": L["K"], "V": L["V"], "qI": L["qI"], "kI": L["kI"],
+                 "w": L["w"]}, {"O": self.O})
+
+    def config(self, world):
+        return {"workload": "csa_prefill: one 32,768-token sequence, every position queried, "
+                            "Q [32768,64,128], K,V [32768,128], CSA m=4 (8192 entries), "
+                            "indexer 8x64, top-k 512, window 128 (seed 1)",
+                "seq_len": self.T, "heads": self.H, "head_dim": self.d,
+                "parallelism": f"replicas x{world}",
+                "l2": "inputs larger than L2 (Q 512 MiB)"}
+
+    def roofline(self, stage_ms, peaks, region_ms):
+        w = self.work()
+        return tensor_roofline(self.STAGES, stage_ms,
+                               {"lightning_index+topk": w["index_flop"],
+                                "sparse_mqa_attn": w["attn_flop"]}, peaks, region_ms,
+                               "csa_prefill")
+
+    def path_tflops(self, ms_step):
+        w = self.work()
+        return (w["index_flop"] + w["attn_flop"]) / (ms_step / 1e3) / 1e12
+
+    def cpu_baseline(self, budget_s):
+        import oracle
+        L = _cpu(self.L)
+        Kc = oracle.compress(L["K"], L["G"], self.m)
+        Vc = oracle.compress(L["V"], L["G"], self.m)
+        Kc = torch.from_numpy(Kc).to(torch.bfloat16).double().numpy()
+        Vc = torch.from_numpy(Vc).to(torch.bfloat16).double().numpy()
+        kI = L["kI"].double().numpy()
+
+        def run(rows):
+            t = rows.astype(np.int64)
+            I = oracle.index(L["qI"][rows], L["w"][rows], kI, t, self.m)
+            sel = oracle.topk(I, (t + 1) // self.m, self.k)
+            oracle.sparse_attn(L["Q"][rows], Kc, Vc, sel, L["K"], L["V"], 0, t, self.W,
+                               L["scale"])
+        return sampled_rows_baseline(run, self.T, budget_s,
+                                     "query rows of the 32,768-token CSA prefill (index over "
+                                     "the visible entries, top-k 512, CSA attention, fp64); "
+                                     "compressed entries built untimed")
+
+
+class HcaPrefill:
+    """A 131,072-token HCA prefill: compress -> dense attention, 64 heads."""
+
+    STAGES = ["hca_compress", "hca_dense_attn"]
+
+    def __init__(self, lc, device):
+        self.lc = lc
+        L = wl.CONFIGS["hca_prefill"](device=device)
+        self.L = L
+        self.T, self.m, self.W, self.H, self.d = L["T"], L["m"], L["W"], L["H"], L["d"]
+        self.chunk = self.T
+        self.b = lc.DeviceBatch.from_workload(L["batch"], device=device)
+        self.Kc = torch.empty((self.T // self.m, self.d), dtype=torch.bfloat16, device=device)
+        self.Vc = torch.empty_like(self.Kc)
+        self.O = torch.empty_like(L["Q"])
+        self.lse = torch.empty((self.T, self.H), dtype=torch.float32, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        torch.cuda.synchronize()
+
+    def work(self):
+        t = np.arange(self.T, dtype=np.int64)
+        keys = (t + 1) // self.m + _n_window(t, self.W)
+        return {"attn_flop": float(4 * self.d * self.H * keys.sum())}
+
+    def step(self, events=None):
+        lc, L = self.lc, self.L
+        ev = events
+        if ev:
+            ev[0].record()
+        lc.hca_compress(L["K"], L["V"], L["G"], m=self.m, Kc=self.Kc, Vc=self.Vc)
+        if ev:
+            ev[1].record()
+        lc.hca_dense_attn(L["Q"], self.Kc, self.Vc, L["K"], L["V"], self.b, self.m, self.W,
+                          L["scale"], O=self.O, lse=self.lse, dev_err=self.err)
+        if ev:
+            ev[2].record()
+
+    def host_io(self):
+        L = self.L
+        return {"Q": L["Q"], "K": L["K"], "V": L["V"]}, {"O": self.O}
+
+    def config(self, world):
+        return {"workload": "hca_prefill: one 131,072-token sequence, every position queried, "
+                            "Q [131072,64,128], K,V [131072,128], HCA m'=128 (1024 entries), "
+                            "window 128 (seed 2)",
+                "seq_len": self.T, "heads": self.H, "head_dim": self.d,
+                "parallelism": f"replicas x{world}",
+                "l2": "inputs larger than L2 (Q 2 GiB)"}
+
+    def roofline(self, stage_ms, peaks, region_ms):
+        return tensor_roofline(self.STAGES, stage_ms, {"hca_dense_attn": self.work()["attn_flop"]},
+                               peaks, region_ms, "hca_prefill")
+
+    def path_tflops(self, ms_step):
+        return self.work()["attn_flop"] / (ms_step / 1e3) / 1e12
+
+    def cpu_baseline(self, budget_s):
+        import oracle
+        L = _cpu(self.L)
+        Kc = torch.from_numpy(oracle.compress(L["K"], L["G"], self.m)).to(torch.bfloat16)
+        Vc = torch.from_numpy(oracle.compress(L["V"], L["G"], self.m)).to(torch.bfloat16)
+        Kc, Vc = Kc.double().numpy(), Vc.double().numpy()
+
+        def run(rows):
+            oracle.hca_attn(L["Q"][rows], Kc, Vc, self.m, L["K"], L["V"], 0,
+                            rows.astype(np.int64), self.W, L["scale"])
+        return sampled_rows_baseline(run, self.T, budget_s,
+                                     "query rows of the 131,072-token HCA prefill (dense "
+                                     "attention over the visible entries and the window, "
+                                     "fp64); compressed entries built untimed")
+
+
+WORKLOADS = {"layer_pair_1m": LayerPair, "csa_decode": Decode, "csa_prefill": CsaPrefill,
+             "hca_prefill": HcaPrefill}
+SUB_RECORDS = {"csa_decode": "decode", "csa_prefill": "csa_prefill", "hca_prefill": "hca_prefill"}
 
 
 # ---------------------------------------------------------------- ranks
@@ -369,23 +564,10 @@ def whole_job_rate(units_per_rank: int, world: int, ms_per_step: float) -> float
 
 # ---------------------------------------------------------------- our arm
 
-def run_ours(args):
-    import long_context_compressed_13_b300 as lc
-    lc.load_library()
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py: no CUDA device")
-    torch.cuda.set_device(local)
-    device = f"cuda:{local}"
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device(device))
-    peaks = load_peaks()
-
-    wk = Decode(lc, device) if args.workload == "csa_decode" else LayerPair(lc, device, ctx=args.ctx)
+def measure(wk, args, dist, device, peaks, world, rank, cpu_budget):
+    """Device-timed region, end-to-end region and CPU baseline of one workload.
+    Returns the record (the fields of the JSON line)."""
+    lc = wk.lc
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
         wk.step()
@@ -424,44 +606,78 @@ def run_ours(args):
     h2d = sum(v.numel() * v.element_size() for v in h_in.values())
     d2h = sum(v.numel() * v.element_size() for v in h_out.values())
     e2e_steps = max(1, min(args.steps, 5))
-    for _ in range(1):
+
+    def e2e_step():
         for k_, v in h_in.items():
             ins[k_].copy_(v, non_blocking=True)
         wk.step()
         for k_, v in h_out.items():
             v.copy_(outs[k_], non_blocking=True)
+
+    e2e_step()
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     e0 = time.perf_counter()
     for _ in range(e2e_steps):
-        for k_, v in h_in.items():
-            ins[k_].copy_(v, non_blocking=True)
-        wk.step()
-        for k_, v in h_out.items():
-            v.copy_(outs[k_], non_blocking=True)
+        e2e_step()
         torch.cuda.synchronize()
     e2e_s = max_over_ranks(dist, (time.perf_counter() - e0) / e2e_steps, device)
+    del h_in, h_out
 
     ms_step = ms / args.steps
-    value = whole_job_rate(wk.chunk, world, ms_step)
-    out = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+    rec = {
+        "metric": METRIC, "value": whole_job_rate(wk.chunk, world, ms_step), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
         "config": wk.config(world),
         "roofline": wk.roofline(stage_ms, peaks, ms),
         "stages_ms": dict(zip(wk.STAGES, stage_ms)),
         "path_tflops": wk.path_tflops(ms_step),
         "e2e": {"value": whole_job_rate(wk.chunk, world, e2e_s * 1e3), "unit": UNIT,
-                "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
         "dev_err": err,
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = wk.cpu_baseline(args.cpu_budget)
+        rec["cpu_baseline"] = wk.cpu_baseline(cpu_budget)
+    return rec
+
+
+def run_ours(args):
+    import long_context_compressed_13_b300 as lc
+    lc.load_library()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device")
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(device))
+    peaks = load_peaks()
+
+    names = ["layer_pair_1m", "csa_decode", "csa_prefill", "hca_prefill"] \
+        if args.workload == "all" else [args.workload]
+    recs = {}
+    for name in names:
+        if name == "layer_pair_1m":
+            wk = LayerPair(lc, device, ctx=args.ctx)
+        else:
+            wk = WORKLOADS[name](lc, device)
+        budget = args.cpu_budget if name == names[0] else args.cpu_budget / 2
+        recs[name] = measure(wk, args, dist, device, peaks, world, rank, budget)
+        del wk
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    out = recs[names[0]]
+    for name in names[1:]:
+        out[SUB_RECORDS[name]] = recs[name]
     if rank == 0:
         print(json.dumps(out), flush=True)
     if dist:
@@ -507,30 +723,38 @@ def _oracle_state(P, q0, ctx, m_c, m_h, W):
     return out, raw, kI64
 
 
-def cpu_baseline(wk, budget_s=20.0):
+def sampled_rows_baseline(run, n_rows, budget_s, what):
+    """Times run(rows) on a seeded sample of query rows sized to about
+    budget_s seconds (calibrated on a small first sample)."""
     import oracle
-    P = wk.P
-    Pc = {"csa": {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in P["csa"].items()},
-          "hca": {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in P["hca"].items()}}
-    st, raw, kI64 = _oracle_state(Pc, wk.q0, wk.ctx, wk.m_c, wk.m_h, wk.W)
+    nt = oracle.num_threads()
     rng = np.random.default_rng(0)
-    rows_all = rng.permutation(wk.chunk)
-    # calibrate on one row, then run a sample sized to the budget
+    perm = rng.permutation(n_rows)
+    cal = np.sort(perm[:nt])
     t0 = time.perf_counter()
-    _oracle_rows_step(Pc, rows_all[:1], wk.q0, wk.ctx, wk.m_c, wk.m_h, wk.k, wk.W, st["Kc"],
-                      st["Vc"], st["Kh"], st["Vh"], raw, kI64)
-    one = time.perf_counter() - t0
-    n = int(max(1, min(wk.chunk, budget_s / max(one, 1e-3) * 0.8 * oracle.num_threads() / 1.0)))
-    n = max(oracle.num_threads(), min(n, 512))
-    rows = np.sort(rows_all[:n])
+    run(cal)
+    one = max((time.perf_counter() - t0) / len(cal), 1e-6)
+    n = int(min(n_rows, max(nt, budget_s / one)))
+    rows = np.sort(perm[:n])
     t0 = time.perf_counter()
-    _oracle_rows_step(Pc, rows, wk.q0, wk.ctx, wk.m_c, wk.m_h, wk.k, wk.W, st["Kc"], st["Vc"],
-                      st["Kh"], st["Vh"], raw, kI64)
+    run(rows)
     dt = time.perf_counter() - t0
-    return {"value": n / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{n} of the 4096 query rows of the layer pair (index over all 262144 "
-                      f"entries, top-k 1024, CSA and HCA attention, fp64); compressed caches "
-                      f"built untimed", "seconds": dt}
+    return {"value": n / dt, "unit": UNIT, "cores": nt, "kind": "oracle",
+            "sample": f"{n} of the {n_rows} {what}", "seconds": dt}
+
+
+def layer_pair_cpu_baseline(wk, budget_s=20.0):
+    P = wk.P
+    Pc = {"csa": _cpu(P["csa"]), "hca": _cpu(P["hca"])}
+    st, raw, kI64 = _oracle_state(Pc, wk.q0, wk.ctx, wk.m_c, wk.m_h, wk.W)
+
+    def run(rows):
+        _oracle_rows_step(Pc, rows, wk.q0, wk.ctx, wk.m_c, wk.m_h, wk.k, wk.W, st["Kc"],
+                          st["Vc"], st["Kh"], st["Vh"], raw, kI64)
+    return sampled_rows_baseline(run, wk.chunk, budget_s,
+                                 "query rows of the layer pair (index over all 262144 entries, "
+                                 "top-k 1024, CSA and HCA attention, fp64); compressed caches "
+                                 "built untimed")
 
 
 def decode_cpu_baseline(wk, budget_s=20.0):
@@ -563,6 +787,9 @@ def decode_cpu_baseline(wk, budget_s=20.0):
 
 
 def run_reference(args):
+    """The CPU oracle on the layer-pair workload: each step runs the whole
+    path (index, top-k, CSA and HCA attention) for a seeded sample of the
+    chunk's query rows; ms_per_step is the measured time of that sample."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -582,17 +809,18 @@ def run_reference(args):
                           st["Kh"], st["Vh"], raw, kI64)
         if s >= args.warmup:
             times.append(time.perf_counter() - t0)
-    per_row = sum(times) / (n * len(times))
-    value = 1.0 / per_row
+    step_s = sum(times) / len(times)
+    value = n / step_s
+    sample = (f"{n} seeded query rows per step of the {chunk}-row chunk (the whole path for "
+              f"each row, fp64); ms_per_step is the measured time of those rows")
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-           "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_row * chunk * 1e3,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic",
-           "config": {"workload": "layer_pair_1m (CPU oracle, sampled rows)", "context": ctx,
-                      "query_chunk": chunk},
+           "config": layer_pair_config(ctx, chunk, c["H"], c["d"], world),
+           "sample": sample,
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
-                            "kind": "oracle",
-                            "sample": f"{n} query rows per step of the 4096-row chunk"},
+                            "kind": "oracle", "sample": sample},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
@@ -609,7 +837,7 @@ def main():
     # a shorter context keeps the same kernels on a smaller case (profiler
     # captures); the measured workload is the default 1,048,576 tokens
     ap.add_argument("--ctx", type=int, default=1 << 20)
-    ap.add_argument("--workload", default="layer_pair_1m", choices=["layer_pair_1m", "csa_decode"])
+    ap.add_argument("--workload", default="all", choices=["all", *WORKLOADS])
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -65,7 +65,8 @@ typedef enum {
     LC_DEVERR_INDEX = 1,   /* selected entry index >= stored entries or not visible */
     LC_DEVERR_WINDOW = 2,  /* window position outside the sequence's raw rows */
     LC_DEVERR_BATCH = 4,   /* batch descriptor inconsistent (e.g. n_vis > entries) */
-    LC_DEVERR_TIMEOUT = 8  /* a bounded wait inside a kernel gave up */
+    LC_DEVERR_TIMEOUT = 8, /* a bounded wait inside a kernel gave up */
+    LC_DEVERR_SINK = 16    /* a sink logit is NaN or +inf (that head gets no sink) */
 } lc_dev_error;
 
 /* Ragged batch.  Every array is on the DEVICE (int64); the three maxima are
@@ -148,7 +149,10 @@ lc_status topk_select(const float *scores, int64_t ld, const lc_batch *batch, in
  * empty S gives O = 0 and lse = s_h (-inf without a sink).
  *   Q [total_q, H, d]; Kc, Vc [cu_c[B], d]; Kraw, Vraw [cu_raw[B], d] (dtype)
  *   topk [total_q, k] int32 (-1 = unused slot); O [total_q, H, d] dtype;
- *   sink [H] fp32 (natural-log units, like z) or NULL;
+ *   sink [H] fp32 (natural-log units, like z) or NULL; at least H values,
+ *        on the same device as Q; each finite or -inf (no sink for that
+ *        head); a NaN or +inf value raises LC_DEVERR_SINK and that head is
+ *        computed without a sink;
  *   lse [total_q, H] fp32 or NULL.
  * Supported: d in {64,128}; H % 8 == 0, 8 <= H <= 128; 0 <= W <= 4096. */
 lc_status sparse_mqa_attn(const void *Q, const void *Kc, const void *Vc, const int32_t *topk,
@@ -177,7 +181,12 @@ lc_status hca_dense_attn(const void *Q, const void *Kc, const void *Vc, const vo
  *   - Each device that loads the library's image holds that array until the
  *     process exits.
  *   - The first call on a device looks the array's device address up (with
- *     that device current); make that first call before any stream capture.
+ *     that device current) and keeps it; make that first call before any
+ *     stream capture.  The address is not looked up again, so this entry
+ *     point must not be called after a cudaDeviceReset of that device in the
+ *     same process.
+ *   - LC_DEBUG_SYNC=1 makes it wait and report device errors like the
+ *     other calls.
  *   - Every call on a device shares the one array, so calls that overlap on
  *     the GPU (other streams, other host threads) race.  Nothing needs
  *     clearing between calls: each call writes every score it reads.
@@ -205,7 +214,24 @@ size_t lc_workspace_size(int32_t op, const lc_batch *batch, int32_t H, int32_t d
 const char *lc_status_string(int32_t status);
 int32_t lc_last_cuda_error(void);   /* cudaError_t of the last failed launch */
 uint64_t lc_launch_count(void);     /* kernels this library has launched so far */
+const char *lc_last_kernel(void);   /* name of the last kernel launched by this host
+                                       thread ("" before the first launch) */
 const char *lc_version(void);
+
+/* Test hook for the bounded device waits (the pages have no counterpart).
+ * While set, every launch of the tensor-core kernels named by `kernels`
+ * (a mask of lc_stall_kernel) starts with its MMA issuer waiting, for at most
+ * `clocks` SM clocks, on a barrier that nothing completes, before any copy is
+ * consumed or any MMA issued.  The wait gives up, the CTA abandons its work,
+ * frees its tensor memory and raises LC_DEVERR_TIMEOUT, so the call's output
+ * is not computed.  clocks <= 0 turns the hook off.  Host only; not for
+ * production use. */
+typedef enum {
+    LC_STALL_INDEX_TC = 1,   /* tensor-core Lightning Indexer */
+    LC_STALL_SPARSE_TC = 2,  /* tensor-core CSA attention */
+    LC_STALL_HCA_TC = 4      /* tensor-core HCA attention */
+} lc_stall_kernel;
+void lc_debug_stall(uint32_t kernels, int64_t clocks);
 
 #ifdef __cplusplus
 }

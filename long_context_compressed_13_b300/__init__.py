@@ -24,11 +24,14 @@ LC_OK, LC_ERR_INVALID_ARG, LC_ERR_UNSUPPORTED, LC_ERR_CUDA, LC_ERR_TIMEOUT = 0, 
 LC_ERR_DEVICE_CHECK, LC_ERR_WORKSPACE = 5, 6
 LC_F32, LC_BF16 = 0, 1
 LC_DEVERR_INDEX, LC_DEVERR_WINDOW, LC_DEVERR_BATCH, LC_DEVERR_TIMEOUT = 1, 2, 4, 8
+LC_DEVERR_SINK = 16
 LC_OP_LIGHTNING_INDEX, LC_OP_TOPK_SELECT, LC_OP_SPARSE_MQA_ATTN, LC_OP_HCA_DENSE_ATTN = 0, 1, 2, 3
 
 ENTRY_POINTS = ("csa_compress", "hca_compress", "lightning_index", "topk_select",
                 "sparse_mqa_attn", "hca_dense_attn", "lc_workspace_size", "lc_status_string",
-                "lc_last_cuda_error", "lc_launch_count", "lc_version")
+                "lc_last_cuda_error", "lc_launch_count", "lc_last_kernel", "lc_version",
+                "lc_debug_stall")
+LC_STALL_INDEX_TC, LC_STALL_SPARSE_TC, LC_STALL_HCA_TC = 1, 2, 4
 
 
 class LCError(RuntimeError):
@@ -80,6 +83,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lc_status_string.restype = ctypes.c_char_p
     lib.lc_last_cuda_error.restype = i32
     lib.lc_launch_count.restype = ctypes.c_uint64
+    lib.lc_last_kernel.restype = ctypes.c_char_p
+    lib.lc_debug_stall.argtypes = [ctypes.c_uint32, ctypes.c_int64]
+    lib.lc_debug_stall.restype = None
     lib.lc_version.restype = ctypes.c_char_p
     _lib = lib
     return lib
@@ -88,6 +94,18 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
 def launch_count() -> int:
     """Kernels the library has enqueued in this process."""
     return int(load_library().lc_launch_count())
+
+
+def last_kernel() -> str:
+    """Name of the last kernel the library launched from this thread."""
+    return load_library().lc_last_kernel().decode()
+
+
+def debug_stall(kernels: int, clocks: int) -> None:
+    """Test hook: the named tensor-core kernels (LC_STALL_* mask) start with a
+    bounded wait of `clocks` SM clocks on a barrier nothing completes, so
+    their waits run out; clocks <= 0 turns it off."""
+    load_library().lc_debug_stall(kernels, clocks)
 
 
 def _check(fn: str, status: int):
@@ -246,6 +264,18 @@ def topk_select(scores, batch: DeviceBatch, m: int, k: int, topk=None, dev_err=N
     return topk
 
 
+def _sink_ptr(sink, Q) -> int:
+    """Device pointer of the per-head sink logits [H] fp32 (0 for none)."""
+    if sink is None:
+        return 0
+    H = Q.shape[1]
+    if sink.numel() != H:
+        raise ValueError(f"sink must hold one fp32 logit per head ({H}), got {sink.numel()}")
+    if sink.device != Q.device:
+        raise ValueError(f"sink is on {sink.device}, Q on {Q.device}")
+    return _dev(sink, "sink", torch.float32)
+
+
 def sparse_mqa_attn(Q, Kc, Vc, topk, Kraw, Vraw, batch: DeviceBatch, m: int, W: int,
                     scale: float, O=None, lse: bool | torch.Tensor = True, dev_err=None,
                     stream=None, sink=None):
@@ -266,7 +296,7 @@ def sparse_mqa_attn(Q, Kc, Vc, topk, Kraw, Vraw, batch: DeviceBatch, m: int, W: 
                              _dev(topk, "topk", torch.int32), topk.shape[1],
                              _dev(Kraw, "Kraw", Q.dtype), _dev(Vraw, "Vraw", Q.dtype),
                              ctypes.byref(cb), H, d, m, W, float(scale),
-                             _dev(sink, "sink", torch.float32), _dtype_code(Q),
+                             _sink_ptr(sink, Q), _dtype_code(Q),
                              _dev(O, "O", Q.dtype), _dev(L, "lse", torch.float32), None, 0,
                              _dev(dev_err, "dev_err", torch.int32), _stream(stream))
     _check("sparse_mqa_attn", st)
@@ -292,7 +322,7 @@ def hca_dense_attn(Q, Kc, Vc, Kraw, Vraw, batch: DeviceBatch, m: int, W: int, sc
     st = lib.hca_dense_attn(_dev(Q, "Q"), _dev(Kc, "Kc", Q.dtype), _dev(Vc, "Vc", Q.dtype),
                             _dev(Kraw, "Kraw", Q.dtype), _dev(Vraw, "Vraw", Q.dtype),
                             ctypes.byref(cb), H, d, m, W, float(scale),
-                            _dev(sink, "sink", torch.float32), _dtype_code(Q),
+                            _sink_ptr(sink, Q), _dtype_code(Q),
                             _dev(O, "O", Q.dtype), _dev(L, "lse", torch.float32),
                             _dev(ws, "ws"), ws.numel() if ws is not None else 0,
                             _dev(dev_err, "dev_err", torch.int32), _stream(stream))

@@ -39,9 +39,20 @@ lc_status attn_simt_launch(bool sparse, const void *Q, const void *Kc, const voi
                            int32_t *dev_err, cudaStream_t st);
 
 static std::atomic<uint64_t> g_launches{0};
+static std::atomic<uint32_t> g_stall_mask{0};
+static std::atomic<long long> g_stall_clocks{0};
+
+long long debug_stall_clocks(uint32_t kernel_bit) {
+    return (g_stall_mask.load() & kernel_bit) ? g_stall_clocks.load() : 0;
+}
 static std::atomic<int32_t> g_last_cuda{0};
 
-void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+static thread_local const char *g_last_kernel = "";
+
+void note_launch(const char *name) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    g_last_kernel = name;
+}
 
 lc_status check_launch() {
     cudaError_t e = cudaGetLastError();
@@ -50,6 +61,11 @@ lc_status check_launch() {
         return LC_ERR_CUDA;
     }
     return LC_OK;
+}
+
+lc_status check_launch_error(cudaError_t e) {
+    g_last_cuda.store((int32_t)e);
+    return LC_ERR_CUDA;
 }
 
 static bool debug_sync() {
@@ -62,7 +78,7 @@ static bool debug_sync() {
 }
 
 // With LC_DEBUG_SYNC=1: wait for the call's kernels and surface device errors.
-static lc_status finish(lc_status s, cudaStream_t st, int32_t *dev_err) {
+lc_status finish(lc_status s, cudaStream_t st, int32_t *dev_err) {
     if (s != LC_OK || !debug_sync()) return s;
     cudaError_t e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) {
@@ -79,7 +95,7 @@ static lc_status finish(lc_status s, cudaStream_t st, int32_t *dev_err) {
     return LC_OK;
 }
 
-static bool batch_ok(const lc_batch *b) {
+bool batch_ok(const lc_batch *b) {
     return b && b->B >= 1 && b->cu_q && b->q_pos0 && b->cu_c && b->cu_raw && b->raw_pos0 &&
            b->total_q >= 0 && b->max_q >= 0 && b->max_c >= 0 && b->max_q <= b->total_q &&
            b->total_c >= b->max_c && b->total_raw >= 0;
@@ -250,6 +266,13 @@ const char *lc_status_string(int32_t status) {
 int32_t lc_last_cuda_error(void) { return g_last_cuda.load(); }
 
 uint64_t lc_launch_count(void) { return g_launches.load(); }
+
+const char *lc_last_kernel(void) { return g_last_kernel; }
+
+void lc_debug_stall(uint32_t kernels, int64_t clocks) {
+    g_stall_clocks.store(clocks > 0 ? (long long)clocks : 0);
+    g_stall_mask.store(clocks > 0 ? kernels : 0u);
+}
 
 const char *lc_version(void) { return "lcattn 0.1 sm_103a"; }
 

@@ -48,6 +48,7 @@ constexpr float H_RESCALE = 8.f;
 
 struct HBars {
     uint64_t q_full, k_full[2], v_full[2], kv_empty[2], s_full[2], p_full[2], o_done[2];
+    uint64_t stall;           // test hook: a barrier nothing completes
     uint32_t taddr;
     int abort;
 };
@@ -98,6 +99,8 @@ struct HcaArgs {
     __nv_bfloat16 *O;
     float *lse;
     int32_t *dev_err;
+    long long stall;      // test hook (0: off): the MMA issuer first waits this
+                          // many clocks on a barrier nothing completes
 };
 
 __global__ void __launch_bounds__(H_THREADS, 1)
@@ -131,6 +134,7 @@ __global__ void __launch_bounds__(H_THREADS, 1)
         bars.abort = (smem_u32(smem) & 1023u) != 0 ? 1 : 0;
         if (bars.abort) flag(a.dev_err, LC_DEVERR_TIMEOUT);  // layout assumption broken
         mbar_init(&bars.q_full, 1);
+        mbar_init(&bars.stall, 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars.k_full[s], 1);
             mbar_init(&bars.v_full[s], 1);
@@ -220,7 +224,8 @@ __global__ void __launch_bounds__(H_THREADS, 1)
                 }
                 mma_commit(&bars.o_done[g]);
             };
-            bool ok = mbar_wait(&bars.q_full, 0, abort) && mbar_wait(&bars.k_full[0], 0, abort);
+            bool ok = (a.stall == 0 || mbar_wait(&bars.stall, 0, abort, a.stall)) &&
+                      mbar_wait(&bars.q_full, 0, abort) && mbar_wait(&bars.k_full[0], 0, abort);
             if (ok) {
                 tc_fence_after();
                 issue_s(0, 0);
@@ -353,9 +358,8 @@ __global__ void __launch_bounds__(H_THREADS, 1)
             if (row_ok) flag(a.dev_err, LC_DEVERR_TIMEOUT);
         } else {
             tc_fence_after();
-            const float of = fold_sink(m_used, l, row_ok && a.sink
-                                                      ? __ldg(a.sink + row % a.H) * H_LOG2E
-                                                      : -INFINITY);
+            const float of = fold_sink(
+                m_used, l, row_ok ? sink_log2(a.sink, (int)(row % a.H), a.dev_err) : -INFINITY);
             const float inv = l > 0.f ? of / l : 0.f;
             uint4 *dst = reinterpret_cast<uint4 *>(a.O + row * HHD);
 #pragma unroll 1
@@ -435,6 +439,7 @@ lc_status hca_tc_launch(const void *Q, const void *Kc, const void *Vc, const voi
     a.O = reinterpret_cast<__nv_bfloat16 *>(O);
     a.lse = lse;
     a.dev_err = dev_err;
+    a.stall = debug_stall_clocks(LC_STALL_HCA_TC);
     static bool attr_done = false;
     if (!attr_done) {
         if (cudaFuncSetAttribute(k_hca_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,

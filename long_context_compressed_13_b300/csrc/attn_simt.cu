@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(AT) k_attn_simt(AttnArgs a, Batch bt) {
     if (tid < HG) {
         // the head's sink logit joins the denominator; sA takes the output factor
         float mm = sM[tid], ll = sL[tid];
-        sA[tid] = fold_sink(mm, ll, a.sink ? __ldg(a.sink + h0 + tid) * LOG2E : -INFINITY);
+        sA[tid] = fold_sink(mm, ll, sink_log2(a.sink, h0 + tid, a.dev_err));
         sM[tid] = mm;
         sL[tid] = ll;
     }
@@ -203,7 +203,7 @@ static lc_status launch_hg(const AttnArgs &a, const lc_batch &b, cudaStream_t st
         cudaSuccess)
         return LC_ERR_CUDA;
     dim3 grid((unsigned)b.total_q, (unsigned)(a.H / HG));
-    LC_LAUNCH(kfn, grid, dim3(AT), smem, st, a, to_dev(b));
+    LC_LAUNCH_AS("k_attn_simt", kfn, grid, dim3(AT), smem, st, a, to_dev(b));
     return check_launch();
 }
 

@@ -53,6 +53,7 @@ constexpr float S_RESCALE = 8.f;
 struct SBars {
     uint64_t q_full, k_full[S_NST], v_full[S_NST], kv_empty[S_NST], mask_full[S_NST];
     uint64_t s_full[2], p_full, o_done;
+    uint64_t stall;           // test hook: a barrier nothing completes
     uint32_t mask[S_NST][4];  // valid slots of the selected tile held by each stage
     uint32_t taddr;
     int abort;
@@ -113,6 +114,8 @@ struct SparseArgs {
     __nv_bfloat16 *O;
     float *lse;
     int32_t *dev_err;
+    long long stall;      // test hook (0: off): the MMA issuer first waits this
+                          // many clocks on a barrier nothing completes
 };
 
 __global__ void __launch_bounds__(S_THREADS, 1)
@@ -146,6 +149,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
         bars.abort = (smem_u32(smem) & 1023u) != 0 ? 1 : 0;
         if (bars.abort) flag(a.dev_err, LC_DEVERR_TIMEOUT);  // layout assumption broken
         mbar_init(&bars.q_full, 1);
+        mbar_init(&bars.stall, 1);
         for (int s = 0; s < S_NST; ++s) {
             mbar_init(&bars.k_full[s], NPROD);  // one arrival per producer thread
             mbar_init(&bars.v_full[s], NPROD);
@@ -281,7 +285,8 @@ __global__ void __launch_bounds__(S_THREADS, 1)
                 mma_commit(&bars.s_full[j & 1]);
                 return true;
             };
-            bool ok = mbar_wait(&bars.q_full, 0, abort) && issue_s(0) &&
+            bool ok = (a.stall == 0 || mbar_wait(&bars.stall, 0, abort, a.stall)) &&
+                      mbar_wait(&bars.q_full, 0, abort) && issue_s(0) &&
                       (n_tiles < 2 || issue_s(1));
             for (int j = 0; ok && j < n_tiles; ++j) {
                 const int s = j % S_NST;
@@ -433,8 +438,8 @@ __global__ void __launch_bounds__(S_THREADS, 1)
             if (row_ok) flag(a.dev_err, LC_DEVERR_TIMEOUT);
         } else {
             tc_fence_after();
-            const float of = fold_sink(m_used, l, row_ok && a.sink ? __ldg(a.sink + tid) * S_LOG2E
-                                                                   : -INFINITY);
+            const float of =
+                fold_sink(m_used, l, row_ok ? sink_log2(a.sink, tid, a.dev_err) : -INFINITY);
             const float inv = l > 0.f ? of / l : 0.f;
             uint4 *dst = reinterpret_cast<uint4 *>(a.O + row * SHD);
 #pragma unroll 1
@@ -508,6 +513,7 @@ lc_status sparse_tc_launch(const void *Q, const void *Kc, const void *Vc, const 
     a.O = reinterpret_cast<__nv_bfloat16 *>(O);
     a.lse = lse;
     a.dev_err = dev_err;
+    a.stall = debug_stall_clocks(LC_STALL_SPARSE_TC);
     static bool attr_done = false;
     if (!attr_done) {
         if (cudaFuncSetAttribute(k_sparse_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,

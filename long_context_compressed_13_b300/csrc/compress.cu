@@ -117,7 +117,7 @@ static lc_status launch(const void *K, const void *V, const float *GK, const flo
     if (Tc == 0) return LC_OK;
     if (m >= 32 && d % 32 == 0 && Tc * (d / 32) < (1ll << 31)) {
         auto kl = k_compress_long<T>;
-        LC_LAUNCH(kl, dim3((unsigned)(Tc * (d / 32)), 2), dim3(256), 0, st, (const T *)K,
+        LC_LAUNCH_AS("k_compress_long", kl, dim3((unsigned)(Tc * (d / 32)), 2), dim3(256), 0, st, (const T *)K,
                   (const T *)V, GK, GV, Tc, d, m, (T *)Kc, (T *)Vc);
         return check_launch();
     }
@@ -130,7 +130,7 @@ static lc_status launch(const void *K, const void *V, const float *GK, const flo
     int64_t blocks = (Tc * d + 255) / 256;
     if (blocks > 148 * 4) blocks = 148 * 4;
     auto kfn = k_compress<T>;
-    LC_LAUNCH(kfn, dim3((unsigned)blocks, 2), dim3(256), smem, st, (const T *)K, (const T *)V,
+    LC_LAUNCH_AS("k_compress", kfn, dim3((unsigned)blocks, 2), dim3(256), smem, st, (const T *)K, (const T *)V,
               GK, GV, Tc, d, m, (T *)Kc, (T *)Vc);
     return check_launch();
 }

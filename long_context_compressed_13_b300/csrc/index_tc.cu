@@ -82,6 +82,7 @@ struct IdxBars {
     // releases of each score buffer: every epilogue warp arrives once its
     // reads of a use of the buffer are complete
     uint64_t freed[NBUF];
+    uint64_t stall;           // test hook: a barrier nothing completes
     uint32_t taddr;
     int abort;
 };
@@ -130,6 +131,8 @@ struct IdxTcArgs {
     int gy, cloc;
     int cap;
     int32_t *dev_err;
+    long long stall;         // test hook (0: off): both MMA issuers first wait this
+                             // many clocks on a barrier nothing completes
 };
 
 template <int MODE, int HI>
@@ -160,6 +163,7 @@ __global__ void __launch_bounds__(I_THREADS, 1)
         bars.abort = (smem_u32(smem) & 1023u) != 0 ? 1 : 0;
         if (bars.abort) flag(a.dev_err, LC_DEVERR_TIMEOUT);
         mbar_init(&bars.q_full, 1);
+        mbar_init(&bars.stall, 1);
         for (int s = 0; s < NSB; ++s) {
             mbar_init(&bars.k_full[s], 1);
             mbar_init(&bars.k_empty[s], 1);
@@ -211,7 +215,8 @@ __global__ void __launch_bounds__(I_THREADS, 1)
         const int par = warp - W_MMA;  // head boxes g with g % 2 == par
         if (lane == 0 && !dead && n_t > 0) {
             constexpr uint32_t IDESC = idesc_bf16_f32(IBM, IBN, 0, 0);
-            bool ok = mbar_wait(&bars.q_full, 0, abort);
+            bool ok = (a.stall == 0 || mbar_wait(&bars.stall, 0, abort, a.stall)) &&
+                      mbar_wait(&bars.q_full, 0, abort);
             tc_fence_after();
             const uint32_t q_base = smem_u32(smem + C::SM_Q);
             for (int g = par; ok && g < n_all; g += 2) {
@@ -684,7 +689,7 @@ lc_status launch_tc(const CUtensorMap &mQ, const CUtensorMap &mK, const IdxTcArg
     const int64_t gy = (n_cols + a.chunk - 1) / a.chunk;
     if (gy < 1 || gy > 65535) return LC_ERR_UNSUPPORTED;
     dim3 grid((unsigned)((a.Nq + IBM - 1) / IBM), (unsigned)gy);
-    LC_LAUNCH(kfn, grid, dim3(I_THREADS), SMEM, st, mQ, mK, a);
+    LC_LAUNCH_AS(MODE == MODE_FILTER ? "k_index_tc<filter>" : "k_index_tc<materialize>", kfn, grid, dim3(I_THREADS), SMEM, st, mQ, mK, a);
     return check_launch();
 }
 
@@ -720,6 +725,7 @@ IdxTcArgs base_args(const lc_batch &b, const void *qI, const float *w, int m,
     a.m = m;
     a.w = w;
     a.dev_err = dev_err;
+    a.stall = debug_stall_clocks(LC_STALL_INDEX_TC);
     return a;
 }
 }  // namespace

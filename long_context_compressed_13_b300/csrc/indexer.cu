@@ -275,10 +275,10 @@ static lc_status launch_stream(const void *qI, const float *w, const void *kI, c
     if (gx > 65535) return LC_ERR_UNSUPPORTED;
     const dim3 grid((unsigned)gx, (unsigned)b.total_q);
     if (HI == 8)
-        LC_LAUNCH(k_index_stream<8>, grid, dim3(256), 0, st, (const __nv_bfloat16 *)qI, w,
+        LC_LAUNCH_AS("k_index_stream", k_index_stream<8>, grid, dim3(256), 0, st, (const __nv_bfloat16 *)qI, w,
                   (const __nv_bfloat16 *)kI, to_dev(b), m, scores, ld, chunk, row_mask, dev_err);
     else
-        LC_LAUNCH(k_index_stream<4>, grid, dim3(256), 0, st, (const __nv_bfloat16 *)qI, w,
+        LC_LAUNCH_AS("k_index_stream", k_index_stream<4>, grid, dim3(256), 0, st, (const __nv_bfloat16 *)qI, w,
                   (const __nv_bfloat16 *)kI, to_dev(b), m, scores, ld, chunk, row_mask, dev_err);
     return check_launch();
 }
@@ -294,7 +294,7 @@ static void launch_scan(const void *qI, const float *w, const void *kI, const lc
     if (gx > want) gx = want;
     if (gx < 1) gx = 1;
     auto kfn = k_index_scan<T, DI, HI>;
-    LC_LAUNCH(kfn, dim3((unsigned)gx, (unsigned)rows), dim3(256), 0, st, (const T *)qI, w,
+    LC_LAUNCH_AS("k_index_scan", kfn, dim3((unsigned)gx, (unsigned)rows), dim3(256), 0, st, (const T *)qI, w,
               (const T *)kI, to_dev(b), m, scores, ld, b.total_q, row_mask, dev_err);
 }
 
@@ -349,7 +349,7 @@ static lc_status launch_index(const void *qI, const float *w, const void *kI, co
     dim3 grid((unsigned)((b.max_q + TQ - 1) / TQ), (unsigned)b.B, (unsigned)((ld + TE - 1) / TE));
     if ((ld + TE - 1) / TE > 65535) return LC_ERR_UNSUPPORTED;
     auto kfn = k_index_tiled<T>;
-    LC_LAUNCH(kfn, grid, dim3(256), smem, st, (const T *)qI, w, (const T *)kI, to_dev(b), HI, dI,
+    LC_LAUNCH_AS("k_index_tiled", kfn, grid, dim3(256), smem, st, (const T *)qI, w, (const T *)kI, to_dev(b), HI, dI,
               m, scores, ld, dev_err);
     return check_launch();
 }

@@ -10,16 +10,24 @@
 namespace lc {
 
 // ---------------------------------------------------------------- launches
-// Every kernel launch goes through LC_LAUNCH so the library can report how
-// many kernels it enqueued.
-void note_launch();
+// Every kernel launch goes through LC_LAUNCH (or LC_LAUNCH_AS, which names a
+// kernel reached through a function-pointer variable) so the library can
+// report how many kernels it enqueued and which one it enqueued last.
+void note_launch(const char *name);
 lc_status check_launch();
+lc_status check_launch_error(cudaError_t e);  // records e, returns LC_ERR_CUDA
 
-#define LC_LAUNCH(kernel, grid, block, smem, stream, ...)                         \
+#define LC_LAUNCH_AS(name, kernel, grid, block, smem, stream, ...)                \
     do {                                                                          \
         kernel<<<(grid), (block), (smem), (cudaStream_t)(stream)>>>(__VA_ARGS__); \
-        ::lc::note_launch();                                                      \
+        ::lc::note_launch(name);                                                  \
     } while (0)
+#define LC_LAUNCH(kernel, grid, block, smem, stream, ...) \
+    LC_LAUNCH_AS(#kernel, kernel, grid, block, smem, stream, __VA_ARGS__)
+
+// Test hook (lc_debug_stall): clocks the MMA issuer of the named tensor-core
+// kernel waits at its start on a barrier nothing completes (0 = off).
+long long debug_stall_clocks(uint32_t kernel_bit);
 
 // ---------------------------------------------------------------- dtypes
 template <typename T> struct io;
@@ -74,9 +82,22 @@ __device__ __forceinline__ uint32_t order_key(float s) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Folds a per-head attention-sink logit sk2 (log2 units; -inf or NaN: none)
-// into a softmax row's running max m and sum l (log2 units, l = 0 when the row
-// had no key): the sink is one more logit of the denominator with no value.
+// The sink logit of head h in log2 units, -inf for no sink (sink NULL or
+// -inf).  A NaN or +inf sink is not a usable logit: it is flagged as
+// LC_DEVERR_SINK and the head is treated as having no sink.
+__device__ __forceinline__ float sink_log2(const float *sink, int h, int32_t *dev_err) {
+    if (!sink) return -INFINITY;
+    const float s = __ldg(sink + h);
+    if (!(s < INFINITY)) {  // NaN or +inf
+        flag(dev_err, LC_DEVERR_SINK);
+        return -INFINITY;
+    }
+    return s * 1.4426950408889634f;
+}
+
+// Folds a per-head attention-sink logit sk2 (log2 units; -inf: none) into a
+// softmax row's running max m and sum l (log2 units, l = 0 when the row had
+// no key): the sink is one more logit of the denominator with no value.
 // Returns the factor that rescales the row's unnormalised output.
 __device__ __forceinline__ float fold_sink(float &m, float &l, float sk2) {
     if (!(sk2 > -INFINITY)) return 1.f;

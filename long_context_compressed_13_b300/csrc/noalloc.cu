@@ -23,6 +23,8 @@ lc_status index_launch(const void *qI, const float *w, const void *kI, const lc_
                        cudaStream_t st);
 lc_status topk_launch(const float *scores, int64_t ld, const lc_batch &b, int m, int k,
                       int32_t *topk, int32_t *dev_err, cudaStream_t st);
+lc_status finish(lc_status s, cudaStream_t st, int32_t *dev_err);
+bool batch_ok(const lc_batch *b);
 
 namespace {
 
@@ -38,7 +40,8 @@ float *g_dev_ptr[kMaxDevices];
 std::mutex g_mu;
 
 // Device address of g_scores on the current device (looked up on the first
-// call on each device, with that device current).
+// call on each device, with that device current, and kept for the life of the
+// process: a cudaDeviceReset of that device would leave it stale).
 lc_status scratch_on_current_device(float **out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
@@ -65,10 +68,7 @@ extern "C" lc_status lightning_index_topk_noalloc(const void *qI, const float *w
                                                   lc_stream stream) {
     using namespace lc;
     cudaStream_t st = (cudaStream_t)stream;
-    if (!qI || !w || !kI || !topk || !batch || batch->B < 1 || !batch->cu_q ||
-        !batch->q_pos0 || !batch->cu_c || !batch->cu_raw || !batch->raw_pos0 ||
-        batch->total_q < 0 || batch->max_q < 0 || batch->max_c < 0 ||
-        batch->max_q > batch->total_q || m < 1 || k < 1 ||
+    if (!qI || !w || !kI || !topk || !batch_ok(batch) || m < 1 || k < 1 ||
         (dtype != LC_F32 && dtype != LC_BF16) || (reinterpret_cast<uintptr_t>(kI) & 15u) != 0)
         return LC_ERR_INVALID_ARG;
     if ((HI != 1 && HI != 2 && HI != 4 && HI != 8) || (dI != 32 && dI != 64) || k > 4096)
@@ -83,5 +83,5 @@ extern "C" lc_status lightning_index_topk_noalloc(const void *qI, const float *w
     const int64_t ld = batch->max_c;
     if (ld > 0) s = index_launch(qI, w, kI, *batch, HI, dI, m, dtype, scores, ld, dev_err, st);
     if (s == LC_OK) s = topk_launch(scores, ld, *batch, m, k, topk, dev_err, st);
-    return s;
+    return finish(s, st, dev_err);
 }

@@ -135,6 +135,9 @@ def _sink(sink, H):
         return None, ctypes.cast(None, ctypes.POINTER(ctypes.c_double))
     s = _f64(sink).reshape(-1)
     assert s.shape == (H,)
+    # a sink logit is a real number or -inf (no sink for that head)
+    if np.any(np.isnan(s) | (s == np.inf)):
+        raise ValueError("sink logits must be finite or -inf")
     return s, _p(s, ctypes.c_double)
 
 

@@ -26,7 +26,7 @@ def _declared_functions():
             continue
         text = open(os.path.join(ROOT, "include", hdr)).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-        for m in re.finditer(r"^\s*(?:lc_status|size_t|const char\s*\*|int32_t|uint64_t)\s*"
+        for m in re.finditer(r"^\s*(?:lc_status|size_t|const char\s*\*|int32_t|uint64_t|void)\s*"
                              r"\*?\s*([A-Za-z_]\w*)\s*\(", text, flags=re.M):
             names.append(m.group(1))
     return names

@@ -11,6 +11,9 @@ benchmark times, on sampled outputs the oracle computes one by one.
   tolerance; sampled compressed entries of the chunk within one bf16 ulp.
 - csa_decode: 64 sequences with contexts ~U[65536, 262144]; every sequence
   is checked the same way.
+- csa_prefill (T=32768, 64 heads, k=512) and hca_prefill (T=131072, 64
+  heads, m'=128): the benchmark's steps, 256+ sampled rows each, checked
+  the same way.
 
 The oracle builds its own compressed caches from the raw inputs (rounded to
 bf16, the stored type) and never reads a value the CUDA path produced.
@@ -122,3 +125,74 @@ def test_csa_decode_sampled(lc):
                                     D["Vraw"][r0:r1].cpu(), bt.raw_pos0[s], t, wk.W, D["scale"])
         np.testing.assert_allclose(gO_all[s:s + 1], rO, rtol=0, atol=TOL)
         np.testing.assert_allclose(gl_all[s:s + 1], rl, rtol=0, atol=TOL)
+
+
+def _sample_rows(T, n, rng, fixed):
+    fixed = np.array(sorted(set(int(x) for x in fixed if 0 <= x < T)), dtype=np.int64)
+    rest = np.setdiff1d(np.arange(T), fixed)
+    return np.unique(np.concatenate([fixed, rng.choice(rest, n, replace=False)]))
+
+
+def _check_entries(name, gpu, ref, rng):
+    ents = np.unique(np.concatenate([[0, ref.shape[0] - 1], rng.integers(0, ref.shape[0], 64)]))
+    got = gpu[torch.from_numpy(ents).cuda()].double().cpu().numpy()
+    ulp = np.abs(ref[ents]) * 2.0 ** -7 + 1e-30
+    assert np.all(np.abs(got - ref[ents]) <= ulp), name
+
+
+def test_csa_prefill_32k_sampled(lc):
+    """CSA prefill, T = 32,768, 64 heads x 128, indexer 8 x 64 over 8192
+    entries, top-k 512, window 128: the benchmark's step, 256+ sampled rows."""
+    import bench
+    wk = bench.CsaPrefill(lc, "cuda")
+    wk.step()
+    torch.cuda.synchronize()
+    assert int(wk.err.item()) == 0
+    L = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in wk.L.items()}
+    rng = np.random.default_rng(21)
+    Kc = _bf16_round(oracle.compress(L["K"], L["G"], wk.m))
+    Vc = _bf16_round(oracle.compress(L["V"], L["G"], wk.m))
+    _check_entries("Kc", wk.Kc, Kc, rng)
+    _check_entries("Vc", wk.Vc, Vc, rng)
+    # the first rows (no entry visible), rows around the first entries and the
+    # point where n_vis passes k, tile edges of the indexer, the last rows
+    fixed = [0, 1, 2, 3, 4, 127, 128, 2047, 2048, 2051, 4095, 4096, 16383, 16384, 32766, 32767]
+    rows = _sample_rows(wk.T, 256, rng, fixed)
+    t = rows.astype(np.int64)
+    I = oracle.index(L["qI"][rows], L["w"][rows], L["kI"], t, wk.m)
+    gsel = wk.sel[torch.from_numpy(rows).cuda()].cpu().numpy()
+    rsel, same = _check_rows(gsel, I, (t + 1) // wk.m, wk.k)
+    assert same.mean() >= 0.95
+    rO, rl = oracle.sparse_attn(L["Q"][rows], Kc, Vc, rsel, L["K"], L["V"], 0, t, wk.W,
+                                L["scale"])
+    gO = wk.O[torch.from_numpy(rows).cuda()].double().cpu().numpy()
+    gl = wk.lse[torch.from_numpy(rows).cuda()].double().cpu().numpy()
+    np.testing.assert_allclose(gO[same], rO[same], rtol=0, atol=TOL)
+    np.testing.assert_allclose(gl[same], rl[same], rtol=0, atol=TOL)
+
+
+def test_hca_prefill_128k_sampled(lc):
+    """HCA prefill, T = 131,072, 64 heads x 128, m' = 128 (1024 entries),
+    window 128: the benchmark's step, 256+ sampled rows."""
+    import bench
+    wk = bench.HcaPrefill(lc, "cuda")
+    wk.step()
+    torch.cuda.synchronize()
+    assert int(wk.err.item()) == 0
+    L = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in wk.L.items()}
+    rng = np.random.default_rng(22)
+    Kc = _bf16_round(oracle.compress(L["K"], L["G"], wk.m))
+    Vc = _bf16_round(oracle.compress(L["V"], L["G"], wk.m))
+    _check_entries("Kc", wk.Kc, Kc, rng)
+    _check_entries("Vc", wk.Vc, Vc, rng)
+    # rows before the first entry, around entry boundaries, CTA edges (4
+    # tokens of 64 heads per CTA) and the last rows
+    fixed = [0, 1, 3, 4, 126, 127, 128, 255, 256, 257, 16383, 16384, 65535, 65536,
+             131068, 131071]
+    rows = _sample_rows(wk.T, 256, rng, fixed)
+    rO, rl = oracle.hca_attn(L["Q"][rows], Kc, Vc, wk.m, L["K"], L["V"], 0,
+                             rows.astype(np.int64), wk.W, L["scale"])
+    gO = wk.O[torch.from_numpy(rows).cuda()].double().cpu().numpy()
+    gl = wk.lse[torch.from_numpy(rows).cuda()].double().cpu().numpy()
+    np.testing.assert_allclose(gO, rO, rtol=0, atol=TOL)
+    np.testing.assert_allclose(gl, rl, rtol=0, atol=TOL)

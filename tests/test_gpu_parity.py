@@ -173,9 +173,16 @@ def _score_rows(kind, Nq, ld, seed):
 
 
 @pytest.mark.parametrize("kind", ["normal", "ties", "zeros", "wide"])
-@pytest.mark.parametrize("k,m,ld,Nq,t0", [(1, 4, 300, 64, 900), (32, 4, 512, 200, 0),
-                                          (512, 4, 8192, 48, 20000), (1024, 4, 3000, 40, 9000),
-                                          (4096, 1, 6000, 8, 5990), (7, 128, 40, 30, 4000)])
+@pytest.mark.parametrize("k,m,ld,Nq,t0", [
+    (1, 4, 300, 64, 900), (32, 4, 512, 200, 0), (512, 4, 8192, 48, 20000),
+    (1024, 4, 3000, 40, 9000), (4096, 1, 6000, 8, 5990), (7, 128, 40, 30, 4000),
+    # at most 296 rows of 4096+ entries: one 8-CTA cluster per row
+    (1024, 4, 65536, 64, 200000),   # ~50000 visible entries, slices staged in shared memory
+    (2048, 4, 9000, 100, 30000),    # slices of ~940 entries
+    (4096, 4, 20000, 20, 70000),
+    (64, 1, 140000, 16, 139990),    # slices of 17500 > 16384 entries: read from global memory
+    (4090, 1, 4100, 24, 4080),      # rows of 4081..4100 entries, some with n_vis <= k
+])
 def test_topk_bit_exact(lc, kind, k, m, ld, Nq, t0):
     S = _score_rows(kind, Nq, ld, seed=k + ld)
     nvis = np.minimum((np.arange(t0, t0 + Nq) + 1) // m, ld)
@@ -295,12 +302,59 @@ def test_attention_sink(lc, kind, dtype, H, d, W, T):
         rO, rl = oracle.hca_attn(L["Q"], Kc, Vc, m, L["K"], L["V"], 0, tpos, W, L["scale"],
                                  sink=sink)
     torch.cuda.synchronize()
+    # the path that ran: tensor cores for bf16 with d = 128, SIMT otherwise
+    want = ("k_sparse_tc" if kind == "sparse" else "k_hca_tc") if dtype == "bf16" else "k_attn_simt"
+    assert lc.last_kernel() == want
     tol = TOL_ATTN[dtype]
     np.testing.assert_allclose(f64(O), rO, rtol=0, atol=tol)
     g, fin = f64(lse), np.isfinite(rl)
     assert np.array_equal(np.isneginf(g), np.isneginf(rl))
     np.testing.assert_allclose(g[fin], rl[fin], rtol=0, atol=tol)
     assert np.abs(f64(O)[:, 1]).max() < 1e-6  # the dominant sink leaves almost nothing
+
+
+@pytest.mark.parametrize("kind,dtype,H,d", [("sparse", "bf16", 64, 128), ("hca", "bf16", 64, 128),
+                                            ("sparse", "f32", 8, 64)])
+def test_unusable_sink_is_flagged(lc, kind, dtype, H, d):
+    """A NaN or +inf sink logit is flagged (LC_DEVERR_SINK) and that head is
+    computed without a sink; the other heads keep theirs.  A sink tensor of
+    the wrong length is refused by the binding."""
+    T, W, m = 600, 64, 4
+    sink = _sinks(H, 6)
+    sink[2] = np.nan
+    sink[3] = np.inf
+    clean = sink.copy()
+    clean[2] = clean[3] = -np.inf
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if kind == "sparse":
+        L, Kc, Vc = _attn_case(dtype, H, d, m, 32, W, T, seed=44)
+        tpos = np.array(L["batch"].positions())
+        sel = oracle.topk(np.random.default_rng(5).standard_normal((len(tpos), T // m)),
+                          (tpos + 1) // m, 32)
+        b = lc.DeviceBatch.from_workload(L["batch"])
+        args = (dev(L["Q"]), dev(Kc), dev(Vc), dev(torch.from_numpy(sel)), dev(L["K"]),
+                dev(L["V"]), b, m, W, L["scale"])
+        O, lse = lc.sparse_mqa_attn(*args, sink=dev(torch.from_numpy(sink)), dev_err=err)
+        rO, rl = oracle.sparse_attn(L["Q"], Kc, Vc, sel, L["K"], L["V"], 0, tpos, W, L["scale"],
+                                    sink=clean)
+        with pytest.raises(ValueError, match="one fp32 logit per head"):
+            lc.sparse_mqa_attn(*args, sink=dev(torch.zeros(H - 1)))
+    else:
+        L = wl.hca_layer(T=T, H=H, d=d, m=m, W=W, dtype=dtype, seed=45)
+        Kc = cast(oracle.compress(L["K"], L["G"], m), dtype)
+        Vc = cast(oracle.compress(L["V"], L["G"], m), dtype)
+        tpos = np.array(L["batch"].positions())
+        b = lc.DeviceBatch.from_workload(L["batch"])
+        O, lse = lc.hca_dense_attn(dev(L["Q"]), dev(Kc), dev(Vc), dev(L["K"]), dev(L["V"]), b,
+                                   m, W, L["scale"], sink=dev(torch.from_numpy(sink)), dev_err=err)
+        rO, rl = oracle.hca_attn(L["Q"], Kc, Vc, m, L["K"], L["V"], 0, tpos, W, L["scale"],
+                                 sink=clean)
+    torch.cuda.synchronize()
+    assert int(err.item()) == lc.LC_DEVERR_SINK
+    tol = TOL_ATTN[dtype]
+    np.testing.assert_allclose(f64(O), rO, rtol=0, atol=tol)
+    fin = np.isfinite(rl)
+    np.testing.assert_allclose(f64(lse)[fin], rl[fin], rtol=0, atol=tol)
 
 
 # -------------------------------------------------------------- end to end

@@ -371,3 +371,14 @@ def test_sink_rescales_the_sinkless_result():
     o, l = oracle.sparse_attn(Q[:1], Kc, Vc, np.array([[-1, -1]]), Kc[:0], Vc[:0], 0, [11], 0,
                               0.7, sink=sink)
     assert np.all(o == 0) and np.array_equal(l[0], sink)
+
+
+def test_sink_must_be_a_real_logit_or_minus_inf():
+    # NaN and +inf are not logits: the oracle refuses them (the library flags
+    # them on the device and treats that head as having no sink)
+    rng = np.random.default_rng(9)
+    Q = rng.standard_normal((1, 2, 8))
+    Kc, Vc = rng.standard_normal((4, 8)), rng.standard_normal((4, 8))
+    for bad in (np.nan, np.inf):
+        with pytest.raises(ValueError, match="finite or -inf"):
+            oracle.hca_attn(Q, Kc, Vc, 1, Kc, Vc, 0, [3], 0, 0.5, sink=np.array([0.0, bad]))
