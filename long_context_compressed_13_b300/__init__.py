@@ -113,7 +113,8 @@ def _check(fn: str, status: int):
         lib = load_library()
         msg = lib.lc_status_string(status).decode()
         if status == LC_ERR_CUDA:
-            msg += f" (cudaError {lib.lc_last_cuda_error()})"
+            msg += (f" (cudaError {lib.lc_last_cuda_error()}; last kernel launched: "
+                    f"{lib.lc_last_kernel().decode() or 'none'})")
         raise LCError(fn, status, msg)
 
 

@@ -142,7 +142,6 @@ __global__ void __launch_bounds__(I_THREADS, 1)
     using C = IdxCfg;
     extern __shared__ __align__(1024) uint8_t smem[];
     IdxBars &bars = *reinterpret_cast<IdxBars *>(smem + C::SM_BAR);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int *abort = &bars.abort;
     const unsigned FULL = 0xffffffffu;
 
@@ -158,6 +157,25 @@ __global__ void __launch_bounds__(I_THREADS, 1)
     const int64_t comp_end = min(c_end, nvm);  // computed columns [c0, comp_end)
     const int n_t = comp_end > c0 ? (int)((comp_end - c0 + IBN - 1) / IBN) : 0;
     const int n_all = n_t * HI;  // head boxes / score buffers of this CTA
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (n_t == 0) {
+        // Nothing to compute (every column of the CTA is past its rows' visible
+        // entries): write what the CTA owes and leave before any mbarrier or
+        // tcgen05 instruction, so that every CTA that runs one holds tensor
+        // memory.  MATERIALIZE: columns [c0, c_end) of the rows are -inf.
+        // FILTER: the rows have no candidate in this CTA column.
+        if (MODE == MODE_MATERIALIZE) {
+            for (int r = warp; r < IBM && row0 + r < a.Nq; r += I_THREADS / 32) {
+                float *dst = a.out + (row0 + r) * a.ld;
+                for (int64_t e = c0 + lane; e < c_end; e += 32) dst[e] = -INFINITY;
+            }
+        } else {
+            for (int r = tid; r < IBM; r += I_THREADS)
+                if (row0 + r < a.Nq) a.lcnt[(size_t)(row0 + r) * a.gy + blockIdx.y] = 0;
+        }
+        return;
+    }
 
     if (tid == 0) {
         bars.abort = (smem_u32(smem) & 1023u) != 0 ? 1 : 0;
@@ -177,7 +195,7 @@ __global__ void __launch_bounds__(I_THREADS, 1)
     int *lcount = reinterpret_cast<int *>(smem + C::SM_LCNT);  // FILTER: slots used per row
     for (int i = tid; i < IBM; i += I_THREADS) lcount[i] = 0;
     constexpr int W_PROD = NEPI / 32, W_MMA = NEPI / 32 + 1, W_MMA2 = NEPI / 32 + 2;
-    if (warp == W_MMA && n_t > 0) {
+    if (warp == W_MMA) {
         tmem_alloc(&bars.taddr, I_TMEM_COLS);
         tmem_relinquish();
     }
@@ -189,7 +207,7 @@ __global__ void __launch_bounds__(I_THREADS, 1)
 
     if (warp == W_PROD) {
         // ------------------------------------------------------ TMA producer
-        if (lane == 0 && !dead && n_t > 0) {
+        if (lane == 0 && !dead) {
             prefetch_tmap(&mK);
             mbar_expect_tx(&bars.q_full, HI * C::Q_BOX);
 #pragma unroll
@@ -209,11 +227,16 @@ __global__ void __launch_bounds__(I_THREADS, 1)
             for (int g = max(0, issued - NSB); g < issued; ++g)
                 mbar_wait(&bars.k_full[g % NSB], (g / NSB) & 1, &dummy, 400000000LL);
             mbar_wait(&bars.q_full, 0, &dummy, 400000000LL);
+            // the MMAs' releases of the last boxes: no commit may still be on its
+            // way to this CTA's barriers when it exits (skipped after an abort,
+            // when some of those MMAs are never issued)
+            for (int g = max(0, issued - NSB); g < issued && !*abort; ++g)
+                mbar_wait(&bars.k_empty[g % NSB], (g / NSB) & 1, abort);
         }
     } else if (warp == W_MMA || warp == W_MMA2) {
         // ------------------------------------------------------ MMA issuers
         const int par = warp - W_MMA;  // head boxes g with g % 2 == par
-        if (lane == 0 && !dead && n_t > 0) {
+        if (lane == 0 && !dead) {
             constexpr uint32_t IDESC = idesc_bf16_f32(IBM, IBN, 0, 0);
             bool ok = (a.stall == 0 || mbar_wait(&bars.stall, 0, abort, a.stall)) &&
                       mbar_wait(&bars.q_full, 0, abort);
@@ -373,7 +396,7 @@ __global__ void __launch_bounds__(I_THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == W_MMA && n_t > 0) {
+    if (warp == W_MMA) {
         tc_fence_after();
         tmem_dealloc(taddr, I_TMEM_COLS);
     }
@@ -460,7 +483,7 @@ __global__ void __launch_bounds__(512) k_cand_pick(Batch bt, int m, int k, int c
                                                    const int32_t *__restrict__ lcnt,
                                                    const uint2 *__restrict__ priv, int gy,
                                                    int cloc, int32_t *__restrict__ topk,
-                                                   int32_t *fail) {
+                                                   int32_t *fail, int32_t *dev_err) {
     constexpr int NT = 512, NW = NT / 32;
     const unsigned FULL = 0xffffffffu;
     extern __shared__ uint32_t sbuf[];
@@ -512,8 +535,12 @@ __global__ void __launch_bounds__(512) k_cand_pick(Batch bt, int m, int k, int c
         const uint2 *src = priv + ((size_t)r * gy + y) * cloc;
         for (int i = lane; i < c; i += 32) {
             const uint2 ki = src[i];
-            keys[b + i] = ki.x;
-            idx[b + i] = ki.y;
+            if (b + i < cap) {
+                keys[b + i] = ki.x;
+                idx[b + i] = ki.y;
+            } else {
+                flag(dev_err, LC_DEVERR_BATCH);  // counts inconsistent: never expected
+            }
         }
     }
     for (int i = threadIdx.x; i < n_over; i += NT) {
@@ -566,7 +593,10 @@ __global__ void __launch_bounds__(512) k_cand_pick(Batch bt, int m, int k, int c
     __syncthreads();
     for (int i = threadIdx.x; i < k; i += NT) {
         const uint32_t e = sel[i];
-        atomicOr(&bm[e >> 5], 1u << (e & 31u));
+        if (e < (uint32_t)nv)
+            atomicOr(&bm[e >> 5], 1u << (e & 31u));
+        else
+            flag(dev_err, LC_DEVERR_BATCH);  // a chosen index outside the row: never expected
     }
     __syncthreads();
     // warp w owns words [wb, we); its lanes take consecutive words
@@ -593,7 +623,8 @@ __global__ void __launch_bounds__(512) k_cand_pick(Batch bt, int m, int k, int c
         while (x) {
             const int b = __ffs(x) - 1;
             x &= x - 1;
-            out[pos++] = w * 32 + b;
+            if (pos < k) out[pos] = w * 32 + b;
+            ++pos;
         }
         off += __shfl_sync(FULL, incl, 31);
     }
@@ -840,7 +871,8 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
             attr = smem;
         }
         LC_LAUNCH(k_cand_pick, dim3((unsigned)b.total_q), dim3(512), smem, st, to_dev(b), m, k,
-                  p.cap, p.R, p.PK, p.P, count, cand, lcnt, priv, p.gy, p.cloc, topk, fail);
+                  p.cap, p.R, p.PK, p.P, count, cand, lcnt, priv, p.gy, p.cloc, topk, fail,
+                  dev_err);
         if ((s = check_launch()) != LC_OK) return s;
     }
     // 5. exact fallback for the rows marked in fail[] (no work when none is)
