@@ -111,6 +111,17 @@ lc_status hca_compress(const void *K, const void *V, const float *G_K, const flo
                        int64_t T, int32_t d, int32_t m, lc_dtype dtype, void *Kc, void *Vc,
                        lc_stream stream);
 
+/* Token-gated compressor (same page, §1.1, CSA paragraph: the token-level
+ * compressor is learned, so every token brings its own gate logits).  With
+ * Z [T, d] fp32 holding one gate logit per token and channel,
+ *   Xc[j,c] = sum_{p<m} softmax_p(Z[j*m+p, c]) * X[j*m+p, c],  j < floor(T/m).
+ * Compresses K, V or the token-level indexer keys (d = H_I * d_I) into their
+ * entries; a tail of T mod m tokens makes no entry.
+ *   X [T, d] dtype;  Z [T, d] fp32;  Xc [floor(T/m), d] dtype (written)
+ * Supported: d % 32 == 0, 32 <= d <= 1024; 1 <= m <= 4096; T >= 0. */
+lc_status token_gated_compress(const void *X, const float *Z, int64_t T, int32_t d, int32_t m,
+                               lc_dtype dtype, void *Xc, lc_stream stream);
+
 /* Lightning Indexer (same page, §1.1, CSA paragraph: a light indexer scores
  * the compressed KV blocks against the query), with the form
  *   I[r,j] = sum_{h<HI} w[r,h] * max(0, qI[r,h,:] . kI[cu_c[b]+j,h,:])

@@ -15,6 +15,7 @@ import os
 from dataclasses import dataclass
 from typing import Optional, Sequence
 
+import numpy as np
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -27,7 +28,7 @@ LC_DEVERR_INDEX, LC_DEVERR_WINDOW, LC_DEVERR_BATCH, LC_DEVERR_TIMEOUT = 1, 2, 4,
 LC_DEVERR_SINK = 16
 LC_OP_LIGHTNING_INDEX, LC_OP_TOPK_SELECT, LC_OP_SPARSE_MQA_ATTN, LC_OP_HCA_DENSE_ATTN = 0, 1, 2, 3
 
-ENTRY_POINTS = ("csa_compress", "hca_compress", "lightning_index", "topk_select",
+ENTRY_POINTS = ("csa_compress", "hca_compress", "token_gated_compress", "lightning_index", "topk_select",
                 "sparse_mqa_attn", "hca_dense_attn", "lc_workspace_size", "lc_status_string",
                 "lc_last_cuda_error", "lc_launch_count", "lc_last_kernel", "lc_version",
                 "lc_debug_stall")
@@ -66,6 +67,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     sig = {
         "csa_compress": [vp, vp, vp, vp, i64, i32, i32, i32, vp, vp, vp],
         "hca_compress": [vp, vp, vp, vp, i64, i32, i32, i32, vp, vp, vp],
+        "token_gated_compress": [vp, vp, i64, i32, i32, i32, vp, vp],
         "lightning_index": [vp, vp, vp, bp, i32, i32, i32, i32, vp, i64, i32, vp, vp, sz, vp, vp],
         "topk_select": [vp, i64, bp, i32, i32, vp, vp, sz, vp, vp],
         "sparse_mqa_attn": [vp, vp, vp, vp, i32, vp, vp, bp, i32, i32, i32, i32, f32, vp, i32, vp,
@@ -216,6 +218,25 @@ def csa_compress(K, V, G_K, G_V=None, m: int = 4, Kc=None, Vc=None, stream=None)
 def hca_compress(K, V, G_K, G_V=None, m: int = 128, Kc=None, Vc=None, stream=None):
     """K, V [T,d] -> (Kc, Vc) [floor(T/m), d]; gates [m,d] fp32."""
     return _compress("hca_compress", K, V, G_K, G_K if G_V is None else G_V, m, Kc, Vc, stream)
+
+
+def token_gated_compress(X, Z, m: int, Xc=None, stream=None):
+    """X [T, d] with per-token gate logits Z [T, d] fp32 -> Xc [floor(T/m), d].
+    X may also be [T, H_I, d_I] (token-level indexer keys); Xc then has the
+    same trailing shape."""
+    lib = load_library()
+    T = X.shape[0]
+    d = int(np.prod(X.shape[1:]))
+    if tuple(Z.shape) != tuple(X.shape):
+        raise ValueError("Z must hold one fp32 gate logit per element of X (same shape)")
+    if Xc is None:
+        Xc = torch.empty((T // m, *X.shape[1:]), dtype=X.dtype, device=X.device)
+    if Xc.shape[0] < T // m:
+        raise ValueError("output too small")
+    st = lib.token_gated_compress(_dev(X, "X"), _dev(Z, "Z", torch.float32), T, d, m,
+                                  _dtype_code(X), _dev(Xc, "Xc", X.dtype), _stream(stream))
+    _check("token_gated_compress", st)
+    return Xc
 
 
 def lightning_index(qI, w, kI, batch: DeviceBatch, m: int, *, scores: bool | torch.Tensor = True,

@@ -11,6 +11,8 @@ namespace lc {
 lc_status compress_launch(const void *K, const void *V, const float *GK, const float *GV,
                           int64_t T_, int d, int m, lc_dtype dt, void *Kc, void *Vc,
                           cudaStream_t st);
+lc_status compress_tok_launch(const void *X, const float *Z, int64_t T_, int d, int m,
+                              lc_dtype dt, void *Xc, cudaStream_t st);
 lc_status index_launch(const void *qI, const float *w, const void *kI, const lc_batch &b, int HI,
                        int dI, int m, lc_dtype dt, float *scores, int64_t ld, int32_t *dev_err,
                        cudaStream_t st);
@@ -135,6 +137,15 @@ lc_status hca_compress(const void *K, const void *V, const float *G_K, const flo
                        int64_t T, int32_t d, int32_t m, lc_dtype dtype, void *Kc, void *Vc,
                        lc_stream stream) {
     return compress_common(K, V, G_K, G_V, T, d, m, dtype, Kc, Vc, (cudaStream_t)stream);
+}
+
+lc_status token_gated_compress(const void *X, const float *Z, int64_t T, int32_t d, int32_t m,
+                               lc_dtype dtype, void *Xc, lc_stream stream) {
+    cudaStream_t st = (cudaStream_t)stream;
+    if (T < 0 || m < 1 || !dtype_ok(dtype)) return LC_ERR_INVALID_ARG;
+    if (T / m > 0 && (!X || !Z || !Xc)) return LC_ERR_INVALID_ARG;
+    if (d < 32 || d > 1024 || d % 32 || m > 4096) return LC_ERR_UNSUPPORTED;
+    return finish(compress_tok_launch(X, Z, T, d, m, dtype, Xc, st), st, nullptr);
 }
 
 lc_status lightning_index(const void *qI, const float *w, const void *kI, const lc_batch *batch,

@@ -48,6 +48,10 @@ def _load():
             lib.oracle_num_threads.restype = ctypes.c_int
             lib.oracle_compress.argtypes = [D, D, i64, i32, i32, D]
             lib.oracle_compress.restype = None
+            lib.oracle_compress_tok.argtypes = [D, D, i64, i32, i32, D]
+            lib.oracle_compress_tok.restype = None
+            lib.oracle_rope.argtypes = [D, I64, i64, i32, i32, i32, dbl, i32, D]
+            lib.oracle_rope.restype = None
             lib.oracle_index.argtypes = [D, D, D, I64, i64, i64, i32, i32, i32, D]
             lib.oracle_index.restype = None
             lib.oracle_topk.argtypes = [D, i64, i64, I64, i32, I32]
@@ -102,6 +106,41 @@ def compress(X, G, m: int) -> np.ndarray:
     _load().oracle_compress(_p(X, ctypes.c_double), _p(G, ctypes.c_double), T, d, m,
                             _p(out, ctypes.c_double))
     return out
+
+
+def compress_tok(X, Z, m: int) -> np.ndarray:
+    """Token-gated compressor: X [T, d], per-token gate logits Z [T, d] ->
+    Xc [floor(T/m), d] (fp64)."""
+    X, Z = _f64(X), _f64(Z)
+    T, d = X.shape
+    assert Z.shape == (T, d)
+    out = np.zeros((T // m, d), dtype=np.float64)
+    _load().oracle_compress_tok(_p(X, ctypes.c_double), _p(Z, ctypes.c_double), T, d, m,
+                                _p(out, ctypes.c_double))
+    return out
+
+
+ROPE_DIMS = 64
+ROPE_BASE = 10000.0
+
+
+def rope(X, pos, inverse: bool = False) -> np.ndarray:
+    """Partial RoPE of the last 64 dimensions.  X [n, d] or [n, H, d], pos [n]
+    (every vector of row r at position pos[r]); inverse rotates by -pos."""
+    X, pos = _f64(X), _i64(pos)
+    shape = X.shape
+    n, d = shape[0], shape[-1]
+    hd = int(np.prod(shape[1:-1])) if len(shape) > 2 else 1
+    assert pos.shape == (n,) and d >= ROPE_DIMS
+    Y = np.zeros_like(X)
+    _load().oracle_rope(_p(X, ctypes.c_double), _p(pos, ctypes.c_int64), n, hd, d, ROPE_DIMS,
+                        ROPE_BASE, -1 if inverse else 1, _p(Y, ctypes.c_double))
+    return Y
+
+
+def entry_positions(pos0: int, n: int, m: int) -> np.ndarray:
+    """Position of each compressed entry: its last token, pos0 + (j+1) m - 1."""
+    return pos0 + (np.arange(n, dtype=np.int64) + 1) * m - 1
 
 
 def index(qI, w, kI, tpos, m: int) -> np.ndarray:
@@ -161,6 +200,31 @@ def sparse_attn(Q, Kc, Vc, idx, Kraw, Vraw, raw_pos0: int, tpos, W: int, scale: 
     if rc != 0:
         raise ValueError(f"oracle_sparse_attn: invalid input at row {-rc - 1}")
     return O, lse
+
+
+def sparse_attn_rope(Q, Kc, Vc, idx, Kraw, Vraw, raw_pos0: int, tpos, W: int, scale: float,
+                     m: int, sink=None):
+    """CSA attention with partial RoPE, from unrotated inputs, in the order the
+    reading fixes: each compressed entry rotated at the position of its last
+    token ((j+1) m - 1), each window token at its own position, each query at
+    t; attention; the output rotated back at t.  Returns (O, lse)."""
+    Kc, Vc, Kraw, Vraw = _f64(Kc), _f64(Vc), _f64(Kraw), _f64(Vraw)
+    ep = entry_positions(0, Kc.shape[0], m)
+    rp = raw_pos0 + np.arange(Kraw.shape[0], dtype=np.int64)
+    O, lse = sparse_attn(rope(Q, tpos), rope(Kc, ep), rope(Vc, ep), idx, rope(Kraw, rp),
+                         rope(Vraw, rp), raw_pos0, tpos, W, scale, sink)
+    return rope(O, tpos, inverse=True), lse
+
+
+def hca_attn_rope(Q, Kc, Vc, m: int, Kraw, Vraw, raw_pos0: int, tpos, W: int, scale: float,
+                  sink=None):
+    """HCA attention with partial RoPE, as sparse_attn_rope."""
+    Kc, Vc, Kraw, Vraw = _f64(Kc), _f64(Vc), _f64(Kraw), _f64(Vraw)
+    ep = entry_positions(0, Kc.shape[0], m)
+    rp = raw_pos0 + np.arange(Kraw.shape[0], dtype=np.int64)
+    O, lse = hca_attn(rope(Q, tpos), rope(Kc, ep), rope(Vc, ep), m, rope(Kraw, rp),
+                      rope(Vraw, rp), raw_pos0, tpos, W, scale, sink)
+    return rope(O, tpos, inverse=True), lse
 
 
 def hca_attn(Q, Kc, Vc, m: int, Kraw, Vraw, raw_pos0: int, tpos, W: int, scale: float,

@@ -81,6 +81,67 @@ void oracle_compress(const double *X, const double *G, int64_t T, int32_t d,
     free(wgt);
 }
 
+/* Token-level compressor (the same page, §1.1, CSA paragraph: a token-level
+ * compressor merges every m tokens' KV into one entry; the real one is
+ * learned).  The gate logit of each channel comes from the token itself:
+ * Z [T, d] holds one logit per token and channel (for instance a projection
+ * of the token's hidden state), and
+ *   Xc[j,c] = sum_p softmax_p(Z[j*m+p, c]) * X[j*m+p, c],  p = 0 .. m-1.
+ * X [T, d], Z [T, d] -> Xc [floor(T/m), d]; only full blocks make entries. */
+void oracle_compress_tok(const double *X, const double *Z, int64_t T, int32_t d,
+                         int32_t m, double *Xc)
+{
+    int64_t Tc = T / m;
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < Tc; ++j) {
+        for (int32_t c = 0; c < d; ++c) {
+            double mx = -INFINITY;
+            for (int32_t p = 0; p < m; ++p) {
+                double z = Z[(j * m + p) * d + c];
+                if (z > mx) mx = z;
+            }
+            double s = 0.0, acc = 0.0;
+            for (int32_t p = 0; p < m; ++p) {
+                double e = exp(Z[(j * m + p) * d + c] - mx);
+                s += e;
+                acc += e * X[(j * m + p) * d + c];
+            }
+            Xc[j * d + c] = acc / s;
+        }
+    }
+}
+
+/* Partial RoPE (the same page, §1.1, engineering details: RoPE acts only on
+ * the last 64 dimensions, and the core-attention output gets the inverse
+ * RoPE to restore relative positions).  Reading: the last R = 64 dimensions
+ * of each d-vector form 32 interleaved pairs (2i, 2i+1), i = 0..31, rotated by
+ * the angle p * theta_i with theta_i = base^(-2i/R), base = 10000:
+ *   y[2i]   = x[2i] cos(a) - x[2i+1] sin(a)
+ *   y[2i+1] = x[2i] sin(a) + x[2i+1] cos(a),   a = sign * p * theta_i;
+ * sign = -1 is the inverse rotation.  The first d - R dimensions are copied.
+ * X [n, hd, d] (hd vectors per row, all at the row's position pos[r]). */
+void oracle_rope(const double *X, const int64_t *pos, int64_t n, int32_t hd, int32_t d,
+                 int32_t R, double base, int32_t sign, double *Y)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n; ++r) {
+        for (int32_t h = 0; h < hd; ++h) {
+            const double *x = X + (r * hd + h) * d;
+            double *y = Y + (r * hd + h) * d;
+            for (int32_t c = 0; c < d - R; ++c) y[c] = x[c];
+            const double *xr = x + (d - R);
+            double *yr = y + (d - R);
+            for (int32_t i = 0; i < R / 2; ++i) {
+                double theta = pow(base, -2.0 * i / R);
+                double a = (double)sign * (double)pos[r] * theta;
+                double cs = cos(a), sn = sin(a);
+                yr[2 * i] = xr[2 * i] * cs - xr[2 * i + 1] * sn;
+                yr[2 * i + 1] = xr[2 * i] * sn + xr[2 * i + 1] * cs;
+            }
+        }
+    }
+}
+
 /* Number of compressed entries visible from absolute position t. */
 static int64_t n_visible(int64_t t, int32_t m) { return (t + 1) / m; }
 

@@ -382,3 +382,172 @@ def test_sink_must_be_a_real_logit_or_minus_inf():
     for bad in (np.nan, np.inf):
         with pytest.raises(ValueError, match="finite or -inf"):
             oracle.hca_attn(Q, Kc, Vc, 1, Kc, Vc, 0, [3], 0, 0.5, sink=np.array([0.0, bad]))
+
+
+# ------------------------------------------------------ token-gated compressor
+# The learned compressor of the pages ("DeepSeek-V4 技术解析…", §1.1, CSA
+# paragraph) takes its gates from each token: Z [T, d] holds one gate logit per
+# token and channel, softmax-normalised over the m tokens of a block.
+
+
+def test_token_gates_reduce_to_position_gates():
+    # gates that repeat the same [m, d] pattern in every block are the
+    # position-gated compressor
+    m, d, T = 4, 6, 4 * 9 + 3
+    X = RNG.standard_normal((T, d))
+    G = RNG.standard_normal((m, d))
+    Z = np.tile(G, (T // m + 1, 1))[:T]
+    np.testing.assert_allclose(oracle.compress_tok(X, Z, m), oracle.compress(X, G, m),
+                               rtol=0, atol=1e-14)
+
+
+def test_token_gates_closed_forms():
+    m, d, T = 8, 5, 8 * 6
+    X = RNG.standard_normal((T, d))
+    # equal logits within a block (any value per block and channel): block mean
+    Z = np.repeat(RNG.standard_normal((T // m, d)) * 30, m, axis=0)
+    np.testing.assert_allclose(oracle.compress_tok(X, Z, m),
+                               X.reshape(T // m, m, d).mean(axis=1), rtol=0, atol=1e-13)
+    # one token of each block 60 above the others, per channel: that token
+    pick = RNG.integers(0, m, size=(T // m, d))
+    Z = np.zeros((T, d))
+    for j in range(T // m):
+        for c in range(d):
+            Z[j * m + pick[j, c], c] = 60.0
+    want = np.array([[X[j * m + pick[j, c], c] for c in range(d)] for j in range(T // m)])
+    np.testing.assert_allclose(oracle.compress_tok(X, Z, m), want, rtol=0, atol=1e-24 + 1e-20)
+    # m = 2: the first token's weight is expit(z0 - z1)
+    Z = RNG.standard_normal((2 * 7, d)) * 3
+    X = RNG.standard_normal((2 * 7, d))
+    a = expit(Z[0::2] - Z[1::2])
+    np.testing.assert_allclose(oracle.compress_tok(X, Z, 2), a * X[0::2] + (1 - a) * X[1::2],
+                               rtol=0, atol=1e-14)
+
+
+def test_token_gates_depend_on_each_token():
+    # changing one token's gate changes only its own block, and a logit shift
+    # shared by a block's tokens (per channel) changes nothing
+    m, d, T = 4, 3, 4 * 5
+    X = RNG.standard_normal((T, d))
+    Z = RNG.standard_normal((T, d))
+    base = oracle.compress_tok(X, Z, m)
+    Z2 = Z.copy()
+    Z2[9, 1] += 2.0  # block 2, channel 1
+    out = oracle.compress_tok(X, Z2, m)
+    diff = np.abs(out - base) > 1e-15
+    assert diff[2, 1] and diff.sum() == 1
+    Z3 = Z + np.repeat(RNG.standard_normal((T // m, d)), m, axis=0) * 10
+    np.testing.assert_allclose(oracle.compress_tok(X, Z3, m), base, rtol=0, atol=1e-13)
+
+
+# ------------------------------------------------------------ partial RoPE
+# "DeepSeek-V4 技术解析…", §1.1, engineering details: RoPE acts only on the last
+# 64 dimensions; the core-attention output gets the inverse RoPE to restore
+# relative positions.  The rotation itself is RoPE as RoFormer defines it
+# (pairs as complex numbers multiplied by e^{i p theta_i},
+# theta_i = 10000^(-2i/64)).
+
+
+def _rope_complex(X, pos):
+    # independent formulation: complex multiplication of the interleaved pairs
+    X = np.asarray(X, dtype=np.float64)
+    d = X.shape[-1]
+    z = X[..., d - 64::2] + 1j * X[..., d - 64 + 1::2]
+    theta = 10000.0 ** (-np.arange(0, 64, 2) / 64.0)
+    shape = (len(pos),) + (1,) * (X.ndim - 2) + (32,)
+    rot = np.exp(1j * np.asarray(pos, dtype=np.float64).reshape(-1, *([1] * (X.ndim - 1)))
+                 * theta).reshape(shape)
+    w = z * rot
+    Y = X.copy()
+    Y[..., d - 64::2] = w.real
+    Y[..., d - 64 + 1::2] = w.imag
+    return Y
+
+
+def test_rope_is_roformer_rotation_of_the_last_64_dims():
+    X = RNG.standard_normal((7, 3, 128))
+    pos = np.array([0, 1, 5, 127, 4095, 1048575, 999983])
+    Y = oracle.rope(X, pos)
+    np.testing.assert_allclose(Y, _rope_complex(X, pos), rtol=0, atol=1e-9)
+    assert np.array_equal(Y[..., :64], X[..., :64])            # first d-64 dims untouched
+    np.testing.assert_allclose(Y[0], X[0], rtol=0, atol=0)       # position 0: identity
+    # the rotation keeps each pair's norm
+    nx = X[..., 64::2] ** 2 + X[..., 65::2] ** 2
+    ny = Y[..., 64::2] ** 2 + Y[..., 65::2] ** 2
+    np.testing.assert_allclose(ny, nx, rtol=1e-12)
+    # the inverse undoes it; d = 64 rotates every dimension
+    np.testing.assert_allclose(oracle.rope(Y, pos, inverse=True), X, rtol=0, atol=1e-9)
+    X64 = RNG.standard_normal((4, 64))
+    p4 = np.array([3, 9, 10, 200])
+    np.testing.assert_allclose(oracle.rope(X64, p4), _rope_complex(X64, p4), rtol=0, atol=1e-12)
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    q, k = RNG.standard_normal((1, 128)), RNG.standard_normal((1, 128))
+    for t, s_, delta in ((10, 3, 1000), (500, 499, 123457), (7, 7, 5)):
+        a = oracle.rope(q, [t]) @ oracle.rope(k, [s_]).T
+        b = oracle.rope(q, [t + delta]) @ oracle.rope(k, [s_ + delta]).T
+        np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-10)
+
+
+def _rope_case(m, T, W, H=3, d=128, q_from=0):
+    Q = RNG.standard_normal((T - q_from, H, d))
+    K, V = RNG.standard_normal((T, d)), RNG.standard_normal((T, d))
+    G = RNG.standard_normal((m, d))
+    return Q, K, V, G
+
+
+def test_attention_with_rope_is_invariant_to_a_common_shift():
+    # the output is rotated back at t, so moving every position (queries,
+    # window tokens, entries) by a multiple of m changes nothing; a slip in any
+    # rotation (q, k, v, the output, or an entry's position) breaks this
+    m, W, T, shift = 4, 6, 64, 4 * 37
+    Q, K, V, G = _rope_case(m, T, W)
+    rows = np.arange(W - 1, T)          # windows stay inside the stored tokens
+    Q = Q[rows]
+    Kc, Vc = oracle.compress(K, G, m), oracle.compress(V, G, m)
+    idx = np.full((len(rows), T // m), -1, dtype=np.int32)
+    for i, r in enumerate(rows):
+        nv = (r + 1) // m
+        idx[i, :nv] = np.arange(nv)
+    o1, l1 = oracle.hca_attn_rope(Q, Kc, Vc, m, K, V, 0, rows, W, 0.3)
+    o3, l3 = oracle.sparse_attn_rope(Q, Kc, Vc, idx, K, V, 0, rows, W, 0.3, m)
+    np.testing.assert_allclose(o3, o1, rtol=0, atol=1e-12)      # CSA with all selected == HCA
+    # the same tokens at positions shift .., after shift/m entries nobody selects
+    zc = np.zeros((shift // m, K.shape[1]))
+    idx2 = np.where(idx >= 0, idx + shift // m, -1).astype(np.int32)
+    o2, l2 = oracle.sparse_attn_rope(Q, np.concatenate([zc, Kc]), np.concatenate([zc, Vc]), idx2,
+                                     K, V, shift, rows + shift, W, 0.3, m)
+    np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-9)
+    np.testing.assert_allclose(l2, l1, rtol=0, atol=1e-9)
+    # and RoPE does change the result (the test would be vacuous otherwise)
+    o0, _ = oracle.hca_attn(Q, Kc, Vc, m, K, V, 0, rows, W, 0.3)
+    assert np.abs(o0 - o1).max() > 1e-2
+
+
+def test_rope_single_key_at_the_query_position_returns_its_value():
+    # one key at the query's own position: q.k is unrotated, v is rotated at t
+    # and the output rotated back at t, so O = v exactly
+    d, t = 128, 123457
+    Q = RNG.standard_normal((1, 2, d))
+    K, V = RNG.standard_normal((1, d)), RNG.standard_normal((1, d))
+    o, l = oracle.sparse_attn_rope(Q, K[:0], V[:0], np.full((1, 1), -1, np.int32), K, V, t, [t],
+                                   1, 0.5, 4)
+    np.testing.assert_allclose(o[0], np.repeat(V, 2, axis=0), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l[0], 0.5 * (Q[0] @ K[0]), rtol=0, atol=1e-10)
+
+
+def test_rope_entry_sits_at_its_last_token():
+    # an entry is rotated at the position of its block's last token: a query at
+    # exactly that position attending to that entry alone gets its value back
+    d, m, j = 128, 4, 5
+    t = (j + 1) * m - 1
+    Q = RNG.standard_normal((1, 2, d))
+    Kc, Vc = RNG.standard_normal((8, d)), RNG.standard_normal((8, d))
+    idx = np.array([[j, -1]], dtype=np.int32)
+    o, _ = oracle.sparse_attn_rope(Q, Kc, Vc, idx, Kc[:0], Vc[:0], 0, [t], 0, 0.5, m)
+    np.testing.assert_allclose(o[0], np.repeat(Vc[j:j + 1], 2, axis=0), rtol=0, atol=1e-12)
+    # one position later the value comes back rotated by one step
+    o2, _ = oracle.sparse_attn_rope(Q, Kc, Vc, idx, Kc[:0], Vc[:0], 0, [t + 1], 0, 0.5, m)
+    np.testing.assert_allclose(o2[0], np.repeat(oracle.rope(Vc[j:j + 1], [-1]), 2, axis=0),
+                               rtol=0, atol=1e-12)

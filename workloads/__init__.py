@@ -106,6 +106,32 @@ def csa_layer(*, T: int, H: int, d: int, HI: int, dI: int, m: int, k: int, W: in
     return out
 
 
+def csa_layer_token_gated(*, T: int, H: int, d: int, HI: int, dI: int, m: int, k: int, W: int,
+                          dtype: str, seed: int, device="cpu", q_from: int = 0,
+                          gate_scale: float = 1.0) -> Dict:
+    """A CSA layer whose compressor gates come from each token: per-token gate
+    logits Z_K, Z_V [T, d] and token-level indexer keys kI_tok [T, HI, dI]
+    with their own gate logits Z_I [T, HI, dI] (the indexer-side compressor).
+    Gate logits are N(0, gate_scale^2), the distribution of a random
+    projection of random hidden states.  Draw order: Q, K, V, Z_K, Z_V, q_I,
+    kI_tok, Z_I, w.  No compressed tensor is drawn: both sides compress."""
+    g = _gen(seed, device)
+    Nq = T - q_from
+    out = dict(kind="csa_token_gated", T=T, H=H, d=d, HI=HI, dI=dI, m=m, k=k, W=W,
+               dtype=dtype, scale=1.0 / math.sqrt(d), seed=seed)
+    out["Q"] = normal(g, (Nq, H, d), dtype, device)
+    out["K"] = normal(g, (T, d), dtype, device)
+    out["V"] = normal(g, (T, d), dtype, device)
+    out["ZK"] = normal(g, (T, d), "f32", device) * gate_scale
+    out["ZV"] = normal(g, (T, d), "f32", device) * gate_scale
+    out["qI"] = normal(g, (Nq, HI, dI), dtype, device)
+    out["kI_tok"] = normal(g, (T, HI, dI), dtype, device)
+    out["ZI"] = normal(g, (T, HI, dI), "f32", device) * gate_scale
+    out["w"] = uniform(g, (Nq, HI), "f32", device)
+    out["batch"] = single(T, q_from, Nq, T // m)
+    return out
+
+
 def hca_layer(*, T: int, H: int, d: int, m: int, W: int, dtype: str, seed: int,
               device="cpu", q_from: int = 0) -> Dict:
     """One HCA layer over one sequence.  Draw order: Q, K, V, G'."""
