@@ -98,10 +98,13 @@ typedef struct {
  * and the same for V with G_V.  A tail of T mod m tokens makes no entry.
  *   K, V   [T, d] dtype          G_K, G_V [m, d] fp32 (may alias)
  *   Kc, Vc [floor(T/m), d] dtype (written; must not overlap the inputs)
+ *   rope_pos0: -1, or the absolute position of input row 0: then every entry
+ *          also gets partial RoPE (LC_ROPE_DIMS below) at the position of its
+ *          last token, rope_pos0 + (j+1)*m - 1 (K and V alike).
  * Supported: d in {64, 128}; 1 <= m <= 256; T >= 0. */
 lc_status csa_compress(const void *K, const void *V, const float *G_K, const float *G_V,
                        int64_t T, int32_t d, int32_t m, lc_dtype dtype, void *Kc, void *Vc,
-                       lc_stream stream);
+                       int64_t rope_pos0, lc_stream stream);
 
 /* HCA compressor (same page, §1.1, HCA paragraph: every m' tokens become one
  * entry, m' much larger than m).  Same arithmetic and arguments as
@@ -109,7 +112,7 @@ lc_status csa_compress(const void *K, const void *V, const float *G_K, const flo
  * selects a different launch shape. */
 lc_status hca_compress(const void *K, const void *V, const float *G_K, const float *G_V,
                        int64_t T, int32_t d, int32_t m, lc_dtype dtype, void *Kc, void *Vc,
-                       lc_stream stream);
+                       int64_t rope_pos0, lc_stream stream);
 
 /* Token-gated compressor (same page, §1.1, CSA paragraph: the token-level
  * compressor is learned, so every token brings its own gate logits).  With
@@ -118,9 +121,28 @@ lc_status hca_compress(const void *K, const void *V, const float *G_K, const flo
  * Compresses K, V or the token-level indexer keys (d = H_I * d_I) into their
  * entries; a tail of T mod m tokens makes no entry.
  *   X [T, d] dtype;  Z [T, d] fp32;  Xc [floor(T/m), d] dtype (written)
- * Supported: d % 32 == 0, 32 <= d <= 1024; 1 <= m <= 4096; T >= 0. */
+ *   rope_pos0: as for csa_compress (for attention K and V, whose last 64
+ *          channels are the rotary ones; -1 for indexer keys).
+ * Supported: d % 32 == 0, 32 <= d <= 1024 (d >= 64 with RoPE); 1 <= m <= 4096;
+ * T >= 0. */
 lc_status token_gated_compress(const void *X, const float *Z, int64_t T, int32_t d, int32_t m,
-                               lc_dtype dtype, void *Xc, lc_stream stream);
+                               lc_dtype dtype, void *Xc, int64_t rope_pos0, lc_stream stream);
+
+/* Partial RoPE (same page, §1.1, engineering details: RoPE acts only on the
+ * last 64 dimensions; the core-attention output gets the inverse RoPE to
+ * restore relative positions).  Pairs (2i, 2i+1), i < 32, of the last 64
+ * dimensions of a vector at position p are rotated by p * theta_i,
+ * theta_i = 10000^(-i/32).  With RoPE, queries rotate at their position t,
+ * compressed entries at their last token's position (csa_compress), raw
+ * window tokens at their own positions, values like keys, and the attention
+ * output rotates back by -t.
+ * rope_rotate rotates in place rows i = 0 .. n-1 of X [n, hv, d] (hv vectors
+ * per row) at positions pos0 + i, or back (inverse = 1): use it on the raw
+ * window cache, whose tokens are stored rotated.
+ * Supported: d in {64, 128}; hv >= 1; pos0 >= 0. */
+#define LC_ROPE_DIMS 64
+lc_status rope_rotate(void *X, int64_t n, int32_t hv, int32_t d, int64_t pos0, int32_t inverse,
+                      lc_dtype dtype, lc_stream stream);
 
 /* Lightning Indexer (same page, §1.1, CSA paragraph: a light indexer scores
  * the compressed KV blocks against the query), with the form
@@ -164,22 +186,25 @@ lc_status topk_select(const float *scores, int64_t ld, const lc_batch *batch, in
  *        on the same device as Q; each finite or -inf (no sink for that
  *        head); a NaN or +inf value raises LC_DEVERR_SINK and that head is
  *        computed without a sink;
+ *   rope 0 or 1: with 1, Q is rotated at t (partial RoPE, see rope_rotate)
+ *        and O rotated back at t; Kc/Vc and Kraw/Vraw must hold rotated
+ *        entries and tokens (csa_compress with rope_pos0, rope_rotate);
  *   lse [total_q, H] fp32 or NULL.
  * Supported: d in {64,128}; H % 8 == 0, 8 <= H <= 128; 0 <= W <= 4096. */
 lc_status sparse_mqa_attn(const void *Q, const void *Kc, const void *Vc, const int32_t *topk,
                           int32_t k, const void *Kraw, const void *Vraw, const lc_batch *batch,
                           int32_t H, int32_t d, int32_t m, int32_t W, float scale,
-                          const float *sink, lc_dtype dtype, void *O, float *lse, void *ws,
-                          size_t ws_bytes, int32_t *dev_err, lc_stream stream);
+                          const float *sink, int32_t rope, lc_dtype dtype, void *O, float *lse,
+                          void *ws, size_t ws_bytes, int32_t *dev_err, lc_stream stream);
 
 /* HCA dense attention (same page, §1.1, HCA paragraph: dense attention over
- * every compressed entry).  As sparse_mqa_attn (sink included) with
+ * every compressed entry).  As sparse_mqa_attn (sink and rope included) with
  *   S = { entries j < n_vis(t) in order }  then the window. */
 lc_status hca_dense_attn(const void *Q, const void *Kc, const void *Vc, const void *Kraw,
                          const void *Vraw, const lc_batch *batch, int32_t H, int32_t d,
-                         int32_t m, int32_t W, float scale, const float *sink, lc_dtype dtype,
-                         void *O, float *lse, void *ws, size_t ws_bytes, int32_t *dev_err,
-                         lc_stream stream);
+                         int32_t m, int32_t W, float scale, const float *sink, int32_t rope,
+                         lc_dtype dtype, void *O, float *lse, void *ws, size_t ws_bytes,
+                         int32_t *dev_err, lc_stream stream);
 
 /* Index + top-k that allocates nothing (the pages have no counterpart: this
  * is an addition for callers that cannot allocate device memory, such as a

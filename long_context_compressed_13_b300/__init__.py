@@ -28,7 +28,8 @@ LC_DEVERR_INDEX, LC_DEVERR_WINDOW, LC_DEVERR_BATCH, LC_DEVERR_TIMEOUT = 1, 2, 4,
 LC_DEVERR_SINK = 16
 LC_OP_LIGHTNING_INDEX, LC_OP_TOPK_SELECT, LC_OP_SPARSE_MQA_ATTN, LC_OP_HCA_DENSE_ATTN = 0, 1, 2, 3
 
-ENTRY_POINTS = ("csa_compress", "hca_compress", "token_gated_compress", "lightning_index", "topk_select",
+ENTRY_POINTS = ("csa_compress", "hca_compress", "token_gated_compress", "rope_rotate",
+                "lightning_index", "topk_select",
                 "sparse_mqa_attn", "hca_dense_attn", "lc_workspace_size", "lc_status_string",
                 "lc_last_cuda_error", "lc_launch_count", "lc_last_kernel", "lc_version",
                 "lc_debug_stall")
@@ -65,15 +66,16 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                              ctypes.c_size_t)
     bp = ctypes.POINTER(_LcBatch)
     sig = {
-        "csa_compress": [vp, vp, vp, vp, i64, i32, i32, i32, vp, vp, vp],
-        "hca_compress": [vp, vp, vp, vp, i64, i32, i32, i32, vp, vp, vp],
-        "token_gated_compress": [vp, vp, i64, i32, i32, i32, vp, vp],
+        "csa_compress": [vp, vp, vp, vp, i64, i32, i32, i32, vp, vp, i64, vp],
+        "hca_compress": [vp, vp, vp, vp, i64, i32, i32, i32, vp, vp, i64, vp],
+        "token_gated_compress": [vp, vp, i64, i32, i32, i32, vp, i64, vp],
+        "rope_rotate": [vp, i64, i32, i32, i64, i32, i32, vp],
         "lightning_index": [vp, vp, vp, bp, i32, i32, i32, i32, vp, i64, i32, vp, vp, sz, vp, vp],
         "topk_select": [vp, i64, bp, i32, i32, vp, vp, sz, vp, vp],
-        "sparse_mqa_attn": [vp, vp, vp, vp, i32, vp, vp, bp, i32, i32, i32, i32, f32, vp, i32, vp,
-                            vp, vp, sz, vp, vp],
-        "hca_dense_attn": [vp, vp, vp, vp, vp, bp, i32, i32, i32, i32, f32, vp, i32, vp, vp, vp, sz,
-                           vp, vp],
+        "sparse_mqa_attn": [vp, vp, vp, vp, i32, vp, vp, bp, i32, i32, i32, i32, f32, vp, i32, i32,
+                            vp, vp, vp, sz, vp, vp],
+        "hca_dense_attn": [vp, vp, vp, vp, vp, bp, i32, i32, i32, i32, f32, vp, i32, i32, vp, vp,
+                           vp, sz, vp, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -192,7 +194,15 @@ def workspace_size(op: int, batch: DeviceBatch, H=0, d=0, HI=0, dI=0, k=0) -> in
     return int(load_library().lc_workspace_size(op, ctypes.byref(cb), H, d, HI, dI, k))
 
 
-def _compress(fn_name, K, V, G_K, G_V, m, Kc=None, Vc=None, stream=None):
+def _rope_pos0(rope_pos0) -> int:
+    if rope_pos0 is None:
+        return -1
+    if rope_pos0 < 0:
+        raise ValueError("rope_pos0 is a position (>= 0) or None")
+    return int(rope_pos0)
+
+
+def _compress(fn_name, K, V, G_K, G_V, m, Kc=None, Vc=None, stream=None, rope_pos0=None):
     lib = load_library()
     T, d = K.shape
     if V.shape != K.shape or V.dtype != K.dtype:
@@ -205,22 +215,42 @@ def _compress(fn_name, K, V, G_K, G_V, m, Kc=None, Vc=None, stream=None):
         raise ValueError("output too small")
     st = getattr(lib, fn_name)(_dev(K, "K"), _dev(V, "V"), _dev(G_K, "G_K", torch.float32),
                                _dev(G_V, "G_V", torch.float32), T, d, m, _dtype_code(K),
-                               _dev(Kc, "Kc", K.dtype), _dev(Vc, "Vc", K.dtype), _stream(stream))
+                               _dev(Kc, "Kc", K.dtype), _dev(Vc, "Vc", K.dtype),
+                               _rope_pos0(rope_pos0), _stream(stream))
     _check(fn_name, st)
     return Kc, Vc
 
 
-def csa_compress(K, V, G_K, G_V=None, m: int = 4, Kc=None, Vc=None, stream=None):
-    """K, V [T,d] -> (Kc, Vc) [floor(T/m), d]; gates [m,d] fp32."""
-    return _compress("csa_compress", K, V, G_K, G_K if G_V is None else G_V, m, Kc, Vc, stream)
+def csa_compress(K, V, G_K, G_V=None, m: int = 4, Kc=None, Vc=None, stream=None,
+                 rope_pos0=None):
+    """K, V [T,d] -> (Kc, Vc) [floor(T/m), d]; gates [m,d] fp32.  rope_pos0:
+    position of K[0] to give every entry partial RoPE at its last token, or
+    None."""
+    return _compress("csa_compress", K, V, G_K, G_K if G_V is None else G_V, m, Kc, Vc, stream,
+                     rope_pos0)
 
 
-def hca_compress(K, V, G_K, G_V=None, m: int = 128, Kc=None, Vc=None, stream=None):
-    """K, V [T,d] -> (Kc, Vc) [floor(T/m), d]; gates [m,d] fp32."""
-    return _compress("hca_compress", K, V, G_K, G_K if G_V is None else G_V, m, Kc, Vc, stream)
+def hca_compress(K, V, G_K, G_V=None, m: int = 128, Kc=None, Vc=None, stream=None,
+                 rope_pos0=None):
+    """K, V [T,d] -> (Kc, Vc) [floor(T/m), d]; gates [m,d] fp32 (rope_pos0 as
+    for csa_compress)."""
+    return _compress("hca_compress", K, V, G_K, G_K if G_V is None else G_V, m, Kc, Vc, stream,
+                     rope_pos0)
 
 
-def token_gated_compress(X, Z, m: int, Xc=None, stream=None):
+def rope_rotate(X, pos0: int, inverse: bool = False, stream=None):
+    """Partial RoPE, in place, of rows X[i] ([n, d] or [n, heads, d]) at
+    positions pos0 + i (inverse: rotate back).  Returns X."""
+    lib = load_library()
+    n, d = X.shape[0], X.shape[-1]
+    hv = int(np.prod(X.shape[1:-1])) if X.dim() > 2 else 1
+    st = lib.rope_rotate(_dev(X, "X"), n, hv, d, int(pos0), 1 if inverse else 0, _dtype_code(X),
+                         _stream(stream))
+    _check("rope_rotate", st)
+    return X
+
+
+def token_gated_compress(X, Z, m: int, Xc=None, stream=None, rope_pos0=None):
     """X [T, d] with per-token gate logits Z [T, d] fp32 -> Xc [floor(T/m), d].
     X may also be [T, H_I, d_I] (token-level indexer keys); Xc then has the
     same trailing shape."""
@@ -234,7 +264,8 @@ def token_gated_compress(X, Z, m: int, Xc=None, stream=None):
     if Xc.shape[0] < T // m:
         raise ValueError("output too small")
     st = lib.token_gated_compress(_dev(X, "X"), _dev(Z, "Z", torch.float32), T, d, m,
-                                  _dtype_code(X), _dev(Xc, "Xc", X.dtype), _stream(stream))
+                                  _dtype_code(X), _dev(Xc, "Xc", X.dtype), _rope_pos0(rope_pos0),
+                                  _stream(stream))
     _check("token_gated_compress", st)
     return Xc
 
@@ -300,9 +331,11 @@ def _sink_ptr(sink, Q) -> int:
 
 def sparse_mqa_attn(Q, Kc, Vc, topk, Kraw, Vraw, batch: DeviceBatch, m: int, W: int,
                     scale: float, O=None, lse: bool | torch.Tensor = True, dev_err=None,
-                    stream=None, sink=None):
+                    stream=None, sink=None, rope: bool = False):
     """CSA core attention.  Returns (O [total_q,H,d], lse [total_q,H] or None).
-    sink: per-head attention-sink logits [H] fp32 on the device, or None."""
+    sink: per-head attention-sink logits [H] fp32 on the device, or None.
+    rope: partial RoPE (Q rotated at t, O rotated back; Kc/Vc and the raw
+    window must hold rotated entries and tokens)."""
     lib = load_library()
     Nq, H, d = Q.shape
     if O is None:
@@ -318,7 +351,7 @@ def sparse_mqa_attn(Q, Kc, Vc, topk, Kraw, Vraw, batch: DeviceBatch, m: int, W: 
                              _dev(topk, "topk", torch.int32), topk.shape[1],
                              _dev(Kraw, "Kraw", Q.dtype), _dev(Vraw, "Vraw", Q.dtype),
                              ctypes.byref(cb), H, d, m, W, float(scale),
-                             _sink_ptr(sink, Q), _dtype_code(Q),
+                             _sink_ptr(sink, Q), 1 if rope else 0, _dtype_code(Q),
                              _dev(O, "O", Q.dtype), _dev(L, "lse", torch.float32), None, 0,
                              _dev(dev_err, "dev_err", torch.int32), _stream(stream))
     _check("sparse_mqa_attn", st)
@@ -327,9 +360,9 @@ def sparse_mqa_attn(Q, Kc, Vc, topk, Kraw, Vraw, batch: DeviceBatch, m: int, W: 
 
 def hca_dense_attn(Q, Kc, Vc, Kraw, Vraw, batch: DeviceBatch, m: int, W: int, scale: float,
                    O=None, lse: bool | torch.Tensor = True, dev_err=None, ws=None, stream=None,
-                   sink=None):
+                   sink=None, rope: bool = False):
     """HCA dense attention.  Returns (O [total_q,H,d], lse [total_q,H] or None).
-    sink: per-head attention-sink logits [H] fp32 on the device, or None."""
+    sink and rope: as for sparse_mqa_attn."""
     lib = load_library()
     Nq, H, d = Q.shape
     if O is None:
@@ -344,7 +377,7 @@ def hca_dense_attn(Q, Kc, Vc, Kraw, Vraw, batch: DeviceBatch, m: int, W: int, sc
     st = lib.hca_dense_attn(_dev(Q, "Q"), _dev(Kc, "Kc", Q.dtype), _dev(Vc, "Vc", Q.dtype),
                             _dev(Kraw, "Kraw", Q.dtype), _dev(Vraw, "Vraw", Q.dtype),
                             ctypes.byref(cb), H, d, m, W, float(scale),
-                            _sink_ptr(sink, Q), _dtype_code(Q),
+                            _sink_ptr(sink, Q), 1 if rope else 0, _dtype_code(Q),
                             _dev(O, "O", Q.dtype), _dev(L, "lse", torch.float32),
                             _dev(ws, "ws"), ws.numel() if ws is not None else 0,
                             _dev(dev_err, "dev_err", torch.int32), _stream(stream))

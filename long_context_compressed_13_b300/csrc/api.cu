@@ -10,9 +10,11 @@ namespace lc {
 
 lc_status compress_launch(const void *K, const void *V, const float *GK, const float *GV,
                           int64_t T_, int d, int m, lc_dtype dt, void *Kc, void *Vc,
-                          cudaStream_t st);
+                          int64_t rope_pos0, cudaStream_t st);
+lc_status rope_launch(void *X, int64_t n, int hv, int d, int64_t pos0, int inverse, lc_dtype dt,
+                      cudaStream_t st);
 lc_status compress_tok_launch(const void *X, const float *Z, int64_t T_, int d, int m,
-                              lc_dtype dt, void *Xc, cudaStream_t st);
+                              lc_dtype dt, void *Xc, int64_t rope_pos0, cudaStream_t st);
 lc_status index_launch(const void *qI, const float *w, const void *kI, const lc_batch &b, int HI,
                        int dI, int m, lc_dtype dt, float *scores, int64_t ld, int32_t *dev_err,
                        cudaStream_t st);
@@ -28,16 +30,16 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
 size_t index_tc_workspace(const lc_batch &b, int k);
 lc_status hca_tc_launch(const void *Q, const void *Kc, const void *Vc, const void *Kraw,
                         const void *Vraw, const lc_batch &b, int H, int d, int m, int W,
-                        float scale, const float *sink, lc_dtype dt, void *O, float *lse,
-                        int32_t *dev_err, cudaStream_t st);
+                        float scale, const float *sink, int rope, lc_dtype dt, void *O,
+                        float *lse, int32_t *dev_err, cudaStream_t st);
 lc_status sparse_tc_launch(const void *Q, const void *Kc, const void *Vc, const int32_t *topk,
                            int k, const void *Kraw, const void *Vraw, const lc_batch &b, int H,
-                           int d, int m, int W, float scale, const float *sink, lc_dtype dt,
-                           void *O, float *lse, int32_t *dev_err, cudaStream_t st);
+                           int d, int m, int W, float scale, const float *sink, int rope,
+                           lc_dtype dt, void *O, float *lse, int32_t *dev_err, cudaStream_t st);
 lc_status attn_simt_launch(bool sparse, const void *Q, const void *Kc, const void *Vc,
                            const int32_t *topk, int k, const void *Kraw, const void *Vraw,
                            const lc_batch &b, int H, int d, int m, int W, float scale,
-                           const float *sink, lc_dtype dt, void *O, float *lse,
+                           const float *sink, int rope, lc_dtype dt, void *O, float *lse,
                            int32_t *dev_err, cudaStream_t st);
 
 static std::atomic<uint64_t> g_launches{0};
@@ -113,12 +115,15 @@ static size_t index_ws_bytes(const lc_batch *b) {
 
 static lc_status compress_common(const void *K, const void *V, const float *G_K,
                                  const float *G_V, int64_t T, int32_t d, int32_t m,
-                                 lc_dtype dt, void *Kc, void *Vc, cudaStream_t st) {
-    if (T < 0 || m < 1 || !dtype_ok(dt) || !G_K || !G_V) return LC_ERR_INVALID_ARG;
+                                 lc_dtype dt, void *Kc, void *Vc, int64_t rope_pos0,
+                                 cudaStream_t st) {
+    if (T < 0 || m < 1 || !dtype_ok(dt) || !G_K || !G_V || rope_pos0 < -1)
+        return LC_ERR_INVALID_ARG;
     // with fewer than m tokens there is no entry to write: outputs may be empty
     if (T / m > 0 && (!K || !V || !Kc || !Vc)) return LC_ERR_INVALID_ARG;
     if ((d != 64 && d != 128) || m > 256) return LC_ERR_UNSUPPORTED;
-    return finish(compress_launch(K, V, G_K, G_V, T, d, m, dt, Kc, Vc, st), st, nullptr);
+    return finish(compress_launch(K, V, G_K, G_V, T, d, m, dt, Kc, Vc, rope_pos0, st), st,
+                  nullptr);
 }
 
 }  // namespace lc
@@ -129,23 +134,35 @@ extern "C" {
 
 lc_status csa_compress(const void *K, const void *V, const float *G_K, const float *G_V,
                        int64_t T, int32_t d, int32_t m, lc_dtype dtype, void *Kc, void *Vc,
-                       lc_stream stream) {
-    return compress_common(K, V, G_K, G_V, T, d, m, dtype, Kc, Vc, (cudaStream_t)stream);
+                       int64_t rope_pos0, lc_stream stream) {
+    return compress_common(K, V, G_K, G_V, T, d, m, dtype, Kc, Vc, rope_pos0,
+                           (cudaStream_t)stream);
 }
 
 lc_status hca_compress(const void *K, const void *V, const float *G_K, const float *G_V,
                        int64_t T, int32_t d, int32_t m, lc_dtype dtype, void *Kc, void *Vc,
-                       lc_stream stream) {
-    return compress_common(K, V, G_K, G_V, T, d, m, dtype, Kc, Vc, (cudaStream_t)stream);
+                       int64_t rope_pos0, lc_stream stream) {
+    return compress_common(K, V, G_K, G_V, T, d, m, dtype, Kc, Vc, rope_pos0,
+                           (cudaStream_t)stream);
+}
+
+lc_status rope_rotate(void *X, int64_t n, int32_t hv, int32_t d, int64_t pos0, int32_t inverse,
+                      lc_dtype dtype, lc_stream stream) {
+    cudaStream_t st = (cudaStream_t)stream;
+    if (n < 0 || hv < 1 || pos0 < 0 || !dtype_ok(dtype) || (n > 0 && !X))
+        return LC_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return LC_ERR_UNSUPPORTED;
+    return finish(rope_launch(X, n, hv, d, pos0, inverse, dtype, st), st, nullptr);
 }
 
 lc_status token_gated_compress(const void *X, const float *Z, int64_t T, int32_t d, int32_t m,
-                               lc_dtype dtype, void *Xc, lc_stream stream) {
+                               lc_dtype dtype, void *Xc, int64_t rope_pos0, lc_stream stream) {
     cudaStream_t st = (cudaStream_t)stream;
-    if (T < 0 || m < 1 || !dtype_ok(dtype)) return LC_ERR_INVALID_ARG;
+    if (T < 0 || m < 1 || !dtype_ok(dtype) || rope_pos0 < -1) return LC_ERR_INVALID_ARG;
     if (T / m > 0 && (!X || !Z || !Xc)) return LC_ERR_INVALID_ARG;
     if (d < 32 || d > 1024 || d % 32 || m > 4096) return LC_ERR_UNSUPPORTED;
-    return finish(compress_tok_launch(X, Z, T, d, m, dtype, Xc, st), st, nullptr);
+    if (rope_pos0 >= 0 && d < ROPE_DIMS) return LC_ERR_UNSUPPORTED;
+    return finish(compress_tok_launch(X, Z, T, d, m, dtype, Xc, rope_pos0, st), st, nullptr);
 }
 
 lc_status lightning_index(const void *qI, const float *w, const void *kI, const lc_batch *batch,
@@ -205,42 +222,44 @@ lc_status topk_select(const float *scores, int64_t ld, const lc_batch *batch, in
 lc_status sparse_mqa_attn(const void *Q, const void *Kc, const void *Vc, const int32_t *topk,
                           int32_t k, const void *Kraw, const void *Vraw, const lc_batch *batch,
                           int32_t H, int32_t d, int32_t m, int32_t W, float scale,
-                          const float *sink, lc_dtype dtype, void *O, float *lse, void *ws,
-                          size_t ws_bytes, int32_t *dev_err, lc_stream stream) {
+                          const float *sink, int32_t rope, lc_dtype dtype, void *O, float *lse,
+                          void *ws, size_t ws_bytes, int32_t *dev_err, lc_stream stream) {
     (void)ws;
     (void)ws_bytes;
     cudaStream_t st = (cudaStream_t)stream;
     if (!Q || !Kc || !Vc || !topk || !O || !batch_ok(batch) || k < 1 || m < 1 || W < 0 ||
-        !dtype_ok(dtype) || !(scale > 0.f) || (W > 0 && (!Kraw || !Vraw)))
+        !dtype_ok(dtype) || !(scale > 0.f) || (W > 0 && (!Kraw || !Vraw)) ||
+        (rope != 0 && rope != 1))
         return LC_ERR_INVALID_ARG;
     if ((d != 64 && d != 128) || H < 8 || H > 128 || H % 8 || W > 4096 || k > 4096)
         return LC_ERR_UNSUPPORTED;
     lc_status s = sparse_tc_launch(Q, Kc, Vc, topk, k, Kraw, Vraw, *batch, H, d, m, W, scale,
-                                   sink, dtype, O, lse, dev_err, st);
+                                   sink, rope, dtype, O, lse, dev_err, st);
     if (s == LC_ERR_UNSUPPORTED)
         s = attn_simt_launch(true, Q, Kc, Vc, topk, k, Kraw, Vraw, *batch, H, d, m, W, scale,
-                             sink, dtype, O, lse, dev_err, st);
+                             sink, rope, dtype, O, lse, dev_err, st);
     return finish(s, st, dev_err);
 }
 
 lc_status hca_dense_attn(const void *Q, const void *Kc, const void *Vc, const void *Kraw,
                          const void *Vraw, const lc_batch *batch, int32_t H, int32_t d,
-                         int32_t m, int32_t W, float scale, const float *sink, lc_dtype dtype,
-                         void *O, float *lse, void *ws, size_t ws_bytes, int32_t *dev_err,
-                         lc_stream stream) {
+                         int32_t m, int32_t W, float scale, const float *sink, int32_t rope,
+                         lc_dtype dtype, void *O, float *lse, void *ws, size_t ws_bytes,
+                         int32_t *dev_err, lc_stream stream) {
     (void)ws;
     (void)ws_bytes;
     cudaStream_t st = (cudaStream_t)stream;
     if (!Q || !O || !batch_ok(batch) || m < 1 || W < 0 || !dtype_ok(dtype) || !(scale > 0.f) ||
-        (batch->max_c > 0 && (!Kc || !Vc)) || (W > 0 && (!Kraw || !Vraw)))
+        (batch->max_c > 0 && (!Kc || !Vc)) || (W > 0 && (!Kraw || !Vraw)) ||
+        (rope != 0 && rope != 1))
         return LC_ERR_INVALID_ARG;
     if ((d != 64 && d != 128) || H < 8 || H > 128 || H % 8 || W > 4096)
         return LC_ERR_UNSUPPORTED;
-    lc_status s = hca_tc_launch(Q, Kc, Vc, Kraw, Vraw, *batch, H, d, m, W, scale, sink, dtype, O,
-                                lse, dev_err, st);
+    lc_status s = hca_tc_launch(Q, Kc, Vc, Kraw, Vraw, *batch, H, d, m, W, scale, sink, rope,
+                                dtype, O, lse, dev_err, st);
     if (s == LC_ERR_UNSUPPORTED)
         s = attn_simt_launch(false, Q, Kc, Vc, nullptr, 0, Kraw, Vraw, *batch, H, d, m, W, scale,
-                             sink, dtype, O, lse, dev_err, st);
+                             sink, rope, dtype, O, lse, dev_err, st);
     return finish(s, st, dev_err);
 }
 

@@ -40,7 +40,8 @@ constexpr uint32_t HS_Q = 0;                           // 2 tiles x 2 halves
 constexpr uint32_t HS_K = HS_Q + 4 * H_TILE;           // 2 stages x 2 halves
 constexpr uint32_t HS_V = HS_K + 4 * H_TILE;           // 2 stages x 2 halves
 constexpr uint32_t HS_BAR = HS_V + 4 * H_TILE;
-constexpr uint32_t HS_TOTAL = HS_BAR + 256;
+constexpr uint32_t HS_ROPE = HS_BAR + 256;            // RoPE: (cos, sin) [tokens][32]
+constexpr uint32_t HS_TOTAL = HS_ROPE + 32 * 32 * 8;
 constexpr uint32_t H_TMEM_COLS = 512;
 constexpr uint32_t HT_O = 0, HT_S = 256;               // + 128 * tile
 constexpr float H_LOG2E = 1.4426950408889634f;
@@ -49,6 +50,7 @@ constexpr float H_RESCALE = 8.f;
 struct HBars {
     uint64_t q_full, k_full[2], v_full[2], kv_empty[2], s_full[2], p_full[2], o_done[2];
     uint64_t stall;           // test hook: a barrier nothing completes
+    uint64_t q_ready;         // RoPE: the softmax warps rotated Q0 and Q1
     uint32_t taddr;
     int abort;
 };
@@ -99,6 +101,7 @@ struct HcaArgs {
     __nv_bfloat16 *O;
     float *lse;
     int32_t *dev_err;
+    int rope;             // partial RoPE: Q rotated at t, O rotated back at t
     long long stall;      // test hook (0: off): the MMA issuer first waits this
                           // many clocks on a barrier nothing completes
 };
@@ -134,6 +137,7 @@ __global__ void __launch_bounds__(H_THREADS, 1)
         bars.abort = (smem_u32(smem) & 1023u) != 0 ? 1 : 0;
         if (bars.abort) flag(a.dev_err, LC_DEVERR_TIMEOUT);  // layout assumption broken
         mbar_init(&bars.q_full, 1);
+        mbar_init(&bars.q_ready, 8);  // one arrival per softmax warp
         mbar_init(&bars.stall, 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars.k_full[s], 1);
@@ -225,7 +229,8 @@ __global__ void __launch_bounds__(H_THREADS, 1)
                 mma_commit(&bars.o_done[g]);
             };
             bool ok = (a.stall == 0 || mbar_wait(&bars.stall, 0, abort, a.stall)) &&
-                      mbar_wait(&bars.q_full, 0, abort) && mbar_wait(&bars.k_full[0], 0, abort);
+                      mbar_wait(a.rope ? &bars.q_ready : &bars.q_full, 0, abort) &&
+                      mbar_wait(&bars.k_full[0], 0, abort);
             if (ok) {
                 tc_fence_after();
                 issue_s(0, 0);
@@ -273,6 +278,22 @@ __global__ void __launch_bounds__(H_THREADS, 1)
         const float sl2 = a.scale_log2;
         float m_used = -INFINITY, l = 0.f;
         bool ok = !dead;
+        // RoPE: (cos, sin) of the angles of the CTA's tokens t_first .. t_last
+        const float2 *rope_tab = reinterpret_cast<const float2 *>(smem + HS_ROPE);
+        const float2 *my_cs = rope_tab + (t - t_first) * 32;
+        if (a.rope && ok && n_tiles > 0) {
+            // rotate the query rows in place before the first S MMA
+            if (!__all_sync(FULL, mbar_wait(&bars.q_full, 0, abort))) ok = false;
+            const int ntok = (int)(t_last - t_first + 1);
+            float2 *tab = reinterpret_cast<float2 *>(smem + HS_ROPE);
+            for (int u = tid; u < ntok * 32; u += 256)
+                tab[u] = rope_cs(t_first + u / 32, rope_theta(u % 32));
+            asm volatile("bar.sync 2, 256;" ::: "memory");
+            if (ok && row_ok) rope_smem_row(smem + HS_Q + (2 * g + 1) * H_TILE, r, my_cs);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.q_ready);
+        }
         for (int j = 0; ok && j < n_tiles; ++j) {
             if (!__all_sync(FULL, mbar_wait(&bars.s_full[g], j & 1, abort))) {
                 ok = false;
@@ -372,6 +393,7 @@ __global__ void __launch_bounds__(H_THREADS, 1)
 #pragma unroll
                     for (int u = 0; u < 32; ++u) o[u] = 0.f;
                 }
+                if (a.rope && n_tiles > 0 && c >= HHD - ROPE_DIMS) rope_out32(o, c, HHD, my_cs);
                 if (row_ok) {
 #pragma unroll
                     for (int u = 0; u < 32; u += 8) {
@@ -402,8 +424,8 @@ bool al16h(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; 
 // LC_ERR_UNSUPPORTED when the shape does not fit (the caller falls back).
 lc_status hca_tc_launch(const void *Q, const void *Kc, const void *Vc, const void *Kraw,
                         const void *Vraw, const lc_batch &b, int H, int d, int m, int W,
-                        float scale, const float *sink, lc_dtype dt, void *O, float *lse,
-                        int32_t *dev_err, cudaStream_t st) {
+                        float scale, const float *sink, int rope, lc_dtype dt, void *O,
+                        float *lse, int32_t *dev_err, cudaStream_t st) {
     if (dt != LC_BF16 || d != HHD || b.B != 1 || (HBM_ % H) != 0) return LC_ERR_UNSUPPORTED;
     if (!al16h(Q) || !al16h(O) || (Kc && !al16h(Kc)) || (Vc && !al16h(Vc)) ||
         (Kraw && !al16h(Kraw)) || (Vraw && !al16h(Vraw)))
@@ -439,6 +461,7 @@ lc_status hca_tc_launch(const void *Q, const void *Kc, const void *Vc, const voi
     a.O = reinterpret_cast<__nv_bfloat16 *>(O);
     a.lse = lse;
     a.dev_err = dev_err;
+    a.rope = rope;
     a.stall = debug_stall_clocks(LC_STALL_HCA_TC);
     static bool attr_done = false;
     if (!attr_done) {

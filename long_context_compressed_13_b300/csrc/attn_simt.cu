@@ -28,6 +28,7 @@ struct AttnArgs {
     void *O;
     float *lse;
     int32_t *dev_err;
+    int rope;           // partial RoPE: q rotated at t, O rotated back at t
 };
 
 template <typename T, int D, int HG, bool SPARSE>
@@ -42,6 +43,7 @@ __global__ void __launch_bounds__(AT) k_attn_simt(AttnArgs a, Batch bt) {
     float *sA = sL + HG;                    // [HG] rescale factor of this tile
     int64_t *sRow = reinterpret_cast<int64_t *>(sA + HG);  // [KT] source row, -1 masked
     int *sSrc = reinterpret_cast<int *>(sRow + KT);         // [KT] 0 compressed, 1 raw
+    float2 *sCS = reinterpret_cast<float2 *>(sSrc + KT);     // [32] RoPE (cos, sin) at t
 
     const int tid = threadIdx.x;
     const int64_t r = blockIdx.x;
@@ -68,6 +70,15 @@ __global__ void __launch_bounds__(AT) k_attn_simt(AttnArgs a, Batch bt) {
     if (tid < HG) {
         sM[tid] = -INFINITY;
         sL[tid] = 0.f;
+    }
+    if (a.rope) {
+        // partial RoPE of the row's query heads at position t (fp32, in place)
+        if (tid < 32) sCS[tid] = rope_cs(t, rope_theta(tid));
+        __syncthreads();
+        for (int u = tid; u < HG * 32; u += AT) {
+            float *q = sQ + (u >> 5) * D + (D - ROPE_DIMS) + 2 * (u & 31);
+            rope_pair(q[0], q[1], sCS[u & 31], false);
+        }
     }
 
     constexpr int NO = HG * D / AT;  // outputs per thread in P.V
@@ -185,7 +196,18 @@ __global__ void __launch_bounds__(AT) k_attn_simt(AttnArgs a, Batch bt) {
     for (int i = 0; i < NO; ++i) {
         const int h = oh + HSTEP * i;
         const float l = sL[h];
-        O[(r * a.H + h0 + h) * D + oc] = io<T>::from_f(l > 0.f ? acc[i] * sA[h] / l : 0.f);
+        float o = l > 0.f ? acc[i] * sA[h] / l : 0.f;
+        if (a.rope) {
+            // rotate the output back at t: channel pairs sit in adjacent lanes
+            const float other = __shfl_xor_sync(0xffffffffu, o, 1);
+            const int rc = oc - (D - ROPE_DIMS);
+            if (rc >= 0) {
+                float x = (rc & 1) ? other : o, y = (rc & 1) ? o : other;
+                rope_pair(x, y, sCS[rc >> 1], true);
+                o = (rc & 1) ? y : x;
+            }
+        }
+        O[(r * a.H + h0 + h) * D + oc] = io<T>::from_f(o);
     }
     if (a.lse && tid < HG) {
         const float l = sL[tid];
@@ -197,7 +219,7 @@ template <typename T, int D, int HG, bool SPARSE>
 static lc_status launch_hg(const AttnArgs &a, const lc_batch &b, cudaStream_t st) {
     const size_t smem = sizeof(float) * ((size_t)HG * D + KT * (D + 1) + KT * D + HG * (KT + 1) +
                                          3 * HG) +
-                        KT * (sizeof(int64_t) + sizeof(int));
+                        KT * (sizeof(int64_t) + sizeof(int)) + 32 * sizeof(float2);
     auto kfn = k_attn_simt<T, D, HG, SPARSE>;
     if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
@@ -228,9 +250,10 @@ static lc_status launch_attn(const AttnArgs &a, const lc_batch &b, int d, lc_dty
 lc_status attn_simt_launch(bool sparse, const void *Q, const void *Kc, const void *Vc,
                            const int32_t *topk, int k, const void *Kraw, const void *Vraw,
                            const lc_batch &b, int H, int d, int m, int W, float scale,
-                           const float *sink, lc_dtype dt, void *O, float *lse,
+                           const float *sink, int rope, lc_dtype dt, void *O, float *lse,
                            int32_t *dev_err, cudaStream_t st) {
-    AttnArgs a{Q, Kc, Vc, Kraw, Vraw, topk, sparse ? k : 0, H, m, W, scale, sink, O, lse, dev_err};
+    AttnArgs a{Q, Kc, Vc, Kraw, Vraw, topk, sparse ? k : 0, H, m, W, scale, sink, O, lse, dev_err,
+               rope};
     return sparse ? launch_attn<true>(a, b, d, dt, st) : launch_attn<false>(a, b, d, dt, st);
 }
 

@@ -44,7 +44,7 @@ constexpr uint32_t SS_Q = 0;                           // 2 halves
 constexpr uint32_t SS_K = SS_Q + 2 * S_TILE;           // S_NST stages x 2 halves
 constexpr uint32_t SS_V = SS_K + S_NST * 2 * S_TILE;   // S_NST stages x 2 halves
 constexpr uint32_t SS_BAR = SS_V + S_NST * 2 * S_TILE;
-constexpr uint32_t SS_TOTAL = SS_BAR + 256;
+constexpr uint32_t SS_TOTAL = SS_BAR + 512;
 constexpr uint32_t S_TMEM_COLS = 512;
 constexpr uint32_t ST_O = 0, ST_S = 128;               // + 128 * buffer
 constexpr float S_LOG2E = 1.4426950408889634f;
@@ -54,10 +54,13 @@ struct SBars {
     uint64_t q_full, k_full[S_NST], v_full[S_NST], kv_empty[S_NST], mask_full[S_NST];
     uint64_t s_full[2], p_full, o_done;
     uint64_t stall;           // test hook: a barrier nothing completes
+    uint64_t q_ready;         // RoPE: the softmax warps rotated Q
     uint32_t mask[S_NST][4];  // valid slots of the selected tile held by each stage
     uint32_t taddr;
     int abort;
+    float2 rope_cs[32];       // RoPE: (cos, sin) of the token's angles
 };
+static_assert(sizeof(SBars) <= 512, "barrier block");
 
 __device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
@@ -114,6 +117,7 @@ struct SparseArgs {
     __nv_bfloat16 *O;
     float *lse;
     int32_t *dev_err;
+    int rope;             // partial RoPE: Q rotated at t, O rotated back at t
     long long stall;      // test hook (0: off): the MMA issuer first waits this
                           // many clocks on a barrier nothing completes
 };
@@ -160,6 +164,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
         mbar_init(&bars.s_full[1], 1);
         mbar_init(&bars.p_full, 4);  // one arrival per softmax warp
         mbar_init(&bars.o_done, 1);
+        mbar_init(&bars.q_ready, 4);  // one arrival per softmax warp
         fence_barrier_init();
     }
     if (warp == 6) {
@@ -286,7 +291,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
                 return true;
             };
             bool ok = (a.stall == 0 || mbar_wait(&bars.stall, 0, abort, a.stall)) &&
-                      mbar_wait(&bars.q_full, 0, abort) && issue_s(0) &&
+                      mbar_wait(a.rope ? &bars.q_ready : &bars.q_full, 0, abort) && issue_s(0) &&
                       (n_tiles < 2 || issue_s(1));
             for (int j = 0; ok && j < n_tiles; ++j) {
                 const int s = j % S_NST;
@@ -325,6 +330,17 @@ __global__ void __launch_bounds__(S_THREADS, 1)
         // od = phases of o_done observed (PV(0..od-1) complete).  Phases are
         // waited one at a time and never fall two behind: before P(j) is
         // published PV(j) cannot have started, so at most PV(j-1) is pending.
+        if (a.rope && ok && n_tiles > 0) {
+            // partial RoPE of the token's query heads, in place, before the
+            // first S MMA: angles of position t, then each thread rotates its row
+            if (!__all_sync(FULL, mbar_wait(&bars.q_full, 0, abort))) ok = false;
+            if (tid < 32) bars.rope_cs[tid] = rope_cs(t, rope_theta(tid));
+            asm volatile("bar.sync 2, 128;" ::: "memory");
+            if (ok && row_ok) rope_smem_row(smem + SS_Q + S_TILE, tid, bars.rope_cs);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.q_ready);
+        }
         int od = 0;
         auto wait_pv = [&](int upto) -> bool {  // until PV(0..upto-1) complete
             while (od < upto) {
@@ -452,6 +468,8 @@ __global__ void __launch_bounds__(S_THREADS, 1)
 #pragma unroll
                     for (int u = 0; u < 32; ++u) o[u] = 0.f;
                 }
+                if (a.rope && n_tiles > 0 && c >= SHD - ROPE_DIMS)
+                    rope_out32(o, c, SHD, bars.rope_cs);
                 if (row_ok) {
 #pragma unroll
                     for (int u = 0; u < 32; u += 8) {
@@ -482,8 +500,8 @@ bool al16s(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; 
 // ragged batch (one CTA per query token).  LC_ERR_UNSUPPORTED otherwise.
 lc_status sparse_tc_launch(const void *Q, const void *Kc, const void *Vc, const int32_t *topk,
                            int k, const void *Kraw, const void *Vraw, const lc_batch &b, int H,
-                           int d, int m, int W, float scale, const float *sink, lc_dtype dt,
-                           void *O, float *lse, int32_t *dev_err, cudaStream_t st) {
+                           int d, int m, int W, float scale, const float *sink, int rope,
+                           lc_dtype dt, void *O, float *lse, int32_t *dev_err, cudaStream_t st) {
     if (dt != LC_BF16 || d != SHD || H > SBM || b.total_c < 1 || b.total_q > 0x7fffffff ||
         b.total_q * H >= 0x7fffffff || b.total_c >= 0x7fffffff || b.total_raw >= 0x7fffffff)
         return LC_ERR_UNSUPPORTED;
@@ -513,6 +531,7 @@ lc_status sparse_tc_launch(const void *Q, const void *Kc, const void *Vc, const 
     a.O = reinterpret_cast<__nv_bfloat16 *>(O);
     a.lse = lse;
     a.dev_err = dev_err;
+    a.rope = rope;
     a.stall = debug_stall_clocks(LC_STALL_SPARSE_TC);
     static bool attr_done = false;
     if (!attr_done) {

@@ -16,7 +16,7 @@ __global__ void __launch_bounds__(256) k_compress(const T *__restrict__ K, const
                                                   const float *__restrict__ GK,
                                                   const float *__restrict__ GV, int64_t Tc,
                                                   int d, int m, T *__restrict__ Kc,
-                                                  T *__restrict__ Vc) {
+                                                  T *__restrict__ Vc, int64_t rope_pos0) {
     extern __shared__ float wgt[];  // [m][d]
     const bool is_v = blockIdx.y != 0;
     const T *X = is_v ? V : K;
@@ -38,6 +38,8 @@ __global__ void __launch_bounds__(256) k_compress(const T *__restrict__ K, const
     for (int p = part; p < m; p += P) wgt[p * d + c] = expf(wgt[p * d + c] - mx) * inv;
     __syncthreads();
     const int64_t total = Tc * d;
+    // total is a multiple of 32 (d is), so every warp is either wholly inside
+    // or wholly past the end: the partner channel of a RoPE pair is one lane away
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
          e += (int64_t)gridDim.x * blockDim.x) {
         const int64_t j = e / d;
@@ -45,6 +47,7 @@ __global__ void __launch_bounds__(256) k_compress(const T *__restrict__ K, const
         const T *src = X + j * m * d + ch;
         float acc = 0.f;
         for (int p = 0; p < m; ++p) acc = fmaf(wgt[p * d + ch], io<T>::ld(src + (int64_t)p * d), acc);
+        if (rope_pos0 >= 0) acc = rope_entry(acc, ch, d, rope_pos0 + (j + 1) * m - 1);
         Xc[e] = io<T>::from_f(acc);
     }
 }
@@ -60,7 +63,7 @@ __global__ void __launch_bounds__(256) k_compress_long(const T *__restrict__ K,
                                                        const float *__restrict__ GK,
                                                        const float *__restrict__ GV, int64_t Tc,
                                                        int d, int m, T *__restrict__ Kc,
-                                                       T *__restrict__ Vc) {
+                                                       T *__restrict__ Vc, int64_t rope_pos0) {
     __shared__ float red[8][32];
     __shared__ float stat[2][32];
     const bool is_v = blockIdx.y != 0;
@@ -106,19 +109,21 @@ __global__ void __launch_bounds__(256) k_compress_long(const T *__restrict__ K,
     if (w == 0) {
         float v = 0.f;
         for (int u = 0; u < 8; ++u) v += red[u][lane];
+        if (rope_pos0 >= 0) v = rope_entry(v, c, d, rope_pos0 + (j + 1) * m - 1);
         Xc[j * d + c] = io<T>::from_f(v);
     }
 }
 
 template <typename T>
 static lc_status launch(const void *K, const void *V, const float *GK, const float *GV,
-                        int64_t T_, int d, int m, void *Kc, void *Vc, cudaStream_t st) {
+                        int64_t T_, int d, int m, void *Kc, void *Vc, int64_t rope_pos0,
+                        cudaStream_t st) {
     const int64_t Tc = T_ / m;
     if (Tc == 0) return LC_OK;
     if (m >= 32 && d % 32 == 0 && Tc * (d / 32) < (1ll << 31)) {
         auto kl = k_compress_long<T>;
         LC_LAUNCH_AS("k_compress_long", kl, dim3((unsigned)(Tc * (d / 32)), 2), dim3(256), 0, st, (const T *)K,
-                  (const T *)V, GK, GV, Tc, d, m, (T *)Kc, (T *)Vc);
+                  (const T *)V, GK, GV, Tc, d, m, (T *)Kc, (T *)Vc, rope_pos0);
         return check_launch();
     }
     const size_t smem = sizeof(float) * (size_t)m * d;
@@ -131,15 +136,15 @@ static lc_status launch(const void *K, const void *V, const float *GK, const flo
     if (blocks > 148 * 4) blocks = 148 * 4;
     auto kfn = k_compress<T>;
     LC_LAUNCH_AS("k_compress", kfn, dim3((unsigned)blocks, 2), dim3(256), smem, st, (const T *)K, (const T *)V,
-              GK, GV, Tc, d, m, (T *)Kc, (T *)Vc);
+              GK, GV, Tc, d, m, (T *)Kc, (T *)Vc, rope_pos0);
     return check_launch();
 }
 
 lc_status compress_launch(const void *K, const void *V, const float *GK, const float *GV,
                           int64_t T_, int d, int m, lc_dtype dt, void *Kc, void *Vc,
-                          cudaStream_t st) {
-    if (dt == LC_F32) return launch<float>(K, V, GK, GV, T_, d, m, Kc, Vc, st);
-    return launch<__nv_bfloat16>(K, V, GK, GV, T_, d, m, Kc, Vc, st);
+                          int64_t rope_pos0, cudaStream_t st) {
+    if (dt == LC_F32) return launch<float>(K, V, GK, GV, T_, d, m, Kc, Vc, rope_pos0, st);
+    return launch<__nv_bfloat16>(K, V, GK, GV, T_, d, m, Kc, Vc, rope_pos0, st);
 }
 
 }  // namespace lc

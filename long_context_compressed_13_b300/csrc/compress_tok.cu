@@ -18,7 +18,8 @@ namespace lc {
 template <typename T>
 __global__ void __launch_bounds__(256) k_compress_tok(const T *__restrict__ X,
                                                       const float *__restrict__ Z, int64_t Tc,
-                                                      int d, int m, T *__restrict__ Xc) {
+                                                      int d, int m, T *__restrict__ Xc,
+                                                      int64_t rope_pos0) {
     __shared__ float st_m[8][32], st_s[8][32], st_a[8][32];
     const int ngrp = d / 32;
     const int64_t j = blockIdx.x / ngrp;
@@ -55,23 +56,25 @@ __global__ void __launch_bounds__(256) k_compress_tok(const T *__restrict__ X,
             S = fmaf(st_s[u][lane], f, S);
             A = fmaf(st_a[u][lane], f, A);
         }
-        Xc[j * d + c] = io<T>::from_f(A / S);
+        float v = A / S;
+        if (rope_pos0 >= 0) v = rope_entry(v, c, d, rope_pos0 + (j + 1) * m - 1);
+        Xc[j * d + c] = io<T>::from_f(v);
     }
 }
 
 lc_status compress_tok_launch(const void *X, const float *Z, int64_t T_, int d, int m,
-                              lc_dtype dt, void *Xc, cudaStream_t st) {
+                              lc_dtype dt, void *Xc, int64_t rope_pos0, cudaStream_t st) {
     const int64_t Tc = T_ / m;
     if (Tc == 0) return LC_OK;
     const int64_t blocks = Tc * (d / 32);
     if (blocks >= (1ll << 31)) return LC_ERR_UNSUPPORTED;
     if (dt == LC_F32)
         LC_LAUNCH_AS("k_compress_tok", k_compress_tok<float>, dim3((unsigned)blocks), dim3(256), 0,
-                     st, (const float *)X, Z, Tc, d, m, (float *)Xc);
+                     st, (const float *)X, Z, Tc, d, m, (float *)Xc, rope_pos0);
     else
         LC_LAUNCH_AS("k_compress_tok", k_compress_tok<__nv_bfloat16>, dim3((unsigned)blocks),
                      dim3(256), 0, st, (const __nv_bfloat16 *)X, Z, Tc, d, m,
-                     (__nv_bfloat16 *)Xc);
+                     (__nv_bfloat16 *)Xc, rope_pos0);
     return check_launch();
 }
 

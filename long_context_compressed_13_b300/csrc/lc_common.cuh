@@ -82,6 +82,84 @@ __device__ __forceinline__ uint32_t order_key(float s) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// ---------------------------------------------------------------- partial RoPE
+// RoPE on the last 64 dimensions of a head vector (page "DeepSeek-V4 技术解析…",
+// §1.1, engineering details): 32 interleaved pairs (2i, 2i+1) rotated by the
+// angle p * theta_i, theta_i = 10000^(-i/32).  Positions reach 2^20 and more,
+// so the angle is formed and reduced modulo 2 pi in fp64 before the fp32
+// sine and cosine.
+constexpr int ROPE_DIMS = 64;
+
+__device__ __forceinline__ double rope_theta(int i) {
+    return exp2(-(double)i * 0.41524101186092029);  // log2(10000) / 32
+}
+
+// (cos, sin) of p * theta.
+__device__ __forceinline__ float2 rope_cs(int64_t p, double theta) {
+    const double a = (double)p * theta;
+    const double k = rint(a * 0.15915494309189535);  // 1 / (2 pi)
+    double r = fma(-k, 6.283185307179586, a);       // 2 pi, high part
+    r = fma(-k, 2.4492935982947064e-16, r);         // 2 pi, low part
+    float sn, cs;
+    sincosf((float)r, &sn, &cs);
+    return make_float2(cs, sn);
+}
+
+// Rotates the pair (x, y) by the angle whose (cos, sin) is cs; inverse
+// rotates by minus that angle.
+__device__ __forceinline__ void rope_pair(float &x, float &y, float2 cs, bool inverse) {
+    const float sn = inverse ? -cs.y : cs.y;
+    const float nx = x * cs.x - y * sn;
+    const float ny = x * sn + y * cs.x;
+    x = nx;
+    y = ny;
+}
+
+// Partial RoPE of one bf16 row of 64 rotary values held in shared memory in
+// the 128-byte-swizzled operand layout (16-byte chunk c of row r at chunk
+// position c ^ (r & 7)): row r starts at `half`, cs[i] holds the (cos, sin)
+// of pair i.  Rounds each rotated value to bf16 once.
+__device__ __forceinline__ void rope_smem_row(uint8_t *half, int r, const float2 *cs) {
+    uint8_t *row = half + (size_t)r * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        uint4 *p = reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4));
+        uint4 v = *p;
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&w[u]);
+            float x = __low2float(h), y = __high2float(h);
+            rope_pair(x, y, cs[4 * c + u], false);
+            h = __floats2bfloat162_rn(x, y);
+            w[u] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        *p = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// Inverse partial RoPE of 32 consecutive output columns c0 .. c0+31 of one row
+// (c0 a multiple of 32 at or past d - 64), cs as above.
+__device__ __forceinline__ void rope_out32(float (&o)[32], int c0, int d, const float2 *cs) {
+    const int i0 = (c0 - (d - ROPE_DIMS)) >> 1;
+#pragma unroll
+    for (int u = 0; u < 32; u += 2) rope_pair(o[u], o[u + 1], cs[i0 + u / 2], true);
+}
+
+// Partial RoPE of one channel of a compressed entry at position p, inside a
+// warp whose lanes hold consecutive channels (even channel in an even lane):
+// channels d-64 .. d-1 form the pairs; the partner's value comes by shuffle.
+// Every lane of the warp calls it.
+__device__ __forceinline__ float rope_entry(float v, int ch, int d, int64_t p) {
+    const float other = __shfl_xor_sync(0xffffffffu, v, 1);
+    const int rc = ch - (d - ROPE_DIMS);
+    if (rc < 0) return v;
+    const float2 cs = rope_cs(p, rope_theta(rc >> 1));
+    float x = (rc & 1) ? other : v, y = (rc & 1) ? v : other;
+    rope_pair(x, y, cs, false);
+    return (rc & 1) ? y : x;
+}
+
 // The sink logit of head h in log2 units, -inf for no sink (sink NULL or
 // -inf).  A NaN or +inf sink is not a usable logit: it is flagged as
 // LC_DEVERR_SINK and the head is treated as having no sink.

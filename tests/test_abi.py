@@ -72,13 +72,13 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     N = None
     b = _batch()
     # compressors: null pointers, bad sizes, unsupported d
-    assert lib.csa_compress(N, P, P, P, 16, 64, 4, lc.LC_F32, P, P, N) == lc.LC_ERR_INVALID_ARG
-    assert lib.csa_compress(P, P, N, P, 16, 64, 4, lc.LC_F32, P, P, N) == lc.LC_ERR_INVALID_ARG
-    assert lib.csa_compress(P, P, P, P, 16, 64, 4, lc.LC_F32, N, P, N) == lc.LC_ERR_INVALID_ARG
-    assert lib.csa_compress(P, P, P, P, -1, 64, 4, lc.LC_F32, P, P, N) == lc.LC_ERR_INVALID_ARG
-    assert lib.hca_compress(P, P, P, P, 16, 64, 0, lc.LC_F32, P, P, N) == lc.LC_ERR_INVALID_ARG
-    assert lib.csa_compress(P, P, P, P, 16, 96, 4, lc.LC_F32, P, P, N) == lc.LC_ERR_UNSUPPORTED
-    assert lib.csa_compress(P, P, P, P, 16, 64, 4, 7, P, P, N) == lc.LC_ERR_INVALID_ARG
+    assert lib.csa_compress(N, P, P, P, 16, 64, 4, lc.LC_F32, P, P, -1, N) == lc.LC_ERR_INVALID_ARG
+    assert lib.csa_compress(P, P, N, P, 16, 64, 4, lc.LC_F32, P, P, -1, N) == lc.LC_ERR_INVALID_ARG
+    assert lib.csa_compress(P, P, P, P, 16, 64, 4, lc.LC_F32, N, P, -1, N) == lc.LC_ERR_INVALID_ARG
+    assert lib.csa_compress(P, P, P, P, -1, 64, 4, lc.LC_F32, P, P, -1, N) == lc.LC_ERR_INVALID_ARG
+    assert lib.hca_compress(P, P, P, P, 16, 64, 0, lc.LC_F32, P, P, -1, N) == lc.LC_ERR_INVALID_ARG
+    assert lib.csa_compress(P, P, P, P, 16, 96, 4, lc.LC_F32, P, P, -1, N) == lc.LC_ERR_UNSUPPORTED
+    assert lib.csa_compress(P, P, P, P, 16, 64, 4, 7, P, P, -1, N) == lc.LC_ERR_INVALID_ARG
     # indexer: no output requested, missing batch arrays, bad head shape,
     # ld smaller than the widest sequence, missing workspace
     assert lib.lightning_index(P, P, P, ctypes.byref(b), 8, 64, 4, lc.LC_BF16, N, 0, 0, N, N, 0,
@@ -101,18 +101,26 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     # attention: unsupported heads/dims, negative window, missing raw cache
     args = dict(scale=ctypes.c_float(0.125))
     assert lib.sparse_mqa_attn(P, P, P, P, 8, P, P, ctypes.byref(b), 12, 128, 4, 128,
-                               args["scale"], N, lc.LC_BF16, P, N, N, 0, N, N) == lc.LC_ERR_UNSUPPORTED
+                               args["scale"], N, 0, lc.LC_BF16, P, N, N, 0, N, N) == lc.LC_ERR_UNSUPPORTED
     assert lib.sparse_mqa_attn(P, P, P, P, 8, P, P, ctypes.byref(b), 64, 80, 4, 128,
-                               args["scale"], N, lc.LC_BF16, P, N, N, 0, N, N) == lc.LC_ERR_UNSUPPORTED
+                               args["scale"], N, 0, lc.LC_BF16, P, N, N, 0, N, N) == lc.LC_ERR_UNSUPPORTED
     assert lib.sparse_mqa_attn(P, P, P, P, 8, P, P, ctypes.byref(b), 64, 128, 4, -1,
-                               args["scale"], N, lc.LC_BF16, P, N, N, 0, N, N) == lc.LC_ERR_INVALID_ARG
+                               args["scale"], N, 0, lc.LC_BF16, P, N, N, 0, N, N) == lc.LC_ERR_INVALID_ARG
     assert lib.sparse_mqa_attn(P, P, P, P, 8, N, N, ctypes.byref(b), 64, 128, 4, 16,
-                               args["scale"], N, lc.LC_BF16, P, N, N, 0, N, N) == lc.LC_ERR_INVALID_ARG
+                               args["scale"], N, 0, lc.LC_BF16, P, N, N, 0, N, N) == lc.LC_ERR_INVALID_ARG
     assert lib.hca_dense_attn(P, P, P, P, P, ctypes.byref(b), 64, 128, 128, 128,
-                              ctypes.c_float(0.0), N, lc.LC_BF16, P, N, N, 0,
+                              ctypes.c_float(0.0), N, 0, lc.LC_BF16, P, N, N, 0,
                               N, N) == lc.LC_ERR_INVALID_ARG
     assert lib.hca_dense_attn(N, P, P, P, P, ctypes.byref(b), 64, 128, 128, 128,
-                              args["scale"], N, lc.LC_BF16, P, N, N, 0, N, N) == lc.LC_ERR_INVALID_ARG
+                              args["scale"], N, 0, lc.LC_BF16, P, N, N, 0, N, N) == lc.LC_ERR_INVALID_ARG
+    # RoPE arguments: a negative position other than -1, a rope flag other than 0/1
+    assert lib.csa_compress(P, P, P, P, 16, 64, 4, lc.LC_F32, P, P, -2, N) == lc.LC_ERR_INVALID_ARG
+    assert lib.rope_rotate(P, 4, 1, 128, -1, 0, lc.LC_BF16, N) == lc.LC_ERR_INVALID_ARG
+    assert lib.rope_rotate(P, 4, 1, 96, 0, 0, lc.LC_BF16, N) == lc.LC_ERR_UNSUPPORTED
+    assert lib.hca_dense_attn(P, P, P, P, P, ctypes.byref(b), 64, 128, 128, 128,
+                              args["scale"], N, 2, lc.LC_BF16, P, N, N, 0, N,
+                              N) == lc.LC_ERR_INVALID_ARG
+    assert lib.token_gated_compress(P, P, 16, 48, 4, lc.LC_F32, P, -1, N) == lc.LC_ERR_UNSUPPORTED
     # nothing above reached a kernel
     assert lib.lc_launch_count() == launches_before
 
