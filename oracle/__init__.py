@@ -202,28 +202,42 @@ def sparse_attn(Q, Kc, Vc, idx, Kraw, Vraw, raw_pos0: int, tpos, W: int, scale: 
     return O, lse
 
 
+def _as_operand(X, operand_dtype):
+    """The rotated operand as the method stores it: exact (None) or rounded to
+    bf16 (round to nearest even) in the bf16 setting."""
+    if operand_dtype is None:
+        return X
+    import torch
+    assert operand_dtype == "bf16"
+    return torch.from_numpy(np.ascontiguousarray(X)).to(torch.bfloat16).double().numpy()
+
+
 def sparse_attn_rope(Q, Kc, Vc, idx, Kraw, Vraw, raw_pos0: int, tpos, W: int, scale: float,
-                     m: int, sink=None):
+                     m: int, sink=None, operand_dtype=None):
     """CSA attention with partial RoPE, from unrotated inputs, in the order the
     reading fixes: each compressed entry rotated at the position of its last
     token ((j+1) m - 1), each window token at its own position, each query at
-    t; attention; the output rotated back at t.  Returns (O, lse)."""
+    t; attention; the output rotated back at t.  operand_dtype "bf16": the
+    rotated q, k and v are bf16 values (the operands of the bf16 setting).
+    Returns (O, lse)."""
     Kc, Vc, Kraw, Vraw = _f64(Kc), _f64(Vc), _f64(Kraw), _f64(Vraw)
     ep = entry_positions(0, Kc.shape[0], m)
     rp = raw_pos0 + np.arange(Kraw.shape[0], dtype=np.int64)
-    O, lse = sparse_attn(rope(Q, tpos), rope(Kc, ep), rope(Vc, ep), idx, rope(Kraw, rp),
-                         rope(Vraw, rp), raw_pos0, tpos, W, scale, sink)
+    op = lambda X, pos: _as_operand(rope(X, pos), operand_dtype)
+    O, lse = sparse_attn(op(Q, tpos), op(Kc, ep), op(Vc, ep), idx, op(Kraw, rp), op(Vraw, rp),
+                         raw_pos0, tpos, W, scale, sink)
     return rope(O, tpos, inverse=True), lse
 
 
 def hca_attn_rope(Q, Kc, Vc, m: int, Kraw, Vraw, raw_pos0: int, tpos, W: int, scale: float,
-                  sink=None):
+                  sink=None, operand_dtype=None):
     """HCA attention with partial RoPE, as sparse_attn_rope."""
     Kc, Vc, Kraw, Vraw = _f64(Kc), _f64(Vc), _f64(Kraw), _f64(Vraw)
     ep = entry_positions(0, Kc.shape[0], m)
     rp = raw_pos0 + np.arange(Kraw.shape[0], dtype=np.int64)
-    O, lse = hca_attn(rope(Q, tpos), rope(Kc, ep), rope(Vc, ep), m, rope(Kraw, rp),
-                      rope(Vraw, rp), raw_pos0, tpos, W, scale, sink)
+    op = lambda X, pos: _as_operand(rope(X, pos), operand_dtype)
+    O, lse = hca_attn(op(Q, tpos), op(Kc, ep), op(Vc, ep), m, op(Kraw, rp), op(Vraw, rp),
+                      raw_pos0, tpos, W, scale, sink)
     return rope(O, tpos, inverse=True), lse
 
 

@@ -5,8 +5,9 @@ output) against the CPU oracle.
 The GPU pipeline starts from unrotated tokens like the oracle's: the
 compressors rotate each entry at its last token's position (rope_pos0), the
 window cache is rotated with rope_rotate, and the attention kernels rotate Q
-at t and the output back at t.  Bars: rotated rows fp32 within 1e-5 and bf16
-within one ulp of the fp64 rotation; attention fp32 1e-4 and bf16 2e-2."""
+at t and the output back at t.  Bars: rotated rows as `close` states;
+attention fp32 1e-4 and bf16 2e-2, where in the bf16 setting the oracle's
+rotated q, k and v are bf16 values (the operands the method multiplies)."""
 import numpy as np
 import pytest
 import torch
@@ -33,13 +34,19 @@ def f64(x):
     return x.detach().to("cpu").double().numpy()
 
 
-def close(got, ref, dtype, what):
+def close(got, ref, dtype, what, unrot):
+    """Rotated values: fp32 within 1e-5; bf16 within one bf16 ulp of the exact
+    rotation plus an absolute 1e-5 x the pair's magnitude (the fp32 rotation
+    before the rounding cancels where the result is small, and the angle at
+    positions near 5e9 carries about 1e-6 rad)."""
     g = f64(got)
+    u = np.abs(np.asarray(unrot, dtype=np.float64))
+    pair = np.maximum(u, u.reshape(*u.shape[:-1], -1, 2)[..., ::-1].reshape(u.shape))
     if dtype == "f32":
-        np.testing.assert_allclose(g, ref, rtol=0, atol=1e-5, err_msg=what)
+        bad = np.abs(g - ref) > 1e-5 * np.maximum(pair, 1.0)
     else:
-        bad = np.abs(g - ref) > np.abs(ref) * 2.0 ** -7 + 1e-30
-        assert not bad.any(), f"{what}: {bad.sum()} values off by more than one bf16 ulp"
+        bad = np.abs(g - ref) > np.abs(ref) * 2.0 ** -7 + 1e-5 * pair + 1e-30
+    assert not bad.any(), f"{what}: {bad.sum()} values outside the bound"
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -52,11 +59,11 @@ def test_rope_rotate(lc, dtype, shape, pos0):
     Y = lc.rope_rotate(X.cuda(), pos0)
     torch.cuda.synchronize()
     assert lc.last_kernel() == "k_rope_rows"
-    close(Y, oracle.rope(X, pos), dtype, "rotate")
+    close(Y, oracle.rope(X, pos), dtype, "rotate", f64(X))
     # and back
     Z = lc.rope_rotate(Y.clone(), pos0, inverse=True)
     torch.cuda.synchronize()
-    close(Z, oracle.rope(f64(Y), pos, inverse=True), dtype, "rotate back")
+    close(Z, oracle.rope(f64(Y), pos, inverse=True), dtype, "rotate back", f64(Y))
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -71,14 +78,16 @@ def test_compress_with_rope(lc, dtype, kind, m, T, d, pos0):
         Z = wl.normal(g, (T, d), "f32", "cpu") * 2
         got = lc.token_gated_compress(K.cuda(), Z.cuda(), m, rope_pos0=pos0)
         torch.cuda.synchronize()
-        close(got, oracle.rope(oracle.compress_tok(K, Z, m), ep), dtype, "token-gated entries")
+        ent = oracle.compress_tok(K, Z, m)
+        close(got, oracle.rope(ent, ep), dtype, "token-gated entries", ent)
         return
     G = wl.normal(g, (m, d), "f32", "cpu")
     fn = lc.csa_compress if kind == "csa" else lc.hca_compress
     Kc, Vc = fn(K.cuda(), V.cuda(), G.cuda(), m=m, rope_pos0=pos0)
     torch.cuda.synchronize()
-    close(Kc, oracle.rope(oracle.compress(K, G, m), ep), dtype, "K entries")
-    close(Vc, oracle.rope(oracle.compress(V, G, m), ep), dtype, "V entries")
+    eK, eV = oracle.compress(K, G, m), oracle.compress(V, G, m)
+    close(Kc, oracle.rope(eK, ep), dtype, "K entries", eK)
+    close(Vc, oracle.rope(eV, ep), dtype, "V entries", eV)
 
 
 def _rotated_caches(lc, L, m, dev):
@@ -113,8 +122,9 @@ def test_sparse_attn_with_rope(lc, dtype, H, d, k, W, T, q_from):
     want = "k_sparse_tc" if dtype == "bf16" else "k_attn_simt"
     assert lc.last_kernel() == want
     rKc, rVc = oracle.compress(L["K"], L["G"], m), oracle.compress(L["V"], L["G"], m)
+    op = "bf16" if dtype == "bf16" else None
     rO, rl = oracle.sparse_attn_rope(L["Q"], rKc, rVc, sel, L["K"], L["V"], 0, tpos, W,
-                                     L["scale"], m)
+                                     L["scale"], m, operand_dtype=op)
     np.testing.assert_allclose(f64(O), rO, rtol=0, atol=TOL[dtype])
     fin = np.isfinite(rl)
     np.testing.assert_allclose(f64(lse)[fin], rl[fin], rtol=0, atol=TOL[dtype])
@@ -137,7 +147,9 @@ def test_hca_attn_with_rope(lc, dtype, H, d, m, W, T, q_from):
     want = "k_hca_tc" if dtype == "bf16" else "k_attn_simt"
     assert lc.last_kernel() == want
     rKc, rVc = oracle.compress(L["K"], L["G"], m), oracle.compress(L["V"], L["G"], m)
-    rO, rl = oracle.hca_attn_rope(L["Q"], rKc, rVc, m, L["K"], L["V"], 0, tpos, W, L["scale"])
+    op = "bf16" if dtype == "bf16" else None
+    rO, rl = oracle.hca_attn_rope(L["Q"], rKc, rVc, m, L["K"], L["V"], 0, tpos, W, L["scale"],
+                                  operand_dtype=op)
     np.testing.assert_allclose(f64(O), rO, rtol=0, atol=TOL[dtype])
     fin = np.isfinite(rl)
     np.testing.assert_allclose(f64(lse)[fin], rl[fin], rtol=0, atol=TOL[dtype])
@@ -164,5 +176,5 @@ def test_hca_with_rope_at_a_million_positions(lc):
     rKc = oracle.compress(L["K"], L["G"], m)
     rVc = oracle.compress(L["V"], L["G"], m)
     rO, _ = oracle.hca_attn_rope(L["Q"][rows], rKc, rVc, m, L["K"][lo:], L["V"][lo:], lo, tpos,
-                                 W, L["scale"])
+                                 W, L["scale"], operand_dtype="bf16")
     np.testing.assert_allclose(f64(O)[rows], rO, rtol=0, atol=TOL["bf16"])
