@@ -106,7 +106,10 @@ struct HcaArgs {
                           // many clocks on a barrier nothing completes
 };
 
-__global__ void __launch_bounds__(H_THREADS, 1)
+static_assert(H_THREADS * 200 <= 65536, "register budget of one CTA per SM");
+// at most 200 registers a thread (320 threads: 64,000 of 65,536); under
+// __launch_bounds__(H_THREADS, 1) ptxas settles on 168 and spills
+__global__ void __maxnreg__(200)
     k_hca_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKc,
              const __grid_constant__ CUtensorMap mVc, const __grid_constant__ CUtensorMap mKr,
              const __grid_constant__ CUtensorMap mVr, HcaArgs a) {

@@ -8,18 +8,21 @@
 // 256-byte row, written straight into the 128-byte-swizzled operand layout;
 // a TMA gather moves only 4 rows per instruction and is far slower), then its
 // raw window positions as TMA boxes.
-//   warps 4-5    producers: Q once, then K and V tiles into a 3-stage ring;
-//                for a selected tile each warp looks up 64 of the slots' rows,
-//                publishes its half of the tile's 128-bit slot validity mask
-//                and gathers those rows; each producer thread's copies
-//                complete on the stage barrier
-//   warp 6       TMEM owner and MMA issuer, in the order
+//   warps 4-7    producers: Q once, then K and V tiles into a 3-stage ring;
+//                for a selected tile each warp looks up 32 of the slots' rows,
+//                publishes its quarter of the tile's 128-bit slot validity
+//                mask and gathers those rows (four warps keep more copies in
+//                flight than two: the gather's issue rate bounds the kernel);
+//                each producer thread's copies complete on the stage barrier
+//   warp 8       TMEM owner and MMA issuer, in the order
 //                  S(0), S(1), PV(0), S(2), PV(1), S(3), ...
 //                S (M=128, N=128, K=128) alternates between two TMEM buffers,
 //                so the next tile's scores are ready while the softmax works;
 //                the softmax writes P (bf16) over the S it read, and PV
 //                (M=128, N=128, K=128) reads it as its A operand
-//   warps 0-3    softmax: thread r owns row r (TMEM lane r); the whole row of
+//   warps 0-3    softmax: thread r owns row r (TMEM lane r); with RoPE they
+//                first rotate the token's query rows in shared memory; the
+//                whole row of
 //                S is read with four loads and one wait; the reference max
 //                only moves when the max grows by more than 2^8 (then O and l
 //                are rescaled after PV(j-1) has completed); p = 2^(s*scale*
@@ -36,8 +39,11 @@ using namespace sm100;
 
 namespace {
 constexpr int SBM = 128, SBN = 128, SHD = 128;
-constexpr int S_THREADS = 224;                         // 4 softmax, 2 producer, 1 MMA warps
-constexpr int NPROD = 64;                              // producer threads
+constexpr int NPW = 4;                                 // producer warps
+constexpr int W_MMA_S = 4 + NPW;                       // MMA issuer warp
+constexpr int S_THREADS = 32 * (5 + NPW);              // 4 softmax, NPW producer, 1 MMA warps
+constexpr int NPROD = 32 * NPW;                        // producer threads
+constexpr int SPT = 128 / NPROD;                       // slots of a tile per producer thread
 constexpr int S_NST = 3;                               // K/V stages
 constexpr uint32_t S_TILE = SBN * 128;                 // one 64-column half of a 128-row tile
 constexpr uint32_t SS_Q = 0;                           // 2 halves
@@ -122,7 +128,10 @@ struct SparseArgs {
                           // many clocks on a barrier nothing completes
 };
 
-__global__ void __launch_bounds__(S_THREADS, 1)
+static_assert(S_THREADS * 200 <= 65536, "register budget of one CTA per SM");
+// at most 200 registers a thread (288 threads: 57,600 of 65,536); under
+// __launch_bounds__(S_THREADS, 1) ptxas settles on 168 and spills
+__global__ void __maxnreg__(200)
     k_sparse_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKr,
                 const __grid_constant__ CUtensorMap mVr, SparseArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -158,7 +167,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
             mbar_init(&bars.k_full[s], NPROD);  // one arrival per producer thread
             mbar_init(&bars.v_full[s], NPROD);
             mbar_init(&bars.kv_empty[s], 1);
-            mbar_init(&bars.mask_full[s], 2);   // one per producer warp
+            mbar_init(&bars.mask_full[s], NPW);  // one per producer warp
         }
         mbar_init(&bars.s_full[0], 1);
         mbar_init(&bars.s_full[1], 1);
@@ -167,7 +176,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
         mbar_init(&bars.q_ready, 4);  // one arrival per softmax warp
         fence_barrier_init();
     }
-    if (warp == 6) {
+    if (warp == W_MMA_S) {
         tmem_alloc(&bars.taddr, S_TMEM_COLS);
         tmem_relinquish();
     }
@@ -177,9 +186,9 @@ __global__ void __launch_bounds__(S_THREADS, 1)
     const uint32_t taddr = bars.taddr;
     const bool dead = bars.abort != 0;
 
-    if (warp == 4 || warp == 5) {
+    if (warp >= 4 && warp < 4 + NPW) {
         // ------------------------------------------------------ producer warps
-        const int pt = tid - 128;  // producer thread 0..63
+        const int pt = tid - 128;  // producer thread 0 .. NPROD-1
         if (!dead && n_tiles > 0) {
             if (pt == 0) {
                 prefetch_tmap(&mQ);
@@ -189,23 +198,25 @@ __global__ void __launch_bounds__(S_THREADS, 1)
             }
             const char *kc_base = reinterpret_cast<const char *>(a.Kc) + (lane & 15) * 16;
             const char *vc_base = reinterpret_cast<const char *>(a.Vc) + (lane & 15) * 16;
-            // the selected entries of this warp's slots 64u + 32(warp-4) + lane
-            // (u < 2) of a tile; the next tile's are loaded while the current
+            // the selected entries of this warp's slots NPROD u + 32(warp-4) + lane
+            // (u < SPT) of a tile; the next tile's are loaded while the current
             // tile is gathered
             const int32_t *sel_row = a.topk + qrow * a.k;
-            auto load_sel = [&](int i, int32_t (&jj)[2]) {
+            auto load_sel = [&](int i, int32_t (&jj)[SPT]) {
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int slot = i * SBN + 64 * u + pt;
+                for (int u = 0; u < SPT; ++u) {
+                    const int slot = i * SBN + NPROD * u + pt;
                     jj[u] = (i < nct && slot < a.k) ? __ldg(sel_row + slot) : -1;
                 }
             };
-            int32_t jn[2];
+            int32_t jn[SPT];
             load_sel(0, jn);
             int issued = 0;
             for (int i = 0; i < n_tiles; ++i) {
                 const int s = i % S_NST;
-                int32_t jc[2] = {jn[0], jn[1]};
+                int32_t jc[SPT];
+#pragma unroll
+                for (int u = 0; u < SPT; ++u) jc[u] = jn[u];
                 load_sel(i + 1, jn);
                 if (i >= S_NST &&
                     !__all_sync(FULL, mbar_wait(&bars.kv_empty[s], ((i - S_NST) / S_NST) & 1, abort)))
@@ -214,16 +225,16 @@ __global__ void __launch_bounds__(S_THREADS, 1)
                 if (i < nct) {
                     // rows of this warp's slots, gathered by this warp, the
                     // indices passed by shuffles
-                    int32_t g[2];
+                    int32_t g[SPT];
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
+                    for (int u = 0; u < SPT; ++u) {
                         const int64_t j = jc[u];
                         const bool ok = j >= 0 && j < nv;
                         if (j >= nv) flag(a.dev_err, LC_DEVERR_INDEX);
                         // an empty or invalid slot fetches row 0, which always exists
                         g[u] = ok ? (int32_t)(c_beg + j) : 0;
                         const uint32_t bal = __ballot_sync(FULL, ok);
-                        if (lane == 0) bars.mask[s][2 * u + (warp - 4)] = bal;
+                        if (lane == 0) bars.mask[s][NPW * u + (warp - 4)] = bal;
                     }
                     if (lane == 0) mbar_arrive(&bars.mask_full[s]);
                     // gather: per pass two rows, 16 lanes x 16 bytes each, into the
@@ -231,10 +242,14 @@ __global__ void __launch_bounds__(S_THREADS, 1)
                     const int hw = lane >> 4, chunk = lane & 15, hf = chunk >> 3, cc = chunk & 7;
                     const uint32_t kdst = smem_u32(kd) + hf * S_TILE, vdst = smem_u32(vd) + hf * S_TILE;
 #pragma unroll 8
-                    for (int pass = 0; pass < 32; ++pass) {
-                        const int q = 2 * pass + hw, u = pass >> 4, l = q & 31;
-                        const int64_t gi = __shfl_sync(FULL, u ? g[1] : g[0], l);
-                        const int r = 64 * u + 32 * (warp - 4) + l;
+                    for (int pass = 0; pass < 16 * SPT; ++pass) {
+                        const int q = 2 * pass + hw, u = q >> 5, l = q & 31;
+                        int32_t gu = g[0];
+#pragma unroll
+                        for (int v = 1; v < SPT; ++v)
+                            if (u == v) gu = g[v];
+                        const int64_t gi = __shfl_sync(FULL, gu, l);
+                        const int r = NPROD * u + 32 * (warp - 4) + l;
                         const uint32_t off = (uint32_t)(r * 128 + ((cc ^ (r & 7)) << 4));
                         cp_async16(kdst + off, kc_base + gi * (SHD * 2));
                         cp_async16(vdst + off, vc_base + gi * (SHD * 2));
@@ -267,7 +282,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
             }
             if (pt == 0) mbar_wait(&bars.q_full, 0, &dummy, 400000000LL);
         }
-    } else if (warp == 6) {
+    } else if (warp == W_MMA_S) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0 && !dead && n_tiles > 0) {
             constexpr uint32_t IDESC_S = idesc_bf16_f32(SBM, SBN, 0, 0);
@@ -486,7 +501,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 6) {
+    if (warp == W_MMA_S) {
         tc_fence_after();
         tmem_dealloc(taddr, S_TMEM_COLS);
     }
