@@ -34,7 +34,15 @@ using namespace sm100;
 
 namespace {
 constexpr int HBM_ = 128, HBN = 128, HHD = 128;
-constexpr int H_THREADS = 320;
+constexpr int H_THREADS = 384;                         // three warpgroups
+// Registers are allocated to a CTA in whole warpgroups: launched at 168 a
+// thread (384 x 168 <= 65,536), warpgroup 2 (MMA issuer, producer, two idle
+// warps) gives back down to H_REG_LO and the two softmax warpgroups grow to
+// H_REG_HI, which their 128-float rows of S need without spilling.
+constexpr uint32_t H_REG_LAUNCH = 168, H_REG_HI = 192, H_REG_LO = 96;
+static_assert(128 * (2 * H_REG_HI + H_REG_LO) <= H_THREADS * H_REG_LAUNCH &&
+                  2 * 128 * (H_REG_HI - H_REG_LAUNCH) <= 128 * (H_REG_LAUNCH - H_REG_LO),
+              "register split must fit the launch allocation");
 constexpr uint32_t H_TILE = HBN * 128;                 // one 64-column half of a 128-row tile
 constexpr uint32_t HS_Q = 0;                           // 2 tiles x 2 halves
 constexpr uint32_t HS_K = HS_Q + 4 * H_TILE;           // 2 stages x 2 halves
@@ -106,10 +114,7 @@ struct HcaArgs {
                           // many clocks on a barrier nothing completes
 };
 
-static_assert(H_THREADS * 200 <= 65536, "register budget of one CTA per SM");
-// at most 200 registers a thread (320 threads: 64,000 of 65,536); under
-// __launch_bounds__(H_THREADS, 1) ptxas settles on 168 and spills
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(H_THREADS, 1)
     k_hca_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKc,
              const __grid_constant__ CUtensorMap mVc, const __grid_constant__ CUtensorMap mKr,
              const __grid_constant__ CUtensorMap mVr, HcaArgs a) {
@@ -162,7 +167,10 @@ __global__ void __maxnreg__(200)
     const uint32_t taddr = bars.taddr;
     const bool dead = bars.abort != 0;
 
-    if (warp == 9) {
+    if (warp >= 8) {
+      // warpgroup 2: one register decrease for its four warps, then the roles
+      setmaxnreg_dec<H_REG_LO>();
+      if (warp == 9) {
         // ------------------------------------------------------ producer
         if (lane == 0 && !dead && n_tiles > 0) {
             prefetch_tmap(&mQ);
@@ -261,7 +269,9 @@ __global__ void __maxnreg__(200)
             }
         }
         __syncwarp();
+      }
     } else {
+        setmaxnreg_inc<H_REG_HI>();
         // ------------------------------------------------------ softmax warpgroups
         const int g = warp >> 2;                       // query tile
         const int r = tid & 127;                       // row in the tile (TMEM lane)

@@ -41,7 +41,16 @@ namespace {
 constexpr int SBM = 128, SBN = 128, SHD = 128;
 constexpr int NPW = 4;                                 // producer warps
 constexpr int W_MMA_S = 4 + NPW;                       // MMA issuer warp
-constexpr int S_THREADS = 32 * (5 + NPW);              // 4 softmax, NPW producer, 1 MMA warps
+constexpr int S_THREADS = 384;                         // three warpgroups
+static_assert(NPW == 4, "warpgroup 1 holds the producer warps");
+// Registers are allocated to a CTA in whole warpgroups: launched at 168 a
+// thread (384 x 168 <= 65,536), warpgroups 1 (producers) and 2 (MMA issuer,
+// three idle warps) give back down to S_REG_LO and the softmax warpgroup grows
+// to S_REG_HI, which its 128-float rows of S need without spilling.
+constexpr uint32_t S_REG_LAUNCH = 168, S_REG_HI = 200, S_REG_LO = 120;
+static_assert(128 * (S_REG_HI + 2 * S_REG_LO) <= S_THREADS * S_REG_LAUNCH &&
+                  128 * (S_REG_HI - S_REG_LAUNCH) <= 2 * 128 * (S_REG_LAUNCH - S_REG_LO),
+              "register split must fit the launch allocation");
 constexpr int NPROD = 32 * NPW;                        // producer threads
 constexpr int SPT = 128 / NPROD;                       // slots of a tile per producer thread
 constexpr int S_NST = 3;                               // K/V stages
@@ -128,10 +137,7 @@ struct SparseArgs {
                           // many clocks on a barrier nothing completes
 };
 
-static_assert(S_THREADS * 200 <= 65536, "register budget of one CTA per SM");
-// at most 200 registers a thread (288 threads: 57,600 of 65,536); under
-// __launch_bounds__(S_THREADS, 1) ptxas settles on 168 and spills
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(S_THREADS, 1)
     k_sparse_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKr,
                 const __grid_constant__ CUtensorMap mVr, SparseArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -186,7 +192,10 @@ __global__ void __maxnreg__(200)
     const uint32_t taddr = bars.taddr;
     const bool dead = bars.abort != 0;
 
-    if (warp >= 4 && warp < 4 + NPW) {
+    if (warp >= 4) {
+      // warpgroups 1 and 2: one register decrease per warpgroup, then the roles
+      setmaxnreg_dec<S_REG_LO>();
+      if (warp < 4 + NPW) {
         // ------------------------------------------------------ producer warps
         const int pt = tid - 128;  // producer thread 0 .. NPROD-1
         if (!dead && n_tiles > 0) {
@@ -329,7 +338,9 @@ __global__ void __maxnreg__(200)
             }
         }
         __syncwarp();
+      }
     } else {
+        setmaxnreg_inc<S_REG_HI>();
         // ------------------------------------------------------ softmax warps
         const bool row_ok = tid < a.H;
         const int64_t row = qrow * a.H + tid;
