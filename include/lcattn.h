@@ -206,6 +206,45 @@ lc_status hca_dense_attn(const void *Q, const void *Kc, const void *Vc, const vo
                          lc_dtype dtype, void *O, float *lse, void *ws, size_t ws_bytes,
                          int32_t *dev_err, lc_stream stream);
 
+/* Incremental decode state of one layer (page "DeepSeek V4 详解：1M 上下文背后，
+ * 真正发生了什么", §"第二刀"：the KV cache is a classical cache of compressed
+ * entries plus a per-request state cache of fixed size holding the sliding
+ * window and the tail of tokens that do not fill a block yet).  Every array
+ * is on the device and owned by the caller; per request b:
+ *   classical cache: entry j at row b*cap + j of Kc, Vc [B*cap, d] and, for a
+ *     CSA layer, of the indexer keys kI [B*cap, HI*dI];
+ *   state cache: a mirrored ring of the last R raw tokens, K/V rows
+ *     b*2R + p%R and b*2R + p%R + R both hold position p (Kring, Vring
+ *     [B*2R, d]); for a CSA layer, kI_ring [B*m, HI*dI] holds the token-level
+ *     indexer keys of the open block at slot p % m;
+ *   n_tok[b]: tokens held (the next token's position);
+ *   q_pos0 [B], cu_raw [B+1], raw_pos0 [B]: batch-descriptor arrays that
+ *     decode_append rewrites.  With cu_q = 0..B and cu_c[b] = b*cap they form
+ *     the lc_batch (total_q = B, max_q = 1, max_c = cap, total_c = B*cap,
+ *     total_raw = B*2R) that the step's index and attention calls take: the
+ *     query of request b at its newest position, its window read from the
+ *     ring. */
+typedef struct {
+    int32_t B, R, d, m;   /* requests, ring rows (>= m and >= the window), head dim, ratio */
+    int32_t HI, dI;       /* indexer heads and dim of a CSA layer; HI = 0: none */
+    int64_t cap;          /* entries per request in the classical cache */
+    int64_t *n_tok;
+    void *Kring, *Vring, *kI_ring, *Kc, *Vc, *kI;
+    int64_t *q_pos0, *cu_raw, *raw_pos0;
+} lc_decode_layer;
+
+/* Appends one token per request: K_new, V_new [B, d] (and kI_new [B, HI*dI]
+ * for a CSA layer) go into the state cache; a token that closes a block (its
+ * position t has (t+1) % m == 0) also writes the block's entry
+ * (the csa_compress pooling with gates G_K, G_V [m, d] and, for the indexer
+ * keys, G_I [m, HI*dI]); then the batch arrays advance to the new token.
+ * A block past the classical cache's capacity is skipped and raises
+ * LC_DEVERR_BATCH.  No RoPE (entries and ring hold unrotated values).
+ * Supported: d in {64, 128}; 1 <= m <= R; HI*dI <= 1024. */
+lc_status decode_append(const lc_decode_layer *layer, const void *K_new, const void *V_new,
+                        const void *kI_new, const float *G_K, const float *G_V,
+                        const float *G_I, lc_dtype dtype, int32_t *dev_err, lc_stream stream);
+
 /* Index + top-k that allocates nothing (the pages have no counterpart: this
  * is an addition for callers that cannot allocate device memory, such as a
  * host program whose device memory belongs to another runtime's pool, or a

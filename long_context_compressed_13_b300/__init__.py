@@ -29,7 +29,7 @@ LC_DEVERR_SINK = 16
 LC_OP_LIGHTNING_INDEX, LC_OP_TOPK_SELECT, LC_OP_SPARSE_MQA_ATTN, LC_OP_HCA_DENSE_ATTN = 0, 1, 2, 3
 
 ENTRY_POINTS = ("csa_compress", "hca_compress", "token_gated_compress", "rope_rotate",
-                "lightning_index", "topk_select",
+                "decode_append", "lightning_index", "topk_select",
                 "sparse_mqa_attn", "hca_dense_attn", "lc_workspace_size", "lc_status_string",
                 "lc_last_cuda_error", "lc_launch_count", "lc_last_kernel", "lc_version",
                 "lc_debug_stall")
@@ -48,6 +48,16 @@ class _LcBatch(ctypes.Structure):
                 ("raw_pos0", ctypes.c_void_p), ("total_q", ctypes.c_int64),
                 ("max_q", ctypes.c_int64), ("max_c", ctypes.c_int64),
                 ("total_c", ctypes.c_int64), ("total_raw", ctypes.c_int64)]
+
+
+class _LcDecodeLayer(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("R", ctypes.c_int32), ("d", ctypes.c_int32),
+                ("m", ctypes.c_int32), ("HI", ctypes.c_int32), ("dI", ctypes.c_int32),
+                ("cap", ctypes.c_int64), ("n_tok", ctypes.c_void_p),
+                ("Kring", ctypes.c_void_p), ("Vring", ctypes.c_void_p),
+                ("kI_ring", ctypes.c_void_p), ("Kc", ctypes.c_void_p), ("Vc", ctypes.c_void_p),
+                ("kI", ctypes.c_void_p), ("q_pos0", ctypes.c_void_p), ("cu_raw", ctypes.c_void_p),
+                ("raw_pos0", ctypes.c_void_p)]
 
 
 _lib = None
@@ -81,6 +91,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.argtypes = args
         fn.restype = i32
+    lib.decode_append.argtypes = [ctypes.POINTER(_LcDecodeLayer), vp, vp, vp, vp, vp, vp, i32, vp,
+                                  vp]
+    lib.decode_append.restype = i32
     lib.lc_workspace_size.argtypes = [i32, bp, i32, i32, i32, i32, i32]
     lib.lc_workspace_size.restype = sz
     lib.lc_status_string.argtypes = [i32]
@@ -383,3 +396,54 @@ def hca_dense_attn(Q, Kc, Vc, Kraw, Vraw, batch: DeviceBatch, m: int, W: int, sc
                             _dev(dev_err, "dev_err", torch.int32), _stream(stream))
     _check("hca_dense_attn", st)
     return O, L
+
+
+class DecodeLayer:
+    """Incremental decode state of one layer for B requests (see
+    lc_decode_layer in lcattn.h): the classical cache (cap entries a request),
+    the mirrored ring of the last R raw tokens, for a CSA layer (HI > 0) the
+    indexer keys and the open block's token-level indexer keys, and the batch
+    arrays that decode_append advances.  Torch provides the memory; `batch`
+    is the descriptor the step's index and attention calls take."""
+
+    def __init__(self, B: int, R: int, d: int, m: int, cap: int, HI: int = 0, dI: int = 0,
+                 dtype=torch.bfloat16, device="cuda"):
+        z = lambda *shape, dt=dtype: torch.zeros(shape, dtype=dt, device=device)
+        self.B, self.R, self.d, self.m, self.cap, self.HI, self.dI = B, R, d, m, cap, HI, dI
+        self.dtype = dtype
+        self.n_tok = z(B, dt=torch.int64)
+        self.Kring, self.Vring = z(B * 2 * R, d), z(B * 2 * R, d)
+        self.kI_ring = z(B * m, HI, dI) if HI else None
+        self.Kc, self.Vc = z(B * cap, d), z(B * cap, d)
+        self.kI = z(B * cap, HI, dI) if HI else None
+        self.q_pos0 = z(B, dt=torch.int64)
+        self.cu_raw = torch.arange(B + 1, dtype=torch.int64, device=device) * 2 * R
+        self.raw_pos0 = z(B, dt=torch.int64)
+        cu_q = torch.arange(B + 1, dtype=torch.int64, device=device)
+        cu_c = cu_q * cap
+        self.batch = DeviceBatch(B, cu_q, self.q_pos0, cu_c, self.cu_raw, self.raw_pos0,
+                                 total_q=B, max_q=1, max_c=cap, total_c=B * cap,
+                                 total_raw=B * 2 * R)
+
+    def c_struct(self) -> _LcDecodeLayer:
+        p = lambda t: t.data_ptr() if t is not None else 0
+        return _LcDecodeLayer(self.B, self.R, self.d, self.m, self.HI, self.dI, self.cap,
+                              p(self.n_tok), p(self.Kring), p(self.Vring), p(self.kI_ring),
+                              p(self.Kc), p(self.Vc), p(self.kI), p(self.q_pos0),
+                              p(self.cu_raw), p(self.raw_pos0))
+
+
+def decode_append(layer: DecodeLayer, K_new, V_new, G_K, G_V=None, kI_new=None, G_I=None,
+                  dev_err=None, stream=None):
+    """Appends one token per request (K_new, V_new [B, d]; kI_new [B, HI, dI]
+    for a CSA layer): ring, block entries when a block closes, batch arrays."""
+    lib = load_library()
+    G_V = G_K if G_V is None else G_V
+    cs = layer.c_struct()
+    st = lib.decode_append(ctypes.byref(cs), _dev(K_new, "K_new", layer.dtype),
+                           _dev(V_new, "V_new", layer.dtype),
+                           _dev(kI_new, "kI_new", layer.dtype),
+                           _dev(G_K, "G_K", torch.float32), _dev(G_V, "G_V", torch.float32),
+                           _dev(G_I, "G_I", torch.float32), _dtype_code(K_new),
+                           _dev(dev_err, "dev_err", torch.int32), _stream(stream))
+    _check("decode_append", st)

@@ -15,6 +15,7 @@ lc_status rope_launch(void *X, int64_t n, int hv, int d, int64_t pos0, int inver
                       cudaStream_t st);
 lc_status compress_tok_launch(const void *X, const float *Z, int64_t T_, int d, int m,
                               lc_dtype dt, void *Xc, int64_t rope_pos0, cudaStream_t st);
+lc_status decode_append_launch(const AppendArgs &a, lc_dtype dt, cudaStream_t st);
 lc_status index_launch(const void *qI, const float *w, const void *kI, const lc_batch &b, int HI,
                        int dI, int m, lc_dtype dt, float *scores, int64_t ld, int32_t *dev_err,
                        cudaStream_t st);
@@ -163,6 +164,23 @@ lc_status token_gated_compress(const void *X, const float *Z, int64_t T, int32_t
     if (d < 32 || d > 1024 || d % 32 || m > 4096) return LC_ERR_UNSUPPORTED;
     if (rope_pos0 >= 0 && d < ROPE_DIMS) return LC_ERR_UNSUPPORTED;
     return finish(compress_tok_launch(X, Z, T, d, m, dtype, Xc, rope_pos0, st), st, nullptr);
+}
+
+lc_status decode_append(const lc_decode_layer *L, const void *K_new, const void *V_new,
+                        const void *kI_new, const float *G_K, const float *G_V,
+                        const float *G_I, lc_dtype dtype, int32_t *dev_err, lc_stream stream) {
+    cudaStream_t st = (cudaStream_t)stream;
+    if (!L || L->B < 1 || L->m < 1 || L->R < L->m || L->cap < 1 || L->HI < 0 ||
+        !dtype_ok(dtype) || !L->n_tok || !L->Kring || !L->Vring || !L->Kc || !L->Vc ||
+        !L->q_pos0 || !L->cu_raw || !L->raw_pos0 || !K_new || !V_new || !G_K || !G_V)
+        return LC_ERR_INVALID_ARG;
+    if (L->HI > 0 && (L->dI < 1 || !L->kI_ring || !L->kI || !kI_new || !G_I))
+        return LC_ERR_INVALID_ARG;
+    if ((L->d != 64 && L->d != 128) || (int64_t)L->HI * L->dI > 1024) return LC_ERR_UNSUPPORTED;
+    AppendArgs a{L->B, L->R, L->d, L->m, L->HI > 0 ? L->HI * L->dI : 0, L->cap, L->n_tok,
+                 L->Kring, L->Vring, L->kI_ring, L->Kc, L->Vc, L->kI, L->q_pos0, L->cu_raw,
+                 L->raw_pos0, K_new, V_new, kI_new, G_K, G_V, G_I, dev_err};
+    return finish(decode_append_launch(a, dtype, st), st, dev_err);
 }
 
 lc_status lightning_index(const void *qI, const float *w, const void *kI, const lc_batch *batch,

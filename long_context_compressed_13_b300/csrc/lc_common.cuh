@@ -46,6 +46,19 @@ template <> struct io<__nv_bfloat16> {
     }
 };
 
+// ---------------------------------------------------------------- decode state
+// Arguments of the decode-state append kernel (decode_append).
+struct AppendArgs {
+    int B, R, d, m, dk;            // dk = HI * dI, 0 without an indexer
+    int64_t cap;
+    int64_t *n_tok;
+    void *Kring, *Vring, *kI_ring, *Kc, *Vc, *kI;
+    int64_t *q_pos0, *cu_raw, *raw_pos0;
+    const void *K_new, *V_new, *kI_new;
+    const float *G_K, *G_V, *G_I;
+    int32_t *dev_err;
+};
+
 // ---------------------------------------------------------------- batch
 // Device view of lc_batch.
 struct Batch {

@@ -121,6 +121,14 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
                               args["scale"], N, 2, lc.LC_BF16, P, N, N, 0, N,
                               N) == lc.LC_ERR_INVALID_ARG
     assert lib.token_gated_compress(P, P, 16, 48, 4, lc.LC_F32, P, -1, N) == lc.LC_ERR_UNSUPPORTED
+    # decode state: ring shorter than a block, missing indexer buffers
+    Lbad = lc._LcDecodeLayer(2, 2, 128, 4, 0, 0, 16, *([0x1000] * 10))
+    assert lib.decode_append(ctypes.byref(Lbad), P, P, N, P, P, N, lc.LC_BF16, N,
+                             N) == lc.LC_ERR_INVALID_ARG
+    Lidx = lc._LcDecodeLayer(2, 8, 128, 4, 8, 64, 16, 0x1000, 0x1000, 0x1000, 0, 0x1000, 0x1000,
+                             0, 0x1000, 0x1000, 0x1000)
+    assert lib.decode_append(ctypes.byref(Lidx), P, P, P, P, P, P, lc.LC_BF16, N,
+                             N) == lc.LC_ERR_INVALID_ARG
     # nothing above reached a kernel
     assert lib.lc_launch_count() == launches_before
 
