@@ -13,7 +13,7 @@ Entries of the positions before the chunk come from the same compressors in
 an untimed set-up (they are the layer's KV cache).  Metric: query tokens per
 second (4096 per step per GPU).
 
-The default run also measures two other full-size settings and prints each
+The default run also measures three other full-size settings and prints each
 as a sub-record of the same JSON line (same fields as the main record):
   decode       one decode step of 64 sequences (one query each at its last
                position, contexts ~U[65536, 262144], compressed caches and
@@ -21,11 +21,16 @@ as a sub-record of the same JSON line (same fields as the main record):
                (k=1024) -> sparse_mqa_attn (128 heads, window 128).  HBM-bound:
                its roofline is the whole step's algorithmic bytes over the
                step's time against the measured copy bandwidth.
+  decode_incremental  the decode setting token by token: each step appends
+               one new token per request to the decode state (decode_append:
+               window ring, open block, the block's entry every fourth token)
+               before the index + top-k and the attention.
   hca_prefill  a 131,072-token HCA prefill (64 heads x 128, m'=128, window
                128): hca_compress -> hca_dense_attn.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload all|layer_pair_1m|csa_decode|hca_prefill]
+                  [--workload all|layer_pair_1m|csa_decode|csa_decode_incremental|
+                              hca_prefill]
 
 Prints ONE JSON line on rank 0.  `--impl reference` times the CPU oracle on a
 bounded sample of the layer-pair workload (rank 0 only).
@@ -367,6 +372,120 @@ class Decode:
                 "algorithmic_bytes": w["step_bytes"], "peak_source": peaks["source"]}
 
 
+class DecodeIncremental:
+    """Token-by-token decode of the batch-64 CSA setting through the decode
+    state: each step appends one new token per request (ring, open block and,
+    every fourth token, the block's compressed entry), then runs the fused
+    index + top-k over the request's classical cache and the sparse attention
+    with the window read from the ring.  The state starts from the decode
+    setting's caches (contexts ~U[65536, 262144], seed 3), copied into each
+    request's fixed-capacity region."""
+
+    STAGES = ["decode_append", "lightning_index+topk", "sparse_mqa_attn"]
+
+    def __init__(self, lc, device, seed=3):
+        self.lc = lc
+        D = wl.CONFIGS["csa_decode"](device=device)
+        assert D["seed"] == seed
+        self.ctx0 = list(D["ctx"])
+        B, d, HI, dI, m, W = D["B"], D["d"], D["HI"], D["dI"], D["m"], D["W"]
+        self.B, self.m, self.k, self.W, self.H, self.d = B, m, D["k"], W, D["H"], d
+        self.HI, self.dI = HI, dI
+        self.chunk = B
+        cap = max(self.ctx0) // m + 64
+        L = lc.DecodeLayer(B, W, d, m, cap, HI, dI, device=device)
+        bt = D["batch"]
+        for b in range(B):
+            c0, c1, r0, r1 = bt.cu_c[b], bt.cu_c[b + 1], bt.cu_raw[b], bt.cu_raw[b + 1]
+            L.Kc[b * cap:b * cap + (c1 - c0)] = D["Kc"][c0:c1]
+            L.Vc[b * cap:b * cap + (c1 - c0)] = D["Vc"][c0:c1]
+            L.kI[b * cap:b * cap + (c1 - c0)] = D["kI"][c0:c1]
+            # the ring holds the last W positions: p0 .. ctx-1
+            p0 = bt.raw_pos0[b]
+            rows = torch.arange(p0, p0 + (r1 - r0), device=device) % W + b * 2 * W
+            for off in (0, W):
+                L.Kring[rows + off] = D["Kraw"][r0:r1]
+                L.Vring[rows + off] = D["Vraw"][r0:r1]
+        L.n_tok.copy_(torch.tensor(self.ctx0, dtype=torch.int64, device=device))
+        self.L = L
+        g = wl._gen(seed + 500, device)
+        self.K_new = wl.normal(g, (B, d), "bf16", device)
+        self.V_new = wl.normal(g, (B, d), "bf16", device)
+        self.kI_new = wl.normal(g, (B, HI, dI), "bf16", device)
+        self.G = wl.normal(g, (m, d), "f32", device)
+        self.GI = wl.normal(g, (m, HI * dI), "f32", device)
+        self.Q, self.qI, self.w, self.scale = D["Q"], D["qI"], D["w"], D["scale"]
+        self.ws = torch.empty(lc.workspace_size(lc.LC_OP_LIGHTNING_INDEX, L.batch, HI=HI, dI=dI,
+                                                k=self.k), dtype=torch.uint8, device=device)
+        self.sel = torch.empty((B, self.k), dtype=torch.int32, device=device)
+        self.O = torch.empty_like(self.Q)
+        self.lse = torch.empty((B, self.H), dtype=torch.float32, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        del D
+        torch.cuda.synchronize()
+
+    def step(self, events=None):
+        lc, L = self.lc, self.L
+        ev = events
+        if ev:
+            ev[0].record()
+        lc.decode_append(L, self.K_new, self.V_new, self.G, kI_new=self.kI_new, G_I=self.GI,
+                         dev_err=self.err)
+        if ev:
+            ev[1].record()
+        lc.lightning_index(self.qI, self.w, L.kI, L.batch, self.m, scores=False, k=self.k,
+                           topk=self.sel, ws=self.ws, dev_err=self.err)
+        if ev:
+            ev[2].record()
+        lc.sparse_mqa_attn(self.Q, L.Kc, L.Vc, self.sel, L.Kring, L.Vring, L.batch, self.m,
+                           self.W, self.scale, O=self.O, lse=self.lse, dev_err=self.err)
+        if ev:
+            ev[3].record()
+
+    def work(self):
+        """Algorithmic bytes of one step at the starting contexts: the append
+        (the new token's K, V, indexer keys into the ring, a quarter of the
+        requests writing an entry), then as for the decode setting."""
+        ctx = np.array(self.ctx0, dtype=np.int64) + 1
+        nv = ctx // self.m
+        keys = np.minimum(nv, self.k) + np.minimum(ctx, self.W)
+        B, d, dk = self.B, self.d, self.HI * self.dI
+        append = B * (2 * d * 2 * 3 + dk * 2 * 2) + B / self.m * (2 * d * 2 + dk * 2) * 2
+        idx = nv.sum() * dk * 2 + B * self.HI * (self.dI * 2 + 4) + B * self.k * 4
+        attn = keys.sum() * d * 2 * 2 + 2 * B * self.H * d * 2 + B * self.k * 4
+        return {"step_bytes": float(append + idx + attn),
+                "attn_flop": float(4 * d * self.H * keys.sum())}
+
+    def host_io(self):
+        return ({"K_new": self.K_new, "V_new": self.V_new, "kI_new": self.kI_new, "Q": self.Q,
+                 "qI": self.qI, "w": self.w}, {"O": self.O})
+
+    def config(self, world):
+        return {"workload": "csa_decode_incremental: 64 requests, contexts ~U[65536, 262144] "
+                            "(seed 3), one new token each per step through the decode state "
+                            "(append, index + top-k 1024, CSA attention with window 128)",
+                "batch": self.B, "heads": self.H, "head_dim": self.d,
+                "context_mean": float(np.mean(self.ctx0)), "parallelism": f"replicas x{world}",
+                "l2": "inputs larger than L2 (indexer keys 2.7 GB)"}
+
+    def roofline(self, stage_ms, peaks, region_ms):
+        w = self.work()
+        ms = sum(stage_ms)
+        gbs = w["step_bytes"] / (ms / 1e3) / 1e9
+        return {"bound": "hbm", "kernel": "whole step (decode_append, lightning_index+topk, "
+                                          "sparse_mqa_attn)",
+                "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                "traffic_unit": "DRAM bytes per step of the step's kernels (ncu)",
+                "algorithmic_bytes": w["step_bytes"], "peak_source": peaks["source"]}
+
+    def path_tflops(self, ms_step):
+        return self.work()["attn_flop"] / (ms_step / 1e3) / 1e12
+
+    def cpu_baseline(self, budget_s):
+        return None
+
+
 class HcaPrefill:
     """A 131,072-token HCA prefill: compress -> dense attention, 64 heads."""
 
@@ -439,8 +558,10 @@ class HcaPrefill:
                                      "fp64); compressed entries built untimed")
 
 
-WORKLOADS = {"layer_pair_1m": LayerPair, "csa_decode": Decode, "hca_prefill": HcaPrefill}
-SUB_RECORDS = {"csa_decode": "decode", "hca_prefill": "hca_prefill"}
+WORKLOADS = {"layer_pair_1m": LayerPair, "csa_decode": Decode,
+             "csa_decode_incremental": DecodeIncremental, "hca_prefill": HcaPrefill}
+SUB_RECORDS = {"csa_decode": "decode", "csa_decode_incremental": "decode_incremental",
+               "hca_prefill": "hca_prefill"}
 
 
 # ---------------------------------------------------------------- ranks
@@ -540,7 +661,9 @@ def measure(wk, args, dist, device, peaks, world, rank, cpu_budget):
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rec["cpu_baseline"] = wk.cpu_baseline(cpu_budget)
+        cb = wk.cpu_baseline(cpu_budget)
+        if cb is not None:
+            rec["cpu_baseline"] = cb
     return rec
 
 
@@ -560,7 +683,7 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device(device))
     peaks = load_peaks()
 
-    names = ["layer_pair_1m", "csa_decode", "hca_prefill"] \
+    names = ["layer_pair_1m", "csa_decode", "csa_decode_incremental", "hca_prefill"] \
         if args.workload == "all" else [args.workload]
     recs = {}
     for name in names:
