@@ -210,8 +210,13 @@ __global__ void __launch_bounds__(H_THREADS, 1)
                 mbar_wait(&bars.v_full[j & 1], (j >> 1) & 1, &dummy, 400000000LL);
             }
             mbar_wait(&bars.q_full, 0, &dummy, 400000000LL);
+            // the MMAs' releases of the last tiles: no commit may still be on
+            // its way to this CTA's barriers when it exits (skipped after an
+            // abort, when some of those MMAs are never issued)
+            for (int j = max(0, issued - 2); j < issued && !*abort; ++j)
+                mbar_wait(&bars.kv_empty[j & 1], (j >> 1) & 1, abort);
         }
-    } else if (warp == 8) {
+      } else if (warp == 8) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0 && !dead && n_tiles > 0) {
             constexpr uint32_t IDESC_S = idesc_bf16_f32(HBM_, HBN, 0, 0);

@@ -290,6 +290,11 @@ __global__ void __launch_bounds__(S_THREADS, 1)
                 mbar_wait(&bars.v_full[i % S_NST], (i / S_NST) & 1, &dummy, 400000000LL);
             }
             if (pt == 0) mbar_wait(&bars.q_full, 0, &dummy, 400000000LL);
+            // the MMAs' releases of the last tiles: no commit may still be on
+            // its way to this CTA's barriers when it exits (skipped after an
+            // abort, when some of those MMAs are never issued)
+            for (int i = max(0, issued - S_NST); i < issued && !*abort; ++i)
+                mbar_wait(&bars.kv_empty[i % S_NST], (i / S_NST) & 1, abort);
         }
     } else if (warp == W_MMA_S) {
         // ------------------------------------------------------ MMA issuer
