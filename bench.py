@@ -490,6 +490,101 @@ class DecodeIncremental:
         return None
 
 
+class CsaPrefill:
+    """A 32,768-token CSA prefill: compress -> index + top-k (k=512) ->
+    sparse attention, 64 heads."""
+
+    STAGES = ["csa_compress", "lightning_index+topk", "sparse_mqa_attn"]
+
+    def __init__(self, lc, device):
+        self.lc = lc
+        L = wl.CONFIGS["csa_prefill"](device=device)
+        self.L = L
+        self.T, self.m, self.k, self.W, self.H, self.d = (L["T"], L["m"], L["k"], L["W"], L["H"],
+                                                          L["d"])
+        self.chunk = self.T
+        self.b = lc.DeviceBatch.from_workload(L["batch"], device=device)
+        self.Kc = torch.empty((self.T // self.m, self.d), dtype=torch.bfloat16, device=device)
+        self.Vc = torch.empty_like(self.Kc)
+        self.ws = torch.empty(lc.workspace_size(lc.LC_OP_LIGHTNING_INDEX, self.b, HI=L["HI"],
+                                                dI=L["dI"], k=self.k),
+                              dtype=torch.uint8, device=device)
+        self.sel = torch.empty((self.T, self.k), dtype=torch.int32, device=device)
+        self.O = torch.empty_like(L["Q"])
+        self.lse = torch.empty((self.T, self.H), dtype=torch.float32, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        torch.cuda.synchronize()
+
+    def work(self):
+        L = self.L
+        t = np.arange(self.T, dtype=np.int64)
+        nv = (t + 1) // self.m
+        keys = np.minimum(nv, self.k) + _n_window(t, self.W)
+        return {"index_flop": float(2 * L["HI"] * L["dI"] * nv.sum()),
+                "attn_flop": float(4 * self.d * self.H * keys.sum())}
+
+    def step(self, events=None):
+        lc, L = self.lc, self.L
+        ev = events
+        if ev:
+            ev[0].record()
+        lc.csa_compress(L["K"], L["V"], L["G"], m=self.m, Kc=self.Kc, Vc=self.Vc)
+        if ev:
+            ev[1].record()
+        lc.lightning_index(L["qI"], L["w"], L["kI"], self.b, self.m, scores=False, k=self.k,
+                           topk=self.sel, ws=self.ws, dev_err=self.err)
+        if ev:
+            ev[2].record()
+        lc.sparse_mqa_attn(L["Q"], self.Kc, self.Vc, self.sel, L["K"], L["V"], self.b, self.m,
+                           self.W, L["scale"], O=self.O, lse=self.lse, dev_err=self.err)
+        if ev:
+            ev[3].record()
+
+    def host_io(self):
+        L = self.L
+        return ({"Q": L["Q"], "K": L["K"], "V": L["V"], "qI": L["qI"], "kI": L["kI"],
+                 "w": L["w"]}, {"O": self.O})
+
+    def config(self, world):
+        return {"workload": "csa_prefill: one 32,768-token sequence, every position queried, "
+                            "Q [32768,64,128], K,V [32768,128], CSA m=4 (8192 entries), "
+                            "indexer 8x64, top-k 512, window 128 (seed 1)",
+                "seq_len": self.T, "heads": self.H, "head_dim": self.d,
+                "parallelism": f"replicas x{world}",
+                "l2": "inputs larger than L2 (Q 512 MiB)"}
+
+    def roofline(self, stage_ms, peaks, region_ms):
+        w = self.work()
+        return tensor_roofline(self.STAGES, stage_ms,
+                               {"lightning_index+topk": w["index_flop"],
+                                "sparse_mqa_attn": w["attn_flop"]}, peaks, region_ms,
+                               "csa_prefill")
+
+    def path_tflops(self, ms_step):
+        w = self.work()
+        return (w["index_flop"] + w["attn_flop"]) / (ms_step / 1e3) / 1e12
+
+    def cpu_baseline(self, budget_s):
+        import oracle
+        L = _cpu(self.L)
+        Kc = oracle.compress(L["K"], L["G"], self.m)
+        Vc = oracle.compress(L["V"], L["G"], self.m)
+        Kc = torch.from_numpy(Kc).to(torch.bfloat16).double().numpy()
+        Vc = torch.from_numpy(Vc).to(torch.bfloat16).double().numpy()
+        kI = L["kI"].double().numpy()
+
+        def run(rows):
+            t = rows.astype(np.int64)
+            I = oracle.index(L["qI"][rows], L["w"][rows], kI, t, self.m)
+            sel = oracle.topk(I, (t + 1) // self.m, self.k)
+            oracle.sparse_attn(L["Q"][rows], Kc, Vc, sel, L["K"], L["V"], 0, t, self.W,
+                               L["scale"])
+        return sampled_rows_baseline(run, self.T, budget_s,
+                                     "query rows of the 32,768-token CSA prefill (index over "
+                                     "the visible entries, top-k 512, CSA attention, fp64); "
+                                     "compressed entries built untimed")
+
+
 class HcaPrefill:
     """A 131,072-token HCA prefill: compress -> dense attention, 64 heads."""
 
@@ -563,9 +658,10 @@ class HcaPrefill:
 
 
 WORKLOADS = {"layer_pair_1m": LayerPair, "csa_decode": Decode,
-             "csa_decode_incremental": DecodeIncremental, "hca_prefill": HcaPrefill}
+             "csa_decode_incremental": DecodeIncremental, "csa_prefill": CsaPrefill,
+             "hca_prefill": HcaPrefill}
 SUB_RECORDS = {"csa_decode": "decode", "csa_decode_incremental": "decode_incremental",
-               "hca_prefill": "hca_prefill"}
+               "csa_prefill": "csa_prefill", "hca_prefill": "hca_prefill"}
 
 
 # ---------------------------------------------------------------- ranks

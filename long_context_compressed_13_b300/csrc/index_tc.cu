@@ -82,10 +82,12 @@ struct IdxBars {
     // releases of each score buffer: every epilogue warp arrives once its
     // reads of a use of the buffer are complete
     uint64_t freed[NBUF];
+    uint64_t fin[2];          // each MMA issuer's last commit
     uint64_t stall;           // test hook: a barrier nothing completes
     uint32_t taddr;
     int abort;
 };
+static_assert(sizeof(IdxBars) <= IdxCfg::SM_LCNT - IdxCfg::SM_BAR, "indexer barriers");
 
 
 
@@ -182,6 +184,8 @@ __global__ void __launch_bounds__(I_THREADS, 1)
         if (bars.abort) flag(a.dev_err, LC_DEVERR_TIMEOUT);
         mbar_init(&bars.q_full, 1);
         mbar_init(&bars.stall, 1);
+        mbar_init(&bars.fin[0], 1);
+        mbar_init(&bars.fin[1], 1);
         for (int s = 0; s < NSB; ++s) {
             mbar_init(&bars.k_full[s], 1);
             mbar_init(&bars.k_empty[s], 1);
@@ -242,10 +246,18 @@ __global__ void __launch_bounds__(I_THREADS, 1)
                       mbar_wait(&bars.q_full, 0, abort);
             tc_fence_after();
             const uint32_t q_base = smem_u32(smem + C::SM_Q);
+            int mine = 0;  // MMAs this thread issued
             for (int g = par; ok && g < n_all; g += 2) {
                 const int s = g % NSB, h = g % HI, b = g % NBUF, u = g / NBUF;
-                if (!mbar_wait(&bars.k_full[s], (g / NSB) & 1, abort) ||
-                    (u > 0 && !mbar_wait(&bars.freed[b], (uint32_t)(u - 1) & 1u, abort)))
+                // The release of buffer b (the epilogue's read of head g-4) comes
+                // first: the epilogue reads heads in order, so it also read head
+                // g-NSB, whose box is the previous use of slot s and belongs to
+                // the other issuer.  Only then is k_full[s] at most one phase
+                // behind box g, which a parity wait needs: waited first, it
+                // could pass on the completed phase before that one while box
+                // g-NSB is still landing.
+                if ((u > 0 && !mbar_wait(&bars.freed[b], (uint32_t)(u - 1) & 1u, abort)) ||
+                    !mbar_wait(&bars.k_full[s], (g / NSB) & 1, abort))
                     break;
                 tc_fence_after();
                 const uint32_t k_base = smem_u32(smem + C::SM_K + s * C::HEAD_BOX);
@@ -256,6 +268,14 @@ __global__ void __launch_bounds__(I_THREADS, 1)
                              sw128_desc(k_base + kk * 32, 16, 1024), IDESC, kk > 0);
                 mma_commit(&bars.d_full[b]);
                 mma_commit(&bars.k_empty[s]);
+                ++mine;
+            }
+            // none of this thread's MMAs may still run when the tensor memory is
+            // freed (after an abort the epilogue no longer waits for them)
+            if (mine > 0) {
+                int dummy = 0;
+                mma_commit(&bars.fin[par]);
+                mbar_wait(&bars.fin[par], 0, &dummy, 400000000LL);
             }
         }
         __syncwarp();

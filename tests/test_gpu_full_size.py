@@ -11,8 +11,9 @@ benchmark times, on sampled outputs the oracle computes one by one.
   tolerance; sampled compressed entries of the chunk within one bf16 ulp.
 - csa_decode: 64 sequences with contexts ~U[65536, 262144]; every sequence
   is checked the same way.
-- hca_prefill (T=131072, 64 heads, m'=128): the benchmark's step, 256+
-  sampled rows, checked the same way.
+- csa_prefill (T=32768, 64 heads, k=512) and hca_prefill (T=131072, 64
+  heads, m'=128): the benchmark's steps, 256+ sampled rows each, checked
+  the same way.
 
 The oracle builds its own compressed caches from the raw inputs (rounded to
 bf16, the stored type) and never reads a value the CUDA path produced.
@@ -137,6 +138,38 @@ def _check_entries(name, gpu, ref, rng):
     got = gpu[torch.from_numpy(ents).cuda()].double().cpu().numpy()
     ulp = np.abs(ref[ents]) * 2.0 ** -7 + 1e-30
     assert np.all(np.abs(got - ref[ents]) <= ulp), name
+
+
+def test_csa_prefill_32k_sampled(lc):
+    """CSA prefill, T = 32,768, 64 heads x 128, indexer 8 x 64 over 8192
+    entries, top-k 512, window 128: the benchmark's step, 256+ sampled rows."""
+    import bench
+    wk = bench.CsaPrefill(lc, "cuda")
+    for _ in range(3):  # repeated steps reuse the workspace, as the benchmark does
+        wk.step()
+    torch.cuda.synchronize()
+    assert int(wk.err.item()) == 0
+    L = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in wk.L.items()}
+    rng = np.random.default_rng(21)
+    Kc = _bf16_round(oracle.compress(L["K"], L["G"], wk.m))
+    Vc = _bf16_round(oracle.compress(L["V"], L["G"], wk.m))
+    _check_entries("Kc", wk.Kc, Kc, rng)
+    _check_entries("Vc", wk.Vc, Vc, rng)
+    # the first rows (no entry visible), rows around the first entries and the
+    # point where n_vis passes k, tile edges of the indexer, the last rows
+    fixed = [0, 1, 2, 3, 4, 127, 128, 2047, 2048, 2051, 4095, 4096, 16383, 16384, 32766, 32767]
+    rows = _sample_rows(wk.T, 256, rng, fixed)
+    t = rows.astype(np.int64)
+    I = oracle.index(L["qI"][rows], L["w"][rows], L["kI"], t, wk.m)
+    gsel = wk.sel[torch.from_numpy(rows).cuda()].cpu().numpy()
+    rsel, same = _check_rows(gsel, I, (t + 1) // wk.m, wk.k)
+    assert same.mean() >= 0.95
+    rO, rl = oracle.sparse_attn(L["Q"][rows], Kc, Vc, rsel, L["K"], L["V"], 0, t, wk.W,
+                                L["scale"])
+    gO = wk.O[torch.from_numpy(rows).cuda()].double().cpu().numpy()
+    gl = wk.lse[torch.from_numpy(rows).cuda()].double().cpu().numpy()
+    np.testing.assert_allclose(gO[same], rO[same], rtol=0, atol=TOL)
+    np.testing.assert_allclose(gl[same], rl[same], rtol=0, atol=TOL)
 
 
 def test_hca_prefill_128k_sampled(lc):
