@@ -13,7 +13,7 @@ Entries of the positions before the chunk come from the same compressors in
 an untimed set-up (they are the layer's KV cache).  Metric: query tokens per
 second (4096 per step per GPU).
 
-The default run also measures three other full-size settings and prints each
+The default run also measures four other full-size settings and prints each
 as a sub-record of the same JSON line (same fields as the main record):
   decode       one decode step of 64 sequences (one query each at its last
                position, contexts ~U[65536, 262144], compressed caches and
@@ -25,12 +25,15 @@ as a sub-record of the same JSON line (same fields as the main record):
                one new token per request to the decode state (decode_append:
                window ring, open block, the block's entry every fourth token)
                before the index + top-k and the attention.
+  csa_prefill  a 32,768-token CSA prefill (64 heads x 128, indexer 8 x 64,
+               k=512, window 128): csa_compress -> lightning_index + top-k ->
+               sparse_mqa_attn.
   hca_prefill  a 131,072-token HCA prefill (64 heads x 128, m'=128, window
                128): hca_compress -> hca_dense_attn.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload all|layer_pair_1m|csa_decode|csa_decode_incremental|
-                              hca_prefill]
+                              csa_prefill|hca_prefill]
 
 Prints ONE JSON line on rank 0.  `--impl reference` times the CPU oracle on a
 bounded sample of the layer-pair workload (rank 0 only).
@@ -783,7 +786,8 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device(device))
     peaks = load_peaks()
 
-    names = ["layer_pair_1m", "csa_decode", "csa_decode_incremental", "hca_prefill"] \
+    names = ["layer_pair_1m", "csa_decode", "csa_decode_incremental", "csa_prefill",
+             "hca_prefill"] \
         if args.workload == "all" else [args.workload]
     recs = {}
     for name in names:
