@@ -52,6 +52,10 @@ def _load():
             lib.oracle_compress_tok.restype = None
             lib.oracle_rope.argtypes = [D, I64, i64, i32, i32, i32, dbl, i32, D]
             lib.oracle_rope.restype = None
+            U32 = ctypes.POINTER(ctypes.c_uint32)
+            U8 = ctypes.POINTER(ctypes.c_uint8)
+            lib.oracle_mx_quantize.argtypes = [D, i64, i32, U32, U8, D]
+            lib.oracle_mx_quantize.restype = None
             lib.oracle_index.argtypes = [D, D, D, I64, i64, i64, i32, i32, i32, D]
             lib.oracle_index.restype = None
             lib.oracle_topk.argtypes = [D, i64, i64, I64, i32, I32]
@@ -141,6 +145,36 @@ def rope(X, pos, inverse: bool = False) -> np.ndarray:
 def entry_positions(pos0: int, n: int, m: int) -> np.ndarray:
     """Position of each compressed entry: its last token, pos0 + (j+1) m - 1."""
     return pos0 + (np.arange(n, dtype=np.int64) + 1) * m - 1
+
+
+MXFP8, MXFP4 = 8, 4  # element formats E4M3 and E2M1 (OCP MX v1.0)
+MX_BLOCK = 32
+
+
+def mx_quantize(X, fmt: int):
+    """MX quantization of X (its size a multiple of 32; blocks of 32
+    consecutive values in row-major order).  Returns (codes, scales, deq):
+    per value its element bit pattern (uint8; E2M1 codes are 4-bit), per
+    block the E8M0 scale byte, and the dequantized values (fp64, X's shape)."""
+    X = _f64(X)
+    n = X.size
+    assert n % MX_BLOCK == 0 and fmt in (MXFP8, MXFP4)
+    codes = np.zeros(n, dtype=np.uint32)
+    scales = np.zeros(n // MX_BLOCK, dtype=np.uint8)
+    deq = np.zeros(n, dtype=np.float64)
+    _load().oracle_mx_quantize(_p(X.reshape(-1), ctypes.c_double), n, fmt,
+                               _p(codes, ctypes.c_uint32), _p(scales, ctypes.c_uint8),
+                               _p(deq, ctypes.c_double))
+    return codes.astype(np.uint8).reshape(X.shape), scales, deq.reshape(X.shape)
+
+
+def index_mx(qI, w, kI, tpos, m: int, fmt: int) -> np.ndarray:
+    """The low-precision indexer: q_I and k_I are MX-quantized (blocks of 32
+    along each head's d_I values) and the score is the indexer's formula on
+    the dequantized values, I[t,j] = sum_h w[t,h] max(0, q^_h . k^_h)."""
+    _, _, qd = mx_quantize(qI, fmt)
+    _, _, kd = mx_quantize(kI, fmt)
+    return index(qd, w, kd, tpos, m)
 
 
 def index(qI, w, kI, tpos, m: int) -> np.ndarray:

@@ -142,6 +142,100 @@ void oracle_rope(const double *X, const int64_t *pos, int64_t n, int32_t hd, int
     }
 }
 
+/* ------------------------------------------------------------------------
+ * Low-precision indexer ("DeepSeek V4 详解：1M 上下文背后，真正发生了什么",
+ * §"mHC、Muon、FP4": FP4 runs in the CSA indexer's QK path, and the selector
+ * keeps almost all of the exact selection; "DeepSeek-V4 技术解析…", §1.1:
+ * the indexer computes in FP4).  The pages give neither the element format
+ * nor the scaling, so the reading is the OCP Microscaling (MX) formats
+ * specification v1.0: blocks of 32 consecutive values share one power-of-two
+ * scale X = 2^(floor(log2(amax)) - emax_elem), stored as an E8M0 byte, and
+ * each value becomes the element nearest to v / X (ties to the even
+ * mantissa), clamped to the largest finite element.  Elements:
+ *   E4M3 (MXFP8): bias 7, 3 mantissa bits, no infinity, largest 448
+ *                 (emax_elem 8), smallest normal 2^-6, subnormal step 2^-9
+ *   E2M1 (MXFP4): bias 1, 1 mantissa bit, largest 6 (emax_elem 2), smallest
+ *                 normal 1, subnormal step 1/2
+ * An all-zero block takes the smallest scale, 2^-127.  Shared exponents
+ * outside the E8M0 range are clamped to [-127, 127].
+ * ------------------------------------------------------------------------ */
+
+/* Element format parameters: mantissa bits, smallest normal exponent,
+ * largest finite value, emax, exponent bias. */
+typedef struct { int mbits, emin, emax, bias; double maxv; } mx_elem;
+static mx_elem mx_format(int32_t fmt)
+{
+    mx_elem f;
+    if (fmt == 4) { f.mbits = 1; f.emin = 0; f.emax = 2; f.bias = 1; f.maxv = 6.0; }
+    else          { f.mbits = 3; f.emin = -6; f.emax = 8; f.bias = 7; f.maxv = 448.0; }
+    return f;
+}
+
+/* Nearest element to v (ties to the even mantissa), clamped to +-maxv;
+ * *code receives the element's bit pattern (sign, exponent field, mantissa). */
+static double mx_round(double v, mx_elem f, uint32_t *code)
+{
+    const int neg = signbit(v) != 0;
+    double a = fabs(v), r;
+    if (a >= f.maxv) {
+        r = f.maxv;
+    } else {
+        int E;
+        if (a < ldexp(1.0, f.emin)) {
+            E = f.emin;                       /* subnormal range: fixed step */
+        } else {
+            (void)frexp(a, &E);               /* a = frac * 2^E, frac in [0.5, 1) */
+            E -= 1;                           /* a in [2^E, 2^(E+1)) */
+        }
+        const double q = ldexp(1.0, E - f.mbits);
+        r = nearbyint(a / q) * q;             /* round half to even: default mode */
+        if (r > f.maxv) r = f.maxv;
+    }
+    uint32_t ef, mf;
+    if (r < ldexp(1.0, f.emin)) {
+        ef = 0;
+        mf = (uint32_t)(r / ldexp(1.0, f.emin - f.mbits));
+    } else {
+        int E;
+        (void)frexp(r, &E);
+        E -= 1;
+        ef = (uint32_t)(E + f.bias);
+        mf = (uint32_t)((r / ldexp(1.0, E) - 1.0) * (double)(1 << f.mbits));
+    }
+    *code = ((uint32_t)neg << (f.mbits + (f.mbits == 3 ? 4 : 2))) | (ef << f.mbits) | mf;
+    return neg ? -r : r;
+}
+
+/* MX quantization of n values (n a multiple of 32), fmt 8 = MXFP8 (E4M3),
+ * 4 = MXFP4 (E2M1).  Outputs per value its element code and its dequantized
+ * value code * X; per block of 32 the E8M0 scale byte (shared exponent + 127). */
+void oracle_mx_quantize(const double *x, int64_t n, int32_t fmt, uint32_t *codes,
+                        uint8_t *scales, double *deq)
+{
+    const mx_elem f = mx_format(fmt);
+    for (int64_t b = 0; b < n / 32; ++b) {
+        const double *v = x + b * 32;
+        double amax = 0.0;
+        for (int i = 0; i < 32; ++i) if (fabs(v[i]) > amax) amax = fabs(v[i]);
+        int e = -127;
+        if (amax > 0.0) {
+            int E;
+            (void)frexp(amax, &E);            /* floor(log2(amax)) = E - 1 */
+            e = (E - 1) - f.emax;
+            if (e < -127) e = -127;
+            if (e > 127) e = 127;
+        }
+        scales[b] = (uint8_t)(e + 127);
+        const double X = ldexp(1.0, e);
+        for (int i = 0; i < 32; ++i) {
+            uint32_t c;
+            const double el = mx_round(v[i] / X, f, &c);
+            codes[b * 32 + i] = c;
+            deq[b * 32 + i] = el * X;
+        }
+    }
+}
+
 /* Number of compressed entries visible from absolute position t. */
 static int64_t n_visible(int64_t t, int32_t m) { return (t + 1) / m; }
 

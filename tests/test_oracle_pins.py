@@ -551,3 +551,127 @@ def test_rope_entry_sits_at_its_last_token():
     o2, _ = oracle.sparse_attn_rope(Q, Kc, Vc, idx, Kc[:0], Vc[:0], 0, [t + 1], 0, 0.5, m)
     np.testing.assert_allclose(o2[0], np.repeat(oracle.rope(Vc[j:j + 1], [-1]), 2, axis=0),
                                rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------ MX (microscaling) quantizer
+
+def _elem_table(fmt):
+    """Every non-negative finite element of the format with its code, listed
+    from the format's definition (sign bit clear): E4M3 bias 7, 3 mantissa
+    bits, exponent field 15 with mantissa 7 is NaN; E2M1 bias 1, 1 bit."""
+    mb, bias, ne = (3, 7, 16) if fmt == oracle.MXFP8 else (1, 1, 4)
+    vals = []
+    for ef in range(ne):
+        for mf in range(1 << mb):
+            if fmt == oracle.MXFP8 and ef == 15 and mf == 7:
+                continue
+            v = (mf / (1 << mb)) * 2.0 ** (1 - bias) if ef == 0 else \
+                (1 + mf / (1 << mb)) * 2.0 ** (ef - bias)
+            vals.append((v, (ef << mb) | mf))
+    return vals
+
+
+def _nearest_by_search(x, fmt):
+    """Brute force: the element nearest to |x|, ties to the even code, the
+    largest element for anything beyond it; the sign bit from x."""
+    table = _elem_table(fmt)
+    a = abs(x)
+    best = min(table, key=lambda vc: (abs(vc[0] - a), vc[1] & 1))
+    sbit = 0x80 if fmt == oracle.MXFP8 else 0x8
+    return (math.copysign(best[0], x), best[1] | (sbit if math.copysign(1, x) < 0 else 0))
+
+
+def _block_with_unit_scale(vals, fmt):
+    """Blocks of 32 whose largest magnitude makes the shared scale 1 (the
+    largest element itself), so the codes are those of the raw values."""
+    top = 448.0 if fmt == oracle.MXFP8 else 6.0
+    vals = list(vals)
+    out = []
+    for i in range(0, len(vals), 31):
+        chunk = vals[i:i + 31]
+        out += chunk + [top] * (32 - len(chunk))
+    return np.array(out, dtype=np.float64)
+
+
+@pytest.mark.parametrize("fmt", [8, 4])
+def test_mx_elements_are_the_nearest_by_search(fmt):
+    table = [v for v, _ in _elem_table(fmt)]
+    mids = [(a + b) / 2 for a, b in zip(table[:-1], table[1:])]
+    eps = [math.nextafter(v, math.inf) for v in mids] + [math.nextafter(v, 0) for v in mids]
+    rnd = list(RNG.uniform(0, table[-1], 600))
+    xs = table + mids + eps + rnd
+    xs = xs + [-v for v in xs]
+    X = _block_with_unit_scale(xs, fmt)
+    codes, scales, deq = oracle.mx_quantize(X, fmt)
+    assert np.all(scales == 127)
+    for x, c, dv in zip(X, codes, deq):
+        ev, ec = _nearest_by_search(x, fmt)
+        assert dv == ev and c == ec, (x, dv, ev, c, ec)
+
+
+def test_mxfp8_elements_equal_torch_e4m3():
+    # torch's float8_e4m3fn conversion (round to nearest even) on values the
+    # unit scale keeps within the finite range
+    vals = np.concatenate([RNG.uniform(-448, 448, 3000), RNG.standard_normal(2000) * 4,
+                           RNG.uniform(-2.0 ** -6, 2.0 ** -6, 1000)])
+    X = _block_with_unit_scale(vals, oracle.MXFP8)
+    codes, _, deq = oracle.mx_quantize(X, oracle.MXFP8)
+    t = torch.from_numpy(X).float().to(torch.float8_e4m3fn)
+    np.testing.assert_array_equal(deq, t.double().numpy())
+    np.testing.assert_array_equal(codes, t.view(torch.uint8).numpy())
+
+
+@pytest.mark.parametrize("fmt,emax", [(8, 8), (4, 2)])
+def test_mx_shared_scale_is_floor_log2_amax_minus_emax(fmt, emax):
+    amaxes = np.concatenate([2.0 ** RNG.uniform(-60, 60, 400),
+                             2.0 ** np.arange(-60, 61, dtype=np.float64)])
+    for amax in amaxes:
+        X = RNG.uniform(-1, 1, 32) * amax * 0.999
+        X[RNG.integers(32)] = -amax if RNG.random() < 0.5 else amax
+        _, scales, deq = oracle.mx_quantize(X, fmt)
+        e = int(scales[0]) - 127
+        # 2^(e + emax) <= amax < 2^(e + emax + 1), by exact comparisons
+        assert 2.0 ** (e + emax) <= amax < 2.0 ** (e + emax + 1)
+        # every value is within half an element step of its dequantized value,
+        # or clamped at the largest element
+        top = (448.0 if fmt == 8 else 6.0) * 2.0 ** e
+        mb = 3 if fmt == 8 else 1
+        emin = -6 if fmt == 8 else 0
+        for x, dv in zip(X, deq):
+            a = abs(x) / 2.0 ** e
+            E = max(math.floor(math.log2(a)) if a > 0 else emin, emin)
+            half = 2.0 ** (E - mb - 1) * 2.0 ** e
+            assert abs(dv - x) <= half * (1 + 1e-12) or abs(dv) == top
+
+
+def test_mx_zero_block_and_saturation():
+    _, s, d = oracle.mx_quantize(np.zeros(32), oracle.MXFP8)
+    assert s[0] == 0 and np.all(d == 0)
+    # amax = 500: shared exponent floor(log2 500) - 8 = 0, so 500 clamps to 448
+    X = np.zeros(32)
+    X[3], X[4] = 500.0, -479.0
+    _, s, d = oracle.mx_quantize(X, oracle.MXFP8)
+    assert s[0] == 127 and d[3] == 448.0 and d[4] == -448.0
+    X[3], X[4] = 7.9, -6.5
+    _, s, d = oracle.mx_quantize(X, oracle.MXFP4)
+    assert s[0] == 127 and d[3] == 6.0 and d[4] == -6.0
+
+
+@pytest.mark.parametrize("fmt", [8, 4])
+def test_mx_index_is_the_index_of_representable_inputs(fmt):
+    # inputs already on the element grid (with the block's own top value so the
+    # scale is 1) quantize to themselves: the low-precision score is the exact one
+    table = np.array([v for v, _ in _elem_table(fmt)])
+    top = table[-1]
+    q = RNG.choice(np.concatenate([table, -table]), (3, 2, 64))
+    k = RNG.choice(np.concatenate([table, -table]), (9, 2, 64))
+    q[..., 0], q[..., 32], k[..., 0], k[..., 32] = top, top, top, top
+    w = RNG.uniform(0, 1, (3, 2))
+    t = np.array([35, 20, 8])
+    np.testing.assert_array_equal(oracle.index_mx(q, w, k, t, 4, fmt),
+                                  oracle.index(q, w, k, t, 4))
+    # a generic input differs from the exact score by the quantization only
+    q2, k2 = RNG.standard_normal((3, 2, 64)), RNG.standard_normal((9, 2, 64))
+    I, Iq = oracle.index(q2, w, k2, t, 4), oracle.index_mx(q2, w, k2, t, 4, fmt)
+    vis = np.isfinite(I)
+    assert np.all(np.isfinite(Iq) == vis) and not np.array_equal(I[vis], Iq[vis])
