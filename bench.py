@@ -13,7 +13,7 @@ Entries of the positions before the chunk come from the same compressors in
 an untimed set-up (they are the layer's KV cache).  Metric: query tokens per
 second (4096 per step per GPU).
 
-The default run also measures four other full-size settings and prints each
+The default run also measures six other full-size settings and prints each
 as a sub-record of the same JSON line (same fields as the main record):
   decode       one decode step of 64 sequences (one query each at its last
                position, contexts ~U[65536, 262144], compressed caches and
@@ -25,6 +25,12 @@ as a sub-record of the same JSON line (same fields as the main record):
                one new token per request to the decode state (decode_append:
                window ring, open block, the block's entry every fourth token)
                before the index + top-k and the attention.
+  decode_mxfp4, decode_mxfp8  the decode setting with the low-precision
+               indexer: indexer keys stored in MXFP4 / MXFP8 (OCP MX, blocks of 32
+               values with a power-of-two scale), the step's q_I quantized,
+               scores and top-k on the quantized values, bf16 attention; the
+               record adds the recall of the quantized selection against the
+               exact one.
   csa_prefill  a 32,768-token CSA prefill (64 heads x 128, indexer 8 x 64,
                k=512, window 128): csa_compress -> lightning_index + top-k ->
                sparse_mqa_attn.
@@ -33,7 +39,7 @@ as a sub-record of the same JSON line (same fields as the main record):
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload all|layer_pair_1m|csa_decode|csa_decode_incremental|
-                              csa_prefill|hca_prefill]
+                              csa_decode_mxfp4|csa_decode_mxfp8|csa_prefill|hca_prefill]
 
 Prints ONE JSON line on rank 0.  `--impl reference` times the CPU oracle on a
 bounded sample of the layer-pair workload (rank 0 only).
@@ -379,6 +385,93 @@ class Decode:
                 "algorithmic_bytes": w["step_bytes"], "peak_source": peaks["source"]}
 
 
+class DecodeMX(Decode):
+    """The batch-64 decode step with the low-precision indexer: the indexer
+    keys are stored MX-quantized (quantized once, outside the step, as the
+    layer's indexer-key cache would be), each step quantizes the step's q_I,
+    scores every visible entry on the MX values, selects the top-k of those
+    scores and runs the bf16 CSA attention.  `recall` is the fraction of the
+    exact (bf16 indexer) selection that the quantized selection keeps."""
+
+    STAGES = ["mx_quantize(q)+lightning_index_mx+topk", "sparse_mqa_attn"]
+
+    def __init__(self, lc, device, fmt):
+        super().__init__(lc, device)
+        self.fmt = fmt
+        D = self.D
+        self.kc, self.ks = lc.mx_quantize(D["kI"], fmt)
+        self.qc, self.qs = lc.mx_quantize(D["qI"], fmt)
+        torch.cuda.synchronize()
+
+    @property
+    def DTYPE(self):
+        return f"mxfp{self.fmt} indexer, bf16 attention"
+
+    def work(self):
+        w = super().work()
+        D = self.D
+        nv = np.array(D["ctx"], dtype=np.int64) // self.m
+        per_entry = D["HI"] * (D["dI"] * self.fmt // 8 + D["dI"] // 32)
+        q_bytes = D["B"] * D["HI"] * (D["dI"] * 2 + D["dI"] * self.fmt // 8 + D["dI"] // 32 + 4)
+        w["index_bytes"] = float(nv.sum() * per_entry + q_bytes + D["B"] * self.k * 4)
+        w["step_bytes"] = w["index_bytes"] + w["attn_bytes"]
+        return w
+
+    def step(self, events=None):
+        lc, D = self.lc, self.D
+        ev = events
+        if ev:
+            ev[0].record()
+        lc.mx_quantize(D["qI"], self.fmt, codes=self.qc, scales=self.qs)
+        lc.lightning_index_mx(self.fmt, self.qc, self.qs, D["w"], self.kc, self.ks, self.b,
+                              self.m, scores=False, k=self.k, topk=self.sel, ws=self.ws,
+                              dev_err=self.err)
+        if ev:
+            ev[1].record()
+        lc.sparse_mqa_attn(D["Q"], D["Kc"], D["Vc"], self.sel, D["Kraw"], D["Vraw"], self.b,
+                           self.m, self.W, D["scale"], O=self.O, lse=self.lse, dev_err=self.err)
+        if ev:
+            ev[2].record()
+
+    def config(self, world):
+        c = super().config(world)
+        c["workload"] = (f"csa_decode_mxfp{self.fmt}: " + c["workload"].split(": ", 1)[1] +
+                         f"; indexer q/k in MXFP{self.fmt} (OCP MX, 32-value blocks)")
+        return c
+
+    def roofline(self, stage_ms, peaks, region_ms):
+        r = super().roofline(stage_ms, peaks, region_ms)
+        r["traffic"] = None
+        return r
+
+    def extra(self):
+        """Recall of the quantized selection against the exact selection of
+        the bf16 indexer (the fused exact path, parity-tested on its own)."""
+        D = self.D
+        exact = torch.empty_like(self.sel)
+        self.lc.lightning_index(D["qI"], D["w"], D["kI"], self.b, self.m, scores=False, k=self.k,
+                                topk=exact, ws=self.ws)
+        torch.cuda.synchronize()
+        a, b = exact.cpu().numpy(), self.sel.cpu().numpy()
+        rec = [len(np.intersect1d(a[i][a[i] >= 0], b[i][b[i] >= 0])) / max(1, (a[i] >= 0).sum())
+               for i in range(a.shape[0])]
+        return {"recall": {"mean": float(np.mean(rec)), "min": float(np.min(rec)),
+                           "against": "exact top-k of the bf16 indexer on the same inputs"}}
+
+    def cpu_baseline(self, budget_s):
+        return decode_cpu_baseline(self, budget_s=budget_s, fmt=self.fmt)
+
+
+class DecodeMXFP4(DecodeMX):
+    def __init__(self, lc, device):
+        super().__init__(lc, device, 4)
+
+
+class DecodeMXFP8(DecodeMX):
+    def __init__(self, lc, device):
+        super().__init__(lc, device, 8)
+
+
 class DecodeIncremental:
     """Token-by-token decode of the batch-64 CSA setting through the decode
     state: each step appends one new token per request (ring, open block and,
@@ -661,9 +754,11 @@ class HcaPrefill:
 
 
 WORKLOADS = {"layer_pair_1m": LayerPair, "csa_decode": Decode,
-             "csa_decode_incremental": DecodeIncremental, "csa_prefill": CsaPrefill,
+             "csa_decode_incremental": DecodeIncremental, "csa_decode_mxfp4": DecodeMXFP4,
+             "csa_decode_mxfp8": DecodeMXFP8, "csa_prefill": CsaPrefill,
              "hca_prefill": HcaPrefill}
 SUB_RECORDS = {"csa_decode": "decode", "csa_decode_incremental": "decode_incremental",
+               "csa_decode_mxfp4": "decode_mxfp4", "csa_decode_mxfp8": "decode_mxfp8",
                "csa_prefill": "csa_prefill", "hca_prefill": "hca_prefill"}
 
 
@@ -751,7 +846,8 @@ def measure(wk, args, dist, device, peaks, world, rank, cpu_budget):
     rec = {
         "metric": METRIC, "value": whole_job_rate(wk.chunk, world, ms_step), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": getattr(wk, "DTYPE", "bf16"),
         "data": "synthetic",
         "config": wk.config(world),
         "roofline": wk.roofline(stage_ms, peaks, ms),
@@ -763,6 +859,8 @@ def measure(wk, args, dist, device, peaks, world, rank, cpu_budget):
         "dev_err": err,
         "clocks": clocks,
     }
+    if hasattr(wk, "extra"):
+        rec.update(wk.extra())
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = wk.cpu_baseline(cpu_budget)
         if cb is not None:
@@ -786,8 +884,8 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device(device))
     peaks = load_peaks()
 
-    names = ["layer_pair_1m", "csa_decode", "csa_decode_incremental", "csa_prefill",
-             "hca_prefill"] \
+    names = ["layer_pair_1m", "csa_decode", "csa_decode_incremental", "csa_decode_mxfp4",
+             "csa_decode_mxfp8", "csa_prefill", "hca_prefill"] \
         if args.workload == "all" else [args.workload]
     recs = {}
     for name in names:
@@ -882,9 +980,10 @@ def layer_pair_cpu_baseline(wk, budget_s=20.0):
                                  "built untimed")
 
 
-def decode_cpu_baseline(wk, budget_s=20.0):
+def decode_cpu_baseline(wk, budget_s=20.0, fmt=None):
     """The oracle on whole sequences of the decode batch (index over every
-    visible entry, top-k, CSA attention), as many as fit the time budget."""
+    visible entry, top-k, CSA attention), as many as fit the time budget;
+    with fmt, the indexer runs on MX-quantized q_I and k_I."""
     import oracle
     D = wk.D
     B = D["B"]
@@ -898,7 +997,10 @@ def decode_cpu_baseline(wk, budget_s=20.0):
         Kc = host["Kc"][c0:c1].double().numpy()
         Vc = host["Vc"][c0:c1].double().numpy()
         t0 = time.perf_counter()
-        I = oracle.index(host["qI"][b:b + 1], host["w"][b:b + 1], kI, t, wk.m)
+        if fmt is None:
+            I = oracle.index(host["qI"][b:b + 1], host["w"][b:b + 1], kI, t, wk.m)
+        else:
+            I = oracle.index_mx(host["qI"][b:b + 1], host["w"][b:b + 1], kI, t, wk.m, fmt)
         sel = oracle.topk(I, (t + 1) // wk.m, wk.k)
         oracle.sparse_attn(host["Q"][b:b + 1], Kc, Vc, sel, host["Kraw"][r0:r1],
                            host["Vraw"][r0:r1], D["batch"].raw_pos0[b], t, wk.W, D["scale"])
@@ -908,7 +1010,8 @@ def decode_cpu_baseline(wk, budget_s=20.0):
             break
     return {"value": done / t_used, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{done} of the 64 decode sequences (whole sequences: index over every "
-                      f"visible entry, top-k 1024, CSA attention, fp64)", "seconds": t_used}
+                      f"visible entry" + (f" on MXFP{fmt} q/k" if fmt else "") +
+                      ", top-k 1024, CSA attention, fp64)", "seconds": t_used}
 
 
 def run_reference(args):

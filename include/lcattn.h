@@ -159,6 +159,43 @@ lc_status lightning_index(const void *qI, const float *w, const void *kI, const 
                           int64_t ld, int32_t k, int32_t *topk, void *ws, size_t ws_bytes,
                           int32_t *dev_err, lc_stream stream);
 
+/* Low-precision indexer (page "DeepSeek V4 详解：1M 上下文背后，真正发生了什么",
+ * §"mHC、Muon、FP4": FP4 runs in the CSA indexer's QK path, and the quantized
+ * selector keeps almost all of the exact selection; "DeepSeek-V4 技术解析…",
+ * §1.1: the indexer computes in FP4).  q_I and k_I are stored in an OCP MX
+ * (microscaling, v1.0) format: blocks of 32 consecutive values share one
+ * power-of-two scale X = 2^(floor(log2 amax) - emax), kept as an E8M0 byte
+ * (exponent + 127; an all-zero block gets 2^-127), and each value becomes
+ * the element nearest to v / X (ties to the even mantissa), clamped to the
+ * largest finite element.
+ *   LC_MXFP8  E4M3 elements (largest 448, emax 8), one byte per value;
+ *   LC_MXFP4  E2M1 elements (largest 6, emax 2), two values per byte, the
+ *             even-indexed value in the low nibble. */
+#define LC_MXFP8 8
+#define LC_MXFP4 4
+
+/* X [n] (dtype; n % 32 == 0; block i = values 32i .. 32i+31) ->
+ *   codes [n] bytes (LC_MXFP8) or [n / 2] bytes (LC_MXFP4), scales [n / 32]
+ *   E8M0 bytes.  Values must be finite.  n = 0 enqueues nothing. */
+lc_status mx_quantize(const void *X, int64_t n, int32_t fmt, lc_dtype dtype, uint8_t *codes,
+                      uint8_t *scales, lc_stream stream);
+
+/* lightning_index on MX-quantized indexer queries and keys, each head's d_I
+ * values being d_I / 32 blocks:
+ *   I[r,j] = sum_h w[r,h] * max(0, q^[r,h,:] . k^[cu_c[b]+j,h,:]),
+ *   v^ = element * X (the dequantized value), fp32 accumulation;
+ *   qc, qs: mx_quantize of qI [total_q, HI, dI]; kc, ks: of kI [cu_c[B], HI, dI];
+ *   scores, ld, k, topk, ws, ws_bytes: as lightning_index (the selection is
+ *   the exact top-k of these scores; ws: lc_workspace_size of
+ *   LC_OP_LIGHTNING_INDEX).  qc and kc must be 16-byte aligned, ks 2-byte
+ *   aligned.
+ * Supported: dI = 64; HI in {4, 8}; total_q <= 65535; 1 <= k <= 4096. */
+lc_status lightning_index_mx(int32_t fmt, const uint8_t *qc, const uint8_t *qs, const float *w,
+                             const uint8_t *kc, const uint8_t *ks, const lc_batch *batch,
+                             int32_t HI, int32_t dI, int32_t m, float *scores, int64_t ld,
+                             int32_t k, int32_t *topk, void *ws, size_t ws_bytes,
+                             int32_t *dev_err, lc_stream stream);
+
 /* Causal top-k selector (same page, §1.1: the top-k selector keeps the most
  * relevant compressed entries, 1024 in the Pro setting).  For row r keep the
  * min(k, n_vis(t_r)) columns j < n_vis(t_r) that rank first under the total

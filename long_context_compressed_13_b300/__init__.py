@@ -29,7 +29,8 @@ LC_DEVERR_SINK = 16
 LC_OP_LIGHTNING_INDEX, LC_OP_TOPK_SELECT, LC_OP_SPARSE_MQA_ATTN, LC_OP_HCA_DENSE_ATTN = 0, 1, 2, 3
 
 ENTRY_POINTS = ("csa_compress", "hca_compress", "token_gated_compress", "rope_rotate",
-                "decode_append", "lightning_index", "topk_select",
+                "decode_append", "lightning_index", "topk_select", "mx_quantize",
+                "lightning_index_mx",
                 "sparse_mqa_attn", "hca_dense_attn", "lc_workspace_size", "lc_status_string",
                 "lc_last_cuda_error", "lc_launch_count", "lc_last_kernel", "lc_version",
                 "lc_debug_stall")
@@ -82,6 +83,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "rope_rotate": [vp, i64, i32, i32, i64, i32, i32, vp],
         "lightning_index": [vp, vp, vp, bp, i32, i32, i32, i32, vp, i64, i32, vp, vp, sz, vp, vp],
         "topk_select": [vp, i64, bp, i32, i32, vp, vp, sz, vp, vp],
+        "mx_quantize": [vp, i64, i32, i32, vp, vp, vp],
+        "lightning_index_mx": [i32, vp, vp, vp, vp, vp, bp, i32, i32, i32, vp, i64, i32, vp, vp,
+                               sz, vp, vp],
         "sparse_mqa_attn": [vp, vp, vp, vp, i32, vp, vp, bp, i32, i32, i32, i32, f32, vp, i32, i32,
                             vp, vp, vp, sz, vp, vp],
         "hca_dense_attn": [vp, vp, vp, vp, vp, bp, i32, i32, i32, i32, f32, vp, i32, i32, vp, vp,
@@ -313,6 +317,67 @@ def lightning_index(qI, w, kI, batch: DeviceBatch, m: int, *, scores: bool | tor
                              ws.numel() if ws is not None else 0,
                              _dev(dev_err, "dev_err", torch.int32), _stream(stream))
     _check("lightning_index", st)
+    return sc, tk
+
+
+LC_MXFP8, LC_MXFP4 = 8, 4  # OCP MX element formats E4M3 and E2M1
+
+
+def mx_quantize(X, fmt: int, codes=None, scales=None, stream=None):
+    """MX quantization (blocks of 32 consecutive values, one E8M0 scale each).
+    X [..., D] fp32/bf16, D % 32 == 0 -> (codes uint8 [..., D] for MXFP8 or
+    [..., D/2] for MXFP4 (even value in the low nibble), scales uint8
+    [..., D/32])."""
+    lib = load_library()
+    D = X.shape[-1]
+    if D % 32:
+        raise ValueError(f"the last dimension ({D}) must be a multiple of 32")
+    lead = tuple(X.shape[:-1])
+    if codes is None:
+        codes = torch.empty(lead + (D if fmt == LC_MXFP8 else D // 2,), dtype=torch.uint8,
+                            device=X.device)
+    if scales is None:
+        scales = torch.empty(lead + (D // 32,), dtype=torch.uint8, device=X.device)
+    st = lib.mx_quantize(_dev(X, "X"), X.numel(), fmt, _dtype_code(X),
+                         _dev(codes, "codes", torch.uint8), _dev(scales, "scales", torch.uint8),
+                         _stream(stream))
+    _check("mx_quantize", st)
+    return codes, scales
+
+
+def lightning_index_mx(fmt: int, qc, qs, w, kc, ks, batch: DeviceBatch, m: int, *,
+                       scores: bool | torch.Tensor = True, k: int = 0,
+                       topk: bool | torch.Tensor = False, ws=None, dev_err=None, stream=None):
+    """The indexer on MX-quantized q_I (qc [Nq, HI, dI*bits/8], qs [Nq, HI, dI/32])
+    and k_I (kc, ks likewise over the entries), as returned by mx_quantize.
+    Returns (scores or None, topk or None) like lightning_index."""
+    lib = load_library()
+    Nq, HI = qc.shape[0], qc.shape[1]
+    dI = qc.shape[2] * 8 // fmt
+    if isinstance(scores, torch.Tensor):
+        sc = scores
+    elif scores:
+        sc = torch.empty((Nq, max(batch.max_c, 1)), dtype=torch.float32, device=qc.device)
+    else:
+        sc = None
+    if isinstance(topk, torch.Tensor):
+        tk = topk
+    elif topk:
+        tk = torch.empty((Nq, k), dtype=torch.int32, device=qc.device)
+    else:
+        tk = None
+    if tk is not None and sc is None and ws is None:
+        need = workspace_size(LC_OP_LIGHTNING_INDEX, batch, HI=HI, dI=dI, k=k)
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=qc.device)
+    cb = batch.c_struct()
+    ld = sc.shape[1] if sc is not None else 0
+    st = lib.lightning_index_mx(fmt, _dev(qc, "qc", torch.uint8), _dev(qs, "qs", torch.uint8),
+                                _dev(w, "w", torch.float32), _dev(kc, "kc", torch.uint8),
+                                _dev(ks, "ks", torch.uint8), ctypes.byref(cb), HI, dI, m,
+                                _dev(sc, "scores"), ld, k, _dev(tk, "topk", torch.int32),
+                                _dev(ws, "ws"), ws.numel() if ws is not None else 0,
+                                _dev(dev_err, "dev_err", torch.int32), _stream(stream))
+    _check("lightning_index_mx", st)
     return sc, tk
 
 

@@ -29,6 +29,11 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
                                int32_t *topk, void *ws, size_t ws_bytes, int32_t *dev_err,
                                cudaStream_t st);
 size_t index_tc_workspace(const lc_batch &b, int k);
+lc_status mx_quantize_launch(const void *X, int64_t n, int fmt, lc_dtype dt, uint8_t *codes,
+                             uint8_t *scales, cudaStream_t st);
+lc_status index_mx_launch(int fmt, const uint8_t *qc, const uint8_t *qs, const float *w,
+                          const uint8_t *kc, const uint8_t *ks, const lc_batch &b, int HI, int m,
+                          float *scores, int64_t ld, int32_t *dev_err, cudaStream_t st);
 lc_status hca_tc_launch(const void *Q, const void *Kc, const void *Vc, const void *Kraw,
                         const void *Vraw, const lc_batch &b, int H, int d, int m, int W,
                         float scale, const float *sink, int rope, lc_dtype dt, void *O,
@@ -219,6 +224,45 @@ lc_status lightning_index(const void *qI, const float *w, const void *kI, const 
     if (scores) s = index_tc_materialize(qI, w, kI, *batch, HI, dI, m, dtype, sc, sld, dev_err, st);
     if (s == LC_ERR_UNSUPPORTED)
         s = index_launch(qI, w, kI, *batch, HI, dI, m, dtype, sc, sld, dev_err, st);
+    if (s == LC_OK && topk) s = topk_launch(sc, sld, *batch, m, k, topk, dev_err, st);
+    return finish(s, st, dev_err);
+}
+
+lc_status mx_quantize(const void *X, int64_t n, int32_t fmt, lc_dtype dtype, uint8_t *codes,
+                      uint8_t *scales, lc_stream stream) {
+    cudaStream_t st = (cudaStream_t)stream;
+    if (n < 0 || n % 32 != 0 || (fmt != LC_MXFP8 && fmt != LC_MXFP4) || !dtype_ok(dtype) ||
+        (n > 0 && (!X || !codes || !scales)))
+        return LC_ERR_INVALID_ARG;
+    return finish(mx_quantize_launch(X, n, fmt, dtype, codes, scales, st), st, nullptr);
+}
+
+lc_status lightning_index_mx(int32_t fmt, const uint8_t *qc, const uint8_t *qs, const float *w,
+                             const uint8_t *kc, const uint8_t *ks, const lc_batch *batch,
+                             int32_t HI, int32_t dI, int32_t m, float *scores, int64_t ld,
+                             int32_t k, int32_t *topk, void *ws, size_t ws_bytes,
+                             int32_t *dev_err, lc_stream stream) {
+    cudaStream_t st = (cudaStream_t)stream;
+    auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if ((fmt != LC_MXFP8 && fmt != LC_MXFP4) || !qc || !qs || !w || !kc || !ks ||
+        !batch_ok(batch) || m < 1 || (!scores && !topk) || !al16(qc) || !al16(kc) ||
+        (reinterpret_cast<uintptr_t>(ks) & 1u) != 0)
+        return LC_ERR_INVALID_ARG;
+    if (scores && ld < batch->max_c) return LC_ERR_INVALID_ARG;
+    if (topk && k < 1) return LC_ERR_INVALID_ARG;
+    if ((HI != 4 && HI != 8) || dI != 64 || (topk && k > 4096) || batch->total_q > 65535)
+        return LC_ERR_UNSUPPORTED;
+    if (batch->total_q == 0) return LC_OK;
+    float *sc = scores;
+    int64_t sld = ld;
+    if (!scores) {
+        const size_t need = index_ws_bytes(batch);
+        if (need > 0 && (!ws || ws_bytes < need)) return LC_ERR_WORKSPACE;
+        sc = reinterpret_cast<float *>(ws);
+        sld = batch->max_c;
+    }
+    lc_status s = LC_OK;
+    if (sld > 0) s = index_mx_launch(fmt, qc, qs, w, kc, ks, *batch, HI, m, sc, sld, dev_err, st);
     if (s == LC_OK && topk) s = topk_launch(sc, sld, *batch, m, k, topk, dev_err, st);
     return finish(s, st, dev_err);
 }

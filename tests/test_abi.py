@@ -129,6 +129,20 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
                              0, 0x1000, 0x1000, 0x1000)
     assert lib.decode_append(ctypes.byref(Lidx), P, P, P, P, P, P, lc.LC_BF16, N,
                              N) == lc.LC_ERR_INVALID_ARG
+    # MX quantizer and indexer: size not a multiple of 32, unknown format,
+    # misaligned codes, unsupported head shape
+    assert lib.mx_quantize(P, 48, lc.LC_MXFP8, lc.LC_BF16, P, P, N) == lc.LC_ERR_INVALID_ARG
+    assert lib.mx_quantize(P, 64, 6, lc.LC_BF16, P, P, N) == lc.LC_ERR_INVALID_ARG
+    assert lib.mx_quantize(P, 64, lc.LC_MXFP4, lc.LC_BF16, N, P, N) == lc.LC_ERR_INVALID_ARG
+    A = ctypes.c_void_p(0x1008)
+    assert lib.lightning_index_mx(6, P, P, P, P, P, ctypes.byref(b), 8, 64, 4, P, 8, 0, N, N, 0,
+                                  N, N) == lc.LC_ERR_INVALID_ARG
+    assert lib.lightning_index_mx(lc.LC_MXFP4, P, P, P, A, P, ctypes.byref(b), 8, 64, 4, P, 8, 0,
+                                  N, N, 0, N, N) == lc.LC_ERR_INVALID_ARG
+    assert lib.lightning_index_mx(lc.LC_MXFP8, P, P, P, P, P, ctypes.byref(b), 8, 32, 4, P, 8, 0,
+                                  N, N, 0, N, N) == lc.LC_ERR_UNSUPPORTED
+    assert lib.lightning_index_mx(lc.LC_MXFP8, P, P, P, P, P, ctypes.byref(b), 8, 64, 4, N, 0, 16,
+                                  P, N, 0, N, N) == lc.LC_ERR_WORKSPACE
     # nothing above reached a kernel
     assert lib.lc_launch_count() == launches_before
 
