@@ -151,7 +151,11 @@ lc_status rope_rotate(void *X, int64_t n, int32_t hv, int32_t d, int64_t pos0, i
  *   qI [total_q, HI, dI] dtype;  w [total_q, HI] fp32;  kI [cu_c[B], HI, dI] dtype
  *   scores [total_q, ld] fp32, ld >= max_c, or NULL
  *   topk   [total_q, k] int32 or NULL: when non-NULL the call also selects
- *          (as topk_select) and, if scores is NULL, keeps the scores in ws.
+ *          (as topk_select) and, if scores is NULL, keeps the scores in ws:
+ *          with bf16 inputs, H_I in {4, 8}, d_I = 64, one sequence and at
+ *          least 64 query rows, the fused tensor-core selection (ws at least
+ *          lc_workspace_size); otherwise the scores of as many rows as ws
+ *          holds at a time (ws at least one row, max_c * 4 bytes).
  * At least one of scores / topk must be non-NULL; kI must be 16-byte aligned.
  * Supported: HI in {1,2,4,8}; dI in {32,64}; 1 <= k <= 4096. */
 lc_status lightning_index(const void *qI, const float *w, const void *kI, const lc_batch *batch,
@@ -312,7 +316,10 @@ lc_status lightning_index_topk_noalloc(const void *qI, const float *w, const voi
                                        int32_t *dev_err, lc_stream stream);
 
 /* Bytes of `ws` a call needs (0 = none).  `op` is one of lc_op; unused
- * arguments are ignored.  Host only; reads only the batch's host fields. */
+ * arguments are ignored.  Host only; reads only the batch's host fields.
+ * LC_OP_LIGHTNING_INDEX: the fused tensor-core plan where the shape takes it,
+ * and at most 64 MiB of score rows otherwise (the whole score matrix is
+ * never required). */
 typedef enum {
     LC_OP_LIGHTNING_INDEX = 0, /* with topk != NULL and scores == NULL */
     LC_OP_TOPK_SELECT = 1,

@@ -1,5 +1,6 @@
 // C ABI of the lcattn library: host-side validation, workspace sizing and
 // dispatch to the kernels.  Nothing here allocates device memory.
+#include <algorithm>
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
@@ -31,9 +32,16 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
 size_t index_tc_workspace(const lc_batch &b, int k);
 lc_status mx_quantize_launch(const void *X, int64_t n, int fmt, lc_dtype dt, uint8_t *codes,
                              uint8_t *scales, cudaStream_t st);
+lc_status index_rows_launch(const void *qI, const float *w, const void *kI, const lc_batch &b,
+                            int HI, int dI, int m, lc_dtype dt, float *scores, int64_t ld,
+                            int64_t r0, int64_t nrows, int32_t *dev_err, cudaStream_t st);
+lc_status topk_rows_launch(const float *scores, int64_t ld, const lc_batch &b, int m, int k,
+                           int32_t *topk, int64_t r0, int64_t nrows, int32_t *dev_err,
+                           cudaStream_t st);
 lc_status index_mx_launch(int fmt, const uint8_t *qc, const uint8_t *qs, const float *w,
                           const uint8_t *kc, const uint8_t *ks, const lc_batch &b, int HI, int m,
-                          float *scores, int64_t ld, int32_t *dev_err, cudaStream_t st);
+                          float *scores, int64_t ld, int64_t r0, int64_t nrows, int32_t *dev_err,
+                          cudaStream_t st);
 lc_status hca_tc_launch(const void *Q, const void *Kc, const void *Vc, const void *Kraw,
                         const void *Vraw, const lc_batch &b, int H, int d, int m, int W,
                         float scale, const float *sink, int rope, lc_dtype dt, void *O,
@@ -115,8 +123,16 @@ static bool dtype_ok(lc_dtype dt) { return dt == LC_F32 || dt == LC_BF16; }
 
 static size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Scores kept in the workspace by the fused call without the tensor-core
+// plan: all rows when that fits in INDEX_WS_CHUNK bytes, else as many rows as
+// fit (at least one), taken in turn.
+constexpr size_t INDEX_WS_CHUNK = (size_t)64 << 20;
+
 static size_t index_ws_bytes(const lc_batch *b) {
-    return align_up(sizeof(float) * (size_t)b->total_q * (size_t)b->max_c);
+    const size_t row = sizeof(float) * (size_t)b->max_c;
+    const size_t all = row * (size_t)b->total_q;
+    if (all <= INDEX_WS_CHUNK || row == 0) return align_up(all);
+    return align_up(row > INDEX_WS_CHUNK ? row : INDEX_WS_CHUNK / row * row);
 }
 
 static lc_status compress_common(const void *K, const void *V, const float *G_K,
@@ -211,12 +227,26 @@ lc_status lightning_index(const void *qI, const float *w, const void *kI, const 
     float *sc = scores;
     int64_t sld = ld;
     if (!scores) {
-        const size_t need = index_ws_bytes(batch);
+        // at least one row of scores; lc_workspace_size's size holds all rows
+        // or INDEX_WS_CHUNK bytes of them
+        const size_t need = sizeof(float) * (size_t)batch->max_c;
         if (need > 0 && (!ws || ws_bytes < need)) return LC_ERR_WORKSPACE;
         sc = reinterpret_cast<float *>(ws);
         sld = batch->max_c;
         if (sld == 0) {
             lc_status s = topk_launch(sc, 0, *batch, m, k, topk, dev_err, st);
+            return finish(s, st, dev_err);
+        }
+        const int64_t fit = (int64_t)(ws_bytes / (sizeof(float) * (size_t)sld));
+        if (fit < batch->total_q) {
+            // the scores of `fit` rows at a time, each chunk selected before the next
+            lc_status s = LC_OK;
+            for (int64_t r0 = 0; r0 < batch->total_q && s == LC_OK; r0 += fit) {
+                const int64_t n = std::min(fit, batch->total_q - r0);
+                s = index_rows_launch(qI, w, kI, *batch, HI, dI, m, dtype, sc, sld, r0, n,
+                                      dev_err, st);
+                if (s == LC_OK) s = topk_rows_launch(sc, sld, *batch, m, k, topk, r0, n, dev_err, st);
+            }
             return finish(s, st, dev_err);
         }
     }
@@ -255,15 +285,23 @@ lc_status lightning_index_mx(int32_t fmt, const uint8_t *qc, const uint8_t *qs, 
     if (batch->total_q == 0) return LC_OK;
     float *sc = scores;
     int64_t sld = ld;
+    int64_t fit = batch->total_q;  // rows whose scores are kept at a time
     if (!scores) {
-        const size_t need = index_ws_bytes(batch);
+        const size_t need = sizeof(float) * (size_t)batch->max_c;  // at least one row
         if (need > 0 && (!ws || ws_bytes < need)) return LC_ERR_WORKSPACE;
         sc = reinterpret_cast<float *>(ws);
         sld = batch->max_c;
+        if (sld > 0)
+            fit = std::min(fit, (int64_t)(ws_bytes / (sizeof(float) * (size_t)sld)));
     }
     lc_status s = LC_OK;
-    if (sld > 0) s = index_mx_launch(fmt, qc, qs, w, kc, ks, *batch, HI, m, sc, sld, dev_err, st);
-    if (s == LC_OK && topk) s = topk_launch(sc, sld, *batch, m, k, topk, dev_err, st);
+    for (int64_t r0 = 0; r0 < batch->total_q && s == LC_OK; r0 += fit) {
+        const int64_t n = std::min(fit, batch->total_q - r0);
+        if (sld > 0)
+            s = index_mx_launch(fmt, qc, qs, w, kc, ks, *batch, HI, m, sc, sld, r0, n, dev_err,
+                                st);
+        if (s == LC_OK && topk) s = topk_rows_launch(sc, sld, *batch, m, k, topk, r0, n, dev_err, st);
+    }
     return finish(s, st, dev_err);
 }
 
@@ -335,7 +373,11 @@ size_t lc_workspace_size(int32_t op, const lc_batch *batch, int32_t H, int32_t d
     if (!batch) return 0;
     switch (op) {
         case LC_OP_LIGHTNING_INDEX: {
-            const size_t a = index_ws_bytes(batch), b = index_tc_workspace(*batch, k);
+            // the fused tensor-core plan where the shape takes it (bf16 inputs),
+            // else scores of bounded row chunks
+            const bool tc = batch->B == 1 && (HI == 4 || HI == 8) && dI == 64 &&
+                            batch->max_q >= 64 && batch->max_c > 0;
+            const size_t a = index_ws_bytes(batch), b = tc ? index_tc_workspace(*batch, k) : 0;
             return a > b ? a : b;
         }
         default: return 0;

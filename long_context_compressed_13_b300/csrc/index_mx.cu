@@ -37,11 +37,6 @@ namespace {
 
 constexpr int MX_FP8 = 8, MX_FP4 = 4;
 
-// 2^(s - 127) for an E8M0 byte s (s = 0 is 2^-127, an fp32 subnormal).
-__device__ __forceinline__ float e8m0_value(uint32_t s) {
-    return s == 0u ? __uint_as_float(1u << 22) : __uint_as_float(s << 23);
-}
-
 // Shared exponent of a block with largest magnitude amax: floor(log2 amax) -
 // emax, clamped to the E8M0 range; -127 for an all-zero block.
 __device__ __forceinline__ int mx_shared_exp(float amax, int emax) {
@@ -133,12 +128,13 @@ __global__ void __launch_bounds__(256) k_index_stream_mx(const uint8_t *__restri
                                                          const uint8_t *__restrict__ ks,
                                                          Batch bt, int m,
                                                          float *__restrict__ scores, int64_t ld,
-                                                         int64_t chunk, int32_t *dev_err) {
+                                                         int64_t chunk, int64_t r0,
+                                                         int32_t *dev_err) {
     constexpr int CB = 64 * FMT / 8;      // code bytes per head
     constexpr int EPS = 32 / HI;          // entries per warp step
     constexpr int U = 2;                  // warp steps in flight
     const unsigned FULL = 0xffffffffu;
-    const int64_t r = blockIdx.y;
+    const int64_t r = r0 + blockIdx.y;  // written to scores row blockIdx.y
     const int b = seq_of_row(bt, r);
     const int64_t t = bt.q_pos0[b] + (r - bt.cu_q[b]);
     const int64_t c_beg = bt.cu_c[b], Tc = bt.cu_c[b + 1] - c_beg;
@@ -163,7 +159,7 @@ __global__ void __launch_bounds__(256) k_index_stream_mx(const uint8_t *__restri
     const int64_t e_lo = (int64_t)blockIdx.x * chunk;
     const int64_t e_hi = min(e_lo + chunk, ld);
     const int64_t v_hi = min(e_hi, nv);
-    float *out = scores + r * ld;
+    float *out = scores + (int64_t)blockIdx.y * ld;
     const uint8_t *kbase = kc + (c_beg * HI + h) * CB;
     const uint16_t *sbase = reinterpret_cast<const uint16_t *>(ks) + c_beg * HI + h;
     for (int64_t base = e_lo + (int64_t)warp * EPS * U; base < v_hi; base += 8 * EPS * U) {
@@ -228,35 +224,38 @@ lc_status mx_quantize_launch(const void *X, int64_t n, int fmt, lc_dtype dt, uin
 template <int FMT, int HI>
 static void launch_index_mx(dim3 grid, const uint8_t *qc, const uint8_t *qs, const float *w,
                             const uint8_t *kc, const uint8_t *ks, const lc_batch &b, int m,
-                            float *scores, int64_t ld, int64_t chunk, int32_t *dev_err,
-                            cudaStream_t st) {
+                            float *scores, int64_t ld, int64_t chunk, int64_t r0,
+                            int32_t *dev_err, cudaStream_t st) {
     auto kfn = k_index_stream_mx<FMT, HI>;
     LC_LAUNCH_AS("k_index_stream_mx", kfn, grid, dim3(256), 0, st, qc, qs, w, kc, ks, to_dev(b),
-                 m, scores, ld, chunk, dev_err);
+                 m, scores, ld, chunk, r0, dev_err);
 }
 
-// Scores [total_q, ld] of the MX indexer (d_I = 64, H_I in {4, 8}).
+// Scores of query rows r0 .. r0 + nrows - 1 (into scores rows 0 .. nrows - 1)
+// of the MX indexer (d_I = 64, H_I in {4, 8}).
 lc_status index_mx_launch(int fmt, const uint8_t *qc, const uint8_t *qs, const float *w,
                           const uint8_t *kc, const uint8_t *ks, const lc_batch &b, int HI, int m,
-                          float *scores, int64_t ld, int32_t *dev_err, cudaStream_t st) {
-    if (b.total_q > 65535 || (HI != 4 && HI != 8)) return LC_ERR_UNSUPPORTED;
-    // about eight CTAs per SM over the whole batch, at least 1024 entries each
-    const int64_t want_x = (148 * 8 + b.total_q - 1) / b.total_q;
+                          float *scores, int64_t ld, int64_t r0, int64_t nrows, int32_t *dev_err,
+                          cudaStream_t st) {
+    if (nrows <= 0) return LC_OK;
+    if (nrows > 65535 || (HI != 4 && HI != 8)) return LC_ERR_UNSUPPORTED;
+    // about eight CTAs per SM over the rows, at least 1024 entries each
+    const int64_t want_x = (148 * 8 + nrows - 1) / nrows;
     int64_t chunk = (ld + want_x - 1) / want_x;
     if (chunk < 1024) chunk = 1024;
     chunk = (chunk + 255) / 256 * 256;
     const int64_t gx = (ld + chunk - 1) / chunk;
     if (gx > 65535) return LC_ERR_UNSUPPORTED;
-    const dim3 grid((unsigned)gx, (unsigned)b.total_q);
+    const dim3 grid((unsigned)gx, (unsigned)nrows);
     if (fmt == MX_FP8)
-        HI == 8 ? launch_index_mx<MX_FP8, 8>(grid, qc, qs, w, kc, ks, b, m, scores, ld, chunk,
+        HI == 8 ? launch_index_mx<MX_FP8, 8>(grid, qc, qs, w, kc, ks, b, m, scores, ld, chunk, r0,
                                             dev_err, st)
-                : launch_index_mx<MX_FP8, 4>(grid, qc, qs, w, kc, ks, b, m, scores, ld, chunk,
+                : launch_index_mx<MX_FP8, 4>(grid, qc, qs, w, kc, ks, b, m, scores, ld, chunk, r0,
                                             dev_err, st);
     else
-        HI == 8 ? launch_index_mx<MX_FP4, 8>(grid, qc, qs, w, kc, ks, b, m, scores, ld, chunk,
+        HI == 8 ? launch_index_mx<MX_FP4, 8>(grid, qc, qs, w, kc, ks, b, m, scores, ld, chunk, r0,
                                             dev_err, st)
-                : launch_index_mx<MX_FP4, 4>(grid, qc, qs, w, kc, ks, b, m, scores, ld, chunk,
+                : launch_index_mx<MX_FP4, 4>(grid, qc, qs, w, kc, ks, b, m, scores, ld, chunk, r0,
                                             dev_err, st);
     return check_launch();
 }

@@ -47,12 +47,18 @@ namespace lc {
 
 using namespace sm100;
 
-lc_status index_scan_launch(const void *qI, const float *w, const void *kI, const lc_batch &b,
-                            int HI, int dI, int m, lc_dtype dt, float *scores, int64_t ld,
-                            const int32_t *row_mask, int32_t *dev_err, cudaStream_t st);
-lc_status topk_launch_masked(const float *scores, int64_t ld, const lc_batch &b, int m, int k,
-                             int32_t *topk, const int32_t *row_mask, int32_t *dev_err,
-                             cudaStream_t st);
+lc_status sample_threshold16_launch(const uint16_t *samp, int64_t lds, const lc_batch &b, int m,
+                                    int stride, int k, int rho, uint32_t *theta, int32_t *count,
+                                    int32_t *nfail, cudaStream_t st);
+lc_status cand_pick_warp_launch(const lc_batch &b, int m, int k, int cap, int ocap, int nwmax,
+                                const int32_t *count, const uint2 *cand, const int32_t *lcnt,
+                                const uint2 *priv, int gy, int cloc, int32_t *topk,
+                                int32_t *flist, int32_t *nfail, int32_t *dev_err,
+                                cudaStream_t st);
+lc_status topk_fallback_launch(const void *qI, const float *w, const void *kI, const lc_batch &b,
+                               int HI, int m, int k, const int32_t *flist, const int32_t *nfail,
+                               float *buf, int64_t ldb, int grid, int32_t *topk,
+                               cudaStream_t st);
 
 namespace {
 constexpr int IBM = 128;          // query rows per CTA
@@ -64,7 +70,7 @@ constexpr int EPI_COLS = 32;      // columns of a score buffer per epilogue thre
 constexpr int NBUF = 4;           // TMEM score buffers (one head each)
 constexpr int NSB = 5;            // shared-memory head boxes in flight
 constexpr uint32_t I_TMEM_COLS = 512;
-constexpr int MODE_MATERIALIZE = 0, MODE_FILTER = 1;
+constexpr int MODE_MATERIALIZE = 0, MODE_FILTER = 1, MODE_SAMPLE16 = 2;
 
 struct IdxCfg {
     static constexpr uint32_t HEAD_BOX = IBN * 128;         // 128 entries x 128 B
@@ -120,18 +126,19 @@ struct IdxTcArgs {
     int stride;              // map entry e is entry e*stride
     int m;
     int64_t chunk;           // map entries per CTA (multiple of IBN)
-    int64_t col_end;         // MATERIALIZE: columns [0, col_end) are written
+    int64_t col_end;         // MATERIALIZE, SAMPLE16: map columns [0, col_end)
     const float *w;          // [Nq, HI]
     float *out;              // MATERIALIZE: [Nq, ld]
+    uint16_t *out16;         // SAMPLE16: [Nq, ld] top 16 bits of the order keys
     int64_t ld;
     int vec_out;             // MATERIALIZE: out and ld allow 16-byte stores
     const uint32_t *theta;   // FILTER: [Nq] order-key thresholds
-    uint2 *cand;             // FILTER: [Nq, cap] overflow slots (order key, entry index)
+    uint2 *cand;             // FILTER: [Nq, ocap] overflow slots (order key, entry index)
     int32_t *count;          // FILTER: [Nq] overflow slots used (zeroed beforehand)
     uint2 *priv;             // FILTER: [Nq, gy, cloc] slots private to (row, CTA column)
     int32_t *lcnt;           // FILTER: [Nq, gy] private slots used
     int gy, cloc;
-    int cap;
+    int ocap;                // overflow slots per row
     int32_t *dev_err;
     long long stall;         // test hook (0: off): both MMA issuers first wait this
                              // many clocks on a barrier nothing completes
@@ -154,8 +161,8 @@ __global__ void __launch_bounds__(I_THREADS, 1)
     if (nv_last > a.Tc) nv_last = a.Tc;
     const int64_t nvm = (nv_last + a.stride - 1) / a.stride;  // visible map entries (max)
     const int64_t c0 = (int64_t)blockIdx.y * a.chunk;
-    const int64_t c_end = MODE == MODE_MATERIALIZE ? min(c0 + a.chunk, a.col_end)
-                                                   : min(c0 + a.chunk, nvm);
+    const int64_t c_end = MODE != MODE_FILTER ? min(c0 + a.chunk, a.col_end)
+                                              : min(c0 + a.chunk, nvm);
     const int64_t comp_end = min(c_end, nvm);  // computed columns [c0, comp_end)
     const int n_t = comp_end > c0 ? (int)((comp_end - c0 + IBN - 1) / IBN) : 0;
     const int n_all = n_t * HI;  // head boxes / score buffers of this CTA
@@ -167,12 +174,13 @@ __global__ void __launch_bounds__(I_THREADS, 1)
         // tcgen05 instruction, so that every CTA that runs one holds tensor
         // memory.  MATERIALIZE: columns [c0, c_end) of the rows are -inf.
         // FILTER: the rows have no candidate in this CTA column.
+        // SAMPLE16: nothing (only visible columns are stored, and none is here)
         if (MODE == MODE_MATERIALIZE) {
             for (int r = warp; r < IBM && row0 + r < a.Nq; r += I_THREADS / 32) {
                 float *dst = a.out + (row0 + r) * a.ld;
                 for (int64_t e = c0 + lane; e < c_end; e += 32) dst[e] = -INFINITY;
             }
-        } else {
+        } else if (MODE == MODE_FILTER) {
             for (int r = tid; r < IBM; r += I_THREADS)
                 if (row0 + r < a.Nq) a.lcnt[(size_t)(row0 + r) * a.gy + blockIdx.y] = 0;
         }
@@ -348,6 +356,27 @@ __global__ void __launch_bounds__(I_THREADS, 1)
                         if (c < lim) dst[c] = c < vis ? s : -INFINITY;
                     }
                 }
+            } else if (MODE == MODE_SAMPLE16) {
+                // the top 16 bits of each visible column's order key (a key
+                // truncated this way is a lower bound of the full key)
+                uint16_t *dst = a.out16 + row * a.ld + e0;
+                const int64_t vis = min(nvr, c_end) - e0;
+                if (vis >= EPI_COLS) {
+                    uint32_t p[EPI_COLS / 2];
+#pragma unroll
+                    for (int c = 0; c < EPI_COLS / 2; ++c)
+                        p[c] = (order_key(acc[c].x) >> 16) | (order_key(acc[c].y) & 0xffff0000u);
+#pragma unroll
+                    for (int u = 0; u < EPI_COLS / 8; ++u)
+                        reinterpret_cast<uint4 *>(dst)[u] =
+                            make_uint4(p[4 * u], p[4 * u + 1], p[4 * u + 2], p[4 * u + 3]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < EPI_COLS; ++c) {
+                        const float sv = (c & 1) ? acc[c >> 1].y : acc[c >> 1].x;
+                        if (c < vis) dst[c] = (uint16_t)(order_key(sv) >> 16);
+                    }
+                }
             } else {
                 // bit c of `below` (after the reversal) = column c is under theta
                 const float2 nt = make_float2(-thf, -thf);
@@ -368,7 +397,7 @@ __global__ void __launch_bounds__(I_THREADS, 1)
                     const int n = __popc(cand);
                     const int lb = atomicAdd(lcount + quad * 32 + lane, n);
                     uint2 *pr = a.priv + ((size_t)row * a.gy + blockIdx.y) * a.cloc;
-                    uint2 *cr = a.cand + row * a.cap;
+                    uint2 *cr = a.cand + row * a.ocap;
                     int ob = 0;  // overflow slot of local slot s: s + ob
                     if (lb + n > a.cloc) {
                         const int first = max(lb, a.cloc);
@@ -392,7 +421,7 @@ __global__ void __launch_bounds__(I_THREADS, 1)
                             const uint2 kv = make_uint2(order_key(stg[c]), (uint32_t)(e0 + 8 * rd + c));
                             if (base < a.cloc)
                                 pr[base] = kv;
-                            else if (base + ob < a.cap)
+                            else if (base + ob < a.ocap)
                                 cr[base + ob] = kv;
                             ++base;
                         }
@@ -422,49 +451,6 @@ __global__ void __launch_bounds__(I_THREADS, 1)
     }
 }
 
-// theta[r] = the rho-th largest order key among the row's visible sampled
-// scores (0, i.e. "keep everything", when the row has at most k visible
-// entries or fewer than rho samples); count[r] = fail[r] = 0.  With
-// `staged`, the row's keys are first copied to shared memory (one read of
-// the row) and the radix passes run there.
-__global__ void __launch_bounds__(512) k_sample_threshold(const float *__restrict__ samp,
-                                                          int64_t lds, Batch bt, int m,
-                                                          int stride, int k, int rho, int staged,
-                                                          uint32_t *theta, int32_t *count,
-                                                          int32_t *fail) {
-    constexpr int NT = 512;
-    extern __shared__ uint32_t skeys[];
-    __shared__ RadixScratch rs;
-    const int64_t r = blockIdx.x;
-    const int64_t t = bt.q_pos0[0] + r;
-    const int64_t Tc = bt.cu_c[1] - bt.cu_c[0];
-    int64_t nv = n_vis(t, m);
-    if (nv > Tc) nv = Tc;
-    const int64_t nvs = (nv + stride - 1) / stride;
-    uint32_t th = 0;
-    if (nv > k && rho <= nvs) {
-        int need_left;
-        if (staged) {
-            // lds is a multiple of 4 and the buffer 16-byte aligned
-            const float4 *row4 = reinterpret_cast<const float4 *>(samp + r * lds);
-            for (int j = threadIdx.x; 4 * j < nvs; j += NT) {
-                const float4 x = __ldg(row4 + j);
-                reinterpret_cast<uint4 *>(skeys)[j] =
-                    make_uint4(order_key(x.x), order_key(x.y), order_key(x.z), order_key(x.w));
-            }
-            __syncthreads();
-            th = radix_kth_largest_smem<NT>(skeys, (int)nvs, rho, rs, &need_left);
-        } else {
-            th = radix_kth_largest<NT>(samp + r * lds, nvs, rho, rs, &need_left);
-        }
-    }
-    if (threadIdx.x == 0) {
-        theta[r] = th;
-        count[r] = 0;
-        fail[r] = 0;
-    }
-}
-
 // Ascending bitonic sort of P (power of two) uint32 values in shared memory.
 __device__ __forceinline__ void bitonic_sort_u32_asc(uint32_t *a, int P) {
     constexpr int NT = 512;
@@ -486,24 +472,28 @@ __device__ __forceinline__ void bitonic_sort_u32_asc(uint32_t *a, int P) {
     __syncthreads();
 }
 
-// Exact top-k of each row's candidates: radix selection of the k-th largest
+// Exact top-k of each row's candidates, one CTA per row (for rows too long
+// for the warp-per-row kernel's bitmaps): radix selection of the k-th largest
 // key K* in shared memory; the candidates above K* and the `need` lowest-index
 // candidates equal to K* are collected (in any order, one shared atomic per
 // warp) and written out in ascending index order: through a bitmap over the
 // row's visible entries when it fits in the `R` words that held the keys and
 // indices, else by a bitonic sort.  A row's candidates are the private slots
 // of each of its gy CTA columns (lcnt of them in each) followed by its
-// overflow slots (count); rows with a total outside [k, cap] are marked in
-// fail[].  Shared memory: R >= 2 cap words (keys,
-// indices, later the bitmap), PK collected indices, P tie slots (PK, P: powers
-// of two >= k, cap); the tie slots double as the radix selection's spare.
-__global__ void __launch_bounds__(512) k_cand_pick(Batch bt, int m, int k, int cap, int R, int PK,
-                                                   int P, const int32_t *__restrict__ count,
+// overflow slots (count, in a region of ocap slots); rows with a total
+// outside [k, cap], or an overflow past its region, are appended to the
+// failed-row list.  Shared memory: R >= 2 cap words (keys, indices, later the
+// bitmap), PK collected indices, P tie slots (PK, P: powers of two >= k,
+// cap); the tie slots double as the radix selection's spare.
+__global__ void __launch_bounds__(512) k_cand_pick(Batch bt, int m, int k, int cap, int ocap,
+                                                   int R, int PK, int P,
+                                                   const int32_t *__restrict__ count,
                                                    const uint2 *__restrict__ cand,
                                                    const int32_t *__restrict__ lcnt,
                                                    const uint2 *__restrict__ priv, int gy,
                                                    int cloc, int32_t *__restrict__ topk,
-                                                   int32_t *fail, int32_t *dev_err) {
+                                                   int32_t *flist, int32_t *nfail,
+                                                   int32_t *dev_err) {
     constexpr int NT = 512, NW = NT / 32;
     const unsigned FULL = 0xffffffffu;
     extern __shared__ uint32_t sbuf[];
@@ -542,8 +532,8 @@ __global__ void __launch_bounds__(512) k_cand_pick(Batch bt, int m, int k, int c
     __syncthreads();
     const int n_priv = s_priv, n_over = count[r];
     const int n = n_priv + n_over;
-    if (n < k || n > cap) {
-        if (threadIdx.x == 0) fail[r] = 1;
+    if (n < k || n > cap || n_over > ocap) {
+        if (threadIdx.x == 0) flist[atomicAdd(nfail, 1)] = (int32_t)r;
         return;
     }
     for (int y = warp; y < gy; y += NW) {
@@ -564,7 +554,7 @@ __global__ void __launch_bounds__(512) k_cand_pick(Batch bt, int m, int k, int c
         }
     }
     for (int i = threadIdx.x; i < n_over; i += NT) {
-        const uint2 ki = cand[r * cap + i];
+        const uint2 ki = cand[r * ocap + i];
         keys[n_priv + i] = ki.x;
         idx[n_priv + i] = ki.y;
     }
@@ -660,12 +650,17 @@ int pow2_at_least(int x) {
 int64_t pick_chunk(int64_t Nq, int64_t n_cols);
 
 struct FusedPlan {
-    int stride, rho, cap, P, PK, R, staged, gy, cloc;
-    int64_t ns, lds, chunk;
-    size_t off_samp, off_theta, off_count, off_fail, off_cand, off_lcnt, off_priv, off_full, total;
+    int stride, rho, cap, ocap, P, PK, R, gy, cloc, nwmax, fb_grid;
+    int64_t ns, lds, chunk, ldb;
+    size_t off_samp, off_theta, off_count, off_flist, off_nfail, off_cand, off_lcnt, off_priv,
+        total;
 };
 
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Rows whose visible entries fit the warp-per-row pick's bitmaps (two words
+// per 32 entries, a warp each, eight warps a CTA, 227 KB at most).
+constexpr int NW_WARP_MAX = 1024;
 
 FusedPlan plan_fused(const lc_batch &b, int k) {
     FusedPlan p{};
@@ -684,24 +679,19 @@ FusedPlan plan_fused(const lc_batch &b, int k) {
     cap = (cap + 31) & ~31;
     if (cap > 16384) cap = 16384;
     p.cap = cap;
+    // the overflow region per row: half of cap (a row whose overflow passes
+    // it is redone by the fallback)
+    p.ocap = cap / 2;
     p.P = pow2_at_least(cap);
     p.PK = pow2_at_least(k);
     // k_cand_pick orders its output through a bitmap of the row when that fits
     p.R = 2 * cap;
     const int64_t nw = (n + 31) / 32;
     if (nw > p.R && 4 * (nw + p.PK + p.P) <= 200 * 1024) p.R = (int)nw;
+    p.nwmax = nw <= NW_WARP_MAX ? (int)nw : 0;  // 0: the CTA-per-row pick
     p.ns = (n + p.stride - 1) / p.stride;
-    p.lds = (p.ns + 3) & ~(int64_t)3;
-    p.staged = 4 * p.lds <= 200 * 1024;  // k_sample_threshold keeps the row in shared memory
+    p.lds = (p.ns + 7) & ~(int64_t)7;  // uint16 keys, 16-byte rows
     const size_t Nq = (size_t)b.total_q;
-    size_t o = 0;
-    p.off_samp = o;  o += al256(sizeof(float) * Nq * (size_t)p.lds);
-    p.off_theta = o; o += al256(sizeof(uint32_t) * Nq);
-    p.off_count = o; o += al256(sizeof(int32_t) * Nq);
-    p.off_fail = o;  o += al256(sizeof(int32_t) * Nq);
-    p.off_cand = o;  o += al256(sizeof(uint2) * Nq * (size_t)p.cap);
-    // the candidate pass's CTA columns and each (row, column)'s private slots:
-    // twice the column's share of `cap`, so that overflow needs a skewed row
     p.chunk = pick_chunk(b.total_q, n);
     p.gy = (int)((n + p.chunk - 1) / p.chunk);
     int64_t cl = (2 * (int64_t)p.cap * p.chunk + n - 1) / n;
@@ -709,9 +699,22 @@ FusedPlan plan_fused(const lc_batch &b, int k) {
     if (cl < 32) cl = 32;
     if (cl > p.cap) cl = p.cap;
     p.cloc = (int)cl;
+    // the fallback's row buffers reuse the sample region (dead by then); at
+    // least one row, at most two CTAs per SM
+    p.ldb = (n + 3) & ~(int64_t)3;
+    size_t samp = sizeof(uint16_t) * Nq * (size_t)p.lds;
+    const size_t one_row = sizeof(float) * (size_t)p.ldb;
+    if (samp < one_row) samp = one_row;
+    p.fb_grid = (int)std::min<size_t>(296, samp / one_row);
+    size_t o = 0;
+    p.off_samp = o;  o += al256(samp);
+    p.off_theta = o; o += al256(sizeof(uint32_t) * Nq);
+    p.off_count = o; o += al256(sizeof(int32_t) * Nq);
+    p.off_flist = o; o += al256(sizeof(int32_t) * Nq);
+    p.off_nfail = o; o += al256(sizeof(int32_t));
+    p.off_cand = o;  o += al256(sizeof(uint2) * Nq * (size_t)p.ocap);
     p.off_lcnt = o;  o += al256(sizeof(int32_t) * Nq * (size_t)p.gy);
     p.off_priv = o;  o += al256(sizeof(uint2) * Nq * (size_t)p.gy * (size_t)p.cloc);
-    p.off_full = o;  o += al256(sizeof(float) * Nq * (size_t)n);
     p.total = o;
     return p;
 }
@@ -740,7 +743,10 @@ lc_status launch_tc(const CUtensorMap &mQ, const CUtensorMap &mK, const IdxTcArg
     const int64_t gy = (n_cols + a.chunk - 1) / a.chunk;
     if (gy < 1 || gy > 65535) return LC_ERR_UNSUPPORTED;
     dim3 grid((unsigned)((a.Nq + IBM - 1) / IBM), (unsigned)gy);
-    LC_LAUNCH_AS(MODE == MODE_FILTER ? "k_index_tc<filter>" : "k_index_tc<materialize>", kfn, grid, dim3(I_THREADS), SMEM, st, mQ, mK, a);
+    LC_LAUNCH_AS(MODE == MODE_FILTER      ? "k_index_tc<filter>"
+                 : MODE == MODE_SAMPLE16 ? "k_index_tc<sample16>"
+                                         : "k_index_tc<materialize>",
+                 kfn, grid, dim3(I_THREADS), SMEM, st, mQ, mK, a);
     return check_launch();
 }
 
@@ -817,14 +823,15 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
     const FusedPlan p = plan_fused(b, k);
     if (!ws || ws_bytes < p.total) return LC_ERR_WORKSPACE;
     uint8_t *base = static_cast<uint8_t *>(ws);
-    float *samp = reinterpret_cast<float *>(base + p.off_samp);
+    uint16_t *samp = reinterpret_cast<uint16_t *>(base + p.off_samp);
     uint32_t *theta = reinterpret_cast<uint32_t *>(base + p.off_theta);
     int32_t *count = reinterpret_cast<int32_t *>(base + p.off_count);
-    int32_t *fail = reinterpret_cast<int32_t *>(base + p.off_fail);
+    int32_t *flist = reinterpret_cast<int32_t *>(base + p.off_flist);
+    int32_t *nfail = reinterpret_cast<int32_t *>(base + p.off_nfail);
     uint2 *cand = reinterpret_cast<uint2 *>(base + p.off_cand);
     int32_t *lcnt = reinterpret_cast<int32_t *>(base + p.off_lcnt);
     uint2 *priv = reinterpret_cast<uint2 *>(base + p.off_priv);
-    float *full = reinterpret_cast<float *>(base + p.off_full);
+    float *fbuf = reinterpret_cast<float *>(base + p.off_samp);  // after the sample is read
     const int64_t Tc = b.total_c;
     const uint64_t pitch = (uint64_t)HI * IDI * 2;
 
@@ -835,34 +842,21 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
                            (uint64_t)HI * IDI, pitch * p.stride, IDI, IBN))
         return LC_ERR_CUDA;
     lc_status s;
-    // 1. sampled scores
+    // 1. 16-bit keys of every s-th entry's score (visible columns only)
     {
         IdxTcArgs a = base_args(b, qI, w, m, dev_err);
         a.Tc = Tc;
         a.stride = p.stride;
         a.col_end = p.ns;
-        a.out = samp;
+        a.out16 = samp;
         a.ld = p.lds;
-        a.vec_out = 1;  // 256-byte aligned buffer, ld a multiple of 4
         a.chunk = pick_chunk(b.total_q, p.ns);
-        s = launch_tc_hi<MODE_MATERIALIZE>(HI, mQ, mKs, a, p.ns, st);
+        s = launch_tc_hi<MODE_SAMPLE16>(HI, mQ, mKs, a, p.ns, st);
         if (s != LC_OK) return s;
     }
-    // 2. thresholds
-    {
-        const size_t smem = p.staged ? sizeof(uint32_t) * (size_t)p.lds : 0;
-        static size_t attr = 0;
-        if (smem > 48 * 1024 && smem > attr) {
-            if (cudaFuncSetAttribute(k_sample_threshold,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem) != cudaSuccess)
-                return LC_ERR_CUDA;
-            attr = smem;
-        }
-        LC_LAUNCH(k_sample_threshold, dim3((unsigned)b.total_q), dim3(512), smem, st, samp,
-                  p.lds, to_dev(b), m, p.stride, k, p.rho, p.staged, theta, count, fail);
-    }
-    if ((s = check_launch()) != LC_OK) return s;
+    // 2. thresholds (and the per-row overflow counts and the failed-row count zeroed)
+    s = sample_threshold16_launch(samp, p.lds, b, m, p.stride, k, p.rho, theta, count, nfail, st);
+    if (s != LC_OK) return s;
     // 3. candidates
     {
         IdxTcArgs a = base_args(b, qI, w, m, dev_err);
@@ -870,7 +864,7 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
         a.theta = theta;
         a.count = count;
         a.cand = cand;
-        a.cap = p.cap;
+        a.ocap = p.ocap;
         a.priv = priv;
         a.lcnt = lcnt;
         a.gy = p.gy;
@@ -881,7 +875,11 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
         if (s != LC_OK) return s;
     }
     // 4. exact selection among the candidates
-    {
+    if (p.nwmax > 0) {
+        s = cand_pick_warp_launch(b, m, k, p.cap, p.ocap, p.nwmax, count, cand, lcnt, priv, p.gy,
+                                  p.cloc, topk, flist, nfail, dev_err, st);
+        if (s != LC_OK) return s;
+    } else {
         const size_t smem = sizeof(uint32_t) * (size_t)(p.R + p.PK + p.P);
         static size_t attr = 0;
         if (smem > 48 * 1024 && smem > attr) {
@@ -891,14 +889,13 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
             attr = smem;
         }
         LC_LAUNCH(k_cand_pick, dim3((unsigned)b.total_q), dim3(512), smem, st, to_dev(b), m, k,
-                  p.cap, p.R, p.PK, p.P, count, cand, lcnt, priv, p.gy, p.cloc, topk, fail,
-                  dev_err);
+                  p.cap, p.ocap, p.R, p.PK, p.P, count, cand, lcnt, priv, p.gy, p.cloc, topk,
+                  flist, nfail, dev_err);
         if ((s = check_launch()) != LC_OK) return s;
     }
-    // 5. exact fallback for the rows marked in fail[] (no work when none is)
-    s = index_scan_launch(qI, w, kI, b, HI, dI, m, dt, full, Tc, fail, dev_err, st);
-    if (s != LC_OK) return s;
-    return topk_launch_masked(full, Tc, b, m, k, topk, fail, dev_err, st);
+    // 5. exact top-k of the failed rows from recomputed scores (no work when none failed)
+    return topk_fallback_launch(qI, w, kI, b, HI, m, k, flist, nfail, fbuf, p.ldb, p.fb_grid,
+                                topk, st);
 }
 
 }  // namespace lc

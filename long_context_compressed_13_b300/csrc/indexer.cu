@@ -105,17 +105,16 @@ __global__ void __launch_bounds__(256) k_index_tiled(const T *__restrict__ qI,
     }
 }
 
-// Query rows blockIdx.y, blockIdx.y + gridDim.y, ...; threads cover (entry,
-// head) pairs, HI lanes per entry reduce with shuffles.  DI * sizeof(T) bytes
-// are read per thread with 16-byte vector loads.  row_mask (nullable): rows
-// with row_mask[r] == 0 are skipped.
+// Query rows r0 + blockIdx.y, r0 + blockIdx.y + gridDim.y, ... (nrows of
+// them; row r0 + i is written to scores row i); threads cover (entry, head)
+// pairs, HI lanes per entry reduce with shuffles.  DI * sizeof(T) bytes are
+// read per thread with 16-byte vector loads.
 template <typename T, int DI, int HI>
 __global__ void __launch_bounds__(256) k_index_scan(const T *__restrict__ qI,
                                                     const float *__restrict__ w,
                                                     const T *__restrict__ kI, Batch bt, int m,
                                                     float *__restrict__ scores, int64_t ld,
-                                                    int64_t total_q,
-                                                    const int32_t *__restrict__ row_mask,
+                                                    int64_t r0, int64_t nrows,
                                                     int32_t *dev_err) {
     __shared__ float sq[HI][DI];
     __shared__ float sw[HI];
@@ -124,8 +123,8 @@ __global__ void __launch_bounds__(256) k_index_scan(const T *__restrict__ qI,
     constexpr int EPV = 16 / (int)sizeof(T);      // elements per vector
     const int h = threadIdx.x % HI;
     const int el = threadIdx.x / HI;
-    for (int64_t r = blockIdx.y; r < total_q; r += gridDim.y) {
-        if (row_mask && row_mask[r] == 0) continue;
+    for (int64_t ri = blockIdx.y; ri < nrows; ri += gridDim.y) {
+        const int64_t r = r0 + ri;
         const int b = seq_of_row(bt, r);
         const int64_t t = bt.q_pos0[b] + (r - bt.cu_q[b]);
         const int64_t c_beg = bt.cu_c[b], Tc = bt.cu_c[b + 1] - c_beg;
@@ -139,7 +138,7 @@ __global__ void __launch_bounds__(256) k_index_scan(const T *__restrict__ qI,
             sq[i / DI][i % DI] = io<T>::ld(qI + r * HI * DI + i);
         if (threadIdx.x < HI) sw[threadIdx.x] = w[r * HI + threadIdx.x];
         __syncthreads();
-        float *out = scores + r * ld;
+        float *out = scores + ri * ld;
         for (int64_t j0 = (int64_t)blockIdx.x * EPB; j0 < ld; j0 += (int64_t)gridDim.x * EPB) {
             const int64_t j = j0 + el;
             float part = 0.f;
@@ -181,12 +180,10 @@ __global__ void __launch_bounds__(256) k_index_stream(const __nv_bfloat16 *__res
                                                       const float *__restrict__ w,
                                                       const __nv_bfloat16 *__restrict__ kI,
                                                       Batch bt, int m, float *__restrict__ scores,
-                                                      int64_t ld, int64_t chunk,
-                                                      const int32_t *__restrict__ row_mask,
+                                                      int64_t ld, int64_t chunk, int64_t r0,
                                                       int32_t *dev_err) {
     constexpr int L = HI / 4;  // 512-byte loads per entry
-    const int64_t r = blockIdx.y;
-    if (row_mask && row_mask[r] == 0) return;
+    const int64_t r = r0 + blockIdx.y;  // written to scores row blockIdx.y
     const int b = seq_of_row(bt, r);
     const int64_t t = bt.q_pos0[b] + (r - bt.cu_q[b]);
     const int64_t c_beg = bt.cu_c[b], Tc = bt.cu_c[b + 1] - c_beg;
@@ -213,7 +210,7 @@ __global__ void __launch_bounds__(256) k_index_stream(const __nv_bfloat16 *__res
     const int64_t e_lo = (int64_t)blockIdx.x * chunk;
     const int64_t e_hi = min(e_lo + chunk, ld);
     const int64_t v_hi = min(e_hi, nv);
-    float *out = scores + r * ld;
+    float *out = scores + (int64_t)blockIdx.y * ld;
     const __nv_bfloat16 *krow = kI + (c_beg * HI + g) * 64 + sl * 8;
     for (int64_t base = e_lo + 32 * warp; base < v_hi; base += 32 * 8) {
         const int n_here = (int)min((int64_t)32, v_hi - base);
@@ -263,70 +260,75 @@ static bool stream_ok(const void *qI, const void *kI, int HI, int dI, lc_dtype d
 }
 
 static lc_status launch_stream(const void *qI, const float *w, const void *kI, const lc_batch &b,
-                               int HI, int m, float *scores, int64_t ld,
-                               const int32_t *row_mask, int32_t *dev_err, cudaStream_t st) {
-    if (b.total_q > 65535) return LC_ERR_UNSUPPORTED;
-    // about eight CTAs per SM over the whole batch, at least 1024 entries each
-    const int64_t want_x = (148 * 8 + b.total_q - 1) / b.total_q;
+                               int HI, int m, float *scores, int64_t ld, int64_t r0,
+                               int64_t nrows, int32_t *dev_err, cudaStream_t st) {
+    if (nrows > 65535) return LC_ERR_UNSUPPORTED;
+    // about eight CTAs per SM over the rows, at least 1024 entries each
+    const int64_t want_x = (148 * 8 + nrows - 1) / nrows;
     int64_t chunk = (ld + want_x - 1) / want_x;
     if (chunk < 1024) chunk = 1024;
     chunk = (chunk + 255) / 256 * 256;
     const int64_t gx = (ld + chunk - 1) / chunk;
     if (gx > 65535) return LC_ERR_UNSUPPORTED;
-    const dim3 grid((unsigned)gx, (unsigned)b.total_q);
+    const dim3 grid((unsigned)gx, (unsigned)nrows);
     if (HI == 8)
-        LC_LAUNCH_AS("k_index_stream", k_index_stream<8>, grid, dim3(256), 0, st, (const __nv_bfloat16 *)qI, w,
-                  (const __nv_bfloat16 *)kI, to_dev(b), m, scores, ld, chunk, row_mask, dev_err);
+        LC_LAUNCH_AS("k_index_stream", k_index_stream<8>, grid, dim3(256), 0, st,
+                     (const __nv_bfloat16 *)qI, w, (const __nv_bfloat16 *)kI, to_dev(b), m,
+                     scores, ld, chunk, r0, dev_err);
     else
-        LC_LAUNCH_AS("k_index_stream", k_index_stream<4>, grid, dim3(256), 0, st, (const __nv_bfloat16 *)qI, w,
-                  (const __nv_bfloat16 *)kI, to_dev(b), m, scores, ld, chunk, row_mask, dev_err);
+        LC_LAUNCH_AS("k_index_stream", k_index_stream<4>, grid, dim3(256), 0, st,
+                     (const __nv_bfloat16 *)qI, w, (const __nv_bfloat16 *)kI, to_dev(b), m,
+                     scores, ld, chunk, r0, dev_err);
     return check_launch();
 }
 
 template <typename T, int DI, int HI>
 static void launch_scan(const void *qI, const float *w, const void *kI, const lc_batch &b, int m,
-                        float *scores, int64_t ld, const int32_t *row_mask, int32_t *dev_err,
+                        float *scores, int64_t ld, int64_t r0, int64_t nrows, int32_t *dev_err,
                         cudaStream_t st) {
     constexpr int EPB = 256 / HI;
-    const int64_t rows = b.total_q < 65535 ? b.total_q : 65535;
+    const int64_t rows = nrows < 65535 ? nrows : 65535;
     int64_t gx = (ld + EPB - 1) / EPB;
     int64_t want = (148 * 8 + rows - 1) / rows;  // ~8 blocks per SM overall
     if (gx > want) gx = want;
     if (gx < 1) gx = 1;
     auto kfn = k_index_scan<T, DI, HI>;
-    LC_LAUNCH_AS("k_index_scan", kfn, dim3((unsigned)gx, (unsigned)rows), dim3(256), 0, st, (const T *)qI, w,
-              (const T *)kI, to_dev(b), m, scores, ld, b.total_q, row_mask, dev_err);
+    LC_LAUNCH_AS("k_index_scan", kfn, dim3((unsigned)gx, (unsigned)rows), dim3(256), 0, st,
+                 (const T *)qI, w, (const T *)kI, to_dev(b), m, scores, ld, r0, nrows, dev_err);
 }
 
 template <typename T, int DI>
 static lc_status scan_hi(const void *qI, const float *w, const void *kI, const lc_batch &b, int HI,
-                         int m, float *scores, int64_t ld, const int32_t *row_mask,
+                         int m, float *scores, int64_t ld, int64_t r0, int64_t nrows,
                          int32_t *dev_err, cudaStream_t st) {
     switch (HI) {
-        case 1: launch_scan<T, DI, 1>(qI, w, kI, b, m, scores, ld, row_mask, dev_err, st); break;
-        case 2: launch_scan<T, DI, 2>(qI, w, kI, b, m, scores, ld, row_mask, dev_err, st); break;
-        case 4: launch_scan<T, DI, 4>(qI, w, kI, b, m, scores, ld, row_mask, dev_err, st); break;
-        case 8: launch_scan<T, DI, 8>(qI, w, kI, b, m, scores, ld, row_mask, dev_err, st); break;
+        case 1: launch_scan<T, DI, 1>(qI, w, kI, b, m, scores, ld, r0, nrows, dev_err, st); break;
+        case 2: launch_scan<T, DI, 2>(qI, w, kI, b, m, scores, ld, r0, nrows, dev_err, st); break;
+        case 4: launch_scan<T, DI, 4>(qI, w, kI, b, m, scores, ld, r0, nrows, dev_err, st); break;
+        case 8: launch_scan<T, DI, 8>(qI, w, kI, b, m, scores, ld, r0, nrows, dev_err, st); break;
         default: return LC_ERR_UNSUPPORTED;
     }
     return check_launch();
 }
 
-// Streaming (per-row) scores for the rows with row_mask[r] != 0 (all rows if
-// row_mask is null).
-lc_status index_scan_launch(const void *qI, const float *w, const void *kI, const lc_batch &b,
+// Per-row scores of query rows r0 .. r0 + nrows - 1 into scores rows 0 ..
+// nrows - 1 (streaming kernels: any batch, rows in any sequence).
+lc_status index_rows_launch(const void *qI, const float *w, const void *kI, const lc_batch &b,
                             int HI, int dI, int m, lc_dtype dt, float *scores, int64_t ld,
-                            const int32_t *row_mask, int32_t *dev_err, cudaStream_t st) {
+                            int64_t r0, int64_t nrows, int32_t *dev_err, cudaStream_t st) {
+    if (nrows <= 0) return LC_OK;
     if (stream_ok(qI, kI, HI, dI, dt)) {
-        const lc_status s = launch_stream(qI, w, kI, b, HI, m, scores, ld, row_mask, dev_err, st);
+        const lc_status s = launch_stream(qI, w, kI, b, HI, m, scores, ld, r0, nrows, dev_err, st);
         if (s != LC_ERR_UNSUPPORTED) return s;
     }
     if (dt == LC_F32)
-        return dI == 32 ? scan_hi<float, 32>(qI, w, kI, b, HI, m, scores, ld, row_mask, dev_err, st)
-                        : scan_hi<float, 64>(qI, w, kI, b, HI, m, scores, ld, row_mask, dev_err, st);
-    return dI == 32
-               ? scan_hi<__nv_bfloat16, 32>(qI, w, kI, b, HI, m, scores, ld, row_mask, dev_err, st)
-               : scan_hi<__nv_bfloat16, 64>(qI, w, kI, b, HI, m, scores, ld, row_mask, dev_err, st);
+        return dI == 32
+                   ? scan_hi<float, 32>(qI, w, kI, b, HI, m, scores, ld, r0, nrows, dev_err, st)
+                   : scan_hi<float, 64>(qI, w, kI, b, HI, m, scores, ld, r0, nrows, dev_err, st);
+    return dI == 32 ? scan_hi<__nv_bfloat16, 32>(qI, w, kI, b, HI, m, scores, ld, r0, nrows,
+                                                 dev_err, st)
+                    : scan_hi<__nv_bfloat16, 64>(qI, w, kI, b, HI, m, scores, ld, r0, nrows,
+                                                 dev_err, st);
 }
 
 template <typename T>
@@ -335,11 +337,13 @@ static lc_status launch_index(const void *qI, const float *w, const void *kI, co
                               cudaStream_t st) {
     if (b.max_q < 16) {
         if (std::is_same<T, __nv_bfloat16>::value && stream_ok(qI, kI, HI, dI, LC_BF16)) {
-            const lc_status s = launch_stream(qI, w, kI, b, HI, m, scores, ld, nullptr, dev_err, st);
+            const lc_status s =
+                launch_stream(qI, w, kI, b, HI, m, scores, ld, 0, b.total_q, dev_err, st);
             if (s != LC_ERR_UNSUPPORTED) return s;
         }
-        if (dI == 32) return scan_hi<T, 32>(qI, w, kI, b, HI, m, scores, ld, nullptr, dev_err, st);
-        return scan_hi<T, 64>(qI, w, kI, b, HI, m, scores, ld, nullptr, dev_err, st);
+        if (dI == 32)
+            return scan_hi<T, 32>(qI, w, kI, b, HI, m, scores, ld, 0, b.total_q, dev_err, st);
+        return scan_hi<T, 64>(qI, w, kI, b, HI, m, scores, ld, 0, b.total_q, dev_err, st);
     }
     const size_t smem = sizeof(float) * ((size_t)(TQ + TE) * (dI + 1) + TQ);
     if (smem > 48 * 1024 &&

@@ -29,16 +29,14 @@ namespace {
 constexpr int TK_THREADS = 512;
 }
 
-// row_mask (nullable): rows with row_mask[r] == 0 are skipped.
+// Query row r0 + blockIdx.x, its scores in row blockIdx.x of `scores`.
 __global__ void __launch_bounds__(TK_THREADS) k_topk_radix(const float *__restrict__ scores,
                                                            int64_t ld, Batch bt, int m, int k,
                                                            int32_t *__restrict__ topk,
-                                                           const int32_t *__restrict__ row_mask,
-                                                           int32_t *dev_err) {
+                                                           int64_t r0, int32_t *dev_err) {
     __shared__ RadixScratch rs;
     __shared__ int warp_sums[TK_THREADS / 32];
-    const int64_t r = blockIdx.x;
-    if (row_mask && row_mask[r] == 0) return;
+    const int64_t r = r0 + blockIdx.x;
     const int b = seq_of_row(bt, r);
     const int64_t t = bt.q_pos0[b] + (r - bt.cu_q[b]);
     const int64_t Tc = bt.cu_c[b + 1] - bt.cu_c[b];
@@ -53,28 +51,7 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk_radix(const float *__restri
         for (int i = threadIdx.x; i < k; i += TK_THREADS) out[i] = i < n ? i : -1;
         return;
     }
-    const float *row = scores + r * ld;
-    int need;
-    const uint32_t kstar = radix_kth_largest<TK_THREADS>(row, n, k, rs, &need);
-
-    // ordered compaction: keys > K*, then the first `need` keys == K*
-    int written = 0, eq_seen = 0;
-#pragma unroll 1
-    for (int64_t j0 = 0; j0 < n && written < k; j0 += TK_THREADS) {
-        const int64_t j = j0 + threadIdx.x;
-        uint32_t key = 0;
-        if (j < n) key = order_key(__ldg(row + j));
-        const int gt = (j < n) && key > kstar;
-        const int eq = (j < n) && key == kstar;
-        int eq_tot;
-        const int eq_before = block_exclusive_scan<TK_THREADS>(eq, warp_sums, &eq_tot);
-        const int take = gt || (eq && eq_seen + eq_before < need);
-        int take_tot;
-        const int pos = block_exclusive_scan<TK_THREADS>(take, warp_sums, &take_tot);
-        if (take && written + pos < k) out[written + pos] = (int32_t)j;
-        written += take_tot;
-        eq_seen += eq_tot;
-    }
+    radix_topk_row<TK_THREADS>(scores + (int64_t)blockIdx.x * ld, n, k, out, rs, warp_sums);
 }
 
 namespace cg = cooperative_groups;
@@ -87,8 +64,7 @@ constexpr int TC_STAGE_KEYS = 16384;  // keys of a slice staged in shared memory
 __global__ void __launch_bounds__(TC_THREADS) k_topk_cluster(const float *__restrict__ scores,
                                                              int64_t ld, Batch bt, int m, int k,
                                                              int32_t *__restrict__ topk,
-                                                             const int32_t *__restrict__ row_mask,
-                                                             int32_t *dev_err) {
+                                                             int64_t r0, int32_t *dev_err) {
     constexpr int NT = TC_THREADS, NW = NT / 32;
     cg::cluster_group cl = cg::this_cluster();
     extern __shared__ uint32_t skeys[];          // [TC_STAGE_KEYS]
@@ -100,8 +76,8 @@ __global__ void __launch_bounds__(TC_THREADS) k_topk_cluster(const float *__rest
     __shared__ int warp_sums[NW];
     const int C = (int)cl.num_blocks(), c = (int)cl.block_rank();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t r = blockIdx.x / C;            // every CTA of a cluster has the same row
-    if (row_mask && row_mask[r] == 0) return;    // the whole cluster returns
+    const int64_t rl = blockIdx.x / C;           // every CTA of a cluster has the same row
+    const int64_t r = r0 + rl;                   // its scores: row rl of `scores`
     const int b = seq_of_row(bt, r);
     const int64_t t = bt.q_pos0[b] + (r - bt.cu_q[b]);
     const int64_t Tc = bt.cu_c[b + 1] - bt.cu_c[b];
@@ -117,7 +93,7 @@ __global__ void __launch_bounds__(TC_THREADS) k_topk_cluster(const float *__rest
             out[i] = i < n ? (int32_t)i : -1;
         return;
     }
-    const float *row = scores + r * ld;
+    const float *row = scores + rl * ld;
     const int64_t lo = n * c / C, hi = n * (c + 1) / C;
     const int len = (int)(hi - lo);
     const bool staged = len <= TC_STAGE_KEYS;
@@ -236,14 +212,15 @@ __global__ void __launch_bounds__(TC_THREADS) k_topk_cluster(const float *__rest
     }
 }
 
-// Rows with row_mask[r] == 0 are skipped (row_mask nullable).
-lc_status topk_launch_masked(const float *scores, int64_t ld, const lc_batch &b, int m, int k,
-                             int32_t *topk, const int32_t *row_mask, int32_t *dev_err,
-                             cudaStream_t st) {
-    if (b.total_q == 0) return LC_OK;
+// Top-k of query rows r0 .. r0 + nrows - 1, whose scores are rows 0 .. nrows
+// - 1 of `scores`.
+lc_status topk_rows_launch(const float *scores, int64_t ld, const lc_batch &b, int m, int k,
+                           int32_t *topk, int64_t r0, int64_t nrows, int32_t *dev_err,
+                           cudaStream_t st) {
+    if (nrows <= 0) return LC_OK;
     // a few long rows: one 8-CTA cluster per row keeps the SMs busy
     constexpr int C = 8;
-    if (b.total_q <= 2 * 148 && b.max_c >= 4096 && b.total_q * C < (1ll << 31)) {
+    if (nrows <= 2 * 148 && b.max_c >= 4096 && nrows * C < (1ll << 31)) {
         static bool attr = false;
         if (!attr) {
             if (cudaFuncSetAttribute(k_topk_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -252,7 +229,7 @@ lc_status topk_launch_masked(const float *scores, int64_t ld, const lc_batch &b,
             attr = true;
         }
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(b.total_q * C));
+        cfg.gridDim = dim3((unsigned)(nrows * C));
         cfg.blockDim = dim3(TC_THREADS);
         cfg.dynamicSmemBytes = TC_STAGE_KEYS * sizeof(uint32_t);
         cfg.stream = st;
@@ -264,7 +241,7 @@ lc_status topk_launch_masked(const float *scores, int64_t ld, const lc_batch &b,
         cfg.attrs = at;
         cfg.numAttrs = 1;
         const cudaError_t e = cudaLaunchKernelEx(&cfg, k_topk_cluster, scores, ld, to_dev(b), m,
-                                                 k, topk, row_mask, dev_err);
+                                                 k, topk, r0, dev_err);
         note_launch("k_topk_cluster");
         if (e != cudaSuccess) {
             (void)cudaGetLastError();
@@ -272,14 +249,14 @@ lc_status topk_launch_masked(const float *scores, int64_t ld, const lc_batch &b,
         }
         return check_launch();
     }
-    LC_LAUNCH(k_topk_radix, dim3((unsigned)b.total_q), dim3(TK_THREADS), 0, st, scores, ld,
-              to_dev(b), m, k, topk, row_mask, dev_err);
+    LC_LAUNCH(k_topk_radix, dim3((unsigned)nrows), dim3(TK_THREADS), 0, st, scores, ld,
+              to_dev(b), m, k, topk, r0, dev_err);
     return check_launch();
 }
 
 lc_status topk_launch(const float *scores, int64_t ld, const lc_batch &b, int m, int k,
                       int32_t *topk, int32_t *dev_err, cudaStream_t st) {
-    return topk_launch_masked(scores, ld, b, m, k, topk, nullptr, dev_err, st);
+    return topk_rows_launch(scores, ld, b, m, k, topk, 0, b.total_q, dev_err, st);
 }
 
 }  // namespace lc

@@ -48,7 +48,15 @@ struct RadixScratch {
 // by four 8-bit radix passes (most significant digit first).  Returns the
 // key; *need_left receives how many keys equal to it rank within the top
 // `need`.  Requires 1 <= need <= n.  All threads of the block call it.
-template <int NT>
+// RO = false reads the row with plain loads (for a row this kernel itself
+// wrote: the read-only cache path does not see such writes).
+template <bool RO>
+__device__ __forceinline__ float ld_score(const float *p) {
+    if (RO) return __ldg(p);
+    return *p;
+}
+
+template <int NT, bool RO = true>
 __device__ uint32_t radix_kth_largest(const float *__restrict__ row, int64_t n, int need,
                                       RadixScratch &rs, int *need_left) {
     uint32_t prefix = 0, mask = 0;
@@ -58,7 +66,7 @@ __device__ uint32_t radix_kth_largest(const float *__restrict__ row, int64_t n, 
         for (int i = threadIdx.x; i < 256; i += NT) rs.hist[i] = 0;
         __syncthreads();
         for (int64_t j = threadIdx.x; j < n; j += NT) {
-            const uint32_t key = order_key(__ldg(row + j));
+            const uint32_t key = order_key(ld_score<RO>(row + j));
             if ((key & mask) == prefix) atomicAdd(&rs.hist[(key >> shift) & 255u], 1u);
         }
         __syncthreads();
@@ -179,6 +187,91 @@ __device__ uint32_t radix_kth_largest_smem(const uint32_t *keys, int n, int need
     }
     *need_left = need;
     return prefix;
+}
+
+// Exact top-k of one row of n visible scores (n > k) under the total order
+// (larger score first, then lower index), written as ascending indices to
+// out[0..k): radix selection of the k-th largest key K* and of how many
+// keys equal to K* rank within the top k, then one ordered compaction pass
+// (keys > K*, and the first `need` keys == K*) whose write positions come
+// from block-wide prefix sums.  All NT threads of the block call it.
+template <int NT, bool RO = true>
+__device__ void radix_topk_row(const float *__restrict__ row, int64_t n, int k, int32_t *out,
+                               RadixScratch &rs, int *warp_sums) {
+    int need;
+    const uint32_t kstar = radix_kth_largest<NT, RO>(row, n, k, rs, &need);
+    int written = 0, eq_seen = 0;
+#pragma unroll 1
+    for (int64_t j0 = 0; j0 < n && written < k; j0 += NT) {
+        const int64_t j = j0 + threadIdx.x;
+        uint32_t key = 0;
+        if (j < n) key = order_key(ld_score<RO>(row + j));
+        const int gt = (j < n) && key > kstar;
+        const int eq = (j < n) && key == kstar;
+        int eq_tot;
+        const int eq_before = block_exclusive_scan<NT>(eq, warp_sums, &eq_tot);
+        const int take = gt || (eq && eq_seen + eq_before < need);
+        int take_tot;
+        const int pos = block_exclusive_scan<NT>(take, warp_sums, &take_tot);
+        if (take && written + pos < k) out[written + pos] = (int32_t)j;
+        written += take_tot;
+        eq_seen += eq_tot;
+    }
+}
+
+// One radix digit of a warp-level selection: among the keys that match
+// `prefix` under `mask`, the digit (key >> shift) & 255 of the need-th
+// largest, from a histogram in the warp's own 256 shared-memory words `h`.
+// visit(f) must call f(key) once for every key of the set (each lane its
+// share).  On return `need` is the rank of the wanted key within the chosen
+// digit's bin.  Requires 1 <= need <= (keys matching prefix); all 32 lanes
+// call it.
+template <typename Visit>
+__device__ __forceinline__ uint32_t warp_radix_digit(uint32_t *h, Visit visit, uint32_t prefix,
+                                                     uint32_t mask, int shift, int &need) {
+    const unsigned FULL = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    for (int i = lane; i < 256; i += 32) h[i] = 0u;
+    __syncwarp();
+    visit([&](uint32_t key) {
+        if ((key & mask) == prefix) atomicAdd(&h[(key >> shift) & 255u], 1u);
+    });
+    __syncwarp();
+    // suffix sums over the 256 bins, 8 bins per lane, highest first
+    uint32_t c[8], mine = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        c[u] = h[255 - (lane * 8 + u)];
+        mine += c[u];
+    }
+    uint32_t incl = mine;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(FULL, incl, off);
+        if (lane >= off) incl += y;
+    }
+    const uint32_t excl = incl - mine;
+    const bool has = excl < (uint32_t)need && incl >= (uint32_t)need;
+    uint32_t digit = 0;
+    int rank = need;
+    if (has) {
+        uint32_t cum = excl;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (cum + c[u] >= (uint32_t)need) {
+                digit = 255u - (uint32_t)(lane * 8 + u);
+                rank = need - (int)cum;
+                break;
+            }
+            cum += c[u];
+        }
+    }
+    const unsigned who = __ballot_sync(FULL, has);
+    const int src = who ? __ffs(who) - 1 : 0;
+    digit = __shfl_sync(FULL, digit, src);
+    need = __shfl_sync(FULL, rank, src);
+    __syncwarp();  // h may be reused by the next digit
+    return digit;
 }
 
 }  // namespace lc

@@ -154,6 +154,19 @@ def test_workspace_size_covers_materialised_scores(lib):
     assert lib.lc_workspace_size(lc.LC_OP_TOPK_SELECT, ctypes.byref(b), 0, 0, 0, 0, 16) == 0
 
 
+def test_workspace_is_bounded_without_the_score_matrix(lib):
+    # the 1M-context chunk (4096 rows x 262144 entries: a 4 GiB score matrix)
+    # fits in 512 MiB, for the fused tensor-core plan and for any other path
+    b = _batch(total_q=4096, max_q=4096, max_c=262144)
+    for HI, dI in ((8, 64), (2, 64), (4, 32)):
+        n = lib.lc_workspace_size(lc.LC_OP_LIGHTNING_INDEX, ctypes.byref(b), 0, 0, HI, dI, 1024)
+        assert 0 < n <= 512 << 20, (HI, dI, n)
+    # a score matrix that fits in the chunk bound is kept whole
+    small = _batch(total_q=300, max_q=300, max_c=1000)
+    n = lib.lc_workspace_size(lc.LC_OP_LIGHTNING_INDEX, ctypes.byref(small), 0, 0, 2, 64, 32)
+    assert n >= 300 * 1000 * 4
+
+
 def test_binding_fails_loudly_without_a_device(lib):
     import torch
     if torch.cuda.is_available():

@@ -141,3 +141,48 @@ def test_fused_topk_ties_take_the_fallback(lc):
     for r in list(range(5, 9)) + [100, 101, 102]:
         assert gsel[r].tolist() == list(range(k))
     _check_selection(gsel, I, (tpos + 1) // 4, k)
+
+
+def test_fused_topk_rows_past_the_warp_bitmaps(lc):
+    # 40960 entries per row: more than the warp-per-row pick's bitmaps hold,
+    # so the CTA-per-row pick runs; rows with all-zero scores fail the
+    # candidate check and go through the fallback's recomputed rows
+    T, k = 163840, 256
+    L = wl.csa_layer(T=T, H=8, d=64, HI=8, dI=64, m=4, k=k, W=16, dtype="bf16", seed=76,
+                     q_from=T - 192)
+    qI, w = L["qI"].clone(), L["w"].clone()
+    qI[3] = 0
+    w[150] = 0
+    b = lc.DeviceBatch.from_workload(L["batch"])
+    tpos = np.array(L["batch"].positions())
+    _, sel = lc.lightning_index(qI.cuda(), w.cuda(), L["kI"].cuda(), b, 4, scores=False, k=k,
+                                topk=True)
+    torch.cuda.synchronize()
+    assert lc.last_kernel() == "k_topk_fallback"
+    I = oracle.index(qI, w, L["kI"], tpos, 4)
+    gsel = sel.cpu().numpy()
+    for r in (3, 150):
+        assert gsel[r].tolist() == list(range(k))
+    _check_selection(gsel, I, (tpos + 1) // 4, k)
+
+
+@pytest.mark.parametrize("dtype,HI,dI", [("f32", 4, 32), ("bf16", 2, 64)])
+def test_fused_topk_in_row_chunks_equals_one_pass(lc, dtype, HI, dI):
+    # without the tensor-core plan the fused call keeps the scores of as many
+    # rows as the workspace holds and selects them chunk by chunk: the result
+    # is the one of a workspace that holds every row
+    T, k = 4096, 32
+    L = wl.csa_layer(T=T, H=8, d=64, HI=HI, dI=dI, m=4, k=k, W=16, dtype=dtype, seed=77,
+                     q_from=T - 300)
+    b = lc.DeviceBatch.from_workload(L["batch"])
+    qI, w, kI = L["qI"].cuda(), L["w"].cuda(), L["kI"].cuda()
+    row = 4 * b.max_c
+    full = torch.empty(300 * row, dtype=torch.uint8, device="cuda")
+    small = torch.empty(7 * row + 5, dtype=torch.uint8, device="cuda")  # 7 rows at a time
+    _, a = lc.lightning_index(qI, w, kI, b, 4, scores=False, k=k, topk=True, ws=full)
+    _, c = lc.lightning_index(qI, w, kI, b, 4, scores=False, k=k, topk=True, ws=small)
+    torch.cuda.synchronize()
+    assert torch.equal(a, c)
+    tpos = np.array(L["batch"].positions())
+    I = oracle.index(L["qI"], L["w"], L["kI"], tpos, 4)
+    _check_selection(c.cpu().numpy(), I, (tpos + 1) // 4, k)

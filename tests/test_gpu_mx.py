@@ -147,3 +147,19 @@ def test_mx_index_rejects_bad_arguments(lc):
         lc.lightning_index_mx(8, qc, qs, D["w"].cuda(), kc.view(-1)[1:1 + kc.numel() - 16],
                               ks, b, 4)
     assert e.value.status == 1
+
+
+def test_mx_index_in_row_chunks(lc):
+    D = _layer(8, seed=5, B=9)
+    b = lc.DeviceBatch.from_workload(D["batch"])
+    qc, qs = lc.mx_quantize(D["qI"].cuda(), 4)
+    kc, ks = lc.mx_quantize(D["kI"].cuda(), 4)
+    row = 4 * b.max_c
+    out = []
+    for nbytes in (9 * row, 2 * row + 3):
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        _, sel = lc.lightning_index_mx(4, qc, qs, D["w"].cuda(), kc, ks, b, 4, scores=False,
+                                       k=D["k"], topk=True, ws=ws)
+        out.append(sel)
+    torch.cuda.synchronize()
+    assert torch.equal(out[0], out[1])
