@@ -76,7 +76,30 @@ NCU_STAGE_TRAFFIC = {
     # the decode step's kernels at the full benchmarked size: streaming
     # indexer 2505.4 MB, cluster top-k 9.8 MB, CSA attention 40.2 MB
     ("csa_decode", "step"): 2555.4e6,
+    # the layer pair at 1M: k_hca_tc 140.8 MB read + 84.2 MB written
+    ("layer_pair_1m", "hca_dense_attn"): 225.0e6,
+    # index + top-k: candidate pass 343.1, 16-bit sample 23.4, thresholds
+    # 67.1, candidate pick 79.9, fallback 0 (MB read + written)
+    ("layer_pair_1m", "lightning_index+topk"): 513.5e6,
+    # k_sparse_tc 1121.8 MB read + 128.0 MB written
+    ("layer_pair_1m", "sparse_mqa_attn"): 1249.8e6,
+    # the 32K CSA prefill: k_sparse_tc 625.4 + 503.7 MB; index + top-k
+    # kernels 642.8 MB
+    ("csa_prefill", "sparse_mqa_attn"): 1129.1e6,
+    ("csa_prefill", "lightning_index+topk"): 642.8e6,
 }
+
+
+def gather_bound(keys_sum, d, n_tokens, H, k, ms, peaks):
+    """The CSA attention's gathered bytes over its time, against the measured
+    copy bandwidth: each token reads the K and V rows of its keys (selected
+    entries and window tokens, d bf16 values each) once, its selection (k
+    int32), its Q and writes its O.  The gather of random 256-byte rows, not
+    the tensor cores, bounds that kernel."""
+    b = float(keys_sum * d * 2 * 2 + n_tokens * (k * 4 + 2 * H * d * 2))
+    gbs = b / (ms / 1e3) / 1e9
+    return {"sparse_mqa_attn_gather": {"bytes": b, "achieved": gbs, "unit": "GB/s",
+                                       "peak": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"]}}
 
 
 def load_peaks():
@@ -238,7 +261,12 @@ class LayerPair:
             "index_flop": float(2 * HI * dI * nv_c.sum()),
             "csa_attn_flop": float(4 * self.d * self.H * keys_csa.sum()),
             "hca_attn_flop": float(4 * self.d * self.H * keys_hca.sum()),
+            "csa_keys": int(keys_csa.sum()),
         }
+
+    def stage_extra(self, stage_ms, peaks):
+        return gather_bound(self.work()["csa_keys"], self.d, self.chunk, self.H, self.k,
+                            stage_ms[self.STAGES.index("sparse_mqa_attn")], peaks)
 
     def step(self, events=None):
         lc, c, h = self.lc, self.P["csa"], self.P["hca"]
@@ -617,7 +645,11 @@ class CsaPrefill:
         nv = (t + 1) // self.m
         keys = np.minimum(nv, self.k) + _n_window(t, self.W)
         return {"index_flop": float(2 * L["HI"] * L["dI"] * nv.sum()),
-                "attn_flop": float(4 * self.d * self.H * keys.sum())}
+                "attn_flop": float(4 * self.d * self.H * keys.sum()), "keys": int(keys.sum())}
+
+    def stage_extra(self, stage_ms, peaks):
+        return gather_bound(self.work()["keys"], self.d, self.T, self.H, self.k,
+                            stage_ms[self.STAGES.index("sparse_mqa_attn")], peaks)
 
     def step(self, events=None):
         lc, L = self.lc, self.L
@@ -859,6 +891,8 @@ def measure(wk, args, dist, device, peaks, world, rank, cpu_budget):
         "dev_err": err,
         "clocks": clocks,
     }
+    if hasattr(wk, "stage_extra"):
+        rec.update(wk.stage_extra(stage_ms, peaks))
     if hasattr(wk, "extra"):
         rec.update(wk.extra())
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
