@@ -90,6 +90,20 @@ NCU_STAGE_TRAFFIC = {
 }
 
 
+# --decode-ctx LO,HI: the decode workloads on a shorter context range (a
+# smaller case of the same kernels for profiler captures); None = the
+# configured ~U[65536, 262144]
+DECODE_CTX = None
+
+
+def decode_config(device):
+    if DECODE_CTX is None:
+        return wl.CONFIGS["csa_decode"](device=device)
+    lo, hi = DECODE_CTX
+    return wl.csa_decode(B=64, ctx_lo=lo, ctx_hi=hi, H=128, d=128, HI=8, dI=64, m=4, k=1024,
+                         W=128, dtype="bf16", seed=3, device=device)
+
+
 def gather_bound(keys_sum, d, n_tokens, H, k, ms, peaks):
     """The CSA attention's gathered bytes over its time, against the measured
     copy bandwidth: each token reads the K and V rows of its keys (selected
@@ -333,7 +347,7 @@ class Decode:
 
     def __init__(self, lc, device, seed=3):
         self.lc = lc
-        D = wl.CONFIGS["csa_decode"](device=device)
+        D = decode_config(device)
         assert D["seed"] == seed
         self.D = D
         self.chunk = D["B"]  # query tokens per step
@@ -385,8 +399,9 @@ class Decode:
         return ins, {"O": self.O}
 
     def config(self, world):
+        lo, hi = DECODE_CTX or (65536, 262144)
         return {"workload": "csa_decode: 64 sequences, one query token each at its last "
-                            "position, contexts ~U[65536, 262144] (seed 3), CSA m=4, indexer "
+                            f"position, contexts ~U[{lo}, {hi}] (seed 3), CSA m=4, indexer "
                             "8x64, top-k 1024, window 128, Q [64,128,128]",
                 "batch": self.D["B"], "heads": self.H, "head_dim": self.d,
                 "context_mean": float(np.mean(self.D["ctx"])),
@@ -513,7 +528,7 @@ class DecodeIncremental:
 
     def __init__(self, lc, device, seed=3):
         self.lc = lc
-        D = wl.CONFIGS["csa_decode"](device=device)
+        D = decode_config(device)
         assert D["seed"] == seed
         self.ctx0 = list(D["ctx"])
         B, d, HI, dI, m, W = D["B"], D["d"], D["HI"], D["dI"], D["m"], D["W"]
@@ -1099,8 +1114,13 @@ def main():
     # a shorter context keeps the same kernels on a smaller case (profiler
     # captures); the measured workload is the default 1,048,576 tokens
     ap.add_argument("--ctx", type=int, default=1 << 20)
+    ap.add_argument("--decode-ctx", default=None,
+                    help="LO,HI: decode contexts ~U[LO, HI] (profiler captures)")
     ap.add_argument("--workload", default="all", choices=["all", *WORKLOADS])
     args = ap.parse_args()
+    if args.decode_ctx:
+        global DECODE_CTX
+        DECODE_CTX = tuple(int(x) for x in args.decode_ctx.split(","))
     if args.impl == "reference":
         run_reference(args)
     else:
