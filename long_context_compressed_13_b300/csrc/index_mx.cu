@@ -20,12 +20,15 @@
 //                 step, read as one contiguous span): it loads the head's 64
 //                 key codes (64 B MXFP8, 32 B MXFP4) and its two block scales,
 //                 converts code pairs to f16x2 (exact: every element is a
-//                 half) and accumulates each 32-value block's dot product with
-//                 mixed-precision FMAs (f16 multiplicands, exact products, fp32
-//                 addend), then scales each block by 2^(q exponent + k
-//                 exponent).  Shuffles over the H_I lanes of an entry add the
+//                 half) and accumulates each 32-value block's dot product:
+//                 MXFP4 with packed half FMAs over groups of 8 pairs (exact:
+//                 the products are multiples of 1/4 below 37, a group's sums
+//                 stay below 512) added in fp32; MXFP8 with mixed-precision
+//                 FMAs (f16 multiplicands, exact products, fp32 addend); then
+//                 each block is scaled by 2^(q exponent + k exponent).  Shuffles over the H_I lanes of an entry add the
 //                 ReLU-weighted heads.  HBM-bound: per entry H_I * (d_I * bits
 //                 / 8 + d_I / 32) bytes.
+#include <cuda_fp16.h>
 #include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
@@ -75,15 +78,21 @@ __global__ void __launch_bounds__(256) k_mx_quantize(const T *__restrict__ X, in
 // Element pairs -> f16x2 (every E4M3 and E2M1 element is exactly a half).
 // E4M3: two bytes of a 32-bit word (half 0 or 1); E2M1: one byte (two nibbles,
 // the even-indexed value in the low nibble becomes the low half).
+// One conversion instruction per pair (cvt .f16x2 from .e4m3x2 / .e2m1x2):
+// the lower element goes to the lower half.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t word, int half) {
-    const __nv_fp8x2_storage_t s = (__nv_fp8x2_storage_t)(half ? (word >> 16) : (word & 0xffffu));
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(s, __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+    const uint16_t s = (uint16_t)(half ? (word >> 16) : (word & 0xffffu));
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(s));
+    return h;
 }
 __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t word, int byte) {
-    const __nv_fp4x2_storage_t s = (__nv_fp4x2_storage_t)((word >> (8 * byte)) & 0xffu);
-    const __half2_raw h = __nv_cvt_fp4x2_to_halfraw2(s, __NV_E2M1);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+    const uint32_t b = (word >> (8 * byte)) & 0xffu;
+    uint32_t h;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+        : "=r"(h)
+        : "r"(b));
+    return h;
 }
 
 // acc += a.lo * b.lo + a.hi * b.hi for f16x2 a, b: products of two halves are
@@ -132,7 +141,7 @@ __global__ void __launch_bounds__(256) k_index_stream_mx(const uint8_t *__restri
                                                          int32_t *dev_err) {
     constexpr int CB = 64 * FMT / 8;      // code bytes per head
     constexpr int EPS = 32 / HI;          // entries per warp step
-    constexpr int U = 2;                  // warp steps in flight
+    constexpr int U = FMT == MX_FP4 ? 4 : 2;  // warp steps in flight (16-byte loads: 8)
     const unsigned FULL = 0xffffffffu;
     const int64_t r = r0 + blockIdx.y;  // written to scores row blockIdx.y
     const int b = seq_of_row(bt, r);
@@ -180,10 +189,32 @@ __global__ void __launch_bounds__(256) k_index_stream_mx(const uint8_t *__restri
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             float a0 = 0.f, a1 = 0.f;  // the two 32-value blocks
+            if (FMT == MX_FP4) {
+                // E2M1 x E2M1 products are multiples of 1/4 of magnitude <= 36,
+                // so a packed half FMA chain of 8 products per half stays
+                // below 512 and is exact; each group of 16 products then
+                // joins the block's fp32 sum
 #pragma unroll
-            for (int i = 0; i < 16; ++i) a0 = fma2_f16_f32(qh[i], kv[u].pair(i), a0);
+                for (int grp = 0; grp < 4; ++grp) {
+                    __half2 acc = __float2half2_rn(0.f);
 #pragma unroll
-            for (int i = 16; i < 32; ++i) a1 = fma2_f16_f32(qh[i], kv[u].pair(i), a1);
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t kp = kv[u].pair(8 * grp + i), qp = qh[8 * grp + i];
+                        acc = __hfma2(*reinterpret_cast<const __half2 *>(&qp),
+                                      *reinterpret_cast<const __half2 *>(&kp), acc);
+                    }
+                    const float2 f = __half22float2(acc);
+                    if (grp < 2)
+                        a0 += f.x + f.y;
+                    else
+                        a1 += f.x + f.y;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) a0 = fma2_f16_f32(qh[i], kv[u].pair(i), a0);
+#pragma unroll
+                for (int i = 16; i < 32; ++i) a1 = fma2_f16_f32(qh[i], kv[u].pair(i), a1);
+            }
             const int ke0 = (int)(sk[u] & 0xffu) - 127, ke1 = (int)(sk[u] >> 8) - 127;
             const float d = scalbnf(a0, qe0 + ke0) + scalbnf(a1, qe1 + ke1);
             float p = wh * fmaxf(d, 0.f);
