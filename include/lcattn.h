@@ -152,7 +152,7 @@ lc_status rope_rotate(void *X, int64_t n, int32_t hv, int32_t d, int64_t pos0, i
  *   scores [total_q, ld] fp32, ld >= max_c, or NULL
  *   topk   [total_q, k] int32 or NULL: when non-NULL the call also selects
  *          (as topk_select) and, if scores is NULL, keeps the scores in ws:
- *          with bf16 inputs, H_I in {4, 8}, d_I = 64, one sequence and at
+ *          with bf16 inputs, H_I in {4, 8}, d_I = 64 and a sequence of at
  *          least 64 query rows, the fused tensor-core selection (ws at least
  *          lc_workspace_size); otherwise the scores of as many rows as ws
  *          holds at a time (ws at least one row, max_c * 4 bytes).

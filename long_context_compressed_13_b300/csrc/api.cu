@@ -375,8 +375,8 @@ size_t lc_workspace_size(int32_t op, const lc_batch *batch, int32_t H, int32_t d
         case LC_OP_LIGHTNING_INDEX: {
             // the fused tensor-core plan where the shape takes it (bf16 inputs),
             // else scores of bounded row chunks
-            const bool tc = batch->B == 1 && (HI == 4 || HI == 8) && dI == 64 &&
-                            batch->max_q >= 64 && batch->max_c > 0;
+            const bool tc = (HI == 4 || HI == 8) && dI == 64 && batch->max_q >= 64 &&
+                            batch->max_c > 0;
             const size_t a = index_ws_bytes(batch), b = tc ? index_tc_workspace(*batch, k) : 0;
             return a > b ? a : b;
         }

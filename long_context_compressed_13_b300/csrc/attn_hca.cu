@@ -1,9 +1,10 @@
 // HCA dense attention on the 5th-generation tensor cores, bf16, head dim 128,
-// one sequence (page "DeepSeek-V4 技术解析…", §1.1, HCA paragraph: attention
-// over every compressed entry, plus the sliding-window branch).
+// any ragged batch (page "DeepSeek-V4 技术解析…", §1.1, HCA paragraph:
+// attention over every compressed entry, plus the sliding-window branch).
 //
-// A CTA owns two M = 128 tiles of query rows of Q[total_q*H, 128] (256
-// consecutive rows, 256/H tokens) and walks the union of their keys: the
+// A CTA owns two M = 128 tiles of one sequence's query rows of Q[total_q*H,
+// 128] (256 consecutive rows, 256/H tokens; a sequence's rows are covered by
+// its own run of CTAs) and walks the union of their keys: the
 // compressed entries 0 .. n_vis(t_last)-1, then the raw window positions,
 // in tiles of BN = 128 keys.  Both query tiles share every K/V tile, so each
 // key is read from L2 once per 256 query rows.
@@ -98,11 +99,9 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
 }  // namespace
 
 struct HcaArgs {
-    int64_t n_rows;       // total_q * H
+    Batch bt;             // device batch arrays (any number of sequences)
+    int have_c, have_r;   // compressed entries / raw window present
     int H;
-    const int64_t *q_pos0, *raw_pos0;  // device scalars of the single sequence
-    int64_t Tc;           // stored compressed entries
-    int64_t Nraw;         // stored raw rows
     int m, W;
     float scale_log2;
     const float *sink;    // [H] per-head sink logits or NULL
@@ -124,14 +123,30 @@ __global__ void __launch_bounds__(H_THREADS, 1)
     volatile int *abort = &bars.abort;
     const unsigned FULL = 0xffffffffu;
 
-    // ---- rows, tokens and the key range of the CTA
-    const int64_t q_pos0 = __ldg(a.q_pos0), raw_pos0 = __ldg(a.raw_pos0);
-    const int64_t row0 = (int64_t)blockIdx.x * (2 * HBM_);
-    const int64_t rows_here = min((int64_t)(2 * HBM_), a.n_rows - row0);
+    // ---- the CTA's sequence and its 256-row tile there (rows = token x head):
+    // sequence b owns ceil(rows_b / 256) consecutive CTAs; the grid has up
+    // to one surplus CTA per sequence, which leaves before any barrier
+    int b = 0;
+    int64_t tile = blockIdx.x, q_beg = 0, n_rows = 0;
+    for (; b < a.bt.B; ++b) {
+        q_beg = __ldg(a.bt.cu_q + b);
+        n_rows = (__ldg(a.bt.cu_q + b + 1) - q_beg) * a.H;
+        const int64_t nt = (n_rows + 2 * HBM_ - 1) / (2 * HBM_);
+        if (tile < nt) break;
+        tile -= nt;
+    }
+    if (b == a.bt.B) return;
+    const int64_t q_row_beg = q_beg * a.H;  // the sequence's first row of Q / O
+    const int64_t q_pos0 = __ldg(a.bt.q_pos0 + b), raw_pos0 = __ldg(a.bt.raw_pos0 + b);
+    const int64_t c_beg = __ldg(a.bt.cu_c + b), raw_beg = __ldg(a.bt.cu_raw + b);
+    const int64_t Tc = a.have_c ? __ldg(a.bt.cu_c + b + 1) - c_beg : 0;
+    const int64_t Nraw = a.have_r ? __ldg(a.bt.cu_raw + b + 1) - raw_beg : 0;
+    const int64_t row0 = tile * (2 * HBM_);  // sequence-local
+    const int64_t rows_here = min((int64_t)(2 * HBM_), n_rows - row0);
     const int64_t t_first = q_pos0 + row0 / a.H;
     const int64_t t_last = q_pos0 + (row0 + rows_here - 1) / a.H;
     int64_t n_ent = n_vis(t_last, a.m);
-    if (n_ent > a.Tc) n_ent = a.Tc;
+    if (n_ent > Tc) n_ent = Tc;
     const int nct = (int)((n_ent + HBN - 1) / HBN);
     int64_t wlo = 0;
     int nwt = 0;
@@ -178,7 +193,7 @@ __global__ void __launch_bounds__(H_THREADS, 1)
             for (int g = 0; g < 2; ++g)
                 for (int hf = 0; hf < 2; ++hf)
                     tma_load_2d(smem + HS_Q + (2 * g + hf) * H_TILE, &mQ, &bars.q_full, hf * 64,
-                                (int32_t)(row0 + g * HBM_));
+                                (int32_t)(q_row_beg + row0 + g * HBM_));
             int issued = 0;
             for (int j = 0; j < n_tiles; ++j) {
                 const int s = j & 1;
@@ -188,11 +203,11 @@ __global__ void __launch_bounds__(H_THREADS, 1)
                 if (j < nct) {
                     mk = &mKc;
                     mv = &mVc;
-                    y = (int32_t)((int64_t)j * HBN);
+                    y = (int32_t)(c_beg + (int64_t)j * HBN);
                 } else {
                     mk = &mKr;
                     mv = &mVr;
-                    y = (int32_t)(wlo + (int64_t)(j - nct) * HBN - raw_pos0);
+                    y = (int32_t)(raw_beg + wlo + (int64_t)(j - nct) * HBN - raw_pos0);
                 }
                 uint8_t *kd = smem + HS_K + s * 2 * H_TILE, *vd = smem + HS_V + s * 2 * H_TILE;
                 mbar_expect_tx(&bars.k_full[s], 2 * H_TILE);
@@ -284,11 +299,11 @@ __global__ void __launch_bounds__(H_THREADS, 1)
         const bool row_ok = (int64_t)(g * HBM_ + r) < rows_here;
         const int64_t t = q_pos0 + (row_ok ? row : row0 + rows_here - 1) / a.H;
         int64_t nv = n_vis(t, a.m);
-        if (nv > a.Tc) nv = a.Tc;
+        if (nv > Tc) nv = Tc;
         if (!row_ok) nv = 0;
         const int64_t w_lo = a.W > 0 ? max((int64_t)0, t - a.W + 1) : t + 1;
         // window positions the raw cache does not hold are skipped and flagged
-        int64_t c_lo = max(w_lo, raw_pos0), c_hi = min(t, raw_pos0 + a.Nraw - 1);
+        int64_t c_lo = max(w_lo, raw_pos0), c_hi = min(t, raw_pos0 + Nraw - 1);
         if (row_ok && a.W > 0 && (c_lo > w_lo || c_hi < t)) flag(a.dev_err, LC_DEVERR_WINDOW);
         if (!row_ok) c_hi = c_lo - 1;
         const uint32_t lane_base = taddr + ((uint32_t)((warp & 3) * 32) << 16);
@@ -400,7 +415,7 @@ __global__ void __launch_bounds__(H_THREADS, 1)
             const float of = fold_sink(
                 m_used, l, row_ok ? sink_log2(a.sink, (int)(row % a.H), a.dev_err) : -INFINITY);
             const float inv = l > 0.f ? of / l : 0.f;
-            uint4 *dst = reinterpret_cast<uint4 *>(a.O + row * HHD);
+            uint4 *dst = reinterpret_cast<uint4 *>(a.O + (q_row_beg + row) * HHD);
 #pragma unroll 1
             for (int c = 0; c < HHD; c += 32) {
                 float o[32];
@@ -423,7 +438,8 @@ __global__ void __launch_bounds__(H_THREADS, 1)
                     }
                 }
             }
-            if (row_ok && a.lse) a.lse[row] = l > 0.f ? (m_used + log2f(l)) / H_LOG2E : -INFINITY;
+            if (row_ok && a.lse)
+                a.lse[q_row_beg + row] = l > 0.f ? (m_used + log2f(l)) / H_LOG2E : -INFINITY;
         }
     }
     tc_fence_before();
@@ -438,13 +454,13 @@ namespace {
 bool al16h(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 }  // namespace
 
-// HCA on the tensor cores: bf16, d = 128, one sequence, H dividing 128.
+// HCA on the tensor cores: bf16, d = 128, any ragged batch, H dividing 128.
 // LC_ERR_UNSUPPORTED when the shape does not fit (the caller falls back).
 lc_status hca_tc_launch(const void *Q, const void *Kc, const void *Vc, const void *Kraw,
                         const void *Vraw, const lc_batch &b, int H, int d, int m, int W,
                         float scale, const float *sink, int rope, lc_dtype dt, void *O,
                         float *lse, int32_t *dev_err, cudaStream_t st) {
-    if (dt != LC_BF16 || d != HHD || b.B != 1 || (HBM_ % H) != 0) return LC_ERR_UNSUPPORTED;
+    if (dt != LC_BF16 || d != HHD || (HBM_ % H) != 0) return LC_ERR_UNSUPPORTED;
     if (!al16h(Q) || !al16h(O) || (Kc && !al16h(Kc)) || (Vc && !al16h(Vc)) ||
         (Kraw && !al16h(Kraw)) || (Vraw && !al16h(Vraw)))
         return LC_ERR_UNSUPPORTED;
@@ -466,12 +482,10 @@ lc_status hca_tc_launch(const void *Q, const void *Kc, const void *Vc, const voi
                            64, HBN))
         return LC_ERR_CUDA;
     HcaArgs a{};
-    a.n_rows = n_rows;
+    a.bt = to_dev(b);
+    a.have_c = have_c;
+    a.have_r = have_r;
     a.H = H;
-    a.q_pos0 = b.q_pos0;
-    a.raw_pos0 = b.raw_pos0;
-    a.Tc = have_c ? b.total_c : 0;
-    a.Nraw = have_r ? b.total_raw : 0;
     a.m = m;
     a.W = have_r ? W : 0;
     a.scale_log2 = scale * H_LOG2E;
@@ -488,7 +502,10 @@ lc_status hca_tc_launch(const void *Q, const void *Kc, const void *Vc, const voi
             return LC_ERR_CUDA;
         attr_done = true;
     }
-    const unsigned grid = (unsigned)((n_rows + 2 * HBM_ - 1) / (2 * HBM_));
+    // every sequence's tiles, at most one partial tile each: the surplus CTAs exit
+    const int64_t grid64 = (n_rows + 2 * HBM_ - 1) / (2 * HBM_) + b.B;
+    if (grid64 >= (1ll << 31)) return LC_ERR_UNSUPPORTED;
+    const unsigned grid = (unsigned)grid64;
     LC_LAUNCH(k_hca_tc, dim3(grid), dim3(H_THREADS), HS_TOTAL, st, maps[0], maps[1], maps[2],
               maps[3], maps[4], a);
     return check_launch();

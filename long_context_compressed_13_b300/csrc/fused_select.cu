@@ -42,8 +42,9 @@ __global__ void __launch_bounds__(SEL_WARPS * 32) k_sample_threshold16(
     if (blockIdx.x == 0 && threadIdx.x == 0) *nfail = 0;
     const int64_t r = (int64_t)blockIdx.x * SEL_WARPS + warp;
     if (r >= total_q) return;  // the whole warp
-    const int64_t t = bt.q_pos0[0] + r;
-    const int64_t Tc = bt.cu_c[1] - bt.cu_c[0];
+    const int bq = seq_of_row(bt, r);
+    const int64_t t = bt.q_pos0[bq] + (r - bt.cu_q[bq]);
+    const int64_t Tc = bt.cu_c[bq + 1] - bt.cu_c[bq];
     int64_t nv = n_vis(t, m);
     if (nv > Tc) nv = Tc;
     const int64_t nvs = (nv + stride - 1) / stride;
@@ -51,13 +52,24 @@ __global__ void __launch_bounds__(SEL_WARPS * 32) k_sample_threshold16(
     if (nv > k && rho <= nvs) {
         const uint16_t *row = samp + r * lds;  // 16-byte aligned (lds % 8 == 0)
         const int n = (int)nvs;
+        // the whole warp steps together, four 16-byte loads per lane in flight
         auto visit = [&](auto f) {
-            for (int j8 = lane; 8 * j8 < n; j8 += 32) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(row + 8 * j8);
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            for (int b8 = 0; 8 * b8 < n; b8 += 128) {
+                uint4 v[4];
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (8 * j8 + u < n) f((w[u >> 1] >> (16 * (u & 1))) & 0xffffu);
+                for (int q = 0; q < 4; ++q) {
+                    const int j8 = b8 + 32 * q + lane;
+                    v[q] = 8 * j8 < n ? *reinterpret_cast<const uint4 *>(row + 8 * j8)
+                                      : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int j8 = b8 + 32 * q + lane;
+                    const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        f((w[u >> 1] >> (16 * (u & 1))) & 0xffffu, 8 * j8 + u < n);
+                }
             }
         };
         int need = rho;
@@ -84,8 +96,9 @@ __global__ void __launch_bounds__(SEL_WARPS * 32) k_cand_pick_warp(
     if (r >= total_q) return;
     uint32_t *hist = sm_sel + warp * (256 + 2 * nwmax);
     uint32_t *A = hist + 256, *E = A + nwmax;
-    const int64_t t = bt.q_pos0[0] + r;
-    const int64_t Tc = bt.cu_c[1] - bt.cu_c[0];
+    const int bq = seq_of_row(bt, r);
+    const int64_t t = bt.q_pos0[bq] + (r - bt.cu_q[bq]);
+    const int64_t Tc = bt.cu_c[bq + 1] - bt.cu_c[bq];
     int64_t nv = n_vis(t, m);
     if (nv > Tc) nv = Tc;
     int32_t *out = topk + r * k;
@@ -103,17 +116,24 @@ __global__ void __launch_bounds__(SEL_WARPS * 32) k_cand_pick_warp(
         if (lane == 0) flist[atomicAdd(nfail, 1)] = (int32_t)r;
         return;
     }
-    // every candidate of the row: (order key, entry index)
+    // every candidate of the row: (order key, entry index); all 32 lanes step
+    // together, lanes past a segment's end get valid = false
     auto each = [&](auto f) {
         for (int y = 0; y < gy; ++y) {
             const int c = lcnt[r * gy + y];
             const uint2 *seg = priv + ((size_t)r * gy + y) * cloc;
-            for (int i = lane; i < c; i += 32) f(seg[i]);
+            for (int i0 = 0; i0 < c; i0 += 32) {
+                const bool ok = i0 + lane < c;
+                f(ok ? seg[i0 + lane] : make_uint2(0u, 0u), ok);
+            }
         }
         const uint2 *ov = cand + (size_t)r * ocap;
-        for (int i = lane; i < n_over; i += 32) f(ov[i]);
+        for (int i0 = 0; i0 < n_over; i0 += 32) {
+            const bool ok = i0 + lane < n_over;
+            f(ok ? ov[i0 + lane] : make_uint2(0u, 0u), ok);
+        }
     };
-    auto keys = [&](auto f) { each([&](uint2 kv) { f(kv.x); }); };
+    auto keys = [&](auto f) { each([&](uint2 kv, bool ok) { f(kv.x, ok); }); };
     int need = k;
     uint32_t prefix = 0, mask = 0;
 #pragma unroll 1
@@ -129,7 +149,8 @@ __global__ void __launch_bounds__(SEL_WARPS * 32) k_cand_pick_warp(
         E[w] = 0u;
     }
     __syncwarp();
-    each([&](uint2 kv) {
+    each([&](uint2 kv, bool ok) {
+        if (!ok) return;
         const uint32_t e = kv.y;
         if (e >= (uint32_t)nv) {
             flag(dev_err, LC_DEVERR_BATCH);  // a candidate outside the row: never expected
@@ -204,10 +225,11 @@ __global__ void __launch_bounds__(512) k_topk_fallback(const __nv_bfloat16 *__re
     const int h = lane / LPH, sl = lane % LPH;
     const int total = *nfail;
     float *row = buf + (int64_t)blockIdx.x * ldb;
-    const int64_t Tc = bt.cu_c[1] - bt.cu_c[0];
     for (int i = blockIdx.x; i < total; i += gridDim.x) {
         const int64_t r = flist[i];
-        const int64_t t = bt.q_pos0[0] + r;
+        const int bq = seq_of_row(bt, r);
+        const int64_t t = bt.q_pos0[bq] + (r - bt.cu_q[bq]);
+        const int64_t c_beg = bt.cu_c[bq], Tc = bt.cu_c[bq + 1] - c_beg;
         int64_t nv = n_vis(t, m);
         if (nv > Tc) nv = Tc;
         if (nv > ldb) nv = ldb;
@@ -217,7 +239,7 @@ __global__ void __launch_bounds__(512) k_topk_fallback(const __nv_bfloat16 *__re
         if (threadIdx.x < HI) sw[threadIdx.x] = w[r * HI + threadIdx.x];
         __syncthreads();
         for (int64_t j = warp; j < nv; j += NW) {
-            const __nv_bfloat16 *kr = kI + ((bt.cu_c[0] + j) * HI + h) * DI + sl * DPL;
+            const __nv_bfloat16 *kr = kI + ((c_beg + j) * HI + h) * DI + sl * DPL;
             float d = 0.f;
 #pragma unroll
             for (int u = 0; u < DPL; u += 8) {

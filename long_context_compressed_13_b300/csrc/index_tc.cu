@@ -1,5 +1,5 @@
 // Lightning Indexer on the tensor cores (tcgen05 + TMEM), bf16 q/k with
-// d_I = 64, H_I in {4, 8}, one sequence, plus the fused exact top-k that
+// d_I = 64, H_I in {4, 8}, any ragged batch, plus the fused exact top-k that
 // never writes the full score matrix.
 //
 // k_index_tc: one CTA = 128 query rows x a contiguous range of entries.
@@ -119,11 +119,10 @@ __device__ __forceinline__ float key_to_float(uint32_t key) {
 }  // namespace
 
 struct IdxTcArgs {
-    int64_t Nq;              // query rows of the (single) sequence
-    const int64_t *q_pos0;   // device: absolute position of row 0
-    const __nv_bfloat16 *qI; // [Nq, HI, 64]
-    int64_t Tc;              // stored entries
-    int stride;              // map entry e is entry e*stride
+    Batch bt;                // device batch arrays (any number of sequences)
+    int64_t total_q;         // host: query rows of the batch (grid size)
+    const __nv_bfloat16 *qI; // [total_q, HI, 64]
+    int stride;              // map entry e of a sequence is its entry e*stride
     int m;
     int64_t chunk;           // map entries per CTA (multiple of IBN)
     int64_t col_end;         // MATERIALIZE, SAMPLE16: map columns [0, col_end)
@@ -154,11 +153,25 @@ __global__ void __launch_bounds__(I_THREADS, 1)
     volatile int *abort = &bars.abort;
     const unsigned FULL = 0xffffffffu;
 
-    const int64_t q_pos0 = __ldg(a.q_pos0);
-    const int64_t row0 = (int64_t)blockIdx.x * IBM;
-    const int64_t last_row = min(row0 + IBM, a.Nq) - 1;
+    // the CTA's sequence and its 128-row tile there: sequence b owns
+    // ceil(rows_b / 128) consecutive CTAs along x; the grid has up to one
+    // surplus CTA per sequence, which leaves before any barrier
+    int bq = 0;
+    int64_t tile = blockIdx.x, q_beg = 0, nq = 0;
+    for (; bq < a.bt.B; ++bq) {
+        q_beg = __ldg(a.bt.cu_q + bq);
+        nq = __ldg(a.bt.cu_q + bq + 1) - q_beg;
+        const int64_t nt = (nq + IBM - 1) / IBM;
+        if (tile < nt) break;
+        tile -= nt;
+    }
+    if (bq == a.bt.B) return;
+    const int64_t q_pos0 = __ldg(a.bt.q_pos0 + bq);
+    const int64_t c_beg = __ldg(a.bt.cu_c + bq), Tc = __ldg(a.bt.cu_c + bq + 1) - c_beg;
+    const int64_t row0 = tile * IBM;  // sequence-local; global row = q_beg + local
+    const int64_t last_row = min(row0 + IBM, nq) - 1;
     int64_t nv_last = n_vis(q_pos0 + last_row, a.m);
-    if (nv_last > a.Tc) nv_last = a.Tc;
+    if (nv_last > Tc) nv_last = Tc;
     const int64_t nvm = (nv_last + a.stride - 1) / a.stride;  // visible map entries (max)
     const int64_t c0 = (int64_t)blockIdx.y * a.chunk;
     const int64_t c_end = MODE != MODE_FILTER ? min(c0 + a.chunk, a.col_end)
@@ -176,13 +189,13 @@ __global__ void __launch_bounds__(I_THREADS, 1)
         // FILTER: the rows have no candidate in this CTA column.
         // SAMPLE16: nothing (only visible columns are stored, and none is here)
         if (MODE == MODE_MATERIALIZE) {
-            for (int r = warp; r < IBM && row0 + r < a.Nq; r += I_THREADS / 32) {
-                float *dst = a.out + (row0 + r) * a.ld;
+            for (int r = warp; r < IBM && row0 + r < nq; r += I_THREADS / 32) {
+                float *dst = a.out + (q_beg + row0 + r) * a.ld;
                 for (int64_t e = c0 + lane; e < c_end; e += 32) dst[e] = -INFINITY;
             }
         } else if (MODE == MODE_FILTER) {
             for (int r = tid; r < IBM; r += I_THREADS)
-                if (row0 + r < a.Nq) a.lcnt[(size_t)(row0 + r) * a.gy + blockIdx.y] = 0;
+                if (row0 + r < nq) a.lcnt[(size_t)(q_beg + row0 + r) * a.gy + blockIdx.y] = 0;
         }
         return;
     }
@@ -225,14 +238,21 @@ __global__ void __launch_bounds__(I_THREADS, 1)
 #pragma unroll
             for (int h = 0; h < HI; ++h)
                 tma_load_2d(smem + C::SM_Q + h * C::Q_BOX, &mQ, &bars.q_full, h * IDI,
-                            (int32_t)row0);
+                            (int32_t)(q_beg + row0));
             int issued = 0;
             for (int g = 0; g < n_all; ++g) {
                 const int s = g % NSB, i = g / HI, h = g % HI;
                 if (g >= NSB && !mbar_wait(&bars.k_empty[s], ((g - NSB) / NSB) & 1, abort)) break;
                 mbar_expect_tx(&bars.k_full[s], C::HEAD_BOX);
-                tma_load_2d(smem + C::SM_K + s * C::HEAD_BOX, &mK, &bars.k_full[s], h * IDI,
-                            (int32_t)(c0 + (int64_t)i * IBN));
+                if (MODE == MODE_SAMPLE16)
+                    // the sequence's entry c_beg + e*stride: phase c_beg % stride,
+                    // strided row c_beg / stride + e of the 3-D view
+                    tma_load_3d(smem + C::SM_K + s * C::HEAD_BOX, &mK, &bars.k_full[s], h * IDI,
+                                (int32_t)(c_beg % a.stride),
+                                (int32_t)(c_beg / a.stride + c0 + (int64_t)i * IBN));
+                else
+                    tma_load_2d(smem + C::SM_K + s * C::HEAD_BOX, &mK, &bars.k_full[s], h * IDI,
+                                (int32_t)(c_beg + c0 + (int64_t)i * IBN));
                 ++issued;
             }
             int dummy = 0;
@@ -290,11 +310,12 @@ __global__ void __launch_bounds__(I_THREADS, 1)
     } else {
         // ------------------------------------------------------ epilogue
         const int quad = warp & 3, part = warp >> 2;
-        const int64_t row = row0 + quad * 32 + lane;
-        const bool row_ok = row < a.Nq;
-        const int64_t t = q_pos0 + (row_ok ? row : last_row);
+        const int64_t lrow = row0 + quad * 32 + lane;  // sequence-local
+        const bool row_ok = lrow < nq;
+        const int64_t row = q_beg + lrow;              // global
+        const int64_t t = q_pos0 + (row_ok ? lrow : last_row);
         int64_t nv = n_vis(t, a.m);
-        if (nv > a.Tc) nv = a.Tc;
+        if (nv > Tc) nv = Tc;
         const int64_t nvr = (nv + a.stride - 1) / a.stride;  // this row's visible map entries
         float wh[HI];
 #pragma unroll
@@ -503,11 +524,12 @@ __global__ void __launch_bounds__(512) k_cand_pick(Batch bt, int m, int k, int c
     uint32_t *sel = sbuf + R;                                   // [PK]
     uint32_t *tl = sel + PK;                                    // [P]
     __shared__ RadixScratch rs;
-    __shared__ int s_n, s_ties, s_fill, s_priv, wsum[NW];
+    __shared__ int s_n, s_ties, s_priv, wsum[NW];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t r = blockIdx.x;
-    const int64_t t = bt.q_pos0[0] + r;
-    const int64_t Tc = bt.cu_c[1] - bt.cu_c[0];
+    const int bq = seq_of_row(bt, r);
+    const int64_t t = bt.q_pos0[bq] + (r - bt.cu_q[bq]);
+    const int64_t Tc = bt.cu_c[bq + 1] - bt.cu_c[bq];
     int64_t nv = n_vis(t, m);
     if (nv > Tc) nv = Tc;
     int32_t *out = topk + r * k;
@@ -518,7 +540,6 @@ __global__ void __launch_bounds__(512) k_cand_pick(Batch bt, int m, int k, int c
     // candidates: the private slots of the row's CTA columns, then its overflow slots
     if (threadIdx.x == 0) {
         s_priv = 0;
-        s_fill = 0;
         s_n = 0;
         s_ties = 0;
     }
@@ -536,22 +557,47 @@ __global__ void __launch_bounds__(512) k_cand_pick(Batch bt, int m, int k, int c
         if (threadIdx.x == 0) flist[atomicAdd(nfail, 1)] = (int32_t)r;
         return;
     }
-    for (int y = warp; y < gy; y += NW) {
-        const int c = lcnt[r * gy + y];
-        if (c == 0) continue;
-        int b = 0;
-        if (lane == 0) b = atomicAdd(&s_fill, c);
-        b = __shfl_sync(FULL, b, 0);
-        const uint2 *src = priv + ((size_t)r * gy + y) * cloc;
-        for (int i = lane; i < c; i += 32) {
-            const uint2 ki = src[i];
-            if (b + i < cap) {
-                keys[b + i] = ki.x;
-                idx[b + i] = ki.y;
-            } else {
-                flag(dev_err, LC_DEVERR_BATCH);  // counts inconsistent: never expected
+    // the private segments, NT CTA columns at a time: a block-wide prefix over
+    // their counts places each segment, then every thread loads its share of
+    // all of them at once (one memory round trip, not one per segment)
+    __shared__ int seg_off[NT];
+    int filled = 0;
+    for (int y0 = 0; y0 < gy; y0 += NT) {
+        const int y = y0 + threadIdx.x;
+        const int c = y < gy ? lcnt[r * gy + y] : 0;
+        int tot;
+        seg_off[threadIdx.x] = block_exclusive_scan<NT>(c, wsum, &tot);
+        __syncthreads();
+        const int nseg = min(NT, gy - y0);
+        if (filled + tot > cap) {
+            flag(dev_err, LC_DEVERR_BATCH);  // counts inconsistent: never expected
+            tot = cap - filled;
+        }
+        for (int j0 = threadIdx.x; j0 < tot; j0 += 4 * NT) {
+            uint2 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = j0 + u * NT;
+                if (j < tot) {
+                    // the last segment whose first slot is at or before j
+                    int sg = 0;
+#pragma unroll
+                    for (int step = NT / 2; step > 0; step >>= 1)
+                        if (sg + step < nseg && seg_off[sg + step] <= j) sg += step;
+                    v[u] = priv[((size_t)r * gy + y0 + sg) * cloc + (j - seg_off[sg])];
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = j0 + u * NT;
+                if (j < tot) {
+                    keys[filled + j] = v[u].x;
+                    idx[filled + j] = v[u].y;
+                }
             }
         }
+        filled += tot;
+        __syncthreads();  // seg_off is rewritten by the next group
     }
     for (int i = threadIdx.x; i < n_over; i += NT) {
         const uint2 ki = cand[r * ocap + i];
@@ -722,7 +768,7 @@ FusedPlan plan_fused(const lc_batch &b, int k) {
 bool index_tc_eligible(const void *qI, const void *kI, const lc_batch &b, int HI, int dI,
                        lc_dtype dt) {
     auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-    return dt == LC_BF16 && dI == IDI && (HI == 4 || HI == 8) && b.B == 1 && b.max_q >= 64 &&
+    return dt == LC_BF16 && dI == IDI && (HI == 4 || HI == 8) && b.max_q >= 64 &&
            b.max_c > 0 && al16(qI) && al16(kI) && b.total_q < (1ll << 31) &&
            b.max_c < (1ll << 31);
 }
@@ -742,7 +788,11 @@ lc_status launch_tc(const CUtensorMap &mQ, const CUtensorMap &mK, const IdxTcArg
     }
     const int64_t gy = (n_cols + a.chunk - 1) / a.chunk;
     if (gy < 1 || gy > 65535) return LC_ERR_UNSUPPORTED;
-    dim3 grid((unsigned)((a.Nq + IBM - 1) / IBM), (unsigned)gy);
+    // every sequence's row tiles, at most one partial tile each: the surplus
+    // CTAs exit at once
+    const int64_t gx = (a.total_q + IBM - 1) / IBM + a.bt.B;
+    if (gx >= (1ll << 31)) return LC_ERR_UNSUPPORTED;
+    dim3 grid((unsigned)gx, (unsigned)gy);
     LC_LAUNCH_AS(MODE == MODE_FILTER      ? "k_index_tc<filter>"
                  : MODE == MODE_SAMPLE16 ? "k_index_tc<sample16>"
                                          : "k_index_tc<materialize>",
@@ -774,10 +824,9 @@ int64_t pick_chunk(int64_t Nq, int64_t n_cols) {
 IdxTcArgs base_args(const lc_batch &b, const void *qI, const float *w, int m,
                     int32_t *dev_err) {
     IdxTcArgs a{};
-    a.Nq = b.total_q;
+    a.bt = to_dev(b);
+    a.total_q = b.total_q;
     a.qI = static_cast<const __nv_bfloat16 *>(qI);
-    a.q_pos0 = b.q_pos0;
-    a.Tc = b.max_c;
     a.stride = 1;
     a.m = m;
     a.w = w;
@@ -788,7 +837,7 @@ IdxTcArgs base_args(const lc_batch &b, const void *qI, const float *w, int m,
 }  // namespace
 
 size_t index_tc_workspace(const lc_batch &b, int k) {
-    if (b.B != 1 || k < 1) return 0;
+    if (k < 1) return 0;
     return plan_fused(b, k).total;
 }
 
@@ -804,7 +853,6 @@ lc_status index_tc_materialize(const void *qI, const float *w, const void *kI, c
                            IBN))
         return LC_ERR_CUDA;
     IdxTcArgs a = base_args(b, qI, w, m, dev_err);
-    a.Tc = b.total_c;
     a.col_end = ld;
     a.out = scores;
     a.ld = ld;
@@ -838,14 +886,13 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
     CUtensorMap mQ, mKs, mK;
     if (!make_tmap_bf16_2d(&mQ, qI, (uint64_t)b.total_q, (uint64_t)HI * IDI, pitch, IDI, IBM) ||
         !make_tmap_bf16_2d(&mK, kI, (uint64_t)Tc, (uint64_t)HI * IDI, pitch, IDI, IBN) ||
-        !make_tmap_bf16_2d(&mKs, kI, (uint64_t)((Tc + p.stride - 1) / p.stride),
-                           (uint64_t)HI * IDI, pitch * p.stride, IDI, IBN))
+        !make_tmap_bf16_strided_rows(&mKs, kI, (uint64_t)Tc, (uint64_t)HI * IDI, pitch,
+                                     (uint32_t)p.stride, IDI, IBN))
         return LC_ERR_CUDA;
     lc_status s;
     // 1. 16-bit keys of every s-th entry's score (visible columns only)
     {
         IdxTcArgs a = base_args(b, qI, w, m, dev_err);
-        a.Tc = Tc;
         a.stride = p.stride;
         a.col_end = p.ns;
         a.out16 = samp;
@@ -860,7 +907,6 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
     // 3. candidates
     {
         IdxTcArgs a = base_args(b, qI, w, m, dev_err);
-        a.Tc = Tc;
         a.theta = theta;
         a.count = count;
         a.cand = cand;
@@ -870,8 +916,8 @@ lc_status index_topk_tc_launch(const void *qI, const float *w, const void *kI,
         a.gy = p.gy;
         a.cloc = p.cloc;
         a.chunk = p.chunk;
-        if ((Tc + p.chunk - 1) / p.chunk != p.gy) return LC_ERR_INVALID_ARG;  // gridDim.y == gy
-        s = launch_tc_hi<MODE_FILTER>(HI, mQ, mK, a, Tc, st);
+        if ((b.max_c + p.chunk - 1) / p.chunk != p.gy) return LC_ERR_INVALID_ARG;  // gridDim.y == gy
+        s = launch_tc_hi<MODE_FILTER>(HI, mQ, mK, a, b.max_c, st);
         if (s != LC_OK) return s;
     }
     // 4. exact selection among the candidates

@@ -92,6 +92,15 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int32_t x, int32_t y, int32_t z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -230,5 +239,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // box of box_cols x box_rows and 128-byte swizzle.  Returns false on failure.
 bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                        uint64_t row_pitch_bytes, uint32_t box_cols, uint32_t box_rows);
+
+// Host: a 3-D view of a row-major bf16 matrix [n_rows, cols] that reaches
+// every `step`-th row from any phase: element (x, p, e) is row e*step + p.
+// Extents {cols, step, floor(n_rows / step)}, so no coordinate inside the
+// extents lies past the matrix; box {box_cols, 1, box_rows}, 128-byte swizzle
+// (the box lands in shared memory like a box_rows x box_cols 2-D box).
+bool make_tmap_bf16_strided_rows(CUtensorMap *map, const void *base, uint64_t n_rows,
+                                 uint64_t cols, uint64_t row_pitch_bytes, uint32_t step,
+                                 uint32_t box_cols, uint32_t box_rows);
 
 }  // namespace lc

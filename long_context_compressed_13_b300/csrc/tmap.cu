@@ -33,4 +33,27 @@ bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64
     return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_bf16_strided_rows(CUtensorMap *map, const void *base, uint64_t n_rows,
+                                 uint64_t cols, uint64_t row_pitch_bytes, uint32_t step,
+                                 uint32_t box_cols, uint32_t box_rows) {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode || !base || step == 0 || n_rows / step == 0 || cols == 0) return false;
+    cuuint64_t dims[3] = {cols, step, n_rows / step};
+    cuuint64_t strides[2] = {row_pitch_bytes, row_pitch_bytes * step};
+    cuuint32_t box[3] = {box_cols, 1, box_rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace lc

@@ -222,10 +222,11 @@ __device__ void radix_topk_row(const float *__restrict__ row, int64_t n, int k, 
 // One radix digit of a warp-level selection: among the keys that match
 // `prefix` under `mask`, the digit (key >> shift) & 255 of the need-th
 // largest, from a histogram in the warp's own 256 shared-memory words `h`.
-// visit(f) must call f(key) once for every key of the set (each lane its
-// share).  On return `need` is the rank of the wanted key within the chosen
-// digit's bin.  Requires 1 <= need <= (keys matching prefix); all 32 lanes
-// call it.
+// visit(f) must call f(key, valid) on all 32 lanes together (warp-uniform
+// trip counts), once with valid = true for every key of the set (each lane
+// its share); lanes without a key pass valid = false.  On return `need` is
+// the rank of the wanted key within the chosen digit's bin.  Requires
+// 1 <= need <= (keys matching prefix); all 32 lanes call it.
 template <typename Visit>
 __device__ __forceinline__ uint32_t warp_radix_digit(uint32_t *h, Visit visit, uint32_t prefix,
                                                      uint32_t mask, int shift, int &need) {
@@ -233,8 +234,8 @@ __device__ __forceinline__ uint32_t warp_radix_digit(uint32_t *h, Visit visit, u
     const int lane = threadIdx.x & 31;
     for (int i = lane; i < 256; i += 32) h[i] = 0u;
     __syncwarp();
-    visit([&](uint32_t key) {
-        if ((key & mask) == prefix) atomicAdd(&h[(key >> shift) & 255u], 1u);
+    visit([&](uint32_t key, bool valid) {
+        if (valid && (key & mask) == prefix) atomicAdd(&h[(key >> shift) & 255u], 1u);
     });
     __syncwarp();
     // suffix sums over the 256 bins, 8 bins per lane, highest first

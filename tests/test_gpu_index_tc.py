@@ -186,3 +186,73 @@ def test_fused_topk_in_row_chunks_equals_one_pass(lc, dtype, HI, dI):
     tpos = np.array(L["batch"].positions())
     I = oracle.index(L["qI"], L["w"], L["kI"], tpos, 4)
     _check_selection(c.cpu().numpy(), I, (tpos + 1) // 4, k)
+
+
+# ---------------------------------------------------- ragged batches
+
+# (T, q_from) per sequence: sequence-local row tiles that end part-way, a
+# sequence of five rows, one without query rows, entries that start at
+# offsets which are not multiples of any tile or sampling stride
+RAGGED_SEQS = [(1400, 0), (3000, 2900), (700, 695), (2048, 2048), (2500, 2300)]
+
+
+@pytest.mark.parametrize("HI", [8, 4])
+def test_tc_scores_ragged(lc, HI):
+    parts = [wl.csa_layer(T=T, H=8, d=64, HI=HI, dI=64, m=4, k=16, W=16, dtype="bf16",
+                          seed=80 + i, q_from=q) for i, (T, q) in enumerate(RAGGED_SEQS)]
+    R = wl.ragged(parts, ["qI", "w", "kI"])
+    bt = R["batch"]
+    b = lc.DeviceBatch.from_workload(bt)
+    ld = b.max_c + 12
+    sc = torch.full((b.total_q, ld), 7.0, device="cuda")
+    lc.lightning_index(R["qI"].cuda(), R["w"].cuda(), R["kI"].cuda(), b, 4, scores=sc)
+    torch.cuda.synchronize()
+    assert lc.last_kernel() == "k_index_tc<materialize>"
+    got = sc.cpu().double().numpy()
+    for s, L in enumerate(parts):
+        rows = got[bt.cu_q[s]:bt.cu_q[s + 1]]
+        Tc = bt.cu_c[s + 1] - bt.cu_c[s]
+        assert np.all(np.isneginf(rows[:, Tc:])), f"sequence {s}"
+        tpos = np.array(L["batch"].positions())
+        if len(tpos) == 0:
+            continue
+        ref = oracle.index(L["qI"], L["w"], L["kI"], tpos, 4)
+        rows = rows[:, :Tc]
+        vis = np.isfinite(ref)
+        assert np.array_equal(np.isneginf(rows), ~vis), f"sequence {s}"
+        bound = _bound(L["qI"], L["w"], L["kI"])
+        assert np.all(np.abs(rows[vis] - ref[vis]) <= bound[vis]), f"sequence {s}"
+
+
+@pytest.mark.parametrize("long_T", [32768, 140000])
+def test_fused_topk_ragged(lc, long_T):
+    # one batch of sequences of very different lengths.  The sampled threshold
+    # reads every s-th entry of each sequence from that sequence's own first
+    # entry (s = 16 here, and sequence starts that are not multiples of it);
+    # rows of the short sequences hold k or fewer visible entries; sequence 1's
+    # rows see 4000 tied best entries, more than the candidate capacity, which
+    # the fallback settles from that sequence's own keys (the lowest indices).
+    # long_T = 140000 gives rows past the warp pick's bitmaps: the CTA-per-row
+    # pick runs for every row.
+    k = 64
+    seqs = [(long_T, long_T - 40), (20000, 19900), (777, 700), (300, 0), (5001, 4990)]
+    parts = [wl.csa_layer(T=T, H=8, d=64, HI=8, dI=64, m=4, k=k, W=16, dtype="bf16",
+                          seed=90 + i, q_from=q) for i, (T, q) in enumerate(seqs)]
+    parts[1]["qI"] = parts[1]["qI"].abs()
+    parts[1]["kI"] = parts[1]["kI"].clone()
+    parts[1]["kI"][:4000] = 3.0
+    R = wl.ragged(parts, ["qI", "w", "kI"])
+    bt = R["batch"]
+    b = lc.DeviceBatch.from_workload(bt)
+    _, sel = lc.lightning_index(R["qI"].cuda(), R["w"].cuda(), R["kI"].cuda(), b, 4,
+                                scores=False, k=k, topk=True)
+    torch.cuda.synchronize()
+    assert lc.last_kernel() == "k_topk_fallback"
+    gsel = sel.cpu().numpy()
+    for s, L in enumerate(parts):
+        g = gsel[bt.cu_q[s]:bt.cu_q[s + 1]]
+        tpos = np.array(L["batch"].positions())
+        I = oracle.index(L["qI"], L["w"], L["kI"], tpos, 4)
+        if s == 1:
+            assert all(r.tolist() == list(range(k)) for r in g)
+        _check_selection(g, I, (tpos + 1) // 4, k)

@@ -258,6 +258,40 @@ def test_hca_attn(lc, dtype, H, d, m, W, T, q_from):
     np.testing.assert_allclose(f64(lse)[fin], rl[fin], rtol=0, atol=tol)
 
 
+@pytest.mark.parametrize("H", [64, 128])
+def test_hca_attn_ragged(lc, H):
+    # one ragged batch: row tiles of each sequence end part-way, a sequence
+    # without query rows, one whose window starts before its first query, one
+    # with a single compressed entry; every sequence against the oracle alone
+    m, W, dtype = 128, 128, "bf16"
+    seqs = [(2100, 0), (301, 0), (8192 + 300, 8192 - 200), (700, 650), (500, 500), (257, 200)]
+    parts = [wl.hca_layer(T=T, H=H, d=128, m=m, W=W, dtype=dtype, seed=95 + i, q_from=q)
+             for i, (T, q) in enumerate(seqs)]
+    for L in parts:
+        L["Kc"] = cast(oracle.compress(L["K"], L["G"], m), dtype)
+        L["Vc"] = cast(oracle.compress(L["V"], L["G"], m), dtype)
+    R = wl.ragged(parts, ["Q", "K", "V", "Kc", "Vc"])
+    bt = R["batch"]
+    b = lc.DeviceBatch.from_workload(bt)
+    O, lse = lc.hca_dense_attn(dev(R["Q"]), dev(R["Kc"]), dev(R["Vc"]), dev(R["K"]), dev(R["V"]),
+                               b, m, W, parts[0]["scale"])
+    torch.cuda.synchronize()
+    assert lc.last_kernel() == "k_hca_tc"
+    gO, gl = f64(O), f64(lse)
+    tol = TOL_ATTN[dtype]
+    for s, L in enumerate(parts):
+        tpos = np.array(L["batch"].positions())
+        if len(tpos) == 0:
+            continue
+        rO, rl = oracle.hca_attn(L["Q"], L["Kc"], L["Vc"], m, L["K"], L["V"], 0, tpos, W,
+                                 L["scale"])
+        q0, q1 = bt.cu_q[s], bt.cu_q[s + 1]
+        np.testing.assert_allclose(gO[q0:q1], rO, rtol=0, atol=tol, err_msg=f"sequence {s}")
+        fin = np.isfinite(rl)
+        assert np.array_equal(np.isneginf(gl[q0:q1]), ~fin)
+        np.testing.assert_allclose(gl[q0:q1][fin], rl[fin], rtol=0, atol=tol)
+
+
 # ------------------------------------------------------- attention sink
 
 def _sinks(H, seed):

@@ -178,6 +178,29 @@ def csa_decode(*, B: int, ctx_lo: int, ctx_hi: int, H: int, d: int, HI: int, dI:
     return out
 
 
+def ragged(layers, keys) -> Dict:
+    """A ragged batch made of single-sequence workloads (each from csa_layer,
+    csa_layer_token_gated or hca_layer, in the given order): the tensors named
+    in ``keys`` are concatenated along their first (row) axis and the batch
+    arrays are offset accordingly.  The per-sequence workloads are kept under
+    "parts" so that a check can slice each sequence back out."""
+    cu_q, q_pos0, cu_c, cu_raw, raw_pos0 = [0], [], [0], [0], []
+    for L in layers:
+        b = L["batch"]
+        cu_q.append(cu_q[-1] + b.cu_q[1] - b.cu_q[0])
+        q_pos0.append(b.q_pos0[0])
+        cu_c.append(cu_c[-1] + b.cu_c[1] - b.cu_c[0])
+        cu_raw.append(cu_raw[-1] + b.cu_raw[1] - b.cu_raw[0])
+        raw_pos0.append(b.raw_pos0[0])
+    out = {key: val for key, val in layers[0].items() if not isinstance(val, torch.Tensor)}
+    for key in keys:
+        out[key] = torch.cat([L[key] for L in layers], dim=0)
+    out["batch"] = Batch(cu_q=cu_q, q_pos0=q_pos0, cu_c=cu_c, cu_raw=cu_raw,
+                         raw_pos0=raw_pos0)
+    out["parts"] = list(layers)
+    return out
+
+
 def layer_pair(*, ctx: int = 1 << 20, chunk: int = 4096, H: int = 128, d: int = 128,
                HI: int = 8, dI: int = 64, m_csa: int = 4, m_hca: int = 128, k: int = 1024,
                W: int = 128, dtype: str = "bf16", seed: int = 4, device="cpu") -> Dict:
