@@ -152,6 +152,11 @@ class ClockSampler:
             return
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
+        # nvidia-smi's own start-up (driver queries) must not overlap the timed
+        # region: wait for its first sample
+        t0 = time.perf_counter()
+        while not self.lines and self.proc.poll() is None and time.perf_counter() - t0 < 10:
+            time.sleep(0.01)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -842,7 +847,8 @@ def measure(wk, args, dist, device, peaks, world, rank, cpu_budget):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
-    time.sleep(0.3)
+    for _ in range(2):  # the clocks back up after the sampler's start-up wait
+        wk.step()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -863,31 +869,68 @@ def measure(wk, args, dist, device, peaks, world, rank, cpu_budget):
                 for i in range(nst)]
     err = int(wk.err.item())
 
-    # ---- end-to-end region: pinned host inputs -> device -> step -> host outputs
+    # ---- end-to-end region: pinned host inputs -> device -> step -> host
+    # outputs, every step.  Pipelined as a serving loop runs it: uploads on one
+    # copy stream, downloads on another, device staging double-buffered, so
+    # step i+1's upload and step i-1's download overlap step i's kernels.  The
+    # step itself takes its inputs from the staging buffer by a device copy
+    # and leaves its outputs there the same way.
     ins, outs = wk.host_io()
     h_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v) for k, v in ins.items()}
     h_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
     h2d = sum(v.numel() * v.element_size() for v in h_in.values())
     d2h = sum(v.numel() * v.element_size() for v in h_out.values())
-    e2e_steps = max(1, min(args.steps, 5))
+    e2e_steps = max(4, min(args.steps, 10))
+    st_in = [{k: torch.empty_like(v) for k, v in ins.items()} for _ in range(2)]
+    st_out = [{k: torch.empty_like(v) for k, v in outs.items()} for _ in range(2)]
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    uploaded = [torch.cuda.Event() for _ in range(2)]  # st_in[j] holds a step's inputs
+    consumed = [torch.cuda.Event() for _ in range(2)]  # the step has copied st_in[j] in
+    produced = [torch.cuda.Event() for _ in range(2)]  # st_out[j] holds a step's outputs
+    drained = [torch.cuda.Event() for _ in range(2)]   # st_out[j] is on the host
 
-    def e2e_step():
-        for k_, v in h_in.items():
-            ins[k_].copy_(v, non_blocking=True)
+    def upload(i):
+        j = i % 2
+        with torch.cuda.stream(up):
+            if i >= 2:
+                up.wait_event(consumed[j])
+            for k_, v in h_in.items():
+                st_in[j][k_].copy_(v, non_blocking=True)
+            uploaded[j].record(up)
+
+    def run(i):
+        j = i % 2
+        stream.wait_event(uploaded[j])
+        for k_, v in ins.items():
+            v.copy_(st_in[j][k_], non_blocking=True)
+        consumed[j].record(stream)
         wk.step()
-        for k_, v in h_out.items():
-            v.copy_(outs[k_], non_blocking=True)
+        if i >= 2:
+            stream.wait_event(drained[j])
+        for k_, v in outs.items():
+            st_out[j][k_].copy_(v, non_blocking=True)
+        produced[j].record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(produced[j])
+            for k_, v in h_out.items():
+                v.copy_(st_out[j][k_], non_blocking=True)
+            drained[j].record(down)
 
-    e2e_step()
-    torch.cuda.synchronize()
+    def pipeline(n):
+        upload(0)
+        for i in range(n):
+            if i + 1 < n:
+                upload(i + 1)
+            run(i)
+        torch.cuda.synchronize()
+
+    pipeline(2)
     if dist:
         dist.barrier()
     e0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
-        torch.cuda.synchronize()
+    pipeline(e2e_steps)
     e2e_s = max_over_ranks(dist, (time.perf_counter() - e0) / e2e_steps, device)
-    del h_in, h_out
+    del h_in, h_out, st_in, st_out
 
     ms_step = ms / args.steps
     rec = {
@@ -901,7 +944,10 @@ def measure(wk, args, dist, device, peaks, world, rank, cpu_budget):
         "stages_ms": dict(zip(wk.STAGES, stage_ms)),
         "path_tflops": wk.path_tflops(ms_step),
         "e2e": {"value": whole_job_rate(wk.chunk, world, e2e_s * 1e3), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "overlap": "uploads and downloads on two copy streams, double-buffered device "
+                           "staging: step i+1's upload and step i-1's download run during step "
+                           "i"},
         "gpu_launches": int(launches),
         "dev_err": err,
         "clocks": clocks,
