@@ -126,21 +126,14 @@ __global__ void __launch_bounds__(H_THREADS, 1)
     // ---- the CTA's sequence and its 256-row tile there (rows = token x head):
     // sequence b owns ceil(rows_b / 256) consecutive CTAs; the grid has up
     // to one surplus CTA per sequence, which leaves before any barrier
-    int b = 0;
-    int64_t tile = blockIdx.x, q_beg = 0, n_rows = 0;
-    for (; b < a.bt.B; ++b) {
-        q_beg = __ldg(a.bt.cu_q + b);
-        n_rows = (__ldg(a.bt.cu_q + b + 1) - q_beg) * a.H;
-        const int64_t nt = (n_rows + 2 * HBM_ - 1) / (2 * HBM_);
-        if (tile < nt) break;
-        tile -= nt;
-    }
-    if (b == a.bt.B) return;
-    const int64_t q_row_beg = q_beg * a.H;  // the sequence's first row of Q / O
-    const int64_t q_pos0 = __ldg(a.bt.q_pos0 + b), raw_pos0 = __ldg(a.bt.raw_pos0 + b);
-    const int64_t c_beg = __ldg(a.bt.cu_c + b), raw_beg = __ldg(a.bt.cu_raw + b);
-    const int64_t Tc = a.have_c ? __ldg(a.bt.cu_c + b + 1) - c_beg : 0;
-    const int64_t Nraw = a.have_r ? __ldg(a.bt.cu_raw + b + 1) - raw_beg : 0;
+    const SeqTile sq = locate_tile(a.bt, blockIdx.x, a.H, 2 * HBM_);
+    if (sq.b == a.bt.B) return;
+    const int64_t tile = sq.tile, n_rows = sq.nq * a.H;
+    const int64_t q_row_beg = sq.q_beg * a.H;  // the sequence's first row of Q / O
+    const int64_t q_pos0 = sq.q_pos0, raw_pos0 = sq.raw_pos0;
+    const int64_t c_beg = sq.c_beg, raw_beg = sq.raw_beg;
+    const int64_t Tc = a.have_c ? sq.c_end - c_beg : 0;
+    const int64_t Nraw = a.have_r ? sq.raw_end - raw_beg : 0;
     const int64_t row0 = tile * (2 * HBM_);  // sequence-local
     const int64_t rows_here = min((int64_t)(2 * HBM_), n_rows - row0);
     const int64_t t_first = q_pos0 + row0 / a.H;

@@ -156,18 +156,10 @@ __global__ void __launch_bounds__(I_THREADS, 1)
     // the CTA's sequence and its 128-row tile there: sequence b owns
     // ceil(rows_b / 128) consecutive CTAs along x; the grid has up to one
     // surplus CTA per sequence, which leaves before any barrier
-    int bq = 0;
-    int64_t tile = blockIdx.x, q_beg = 0, nq = 0;
-    for (; bq < a.bt.B; ++bq) {
-        q_beg = __ldg(a.bt.cu_q + bq);
-        nq = __ldg(a.bt.cu_q + bq + 1) - q_beg;
-        const int64_t nt = (nq + IBM - 1) / IBM;
-        if (tile < nt) break;
-        tile -= nt;
-    }
-    if (bq == a.bt.B) return;
-    const int64_t q_pos0 = __ldg(a.bt.q_pos0 + bq);
-    const int64_t c_beg = __ldg(a.bt.cu_c + bq), Tc = __ldg(a.bt.cu_c + bq + 1) - c_beg;
+    const SeqTile sq = locate_tile(a.bt, blockIdx.x, 1, IBM);
+    if (sq.b == a.bt.B) return;
+    const int64_t tile = sq.tile, q_beg = sq.q_beg, nq = sq.nq;
+    const int64_t q_pos0 = sq.q_pos0, c_beg = sq.c_beg, Tc = sq.c_end - sq.c_beg;
     const int64_t row0 = tile * IBM;  // sequence-local; global row = q_beg + local
     const int64_t last_row = min(row0 + IBM, nq) - 1;
     int64_t nv_last = n_vis(q_pos0 + last_row, a.m);
@@ -499,13 +491,16 @@ __device__ __forceinline__ void bitonic_sort_u32_asc(uint32_t *a, int P) {
 // candidates equal to K* are collected (in any order, one shared atomic per
 // warp) and written out in ascending index order: through a bitmap over the
 // row's visible entries when it fits in the `R` words that held the keys and
-// indices, else by a bitonic sort.  A row's candidates are the private slots
+// indices (only the words holding a chosen entry are touched, found through
+// a summary bitmap of them), else by a bitonic sort.  A row's candidates are
+// the private slots
 // of each of its gy CTA columns (lcnt of them in each) followed by its
 // overflow slots (count, in a region of ocap slots); rows with a total
 // outside [k, cap], or an overflow past its region, are appended to the
 // failed-row list.  Shared memory: R >= 2 cap words (keys, indices, later the
 // bitmap), PK collected indices, P tie slots (PK, P: powers of two >= k,
-// cap); the tie slots double as the radix selection's spare.
+// cap); the tie slots double as the radix selection's spare and, at the end,
+// as the summary bitmap (R / 32 <= P words).
 __global__ void __launch_bounds__(512) k_cand_pick(Batch bt, int m, int k, int cap, int ocap,
                                                    int R, int PK, int P,
                                                    const int32_t *__restrict__ count,
@@ -544,46 +539,57 @@ __global__ void __launch_bounds__(512) k_cand_pick(Batch bt, int m, int k, int c
         s_ties = 0;
     }
     __syncthreads();
-    {
+    const int n_over = count[r];
+    // each CTA column's count and, with at most NT columns (the usual case),
+    // their block-wide prefix (the place of each column's segment) at once
+    __shared__ int seg_off[NT];
+    int n_priv;
+    if (gy <= NT) {
+        const int c = threadIdx.x < gy ? lcnt[r * gy + threadIdx.x] : 0;
+        seg_off[threadIdx.x] = block_exclusive_scan<NT>(c, wsum, &n_priv);
+    } else {
         int c = 0;
         for (int y = threadIdx.x; y < gy; y += NT) c += lcnt[r * gy + y];
         c = __reduce_add_sync(FULL, c);
         if (lane == 0 && c) atomicAdd(&s_priv, c);
+        __syncthreads();
+        n_priv = s_priv;
     }
-    __syncthreads();
-    const int n_priv = s_priv, n_over = count[r];
     const int n = n_priv + n_over;
     if (n < k || n > cap || n_over > ocap) {
         if (threadIdx.x == 0) flist[atomicAdd(nfail, 1)] = (int32_t)r;
         return;
     }
-    // the private segments, NT CTA columns at a time: a block-wide prefix over
-    // their counts places each segment, then every thread loads its share of
-    // all of them at once (one memory round trip, not one per segment)
-    __shared__ int seg_off[NT];
+    // the private segments, NT CTA columns at a time; the index array first
+    // holds the owner (group-local CTA column) of each place, so that every
+    // thread loads its share of all segments at once, one memory round trip
+    // per group
     int filled = 0;
     for (int y0 = 0; y0 < gy; y0 += NT) {
-        const int y = y0 + threadIdx.x;
-        const int c = y < gy ? lcnt[r * gy + y] : 0;
-        int tot;
-        seg_off[threadIdx.x] = block_exclusive_scan<NT>(c, wsum, &tot);
-        __syncthreads();
-        const int nseg = min(NT, gy - y0);
-        if (filled + tot > cap) {
-            flag(dev_err, LC_DEVERR_BATCH);  // counts inconsistent: never expected
-            tot = cap - filled;
+        int tot = n_priv;
+        if (gy > NT) {
+            const int y = y0 + threadIdx.x;
+            const int c = y < gy ? lcnt[r * gy + y] : 0;
+            seg_off[threadIdx.x] = block_exclusive_scan<NT>(c, wsum, &tot);
         }
+        __syncthreads();
+        if (filled + tot > cap) {
+            flag(dev_err, LC_DEVERR_BATCH);  // counts changed under us: never expected
+            break;
+        }
+        const int nseg = min(NT, gy - y0);
+        for (int sg = warp; sg < nseg; sg += NW) {
+            const int b0 = seg_off[sg], b1 = sg + 1 < nseg ? seg_off[sg + 1] : tot;
+            for (int i = b0 + lane; i < b1; i += 32) idx[filled + i] = (uint32_t)sg;
+        }
+        __syncthreads();
         for (int j0 = threadIdx.x; j0 < tot; j0 += 4 * NT) {
             uint2 v[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int j = j0 + u * NT;
                 if (j < tot) {
-                    // the last segment whose first slot is at or before j
-                    int sg = 0;
-#pragma unroll
-                    for (int step = NT / 2; step > 0; step >>= 1)
-                        if (sg + step < nseg && seg_off[sg + step] <= j) sg += step;
+                    const int sg = (int)idx[filled + j];
                     v[u] = priv[((size_t)r * gy + y0 + sg) * cloc + (j - seg_off[sg])];
                 }
             }
@@ -643,31 +649,46 @@ __global__ void __launch_bounds__(512) k_cand_pick(Batch bt, int m, int k, int c
         for (int i = threadIdx.x; i < k; i += NT) out[i] = (int32_t)sel[i];
         return;
     }
-    // ascending order through a bitmap of the chosen entries (keys and indices are dead)
-    __syncthreads();
-    for (int w = threadIdx.x; w < nw; w += NT) bm[w] = 0u;
+    // ascending order through a bitmap of the chosen entries (keys and indices
+    // are dead) and a summary bitmap of its non-zero words (in the tie slots,
+    // dead too): only the words that hold a chosen entry are cleared, marked
+    // and read back
+    uint32_t *sm = tl;
+    const int ns = (nw + 31) >> 5;
     __syncthreads();
     for (int i = threadIdx.x; i < k; i += NT) {
         const uint32_t e = sel[i];
-        if (e < (uint32_t)nv)
+        if (e < (uint32_t)nv) bm[e >> 5] = 0u;
+    }
+    for (int w = threadIdx.x; w < ns; w += NT) sm[w] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < k; i += NT) {
+        const uint32_t e = sel[i];
+        if (e < (uint32_t)nv) {
             atomicOr(&bm[e >> 5], 1u << (e & 31u));
-        else
+            atomicOr(&sm[e >> 10], 1u << ((e >> 5) & 31u));
+        } else {
             flag(dev_err, LC_DEVERR_BATCH);  // a chosen index outside the row: never expected
+        }
     }
     __syncthreads();
-    // warp w owns words [wb, we); its lanes take consecutive words
-    const int per_w = (nw + NW - 1) / NW;
-    const int wb = min(warp * per_w, nw), we = min(wb + per_w, nw);
+    // the non-zero bitmap words in ascending order, listed in `sel` (dead
+    // now; at most k of them): warp w lists those of summary words [sb, se)
+    const int per_w = (ns + NW - 1) / NW;
+    const int sb = min(warp * per_w, ns), se = min(sb + per_w, ns);
     int cnt = 0;
-    for (int w = wb + lane; w < we; w += 32) cnt += __popc(bm[w]);
+    for (int s0 = sb + lane; s0 < se; s0 += 32) cnt += __popc(sm[s0]);
     cnt = __reduce_add_sync(FULL, cnt);
     if (lane == 0) wsum[warp] = cnt;
     __syncthreads();
-    int off = 0;
-    for (int u = 0; u < warp; ++u) off += wsum[u];
-    for (int w0 = wb; w0 < we; w0 += 32) {
-        const int w = w0 + lane;
-        uint32_t x = w < we ? bm[w] : 0u;
+    int off = 0, nz = 0;
+    for (int u = 0; u < NW; ++u) {
+        if (u < warp) off += wsum[u];
+        nz += wsum[u];
+    }
+    for (int s0 = sb; s0 < se; s0 += 32) {
+        const int sw = s0 + lane;
+        uint32_t x = sw < se ? sm[sw] : 0u;
         const int c = __popc(x);
         int incl = c;
 #pragma unroll
@@ -676,10 +697,35 @@ __global__ void __launch_bounds__(512) k_cand_pick(Batch bt, int m, int k, int c
             if (lane >= o) incl += y;
         }
         int pos = off + incl - c;
-        while (x) {
-            const int b = __ffs(x) - 1;
-            x &= x - 1;
-            if (pos < k) out[pos] = w * 32 + b;
+        for (; x; x &= x - 1) sel[pos++] = (uint32_t)(sw * 32 + __ffs(x) - 1);
+        off += __shfl_sync(FULL, incl, 31);
+    }
+    __syncthreads();
+    // the listed words, an equal share per warp, lanes on consecutive words;
+    // each chosen entry's place is the count of chosen entries before it
+    const int per_l = (nz + NW - 1) / NW;
+    const int lb = min(warp * per_l, nz), le = min(lb + per_l, nz);
+    cnt = 0;
+    for (int i = lb + lane; i < le; i += 32) cnt += __popc(bm[sel[i]]);
+    cnt = __reduce_add_sync(FULL, cnt);
+    if (lane == 0) wsum[warp] = cnt;  // the first counts were read before the last barrier
+    __syncthreads();
+    off = 0;
+    for (int u = 0; u < warp; ++u) off += wsum[u];
+    for (int i0 = lb; i0 < le; i0 += 32) {
+        const int i = i0 + lane;
+        const uint32_t w = i < le ? sel[i] : 0u;
+        uint32_t bits = i < le ? bm[w] : 0u;
+        const int c = __popc(bits);
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(FULL, incl, o);
+            if (lane >= o) incl += y;
+        }
+        int pos = off + incl - c;
+        for (; bits; bits &= bits - 1) {
+            if (pos < k) out[pos] = (int32_t)(w * 32 + __ffs(bits) - 1);
             ++pos;
         }
         off += __shfl_sync(FULL, incl, 31);
@@ -814,8 +860,8 @@ int64_t pick_chunk(int64_t Nq, int64_t n_cols) {
     if (want_y < 1) want_y = 1;
     int64_t chunk = (n_cols + want_y - 1) / want_y;
     chunk = (chunk + IBN - 1) / IBN * IBN;
-    // a CTA first moves its 128 query rows into TMEM; amortise that over at
-    // least 16 tiles
+    // a CTA first moves its 128 query rows into shared memory; amortise that
+    // over at least 16 tiles
     if (chunk < 16 * IBN) chunk = 16 * IBN;
     while ((n_cols + chunk - 1) / chunk > 65535) chunk *= 2;
     return chunk;

@@ -80,6 +80,53 @@ __device__ __forceinline__ int seq_of_row(const Batch &bt, int64_t r) {
     return lo;
 }
 
+// The tile of a CTA of a grid in which sequence b owns ceil(rows_b / per_cta)
+// consecutive CTAs (rows_b = its query rows x rows_per_q), in blockIdx.x
+// order, and that sequence's fields.  b == bt.B: a surplus CTA (the grid
+// adds one per sequence for the partial tiles).  Sequence 0's fields are
+// loaded together with the first bounds, so a one-sequence batch costs one
+// round trip of global loads before the CTA can start its copies.
+struct SeqTile {
+    int b;
+    int64_t tile;                 // tile index within the sequence
+    int64_t q_beg, nq, q_pos0;    // first global query row, rows, position of row 0
+    int64_t c_beg, c_end;         // entries [c_beg, c_end)
+    int64_t raw_beg, raw_end, raw_pos0;
+};
+
+__device__ __forceinline__ SeqTile locate_tile(const Batch &bt, int64_t cta, int64_t rows_per_q,
+                                               int64_t per_cta) {
+    SeqTile s;
+    const int64_t q1 = __ldg(bt.cu_q + 1);
+    s.q_beg = __ldg(bt.cu_q);
+    s.q_pos0 = __ldg(bt.q_pos0);
+    s.c_beg = __ldg(bt.cu_c);
+    s.c_end = __ldg(bt.cu_c + 1);
+    s.raw_beg = __ldg(bt.cu_raw);
+    s.raw_end = __ldg(bt.cu_raw + 1);
+    s.raw_pos0 = __ldg(bt.raw_pos0);
+    s.nq = q1 - s.q_beg;
+    s.tile = cta;
+    s.b = 0;
+    int64_t nt = (s.nq * rows_per_q + per_cta - 1) / per_cta;
+    while (s.tile >= nt) {
+        s.tile -= nt;
+        if (++s.b == bt.B) return s;
+        s.q_beg = __ldg(bt.cu_q + s.b);
+        s.nq = __ldg(bt.cu_q + s.b + 1) - s.q_beg;
+        nt = (s.nq * rows_per_q + per_cta - 1) / per_cta;
+    }
+    if (s.b > 0) {
+        s.q_pos0 = __ldg(bt.q_pos0 + s.b);
+        s.c_beg = __ldg(bt.cu_c + s.b);
+        s.c_end = __ldg(bt.cu_c + s.b + 1);
+        s.raw_beg = __ldg(bt.cu_raw + s.b);
+        s.raw_end = __ldg(bt.cu_raw + s.b + 1);
+        s.raw_pos0 = __ldg(bt.raw_pos0 + s.b);
+    }
+    return s;
+}
+
 // Entries visible from absolute position t under ratio m.
 __device__ __forceinline__ int64_t n_vis(int64_t t, int m) { return (t + 1) / m; }
 

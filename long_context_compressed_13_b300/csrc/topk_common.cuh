@@ -42,6 +42,7 @@ struct RadixScratch {
     int need;
     int cnt;   // keys in the chosen bin
     int fill;  // compaction cursor
+    uint32_t all_and, all_or;  // common bits of the keys (shared-memory selection)
 };
 
 // The `need`-th largest order key (1-based) among order_key(row[0..n-1]),
@@ -110,24 +111,85 @@ __device__ uint32_t radix_kth_largest(const float *__restrict__ row, int64_t n, 
     return prefix;
 }
 
-// As radix_kth_largest, over n order keys held in shared memory.  With
+// As radix_kth_largest, over n order keys held in shared memory.  The bits
+// that every key shares are found first (an AND and an OR over the keys) and
+// need no pass; the 8-bit digits start at the highest bit where keys differ
+// (keys of a selection share their top bits: byte-aligned digits would send
+// nearly every key of the first pass to one or two histogram bins).  With
 // `spare` (room for n keys, NT a multiple of 32), the keys that still match
 // after the first pass are copied there when they are at most half of all,
-// and the last three passes scan only them.
+// and the later passes scan only them.  Once at most 64 keys are left, all
+// matching the digits found so far, one warp ranks them directly.
 template <int NT>
 __device__ uint32_t radix_kth_largest_smem(const uint32_t *keys, int n, int need,
                                            RadixScratch &rs, int *need_left,
                                            uint32_t *spare = nullptr) {
-    uint32_t prefix = 0, mask = 0;
+    if (threadIdx.x == 0) {
+        rs.all_and = 0xffffffffu;
+        rs.all_or = 0u;
+    }
+    __syncthreads();
+    {
+        uint32_t a = 0xffffffffu, o = 0u;
+        for (int j = threadIdx.x; j < n; j += NT) {
+            a &= keys[j];
+            o |= keys[j];
+        }
+        a = __reduce_and_sync(0xffffffffu, a);
+        o = __reduce_or_sync(0xffffffffu, o);
+        if ((threadIdx.x & 31) == 0) {
+            atomicAnd(&rs.all_and, a);
+            atomicOr(&rs.all_or, o);
+        }
+    }
+    __syncthreads();
+    const uint32_t diff = rs.all_and ^ rs.all_or;
+    int hi = 32 - __clz(diff);  // bits [0, hi) still open (0: all keys are equal)
+    uint32_t mask = hi == 32 ? 0u : ~((1u << hi) - 1u);
+    uint32_t prefix = rs.all_and & mask;
     const uint32_t *src = keys;
+    bool first = true, all_match = true;  // all_match: every key of src matches prefix
 #pragma unroll 1
-    for (int pass = 0; pass < 4; ++pass) {
-        const int shift = 24 - 8 * pass;
+    while (hi > 0) {
+        if (all_match && n <= 64) {
+            // few keys left, all matching the prefix: one warp ranks them by
+            // counting (the need-th largest x has fewer than need keys above
+            // it and at least need at or above it)
+            if (threadIdx.x < 32) {
+                const int lane = threadIdx.x;
+                const uint32_t a = lane < n ? src[lane] : 0u;
+                const uint32_t b = lane + 32 < n ? src[lane + 32] : 0u;
+                int ga = 0, ea = 0, gb = 0, eb = 0;
+                for (int j = 0; j < n; ++j) {
+                    const uint32_t x = src[j];
+                    ga += x > a;
+                    ea += x == a;
+                    gb += x > b;
+                    eb += x == b;
+                }
+                const bool ha = lane < n && ga < need && ga + ea >= need;
+                const bool hb = lane + 32 < n && gb < need && gb + eb >= need;
+                const unsigned wa = __ballot_sync(0xffffffffu, ha);
+                const unsigned wb = __ballot_sync(0xffffffffu, hb);
+                const int who = wa ? __ffs(wa) - 1 : __ffs(wb) - 1;  // one of them is set
+                if (lane == who) {
+                    rs.digit = wa ? a : b;
+                    rs.need = need - (wa ? ga : gb);
+                }
+            }
+            __syncthreads();
+            prefix = rs.digit;
+            need = rs.need;
+            __syncthreads();
+            break;
+        }
+        const int lo = hi > 8 ? hi - 8 : 0;  // the digit: bits [lo, hi)
+        const uint32_t dmask = (1u << (hi - lo)) - 1u;
         for (int i = threadIdx.x; i < 256; i += NT) rs.hist[i] = 0;
         __syncthreads();
         for (int j = threadIdx.x; j < n; j += NT) {
             const uint32_t key = src[j];
-            if ((key & mask) == prefix) atomicAdd(&rs.hist[(key >> shift) & 255u], 1u);
+            if ((key & mask) == prefix) atomicAdd(&rs.hist[(key >> lo) & dmask], 1u);
         }
         __syncthreads();
         if (threadIdx.x < 32) {
@@ -162,12 +224,12 @@ __device__ uint32_t radix_kth_largest_smem(const uint32_t *keys, int n, int need
             if (lane == 0) rs.fill = 0;
         }
         __syncthreads();
-        prefix |= rs.digit << shift;
-        mask |= 255u << shift;
+        prefix |= rs.digit << lo;
+        mask |= dmask << lo;
         need = rs.need;
         const int nsel = rs.cnt;
         __syncthreads();
-        if (spare != nullptr && pass == 0 && 2 * nsel <= n) {
+        if (spare != nullptr && first && 2 * nsel <= n) {
             // the keys of the chosen bin, in any order; one shared atomic per warp
             const int lane = threadIdx.x & 31;
             for (int j0 = threadIdx.x & ~31; j0 < n; j0 += NT) {
@@ -183,7 +245,12 @@ __device__ uint32_t radix_kth_largest_smem(const uint32_t *keys, int n, int need
             __syncthreads();
             src = spare;
             n = nsel;
+            all_match = true;
+        } else {
+            all_match = false;
         }
+        first = false;
+        hi = lo;
     }
     *need_left = need;
     return prefix;
