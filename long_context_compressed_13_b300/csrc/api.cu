@@ -63,6 +63,22 @@ static std::atomic<long long> g_stall_clocks{0};
 long long debug_stall_clocks(uint32_t kernel_bit) {
     return (g_stall_mask.load() & kernel_bit) ? g_stall_clocks.load() : 0;
 }
+
+int sm_count() {
+    constexpr int kMax = 64;
+    static std::atomic<int> cache[kMax];
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    if (dev < kMax) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < kMax) cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
 static std::atomic<int32_t> g_last_cuda{0};
 
 static thread_local const char *g_last_kernel = "";

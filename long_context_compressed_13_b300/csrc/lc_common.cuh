@@ -28,6 +28,9 @@ lc_status check_launch_error(cudaError_t e);  // records e, returns LC_ERR_CUDA
 // Test hook (lc_debug_stall): clocks the MMA issuer of the named tensor-core
 // kernel waits at its start on a barrier nothing completes (0 = off).
 long long debug_stall_clocks(uint32_t kernel_bit);
+// Streaming multiprocessors of the current device (looked up once per
+// device); 0 when the query fails.
+int sm_count();
 
 // ---------------------------------------------------------------- dtypes
 template <typename T> struct io;
