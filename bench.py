@@ -807,8 +807,6 @@ class HcaPrefill:
                                      "fp64); compressed entries built untimed")
 
 
-SETTLE_S = 5.0  # idle seconds between the workloads of one run
-
 WORKLOADS = {"layer_pair_1m": LayerPair, "csa_decode": Decode,
              "csa_decode_incremental": DecodeIncremental, "csa_decode_mxfp4": DecodeMXFP4,
              "csa_decode_mxfp8": DecodeMXFP8, "csa_prefill": CsaPrefill,
@@ -968,11 +966,39 @@ def measure(wk, args, dist, device, peaks, world, rank, cpu_budget):
 
 
 def run_ours(args):
-    import long_context_compressed_13_b300 as lc
-    lc.load_library()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    names = ["layer_pair_1m", "csa_decode", "csa_decode_incremental", "csa_decode_mxfp4",
+             "csa_decode_mxfp8", "csa_prefill", "hca_prefill"] \
+        if args.workload == "all" else [args.workload]
+    recs = {}
+    if len(names) > 1 and world == 1:
+        # one process per workload: run in one process after the others, the
+        # decode steps measured up to 7x slower in places (the random gathers
+        # of the CSA attention most), a state of the device that a pause did
+        # not clear and a fresh process does not have
+        for name in names:
+            budget = args.cpu_budget if name == names[0] else args.cpu_budget / 2
+            cmd = [sys.executable, os.path.abspath(__file__), "--workload", name,
+                   "--steps", str(args.steps), "--warmup", str(args.warmup),
+                   "--cpu-budget", str(budget), "--ctx", str(args.ctx)]
+            if args.no_cpu_baseline:
+                cmd.append("--no-cpu-baseline")
+            if args.decode_ctx:
+                cmd += ["--decode-ctx", args.decode_ctx]
+            res = subprocess.run(cmd, stdout=subprocess.PIPE, text=True)
+            if res.returncode != 0:
+                raise SystemExit(f"bench.py: workload {name} failed ({res.returncode})")
+            lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+            recs[name] = json.loads(lines[-1])
+        out = recs[names[0]]
+        for name in names[1:]:
+            out[SUB_RECORDS[name]] = recs[name]
+        print(json.dumps(out), flush=True)
+        return
+    import long_context_compressed_13_b300 as lc
+    lc.load_library()
     if not torch.cuda.is_available():
         raise SystemExit("bench.py: no CUDA device")
     torch.cuda.set_device(local)
@@ -983,10 +1009,6 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device(device))
     peaks = load_peaks()
 
-    names = ["layer_pair_1m", "csa_decode", "csa_decode_incremental", "csa_decode_mxfp4",
-             "csa_decode_mxfp8", "csa_prefill", "hca_prefill"] \
-        if args.workload == "all" else [args.workload]
-    recs = {}
     for name in names:
         if name == "layer_pair_1m":
             wk = LayerPair(lc, device, ctx=args.ctx)
@@ -994,15 +1016,9 @@ def run_ours(args):
             wk = WORKLOADS[name](lc, device)
         budget = args.cpu_budget if name == names[0] else args.cpu_budget / 2
         recs[name] = measure(wk, args, dist, device, peaks, world, rank, budget)
-        recs[name]["settle_s"] = SETTLE_S if name != names[0] else 0.0
         del wk
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
-        if name != names[-1]:
-            # the next workload starts from an idle GPU: right after a heavy
-            # one (without a CPU baseline in between) the short decode steps
-            # measured up to 1.6x slower
-            time.sleep(SETTLE_S)
     out = recs[names[0]]
     for name in names[1:]:
         out[SUB_RECORDS[name]] = recs[name]

@@ -757,8 +757,11 @@ constexpr int NW_WARP_MAX = 1024;
 FusedPlan plan_fused(const lc_batch &b, int k) {
     FusedPlan p{};
     const int64_t n = b.max_c;
+    // the sampling stride: at most 32, at least 2k samples per longest row
+    // (the candidate count is then rho * stride +- stride * sqrt(rho), far
+    // above k: a row whose count still falls short goes to the fallback)
     p.stride = 1;
-    while (p.stride < 32 && n / (2 * p.stride) >= 8 * (int64_t)k) p.stride *= 2;
+    while (p.stride < 32 && n / (2 * p.stride) >= 2 * (int64_t)k) p.stride *= 2;
     if (p.stride == 1) {
         p.rho = k;
     } else {

@@ -228,7 +228,7 @@ def test_tc_scores_ragged(lc, HI):
 def test_fused_topk_ragged(lc, long_T):
     # one batch of sequences of very different lengths.  The sampled threshold
     # reads every s-th entry of each sequence from that sequence's own first
-    # entry (s = 16 here, and sequence starts that are not multiples of it);
+    # entry (s = 32 here, and sequence starts that are not multiples of it);
     # rows of the short sequences hold k or fewer visible entries; sequence 1's
     # rows see 4000 tied best entries, more than the candidate capacity, which
     # the fallback settles from that sequence's own keys (the lowest indices).
