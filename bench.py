@@ -83,10 +83,10 @@ NCU_STAGE_TRAFFIC = {
     ("layer_pair_1m", "lightning_index+topk"): 513.0e6,
     # k_sparse_tc 1122.2 MB read + 128.0 MB written
     ("layer_pair_1m", "sparse_mqa_attn"): 1250.2e6,
-    # the 32K CSA prefill: k_sparse_tc 625.2 + 503.7 MB; index + top-k
-    # kernels 643.4 MB
+    # the 32K CSA prefill: k_sparse_tc 625.3 + 503.6 MB; index + top-k
+    # kernels 564.4 MB (every 8th entry sampled)
     ("csa_prefill", "sparse_mqa_attn"): 1128.9e6,
-    ("csa_prefill", "lightning_index+topk"): 643.4e6,
+    ("csa_prefill", "lightning_index+topk"): 564.4e6,
     # the 128K HCA prefill: k_hca_tc 2215.7 MB read + 2127.5 MB written
     ("hca_prefill", "hca_dense_attn"): 4343.2e6,
 }
