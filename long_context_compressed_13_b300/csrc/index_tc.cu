@@ -20,8 +20,10 @@
 //               add and FMA, then either stores the 32 scores of the tile
 //               (MATERIALIZE) or appends the entries whose score reaches the
 //               row's threshold to the row's candidates (FILTER).  The
-//               threshold test is a sign-bit collect of acc - theta; the
-//               candidates are staged eight columns at a time.  A buffer is
+//               threshold test is a sign-bit collect of acc - theta; each
+//               lane then takes one of its candidates per round, its score
+//               picked from the registers by a select tree on the column's
+//               bits (about 1.5 rounds per warp and tile).  A buffer is
 //               handed back to its issuer through an mbarrier (one arrival
 //               per warp) as soon as the warp's TMEM read completes.
 // The fused top-k of a row (see index_topk_tc_launch):
@@ -77,8 +79,7 @@ struct IdxCfg {
     static constexpr uint32_t Q_BOX = IBM * 128;             // 128 query rows x 128 B
     static constexpr uint32_t SM_Q = 0;                      // 8 heads of q_I
     static constexpr uint32_t SM_K = SM_Q + 8 * Q_BOX;       // ring of head boxes
-    static constexpr uint32_t SM_STG = SM_K + NSB * HEAD_BOX;  // FILTER staging, 32 B / thread
-    static constexpr uint32_t SM_BAR = SM_STG + NEPI * 8 * 4;
+    static constexpr uint32_t SM_BAR = SM_K + NSB * HEAD_BOX;
     static constexpr uint32_t SM_LCNT = SM_BAR + 256;          // FILTER: per-row slot counters
     static constexpr uint32_t SMEM = SM_LCNT + IBM * 4;
 };
@@ -107,6 +108,22 @@ __device__ __forceinline__ void arrive_lane0(uint64_t *bar, int lane) {
         "@p mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n\t}" ::"r"(smem_u32(bar)),
         "r"(lane)
         : "memory");
+}
+
+// Column c (0..31) of an epilogue thread's scores, held as pairs (column 2j
+// in p[j].x, 2j+1 in p[j].y), taken by a select tree on the bits of c, so
+// that a candidate's score needs neither a dynamically indexed register nor
+// a round trip through shared memory.
+__device__ __forceinline__ float col_of(const float2 (&p)[EPI_COLS / 2], int c) {
+    float2 l8[8], l4[4], l2[2];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) l8[i] = (c & 16) ? p[i + 8] : p[i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) l4[i] = (c & 8) ? l8[i + 4] : l8[i];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) l2[i] = (c & 4) ? l4[i + 2] : l4[i];
+    const float2 q = (c & 2) ? l2[1] : l2[0];
+    return (c & 1) ? q.y : q.x;
 }
 
 // Inverse of order_key: the float whose key is `key` (+0 for the key of
@@ -317,7 +334,6 @@ __global__ void __launch_bounds__(I_THREADS, 1)
         const uint32_t lane_addr = taddr + ((uint32_t)(quad * 32) << 16);
         const uint32_t buf_addr = lane_addr + part * EPI_COLS;
         bool ok = !dead;
-        float *stg = reinterpret_cast<float *>(smem + C::SM_STG) + tid * 8;
         float2 acc[EPI_COLS / 2];
         for (int i = 0; ok && i < n_t; ++i) {
 #pragma unroll
@@ -417,27 +433,17 @@ __global__ void __launch_bounds__(I_THREADS, 1)
                         ob = atomicAdd(a.count + row, lb + n - first) - first;
                     }
                     int base = lb;
-                    // stage eight columns at a time so a candidate can be read by column
-#pragma unroll
-                    for (int rd = 0; rd < EPI_COLS / 8; ++rd) {
-                        uint32_t m8 = (cand >> (8 * rd)) & 0xffu;
-                        if (!m8) continue;
-                        reinterpret_cast<float4 *>(stg)[0] =
-                            make_float4(acc[4 * rd].x, acc[4 * rd].y, acc[4 * rd + 1].x,
-                                        acc[4 * rd + 1].y);
-                        reinterpret_cast<float4 *>(stg)[1] =
-                            make_float4(acc[4 * rd + 2].x, acc[4 * rd + 2].y, acc[4 * rd + 3].x,
-                                        acc[4 * rd + 3].y);
-                        while (m8) {
-                            const int c = __ffs(m8) - 1;
-                            m8 &= m8 - 1;
-                            const uint2 kv = make_uint2(order_key(stg[c]), (uint32_t)(e0 + 8 * rd + c));
-                            if (base < a.cloc)
-                                pr[base] = kv;
-                            else if (base + ob < a.ocap)
-                                cr[base + ob] = kv;
-                            ++base;
-                        }
+                    // one candidate per lane and round, lowest column first
+                    while (cand) {
+                        const int c = __ffs(cand) - 1;
+                        cand &= cand - 1;
+                        const uint2 kv =
+                            make_uint2(order_key(col_of(acc, c)), (uint32_t)(e0 + c));
+                        if (base < a.cloc)
+                            pr[base] = kv;
+                        else if (base + ob < a.ocap)
+                            cr[base + ob] = kv;
+                        ++base;
                     }
                 }
             }
