@@ -282,7 +282,10 @@ __global__ void __launch_bounds__(I_THREADS, 1)
             bool ok = (a.stall == 0 || mbar_wait(&bars.stall, 0, abort, a.stall)) &&
                       mbar_wait(&bars.q_full, 0, abort);
             tc_fence_after();
-            const uint32_t q_base = smem_u32(smem + C::SM_Q);
+            // operand descriptors of the first q box and the first ring slot; each
+            // MMA adds its box and K-step offset
+            const uint64_t qd0 = sw128_desc(smem_u32(smem + C::SM_Q), 16, 1024);
+            const uint64_t kd0 = sw128_desc(smem_u32(smem + C::SM_K), 16, 1024);
             int mine = 0;  // MMAs this thread issued
             for (int g = par; ok && g < n_all; g += 2) {
                 const int s = g % NSB, h = g % HI, b = g % NBUF, u = g / NBUF;
@@ -297,12 +300,12 @@ __global__ void __launch_bounds__(I_THREADS, 1)
                     !mbar_wait(&bars.k_full[s], (g / NSB) & 1, abort))
                     break;
                 tc_fence_after();
-                const uint32_t k_base = smem_u32(smem + C::SM_K + s * C::HEAD_BOX);
-                const uint32_t qh = q_base + h * C::Q_BOX;
+                const uint64_t qd = desc_add(qd0, h * C::Q_BOX);
+                const uint64_t kd = desc_add(kd0, s * C::HEAD_BOX);
 #pragma unroll
                 for (int kk = 0; kk < IDI / 16; ++kk)
-                    mma_bf16(taddr + b * IBN, sw128_desc(qh + kk * 32, 16, 1024),
-                             sw128_desc(k_base + kk * 32, 16, 1024), IDESC, kk > 0);
+                    mma_bf16(taddr + b * IBN, desc_add(qd, kk * 32), desc_add(kd, kk * 32), IDESC,
+                             kk > 0);
                 mma_commit(&bars.d_full[b]);
                 mma_commit(&bars.k_empty[s]);
                 ++mine;

@@ -215,6 +215,14 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t start, uint32_t lbo, uin
     return d;
 }
 
+// The descriptor of the same layout starting `bytes` (a multiple of 16) further
+// on: only the 14-bit start-address field (16-byte units) moves, and it cannot
+// carry out for shared-memory offsets below 256 KB.  Lets an MMA issuer build
+// each operand's descriptor once and add offsets.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) {
+    return d + (bytes >> 4);
+}
+
 // Instruction descriptor of kind::f16 with bf16 A and B, fp32 D, dense.
 // a_mn / b_mn: operand stored MN-major (1) instead of K-major (0).
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {
