@@ -76,17 +76,15 @@ NCU_STAGE_TRAFFIC = {
     # the decode step's kernels at the full benchmarked size: streaming
     # indexer 2505.4 MB, cluster top-k 9.8 MB, CSA attention 40.2 MB
     ("csa_decode", "step"): 2555.4e6,
-    # the layer pair at 1M: k_hca_tc 140.8 MB read + 84.1 MB written
-    ("layer_pair_1m", "hca_dense_attn"): 224.9e6,
-    # index + top-k: candidate pass 342.4, 16-bit sample 23.6, thresholds
+    # the layer pair at 1M: k_hca_tc 140.9 MB read + 84.2 MB written
+    ("layer_pair_1m", "hca_dense_attn"): 225.1e6,
+    # index + top-k: candidate pass 341.8, 16-bit sample 23.7, thresholds
     # 67.1, candidate pick 79.9, fallback 0 (MB read + written)
-    ("layer_pair_1m", "lightning_index+topk"): 513.0e6,
-    # k_sparse_tc 1122.2 MB read + 128.0 MB written
-    ("layer_pair_1m", "sparse_mqa_attn"): 1250.2e6,
-    # the 32K CSA prefill: k_sparse_tc 625.3 + 503.6 MB; index + top-k
-    # kernels 564.4 MB (every 8th entry sampled)
+    ("layer_pair_1m", "lightning_index+topk"): 512.5e6,
+    # k_sparse_tc 1121.8 MB read + 128.1 MB written
+    ("layer_pair_1m", "sparse_mqa_attn"): 1249.9e6,
+    # the 32K CSA prefill: k_sparse_tc 625.3 + 503.6 MB
     ("csa_prefill", "sparse_mqa_attn"): 1128.9e6,
-    ("csa_prefill", "lightning_index+topk"): 564.4e6,
     # the 128K HCA prefill: k_hca_tc 2215.7 MB read + 2127.5 MB written
     ("hca_prefill", "hca_dense_attn"): 4343.2e6,
 }
@@ -319,7 +317,7 @@ class LayerPair:
     def config(self, world):
         return layer_pair_config(self.ctx, self.chunk, self.H, self.d, world)
 
-    def roofline(self, stage_ms, peaks, region_ms):
+    def roofline(self, stage_ms, peaks, region_ms, step_ms):
         w = self.work()
         flops_of = {"lightning_index+topk": w["index_flop"], "sparse_mqa_attn": w["csa_attn_flop"],
                     "hca_dense_attn": w["hca_attn_flop"]}
@@ -421,12 +419,11 @@ class Decode:
     def cpu_baseline(self, budget_s):
         return decode_cpu_baseline(self, budget_s=budget_s)
 
-    def roofline(self, stage_ms, peaks, region_ms):
+    def roofline(self, stage_ms, peaks, region_ms, step_ms):
         """HBM roofline of the whole step: its algorithmic bytes over the
-        step's time (the sum of its stages' event times)."""
+        timed step (a graph replay of its kernels, or the eager calls)."""
         w = self.work()
-        ms = sum(stage_ms)
-        gbs = w["step_bytes"] / (ms / 1e3) / 1e9
+        gbs = w["step_bytes"] / (step_ms / 1e3) / 1e9
         return {"bound": "hbm", "kernel": "whole step (lightning_index+topk, sparse_mqa_attn)",
                 "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": gbs / peaks["hbm_gbs"],
@@ -489,8 +486,8 @@ class DecodeMX(Decode):
                          f"; indexer q/k in MXFP{self.fmt} (OCP MX, 32-value blocks)")
         return c
 
-    def roofline(self, stage_ms, peaks, region_ms):
-        r = super().roofline(stage_ms, peaks, region_ms)
+    def roofline(self, stage_ms, peaks, region_ms, step_ms):
+        r = super().roofline(stage_ms, peaks, region_ms, step_ms)
         r["traffic"] = None
         return r
 
@@ -618,10 +615,9 @@ class DecodeIncremental:
                 "context_mean": float(np.mean(self.ctx0)), "parallelism": f"replicas x{world}",
                 "l2": "inputs larger than L2 (indexer keys 2.7 GB)"}
 
-    def roofline(self, stage_ms, peaks, region_ms):
+    def roofline(self, stage_ms, peaks, region_ms, step_ms):
         w = self.work()
-        ms = sum(stage_ms)
-        gbs = w["step_bytes"] / (ms / 1e3) / 1e9
+        gbs = w["step_bytes"] / (step_ms / 1e3) / 1e9
         return {"bound": "hbm", "kernel": "whole step (decode_append, lightning_index+topk, "
                                           "sparse_mqa_attn)",
                 "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -703,7 +699,7 @@ class CsaPrefill:
                 "parallelism": f"replicas x{world}",
                 "l2": "inputs larger than L2 (Q 512 MiB)"}
 
-    def roofline(self, stage_ms, peaks, region_ms):
+    def roofline(self, stage_ms, peaks, region_ms, step_ms):
         w = self.work()
         return tensor_roofline(self.STAGES, stage_ms,
                                {"lightning_index+topk": w["index_flop"],
@@ -784,7 +780,7 @@ class HcaPrefill:
                 "parallelism": f"replicas x{world}",
                 "l2": "inputs larger than L2 (Q 2 GiB)"}
 
-    def roofline(self, stage_ms, peaks, region_ms):
+    def roofline(self, stage_ms, peaks, region_ms, step_ms):
         return tensor_roofline(self.STAGES, stage_ms, {"hca_dense_attn": self.work()["attn_flop"]},
                                peaks, region_ms, "hca_prefill")
 
@@ -844,6 +840,25 @@ def measure(wk, args, dist, device, peaks, world, rank, cpu_budget):
         wk.step()
     torch.cuda.synchronize()
 
+    # ---- the step as a CUDA graph: its C-ABI calls captured once, before the
+    # timed region (no kernel runs during capture), so that each timed step is
+    # one replay of the same kernels on the same buffers without per-launch
+    # host gaps; --eager times the calls themselves
+    graph, launch_mode, per_step = None, "eager calls", None
+    if not args.eager:
+        try:
+            l0 = lc.launch_count()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                wk.step()
+            per_step = lc.launch_count() - l0
+            g.replay()
+            torch.cuda.synchronize()
+            graph, launch_mode = g, "one CUDA-graph replay per step (the step's calls captured once)"
+        except RuntimeError as e:  # capture refused: time the calls
+            print(f"graph capture unavailable ({e}); timing eager calls", file=sys.stderr)
+            torch.cuda.synchronize()
+
     # ---- device-timed region
     nst = len(wk.STAGES)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
@@ -859,14 +874,23 @@ def measure(wk, args, dist, device, peaks, world, rank, cpu_budget):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for s in range(args.steps):
-        wk.step(ev[s])
+        if graph is not None:
+            graph.replay()
+        else:
+            wk.step(ev[s])
     t_end.record(stream)
     torch.cuda.synchronize()
-    launches = lc.launch_count() - l0
+    launches = lc.launch_count() - l0 if graph is None else per_step * args.steps
     if dist:
         dist.barrier()
     clocks = sampler.stop()
     ms = max_over_ranks(dist, t_start.elapsed_time(t_end), device)
+    if graph is not None:
+        # per-stage times from as many eager steps with events between the stages
+        for s in range(args.steps):
+            wk.step(ev[s])
+        torch.cuda.synchronize()
+        del graph
     stage_ms = [statistics.mean(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps))
                 for i in range(nst)]
     err = int(wk.err.item())
@@ -942,7 +966,7 @@ def measure(wk, args, dist, device, peaks, world, rank, cpu_budget):
         "dtype": getattr(wk, "DTYPE", "bf16"),
         "data": "synthetic",
         "config": wk.config(world),
-        "roofline": wk.roofline(stage_ms, peaks, ms),
+        "roofline": wk.roofline(stage_ms, peaks, ms, ms_step),
         "stages_ms": dict(zip(wk.STAGES, stage_ms)),
         "path_tflops": wk.path_tflops(ms_step),
         "e2e": {"value": whole_job_rate(wk.chunk, world, e2e_s * 1e3), "unit": UNIT,
@@ -951,6 +975,7 @@ def measure(wk, args, dist, device, peaks, world, rank, cpu_budget):
                            "staging: step i+1's upload and step i-1's download run during step "
                            "i"},
         "gpu_launches": int(launches),
+        "launch": launch_mode,
         "dev_err": err,
         "clocks": clocks,
     }
@@ -985,6 +1010,8 @@ def run_ours(args):
                    "--cpu-budget", str(budget), "--ctx", str(args.ctx)]
             if args.no_cpu_baseline:
                 cmd.append("--no-cpu-baseline")
+            if args.eager:
+                cmd.append("--eager")
             if args.decode_ctx:
                 cmd += ["--decode-ctx", args.decode_ctx]
             res = subprocess.run(cmd, stdout=subprocess.PIPE, text=True)
@@ -1183,6 +1210,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="time the step's calls as launched, not a CUDA-graph replay of them")
     # a shorter context keeps the same kernels on a smaller case (profiler
     # captures); the measured workload is the default 1,048,576 tokens
     ap.add_argument("--ctx", type=int, default=1 << 20)
