@@ -12,7 +12,11 @@
 //               128-column TMEM score buffers (score buffer g % 4 for the g-th
 //               head of the CTA); warp 17 issues the even heads and warp 18
 //               the odd ones, so the short tensor-core queue stays fed while
-//               one issuer waits; a buffer is reused four heads later
+//               one issuer waits; a buffer is reused four heads later.  One
+//               commit per head: its arrival on k_empty of the head box's
+//               ring slot both frees the box for the producer and tells the
+//               epilogue that the head's scores are in TMEM (a commit costs
+//               the tensor pipe about 40 cycles)
 //   warps 0-15  epilogue: warp w owns TMEM lanes 32(w%4).. (its query rows)
 //               and columns 32(w/4).. of each buffer; it folds the heads in
 //               order, acc = fma(w_h / 2, s_h + |s_h|, acc) (= w_h max(s_h, 0)
@@ -70,8 +74,9 @@ constexpr int NEPI = 512;         // epilogue threads (16 warps)
 constexpr int I_THREADS = NEPI + 96;  // + producer warp + two MMA warps
 constexpr int EPI_COLS = 32;      // columns of a score buffer per epilogue thread
 constexpr int NBUF = 4;           // TMEM score buffers (one head each)
-constexpr int NSB = 5;            // shared-memory head boxes in flight
+constexpr int NSB = 4;            // shared-memory head boxes in flight (one per score buffer)
 constexpr uint32_t I_TMEM_COLS = 512;
+static_assert(NSB == NBUF, "the epilogue waits on the key box's slot of its score buffer");
 constexpr int MODE_MATERIALIZE = 0, MODE_FILTER = 1, MODE_SAMPLE16 = 2;
 
 struct IdxCfg {
@@ -85,7 +90,8 @@ struct IdxCfg {
 };
 
 struct IdxBars {
-    uint64_t q_full, k_full[NSB], k_empty[NSB], d_full[NBUF];
+    // k_empty[s]: the MMA of the box in slot s is complete (producer and epilogue)
+    uint64_t q_full, k_full[NSB], k_empty[NSB];
     // releases of each score buffer: every epilogue warp arrives once its
     // reads of a use of the buffer are complete
     uint64_t freed[NBUF];
@@ -220,10 +226,7 @@ __global__ void __launch_bounds__(I_THREADS, 1)
             mbar_init(&bars.k_full[s], 1);
             mbar_init(&bars.k_empty[s], 1);
         }
-        for (int b = 0; b < NBUF; ++b) {
-            mbar_init(&bars.d_full[b], 1);
-            mbar_init(&bars.freed[b], NEPI / 32);
-        }
+        for (int b = 0; b < NBUF; ++b) mbar_init(&bars.freed[b], NEPI / 32);
         fence_barrier_init();
     }
     int *lcount = reinterpret_cast<int *>(smem + C::SM_LCNT);  // FILTER: slots used per row
@@ -291,11 +294,11 @@ __global__ void __launch_bounds__(I_THREADS, 1)
                 const int s = g % NSB, h = g % HI, b = g % NBUF, u = g / NBUF;
                 // The release of buffer b (the epilogue's read of head g-4) comes
                 // first: the epilogue reads heads in order, so it also read head
-                // g-NSB, whose box is the previous use of slot s and belongs to
-                // the other issuer.  Only then is k_full[s] at most one phase
-                // behind box g, which a parity wait needs: waited first, it
-                // could pass on the completed phase before that one while box
-                // g-NSB is still landing.
+                // g-NSB, whose box is the previous use of slot s (the MMA that
+                // read it is complete and the box had landed).  Only then is
+                // k_full[s] at most one phase behind box g, which a parity wait
+                // needs: waited first, it could pass on the completed phase
+                // before that one while box g-NSB is still landing.
                 if ((u > 0 && !mbar_wait(&bars.freed[b], (uint32_t)(u - 1) & 1u, abort)) ||
                     !mbar_wait(&bars.k_full[s], (g / NSB) & 1, abort))
                     break;
@@ -306,7 +309,6 @@ __global__ void __launch_bounds__(I_THREADS, 1)
                 for (int kk = 0; kk < IDI / 16; ++kk)
                     mma_bf16(taddr + b * IBN, desc_add(qd, kk * 32), desc_add(kd, kk * 32), IDESC,
                              kk > 0);
-                mma_commit(&bars.d_full[b]);
                 mma_commit(&bars.k_empty[s]);
                 ++mine;
             }
@@ -338,17 +340,22 @@ __global__ void __launch_bounds__(I_THREADS, 1)
         const uint32_t buf_addr = lane_addr + part * EPI_COLS;
         bool ok = !dead;
         float2 acc[EPI_COLS / 2];
+        // head g's MMA is complete once phase g / NSB of k_empty[g % NSB] (the
+        // release of its key box; the slot is the score buffer, NSB == NBUF) is.
+        // That barrier is never two phases ahead here: its next phase is box
+        // g + NSB's, whose MMA waits for this epilogue's release of head g
         for (int i = 0; ok && i < n_t; ++i) {
 #pragma unroll
             for (int c = 0; c < EPI_COLS / 2; ++c) acc[c] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int h = 0; h < HI; ++h) {
-                // buffer and phase of the g-th head are compile-time for HI = 8
+                // the score buffer of the g-th head is compile-time for HI = 8
+                // slot, buffer and phase of the g-th head are compile-time for HI = 8
                 const int g = i * HI + h, b = g % NBUF;
-                const uint32_t ph = (uint32_t)(g / NBUF) & 1u;
+                const uint32_t kph = (uint32_t)(g / NBUF) & 1u;
                 // the (suspending) try-wait normally succeeds; the bounded loop is the slow path
-                if (!__all_sync(FULL, mbar_try_wait(&bars.d_full[b], ph)) &&
-                    !__all_sync(FULL, mbar_wait(&bars.d_full[b], ph, abort))) {
+                if (!__all_sync(FULL, mbar_try_wait(&bars.k_empty[b], kph)) &&
+                    !__all_sync(FULL, mbar_wait(&bars.k_empty[b], kph, abort))) {
                     ok = false;
                     break;
                 }
