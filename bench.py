@@ -79,7 +79,8 @@ NCU_STAGE_TRAFFIC = {
     # the layer pair at 1M: k_hca_tc 140.9 MB read + 84.2 MB written
     ("layer_pair_1m", "hca_dense_attn"): 225.1e6,
     # index + top-k: candidate pass 341.8, 16-bit sample 23.7, thresholds
-    # 67.1, candidate pick 79.9, fallback 0 (MB read + written)
+    # 67.1, candidate pick 79.9 (its 512-thread build; the 256-thread one
+    # reads the same candidates), fallback 0 (MB read + written)
     ("layer_pair_1m", "lightning_index+topk"): 512.5e6,
     # k_sparse_tc 1121.8 MB read + 128.1 MB written
     ("layer_pair_1m", "sparse_mqa_attn"): 1249.9e6,
