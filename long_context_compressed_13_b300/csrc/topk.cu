@@ -58,7 +58,11 @@ namespace cg = cooperative_groups;
 
 namespace {
 constexpr int TC_THREADS = 512;
-constexpr int TC_STAGE_KEYS = 16384;  // keys of a slice staged in shared memory (64 KB)
+// keys of a slice staged in shared memory (32 KB): an 8-CTA cluster stages
+// rows of up to 65,536 entries (the decode batch's longest), and four CTAs
+// fit on an SM, so 64 rows x 8 CTAs run as one wave (with 64 KB slices, three
+// per SM, they ran as 1.15 waves: 41 against 56 us for the batch-64 decode)
+constexpr int TC_STAGE_KEYS = 8192;
 }  // namespace
 
 __global__ void __launch_bounds__(TC_THREADS) k_topk_cluster(const float *__restrict__ scores,
