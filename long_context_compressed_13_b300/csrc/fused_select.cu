@@ -107,8 +107,10 @@ __global__ void __launch_bounds__(SEL_WARPS * 32) k_cand_pick_warp(
         return;
     }
     const int nw = (int)((nv + 31) >> 5);
-    int n_priv = 0;
-    for (int y = lane; y < gy; y += 32) n_priv += lcnt[r * gy + y];
+    // the first 32 segments' counts, one per lane (shuffled out below)
+    const int lc0 = lane < gy ? lcnt[r * gy + lane] : 0;
+    int n_priv = lc0;
+    for (int y = lane + 32; y < gy; y += 32) n_priv += lcnt[r * gy + y];
     n_priv = __reduce_add_sync(FULL, n_priv);
     const int n_over = count[r];
     const int n = n_priv + n_over;
@@ -117,21 +119,27 @@ __global__ void __launch_bounds__(SEL_WARPS * 32) k_cand_pick_warp(
         return;
     }
     // every candidate of the row: (order key, entry index); all 32 lanes step
-    // together, lanes past a segment's end get valid = false
+    // together, lanes past a segment's end get valid = false.  Each lane has
+    // four loads in flight before it visits them (the visits are shared-memory
+    // atomics, which the loads would otherwise wait behind one by one)
     auto each = [&](auto f) {
-        for (int y = 0; y < gy; ++y) {
-            const int c = lcnt[r * gy + y];
-            const uint2 *seg = priv + ((size_t)r * gy + y) * cloc;
-            for (int i0 = 0; i0 < c; i0 += 32) {
-                const bool ok = i0 + lane < c;
-                f(ok ? seg[i0 + lane] : make_uint2(0u, 0u), ok);
+        auto run = [&](const uint2 *seg, int c) {
+            for (int i0 = 0; i0 < c; i0 += 128) {
+                uint2 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + 32 * u + lane;
+                    v[u] = i < c ? seg[i] : make_uint2(0u, 0u);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (i0 + 32 * u < c) f(v[u], i0 + 32 * u + lane < c);
             }
-        }
-        const uint2 *ov = cand + (size_t)r * ocap;
-        for (int i0 = 0; i0 < n_over; i0 += 32) {
-            const bool ok = i0 + lane < n_over;
-            f(ok ? ov[i0 + lane] : make_uint2(0u, 0u), ok);
-        }
+        };
+        for (int y = 0; y < gy; ++y)
+            run(priv + ((size_t)r * gy + y) * cloc,
+                y < 32 ? __shfl_sync(FULL, lc0, y) : lcnt[r * gy + y]);
+        run(cand + (size_t)r * ocap, n_over);
     };
     auto keys = [&](auto f) { each([&](uint2 kv, bool ok) { f(kv.x, ok); }); };
     int need = k;
