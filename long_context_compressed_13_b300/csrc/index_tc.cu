@@ -6,7 +6,8 @@
 //   q_I of the 128 rows stays in shared memory (one 16 KB TMA box per head)
 //   for the CTA's lifetime, so all 512 TMEM columns hold score buffers.
 //   warp 16     TMA producer: q_I once, then per tile of 128 entries one 16 KB
-//               box per head into a ring of head boxes
+//               box per head into a ring of four head boxes (one per score
+//               buffer)
 //   warps 17-18 MMA issuers (warp 17 also owns TMEM): per tile, head by
 //               head, one M=128, N=128, K=64 product q_h k_h^T into one of four
 //               128-column TMEM score buffers (score buffer g % 4 for the g-th
@@ -31,16 +32,19 @@
 //               handed back to its issuer through an mbarrier (one arrival
 //               per warp) as soon as the warp's TMEM read completes.
 // The fused top-k of a row (see index_topk_tc_launch):
-//   1. scores of every s-th entry (MATERIALIZE over a strided tensor map);
-//   2. theta = the rho-th largest sampled key, a lower bound for the k-th
-//      largest key of the full row with overwhelming probability;
+//   1. the top 16 bits of the order keys of every s-th entry's score
+//      (SAMPLE16 over a strided tensor map, visible columns only);
+//   2. theta = the rho-th largest sampled key (a lower bound of it, from the
+//      truncated keys), below the k-th largest key of the full row with
+//      overwhelming probability;
 //   3. FILTER pass over all entries: candidates = entries with key >= theta,
 //      written to slots private to (row, CTA column), reserved by a
 //      shared-memory atomic, with a shared overflow region per row;
 //   4. exact top-k of the candidates, valid when the row has between k and
 //      `cap` candidates: then every member of the true top-k is a candidate;
-//   5. rows outside that range (rare: massive ties or an unlucky sample) are
-//      redone exactly from fully materialised scores.
+//   5. rows outside that range (rare: massive ties or an unlucky sample) go
+//      to a list that a fixed grid redoes exactly from recomputed scores, a
+//      row buffer per CTA.
 // Both passes run the same arithmetic, so a sampled score and the FILTER
 // pass's score of the same entry are bit-identical.
 #include <cmath>
